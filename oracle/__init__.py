@@ -1,0 +1,181 @@
+"""HSTU attention fp64 CPU oracle (Python entry points).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs may import this package.  The CUDA
+library never imports, links or calls it, and this package shares no code with
+the CUDA path.
+
+The arithmetic lives in ``hstu_oracle.c`` (plain C, fp64, optional OpenMP);
+this module only builds it, widens the caller's bf16/fp16 tensors to fp64
+exactly, and marshals arguments.  ``naive.py`` holds a pure-Python restatement
+used as a brute-force check on tiny inputs.
+
+Method ("HSTU Attention (Blackwell SM100/SM103)", Overview): per packed
+sequence and head, O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V, no softmax.
+``scaling_seqlen`` None or 0 means max_seqlen_q (same page, Overview and
+"High-level functions").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hstu_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libhstu_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_build/libhstu_oracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-shared", "-fPIC", "-std=c99", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        # No OpenMP runtime: the oracle still works, single-threaded.
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        common = [i64, i64, i32, f64, f64, i32, P, P, i64]
+        lib.hstu_oracle_fwd_rows.argtypes = [P, P, P, P, P] + common + [P, i32]
+        lib.hstu_oracle_dq_rows.argtypes = [P, P, P, P, P, P] + common + [P, i32]
+        lib.hstu_oracle_dkdv_rows.argtypes = [P, P, P, P, P, P] + common + [P, P, i32]
+        lib.hstu_oracle_threads.argtypes = [i32]
+        for f in (lib.hstu_oracle_fwd_rows, lib.hstu_oracle_dq_rows,
+                  lib.hstu_oracle_dkdv_rows, lib.hstu_oracle_threads):
+            f.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def threads(n: int = 0) -> int:
+    """Set (n > 0) and return the OpenMP thread count the oracle uses."""
+    return int(_load().hstu_oracle_threads(int(n)))
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of a (T, H, D) tensor/array to contiguous fp64 numpy."""
+    if hasattr(x, "detach"):  # torch tensor: bf16/fp16 -> fp64 is exact
+        x = x.detach().cpu().double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def resolve_scaling(scaling_seqlen, max_seqlen_q) -> float:
+    """L_scale: ``scaling_seqlen`` when positive, else ``max_seqlen_q``."""
+    if scaling_seqlen is None or int(scaling_seqlen) == 0:
+        return float(max_seqlen_q)
+    if int(scaling_seqlen) < 0:
+        raise ValueError("scaling_seqlen must be positive")
+    return float(scaling_seqlen)
+
+
+def _rows_all(T: int, H: int):
+    tok = np.repeat(np.arange(T, dtype=np.int64), H)
+    head = np.tile(np.arange(H, dtype=np.int64), T)
+    return tok, head
+
+
+def fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
+             tokens, heads, n_threads: int = 0) -> np.ndarray:
+    """O[tokens[r], heads[r], :] for each r, shape (n, D), fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    hd = np.ascontiguousarray(heads, dtype=np.int64)
+    H, D = q.shape[1], q.shape[2]
+    out = np.zeros((tok.shape[0], D), dtype=np.float64)
+    _load().hstu_oracle_fwd_rows(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), cq.shape[0] - 1, H, D,
+        float(alpha), float(L_scale), int(bool(causal)), _ptr(tok), _ptr(hd),
+        tok.shape[0], _ptr(out), int(n_threads))
+    return out
+
+
+def dq_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
+            tokens, heads, n_threads: int = 0) -> np.ndarray:
+    """dQ[tokens[r], heads[r], :] for each r, shape (n, D), fp64."""
+    do, q, k, v = _f64(dout), _f64(q), _f64(k), _f64(v)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    hd = np.ascontiguousarray(heads, dtype=np.int64)
+    H, D = q.shape[1], q.shape[2]
+    out = np.zeros((tok.shape[0], D), dtype=np.float64)
+    _load().hstu_oracle_dq_rows(
+        _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
+        cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
+        int(bool(causal)), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(out),
+        int(n_threads))
+    return out
+
+
+def dkdv_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale,
+              causal, tokens, heads, n_threads: int = 0):
+    """(dK, dV) rows at key-side (tokens[r], heads[r]), each (n, D), fp64."""
+    do, q, k, v = _f64(dout), _f64(q), _f64(k), _f64(v)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    hd = np.ascontiguousarray(heads, dtype=np.int64)
+    H, D = k.shape[1], k.shape[2]
+    dk = np.zeros((tok.shape[0], D), dtype=np.float64)
+    dv = np.zeros((tok.shape[0], D), dtype=np.float64)
+    _load().hstu_oracle_dkdv_rows(
+        _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
+        cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
+        int(bool(causal)), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(dk),
+        _ptr(dv), int(n_threads))
+    return dk, dv
+
+
+def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
+        n_threads: int = 0) -> np.ndarray:
+    """Full O, shape (T_q, H, D), fp64."""
+    T, H, D = q.shape
+    tok, hd = _rows_all(T, H)
+    return fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale,
+                    causal, tok, hd, n_threads).reshape(T, H, D)
+
+
+def bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
+        n_threads: int = 0):
+    """Full (dQ, dK, dV), shapes of q, k, v, fp64."""
+    Tq, H, D = q.shape
+    Tk = k.shape[0]
+    tq, hq = _rows_all(Tq, H)
+    tk, hk = _rows_all(Tk, H)
+    dq = dq_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale,
+                 causal, tq, hq, n_threads).reshape(Tq, H, D)
+    dk, dv = dkdv_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha,
+                       L_scale, causal, tk, hk, n_threads)
+    return dq, dk.reshape(Tk, H, D), dv.reshape(Tk, H, D)

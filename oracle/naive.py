@@ -1,0 +1,86 @@
+"""Pure-Python brute force of HSTU attention, for tiny inputs only.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  It restates the
+forward equations of "HSTU Attention (Blackwell SM100/SM103)", Overview, and
+the chain-rule backward, one scalar at a time, with Python floats and
+``math.exp``.  It is used to brute-force check the C oracle's indexing
+(packed offsets, heads, masks) on inputs of a few tokens; it uses no numpy
+arithmetic, no C and nothing from the C oracle.
+
+Inputs are nested Python lists indexed [t][h][d]; cu_seqlens are lists of
+ints.  ``causal`` selects the top-left aligned causal mask (key j valid iff
+j <= i and j < Lk), else the full mask (j < Lk).
+"""
+from __future__ import annotations
+
+import math
+
+
+def _sigma(x: float) -> float:
+    if x < -700.0:
+        return 0.0
+    return 1.0 / (1.0 + math.exp(-x))
+
+
+def _silu(x: float) -> float:
+    return x * _sigma(x)
+
+
+def _silu_grad(x: float) -> float:
+    s = _sigma(x)
+    return s * (1.0 + x * (1.0 - s))
+
+
+def _zeros(T, H, D):
+    return [[[0.0] * D for _ in range(H)] for _ in range(T)]
+
+
+def _valid(i, j, Lk, causal):
+    return j < Lk and (not causal or j <= i)
+
+
+def forward(q, k, v, cu_q, cu_k, alpha, L_scale, causal):
+    T, H, D = len(q), len(q[0]), len(q[0][0])
+    out = _zeros(T, H, D)
+    for b in range(len(cu_q) - 1):
+        oq, ok = cu_q[b], cu_k[b]
+        Lq, Lk = cu_q[b + 1] - oq, cu_k[b + 1] - ok
+        for h in range(H):
+            for i in range(Lq):
+                for j in range(Lk):
+                    if not _valid(i, j, Lk, causal):
+                        continue
+                    s = 0.0
+                    for d in range(D):
+                        s += q[oq + i][h][d] * k[ok + j][h][d]
+                    a = _silu(alpha * s) / L_scale
+                    for d in range(D):
+                        out[oq + i][h][d] += a * v[ok + j][h][d]
+    return out
+
+
+def backward(dout, q, k, v, cu_q, cu_k, alpha, L_scale, causal):
+    Tq, H, D = len(q), len(q[0]), len(q[0][0])
+    Tk = len(k)
+    dq, dk, dv = _zeros(Tq, H, D), _zeros(Tk, H, D), _zeros(Tk, H, D)
+    for b in range(len(cu_q) - 1):
+        oq, ok = cu_q[b], cu_k[b]
+        Lq, Lk = cu_q[b + 1] - oq, cu_k[b + 1] - ok
+        for h in range(H):
+            for i in range(Lq):
+                for j in range(Lk):
+                    if not _valid(i, j, Lk, causal):
+                        continue
+                    s = 0.0
+                    da = 0.0
+                    for d in range(D):
+                        s += q[oq + i][h][d] * k[ok + j][h][d]
+                        da += dout[oq + i][h][d] * v[ok + j][h][d]
+                    x = alpha * s
+                    a = _silu(x) / L_scale
+                    ds = da * _silu_grad(x) / L_scale
+                    for d in range(D):
+                        dv[ok + j][h][d] += a * dout[oq + i][h][d]
+                        dq[oq + i][h][d] += alpha * ds * k[ok + j][h][d]
+                        dk[ok + j][h][d] += alpha * ds * q[oq + i][h][d]
+    return dq, dk, dv
