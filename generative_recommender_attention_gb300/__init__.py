@@ -1,1 +1,173 @@
-"""HSTU attention for GB300 (sm_103a): C-ABI library plus a thin binding."""
+"""HSTU attention for GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libhstu_attn.so``
+(``include/hstu_attn.h``).  Every step of the computation runs in the
+library's CUDA kernels; this module only checks tensor metadata, allocates
+outputs and the workspace with torch, and passes pointers, strides and the
+current CUDA stream.  There is no CPU fallback: if the library is missing or
+the device is not sm_103, calls raise.
+
+Operation ("HSTU Attention (Blackwell SM100/SM103)", Overview): per packed
+sequence and head, O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V, no softmax.
+``hstu_attn_fwd`` / ``hstu_attn_bwd`` mirror the page's
+``hstu_attention_forward`` / ``hstu_attention_backward`` ("High-level
+functions"): THD tensors, int32 cumulative lengths, ``scaling_seqlen=None``
+meaning ``max_seqlen_q``, ``window_size=(-1, 0)`` causal or ``(-1, -1)`` full.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+from ._lib import (HstuError, HSTU_BF16, HSTU_FP16, library, library_path,
+                   workspace_size, last_device_status, selftest_timeout, CTen, Ten)
+
+__all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "workspace_size", "last_device_status",
+           "selftest_timeout", "HstuError", "library", "library_path"]
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return HSTU_BF16
+    if t.dtype == torch.float16:
+        return HSTU_FP16
+    raise TypeError(f"HSTU attention takes fp16 or bf16 tensors, got {t.dtype}")
+
+
+def _check_thd(name, t, T, H, D, dtype, device):
+    if t.dim() != 3 or tuple(t.shape) != (T, H, D):
+        raise ValueError(f"{name}: expected shape {(T, H, D)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} differs from q's {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if T > 0 and t.stride(2) != 1:
+        raise ValueError(f"{name}: the last (head_dim) dimension must be contiguous")
+
+
+def _cten(t):
+    return CTen(t.data_ptr(), t.stride(0), t.stride(1))
+
+
+def _ten(t):
+    return Ten(t.data_ptr(), t.stride(0), t.stride(1))
+
+
+def _causal(causal, window_size):
+    if window_size is None:
+        return bool(causal)
+    w = tuple(int(x) for x in window_size)
+    if w == (-1, 0):
+        return True
+    if w == (-1, -1):
+        return False
+    raise NotImplementedError(f"window_size {w}: only (-1, 0) causal and (-1, -1) full are built")
+
+
+def _scaling(scaling_seqlen):
+    if scaling_seqlen is None:
+        return 0
+    s = int(scaling_seqlen)
+    if s <= 0:
+        raise ValueError("scaling_seqlen must be positive")
+    return s
+
+
+def _meta(cu_seqlens_q, cu_seqlens_k, device):
+    import torch
+    for n, c in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if c.dtype != torch.int32 or c.dim() != 1 or c.device != device:
+            raise ValueError(f"{n}: expected a 1-D int32 tensor on {device}")
+        if not c.is_contiguous():
+            raise ValueError(f"{n}: must be contiguous")
+    if cu_seqlens_q.shape != cu_seqlens_k.shape:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be (B + 1,)")
+    return cu_seqlens_q.shape[0] - 1
+
+
+def _workspace(workspace, nbytes, device):
+    import torch
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace too small: need {nbytes} bytes")
+    return workspace
+
+
+def _stream(device):
+    import torch
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  scaling_seqlen: Optional[int] = None, causal: bool = True,
+                  alpha: float = 1.0, out=None, workspace=None, window_size=None):
+    """Forward HSTU attention; returns ``out`` of shape ``q.shape``.
+
+    q: (T_q, H, D); k, v: (T_k, H, D); fp16 or bf16 on a CUDA device.
+    cu_seqlens_q/k: int32 (B + 1,) on the same device (values are trusted and
+    never copied to the host).  ``out`` may be supplied (overwritten).
+    """
+    import torch
+    lib = library()
+    T_q, H, D = q.shape
+    T_k = k.shape[0]
+    dev = q.device
+    _check_thd("k", k, T_k, H, D, q.dtype, dev)
+    _check_thd("v", v, T_k, H, D, q.dtype, dev)
+    _check_thd("q", q, T_q, H, D, q.dtype, dev)
+    B = _meta(cu_seqlens_q, cu_seqlens_k, dev)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    _check_thd("out", out, T_q, H, D, q.dtype, dev)
+    causal = _causal(causal, window_size)
+    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, False), dev)
+    st = lib.hstu_attn_fwd(_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
+                           cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
+                           int(max_seqlen_q), int(max_seqlen_k), float(alpha),
+                           _scaling(scaling_seqlen), int(causal), ws.data_ptr(),
+                           ws.numel(), _stream(dev))
+    if st != 0:
+        raise HstuError(st)
+    return out
+
+
+def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, scaling_seqlen: Optional[int] = None,
+                  causal: bool = True, alpha: float = 1.0, dq=None, dk=None, dv=None,
+                  workspace=None, window_size=None) -> Tuple:
+    """Backward HSTU attention; returns ``(dq, dk, dv)``.
+
+    Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
+    ``dq``/``dk``/``dv`` may be supplied (overwritten); dk and dv may be
+    disjoint views of one packed KV buffer.
+    """
+    import torch
+    lib = library()
+    T_q, H, D = q.shape
+    T_k = k.shape[0]
+    dev = q.device
+    _check_thd("q", q, T_q, H, D, q.dtype, dev)
+    _check_thd("dout", dout, T_q, H, D, q.dtype, dev)
+    _check_thd("k", k, T_k, H, D, q.dtype, dev)
+    _check_thd("v", v, T_k, H, D, q.dtype, dev)
+    B = _meta(cu_seqlens_q, cu_seqlens_k, dev)
+    if dq is None:
+        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if dk is None:
+        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
+    if dv is None:
+        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
+    _check_thd("dq", dq, T_q, H, D, q.dtype, dev)
+    _check_thd("dk", dk, T_k, H, D, q.dtype, dev)
+    _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
+    causal = _causal(causal, window_size)
+    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, True), dev)
+    st = lib.hstu_attn_bwd(_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk),
+                           _ten(dv), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q,
+                           T_k, H, D, _dtype_code(q), int(max_seqlen_q), int(max_seqlen_k),
+                           float(alpha), _scaling(scaling_seqlen), int(causal), ws.data_ptr(),
+                           ws.numel(), _stream(dev))
+    if st != 0:
+        raise HstuError(st)
+    return dq, dk, dv

@@ -1,0 +1,351 @@
+// Host side of the C ABI in hstu_attn.h: argument validation, TMA tensor-map
+// encoding, work-list scheduling and kernel launches.  No allocation, no
+// host copy of device metadata, no synchronization (except in the explicit
+// status query).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "hstu_attn.h"
+#include "kernels.h"
+
+using namespace hstu;
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // 4 s per barrier wait
+constexpr int kMaxDevices = 64;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  int max_smem_optin = 0;
+};
+
+bool device_info(DevInfo* out) {
+  static DevInfo cache[kMaxDevices];
+  static bool valid[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!valid[dev]) {
+    DevInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return false;
+    cache[dev] = d;
+    valid[dev] = true;
+  }
+  *out = cache[dev];
+  return true;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a (T, H, D) tensor with a box of 64 elements x 1 head x
+// box_rows tokens, 128-byte swizzle; rows past T read as zeros.
+bool encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D, int64_t st, int64_t sh,
+                int box_rows, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(std::max<int64_t>(T, 1))};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh * 2), static_cast<cuuint64_t>(st * 2)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- validation
+bool supported_dim(int D) { return D == 64 || D == 128 || D == 256; }
+
+// Checks one (T, H, D) tensor with element strides (st, sh, 1).
+hstu_status_t check_tensor(const void* ptr, int64_t st, int64_t sh, int64_t T, int H, int D) {
+  if (T == 0) return HSTU_OK;
+  if (ptr == nullptr) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return HSTU_ERR_MISALIGNED;
+  if (st <= 0 || sh <= 0) return HSTU_ERR_INVALID_ARG;
+  if ((st * 2) % 16 != 0 || (sh * 2) % 16 != 0) return HSTU_ERR_MISALIGNED;
+  if (st * 2 >= (int64_t(1) << 40) || sh * 2 >= (int64_t(1) << 40)) return HSTU_ERR_INVALID_ARG;
+  // no two logical elements at one address: sort dims by stride, each stride
+  // must exceed the span of the smaller ones.
+  struct Dim { int64_t stride, size; } d[3] = {{1, D}, {sh, H}, {st, T}};
+  std::sort(d, d + 3, [](const Dim& x, const Dim& y) { return x.stride < y.stride; });
+  int64_t span = 0;
+  for (auto& x : d) {
+    if (x.size <= 1) continue;
+    if (x.stride <= span) return HSTU_ERR_INVALID_ARG;
+    span += x.stride * (x.size - 1);
+  }
+  return HSTU_OK;
+}
+
+struct Common {
+  DevInfo dev;
+  float inv_L;
+  bool bf16;
+};
+
+hstu_status_t check_common(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_t D,
+                           hstu_dtype_t dtype, int32_t max_q, int32_t max_k, float alpha,
+                           int32_t scaling, const int32_t* cu_q, const int32_t* cu_k, Common* c) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || H <= 0 || max_q < 0 || max_k < 0)
+    return HSTU_ERR_INVALID_ARG;
+  if (total_q > INT32_MAX || total_k > INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  if (!(dtype == HSTU_FP16 || dtype == HSTU_BF16)) return HSTU_ERR_UNSUPPORTED;
+  if (!supported_dim(D)) return HSTU_ERR_UNSUPPORTED;
+  if (max_q > max_k) return HSTU_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha)) return HSTU_ERR_INVALID_ARG;
+  if (scaling < 0) return HSTU_ERR_INVALID_ARG;
+  const int32_t L = scaling > 0 ? scaling : max_q;
+  if (batch > 0 && total_q > 0 && L <= 0) return HSTU_ERR_INVALID_ARG;
+  if (batch > 0 && (cu_q == nullptr || cu_k == nullptr)) return HSTU_ERR_INVALID_ARG;
+  c->inv_L = L > 0 ? 1.0f / static_cast<float>(L) : 0.f;
+  c->bf16 = dtype == HSTU_BF16;
+  return HSTU_OK;
+}
+
+int64_t cap_a(int32_t batch, int64_t total_q, int32_t H) {
+  return static_cast<int64_t>(H) * (cdiv(total_q, kBM) + batch);
+}
+int64_t cap_b(int32_t batch, int64_t total_k, int32_t H, int32_t D) {
+  const int split = D == 256 ? 2 : 1;
+  return static_cast<int64_t>(H) * split * (cdiv(total_k, kBM) + batch);
+}
+
+int bn_for(int D) { return D == 256 ? 64 : 128; }
+
+// Shared memory of the scheduler block: one int per cost bucket.
+bool sched_smem(int cmax, const DevInfo& dev, int* bytes) {
+  const int b = (cmax + 1) * 4;
+  if (b > dev.max_smem_optin) return false;
+  static bool set = false;
+  if (b > 48 * 1024 && !set) {
+    if (cudaFuncSetAttribute(hstu_sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.max_smem_optin) != cudaSuccess)
+      return false;
+    set = true;
+  }
+  *bytes = b;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hstu_attn_version(void) { return 100; }
+
+const char* hstu_attn_status_string(hstu_status_t s) {
+  switch (s) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HSTU_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case HSTU_ERR_CUDA: return "CUDA error";
+    case HSTU_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
+                                int32_t num_heads, int32_t head_dim, int32_t is_bwd) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || num_heads <= 0 || !supported_dim(head_dim))
+    return 0;
+  size_t bytes = kHeaderBytes + 16 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
+  if (is_bwd) bytes += 16 * static_cast<size_t>(cap_b(batch, total_k, num_heads, head_dim));
+  return (bytes + 255) & ~size_t(255);
+}
+
+hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
+                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  Common c;
+  hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
+                                 max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
+  if (s != HSTU_OK) return s;
+  const int H = num_heads, D = head_dim;
+  if ((s = check_tensor(q.ptr, q.stride_t, q.stride_h, total_q, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(k.ptr, k.stride_t, k.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(v.ptr, v.stride_t, v.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(out.ptr, out.stride_t, out.stride_h, total_q, H, D)) != HSTU_OK) return s;
+  if (batch == 0 || total_q == 0) return HSTU_OK;
+  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, H, D, 0);
+  if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
+  if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
+
+  const int BN = bn_for(D);
+  const int64_t capA = cap_a(batch, total_q, H);
+  const int cmax = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
+  int sched_bytes;
+  if (!sched_smem(cmax, c.dev, &sched_bytes)) return HSTU_ERR_UNSUPPORTED;
+
+  CUtensorMap tq, tk, tv;
+  const void* kptr = total_k > 0 ? k.ptr : q.ptr;  // stand-in, never read when total_k == 0
+  const void* vptr = total_k > 0 ? v.ptr : q.ptr;
+  const int64_t kst = total_k > 0 ? k.stride_t : q.stride_t, ksh = total_k > 0 ? k.stride_h : q.stride_h;
+  const int64_t vst = total_k > 0 ? v.stride_t : q.stride_t, vsh = total_k > 0 ? v.stride_h : q.stride_h;
+  if (!encode_thd(&tq, q.ptr, total_q, H, D, q.stride_t, q.stride_h, kBM, c.bf16) ||
+      !encode_thd(&tk, kptr, total_k, H, D, kst, ksh, BN, c.bf16) ||
+      !encode_thd(&tv, vptr, total_k, H, D, vst, vsh, BN, c.bf16))
+    return HSTU_ERR_CUDA;
+
+  int* header = static_cast<int*>(workspace);
+  int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
+  SchedArgs sa{};
+  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
+  sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
+  sa.header = header;
+  hstu_sched_kernel<<<1, kSchedThreads, sched_bytes, stream>>>(sa);
+  if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+
+  AttnArgs a{};
+  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
+  a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.units = units; a.units_slot = kHdrUnitsA; a.timeout_ns = kWaitTimeoutNs;
+  a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
+  const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
+  if (launch_fwd(D, c.bf16, grid, stream, tq, tk, tv, a) != cudaSuccess) return HSTU_ERR_CUDA;
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                            hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
+                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  Common c;
+  hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
+                                 max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
+  if (s != HSTU_OK) return s;
+  const int H = num_heads, D = head_dim;
+  if ((s = check_tensor(dout.ptr, dout.stride_t, dout.stride_h, total_q, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(q.ptr, q.stride_t, q.stride_h, total_q, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(k.ptr, k.stride_t, k.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(v.ptr, v.stride_t, v.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(dq.ptr, dq.stride_t, dq.stride_h, total_q, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(dk.ptr, dk.stride_t, dk.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if ((s = check_tensor(dv.ptr, dv.stride_t, dv.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if (batch == 0 || (total_q == 0 && total_k == 0)) return HSTU_OK;
+  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, H, D, 1);
+  if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
+  if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
+
+  const int BN = bn_for(D);
+  const int BQ = DkdvCfg<64>::BQ;
+  const int split = D == 256 ? 2 : 1;
+  const int64_t capA = cap_a(batch, total_q, H);
+  const int64_t capB = cap_b(batch, total_k, H, D);
+  const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
+  const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));
+  int sched_bytes;
+  if (!sched_smem(std::max(cmaxA, cmaxB), c.dev, &sched_bytes)) return HSTU_ERR_UNSUPPORTED;
+
+  // Stand-ins for empty sides: valid maps that no unit ever reads through.
+  const bool hq = total_q > 0, hk = total_k > 0;
+  const hstu_cten_t qx = hq ? q : k, dox = hq ? dout : k, kx = hk ? k : q, vx = hk ? v : q;
+  CUtensorMap m_q128, m_do128, m_kbn, m_vbn, m_k128, m_v128, m_q64, m_do64;
+  if (!encode_thd(&m_q128, qx.ptr, total_q, H, D, qx.stride_t, qx.stride_h, kBM, c.bf16) ||
+      !encode_thd(&m_do128, dox.ptr, total_q, H, D, dox.stride_t, dox.stride_h, kBM, c.bf16) ||
+      !encode_thd(&m_kbn, kx.ptr, total_k, H, D, kx.stride_t, kx.stride_h, BN, c.bf16) ||
+      !encode_thd(&m_vbn, vx.ptr, total_k, H, D, vx.stride_t, vx.stride_h, BN, c.bf16) ||
+      !encode_thd(&m_k128, kx.ptr, total_k, H, D, kx.stride_t, kx.stride_h, kBM, c.bf16) ||
+      !encode_thd(&m_v128, vx.ptr, total_k, H, D, vx.stride_t, vx.stride_h, kBM, c.bf16) ||
+      !encode_thd(&m_q64, qx.ptr, total_q, H, D, qx.stride_t, qx.stride_h, BQ, c.bf16) ||
+      !encode_thd(&m_do64, dox.ptr, total_q, H, D, dox.stride_t, dox.stride_h, BQ, c.bf16))
+    return HSTU_ERR_CUDA;
+
+  int* header = static_cast<int*>(workspace);
+  int4* unitsA = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
+  int4* unitsB = unitsA + capA;
+  SchedArgs sa{};
+  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
+  sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
+  sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
+  sa.units_b = unitsB; sa.header = header;
+  hstu_sched_kernel<<<2, kSchedThreads, sched_bytes, stream>>>(sa);
+  if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+
+  AttnArgs a{};
+  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
+  a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.timeout_ns = kWaitTimeoutNs;
+  if (total_q > 0) {
+    AttnArgs aq = a;
+    aq.units = unitsA; aq.units_slot = kHdrUnitsA;
+    aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
+    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
+    if (launch_dq(D, c.bf16, grid, stream, m_q128, m_do128, m_kbn, m_vbn, aq) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+  }
+  if (total_k > 0) {
+    AttnArgs ak = a;
+    ak.units = unitsB; ak.units_slot = kHdrUnitsB;
+    ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
+    ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
+    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capB));
+    if (launch_dkdv(D, c.bf16, grid, stream, m_k128, m_v128, m_q64, m_do64, ak) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+  }
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t stream) {
+  if (workspace == nullptr) return HSTU_ERR_INVALID_ARG;
+  int h[8];
+  if (cudaMemcpyAsync(h, workspace, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (h[kHdrStatus] != 0) return static_cast<hstu_status_t>(h[kHdrStatus]);
+  if (h[kHdrOverflow] != 0 || h[kHdrOverflow + 1] != 0) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_selftest_timeout(void* workspace, uint32_t timeout_us, cudaStream_t stream) {
+  if (workspace == nullptr || timeout_us == 0 || timeout_us > 10000000u) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  if (launch_selftest_timeout(static_cast<int*>(workspace), uint64_t(timeout_us) * 1000u, stream) !=
+      cudaSuccess)
+    return HSTU_ERR_CUDA;
+  return HSTU_OK;
+}
+
+}  // extern "C"

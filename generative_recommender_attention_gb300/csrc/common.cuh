@@ -1,0 +1,163 @@
+// Shared definitions of the HSTU attention kernels: workspace layout, kernel
+// parameter blocks, bounded barrier waits, element conversion.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace hstu {
+
+// ---------------------------------------------------------------- workspace
+// Bytes [0, 256): header of int32 words.  Then list A (query-tile work units)
+// and, for the backward, list B (key-tile work units), int4 each.
+enum HeaderWord : int {
+  kHdrStatus = 0,     // 0 = ok, else an hstu_status_t recorded on the device
+  kHdrUnitsA = 1,     // number of units in list A
+  kHdrUnitsB = 2,     // number of units in list B
+  kHdrWhere = 3,      // which wait gave up (role * 256 + barrier id), for debugging
+  kHdrOverflow = 4,   // units dropped because the metadata exceeded the totals
+};
+constexpr int kHeaderBytes = 256;
+constexpr int kStatusTimeout = 5;     // == HSTU_ERR_DEVICE_TIMEOUT
+constexpr int kStatusBadMeta = 1;     // == HSTU_ERR_INVALID_ARG
+
+// Query tiles are always 128 rows (the tcgen05 M of every kernel).
+constexpr int kBM = 128;
+
+// Work unit: x = sequence, y = tile index inside the sequence,
+// z = head (times the D split for list B, plus the split index),
+// w = number of inner tiles the unit iterates over (0 = write zeros).
+struct Unit {
+  int b, tile, hz, n;
+};
+
+__device__ __forceinline__ Unit load_unit(const int4* units, int u) {
+  int4 v = __ldg(units + u);
+  return Unit{v.x, v.y, v.z, v.w};
+}
+
+// ---------------------------------------------------------------- waits
+// Every barrier wait is bounded: after `timeout_ns` the waiting thread records
+// HSTU_ERR_DEVICE_TIMEOUT in the workspace, raises the block's abort flag and
+// returns false; every other wait in the block then returns false at once,
+// so the block drains its own copies and exits.  Nothing traps or spins
+// forever.
+struct WaitCtl {
+  int* status;                 // workspace header (global)
+  volatile int* abort_flag;    // shared
+  uint64_t timeout_ns;
+};
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                       int where) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*c.abort_flag) return false;
+      if (globaltimer_ns() - t0 > c.timeout_ns) {
+        *c.abort_flag = 1;
+        atomicCAS(c.status + kHdrStatus, 0, kStatusTimeout);
+        atomicExch(c.status + kHdrWhere, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                         int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, c, where);
+}
+
+// Warp-uniform wait for the four row warps: lane 0 polls with the bounded
+// wait and broadcasts the outcome, so a give-up never splits a warp in front
+// of a .sync.aligned tcgen05 instruction.  On success the other lanes then
+// observe the (already completed) phase themselves, which gives each of them
+// the barrier's acquire ordering.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                              int where) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c, where);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) {
+    for (uint32_t it = 0; it < (1u << 20) && !mbar_try_wait(bar, parity); ++it) {
+    }
+  }
+  return ok;
+}
+
+// ---------------------------------------------------------------- conversion
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// SiLU(x) = x * sigmoid(x) = h + h * tanh(h), h = x / 2: one MUFU op.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// sigmoid(x) = 1/2 + tanh(x/2)/2.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+}
+
+// Store 32 fp32 values (one TMEM chunk of one row) as 32 16-bit elements,
+// scaled by `scale`, with four 16-byte stores.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(void* dst, const uint32_t (&x)[32], float scale) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    uint4 w;
+    w.x = pack2<BF16>(__uint_as_float(x[8 * v + 0]) * scale, __uint_as_float(x[8 * v + 1]) * scale);
+    w.y = pack2<BF16>(__uint_as_float(x[8 * v + 2]) * scale, __uint_as_float(x[8 * v + 3]) * scale);
+    w.z = pack2<BF16>(__uint_as_float(x[8 * v + 4]) * scale, __uint_as_float(x[8 * v + 5]) * scale);
+    w.w = pack2<BF16>(__uint_as_float(x[8 * v + 6]) * scale, __uint_as_float(x[8 * v + 7]) * scale);
+    p[v] = w;
+  }
+}
+
+__device__ __forceinline__ void store_zero32(void* dst) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) p[v] = z;
+}
+
+// K-major operand descriptor: tile of ROWS rows by D columns, stored as D/64
+// chunks of [ROWS][64] 16-bit elements with the 128-byte swizzle (the TMA box
+// layout).  kk selects the 16-element K step.
+template <int ROWS>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  const uint32_t addr = tile + static_cast<uint32_t>(kk >> 2) * (ROWS * 128) +
+                        static_cast<uint32_t>(kk & 3) * 32;
+  return sdesc_sw128(addr, 16, 1024);
+}
+
+// MN-major B operand read from the same tile layout: K runs down the ROWS
+// (16 rows per step kk), N runs along the columns starting at column n0
+// (a multiple of 64); 64-column chunks are ROWS*128 bytes apart (LBO) and
+// 8-row groups 1024 bytes apart (SBO).
+template <int ROWS>
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, int n0) {
+  const uint32_t addr = tile + static_cast<uint32_t>(n0 >> 6) * (ROWS * 128) +
+                        static_cast<uint32_t>(kk) * 2048;
+  return sdesc_sw128(addr, ROWS * 128, 1024);
+}
+
+}  // namespace hstu

@@ -1,0 +1,285 @@
+// HSTU attention forward ("HSTU Attention (Blackwell SM100/SM103)",
+// Overview): O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V per sequence and head.
+//
+// Persistent, warp-specialised kernel; one CTA per SM walks the longest-first
+// list of 128-row query tiles written by the scheduler kernel.
+//   warp 0      TMA producer: Q tile per unit, K/V tiles per inner step.
+//   warp 1      tcgen05 issuer: S = Q K^T into TMEM (double buffered), then
+//               O += P V with P read straight from TMEM.
+//   warps 2-5   one row each: tcgen05.ld S, alpha scale, SiLU, mask, round to
+//               16 bits, tcgen05.st P; per unit, the epilogue O * (1/L_scale)
+//               with predicated row stores.
+// No softmax, so no running max or rescale: O simply accumulates in TMEM.
+// Causal units only visit key tiles up to their last row (the scheduler's
+// cost); masked entries are set to exactly 0, never -inf, since SiLU(-inf)
+// is NaN.  Rows of a tile past the sequence end are computed but not stored;
+// keys past it are masked, and past the tensor end TMA fills zeros.
+#include "kernels.h"
+
+namespace hstu {
+
+namespace {
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+  using C = FwdCfg<D>;
+  constexpr int BN = C::BN, NQ = C::NQ, NS = C::NS, KCH = D / 64;
+  constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
+  constexpr uint32_t IDESC_PV = idesc_f16(BF16, kBM, D, false, true);
+  // TMEM columns: S0, S1 | O | P0, P1 (16-bit P packed two per column)
+  constexpr uint32_t COL_S = 0, COL_O = 2 * BN, COL_P = 2 * BN + D;
+  static_assert(COL_P + BN <= kTmemCols, "TMEM budget");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sK = sQ + NQ * C::Q_BYTES;
+  const uint32_t sV = sK + NS * C::KV_BYTES;
+
+  enum {
+    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, VFULL = KFULL + NS,
+    KVEMPTY = VFULL + NS, SFULL = KVEMPTY + NS, PFULL = SFULL + 2, OFULL = PFULL + 2,
+    OEMPTY = OFULL + 1, DRAIN = OEMPTY + 1, NBARS = DRAIN + 1
+  };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0] abort, [1] 0
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar(KFULL + i), 1); mbar_init(bar(VFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(SFULL + i), 1); mbar_init(bar(PFULL + i), 128); }
+    mbar_init(bar(OFULL), 1);
+    mbar_init(bar(OEMPTY), 128);
+    mbar_init(bar(DRAIN), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{a.header, flags, a.timeout_ns};
+  const WaitCtl drain{a.header, flags + 1, a.timeout_ns};
+  const int n_units = *reinterpret_cast<volatile int*>(a.header + a.units_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t qi = 0, kvi = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const Unit U = load_unit(a.units, u);
+        if (U.n <= 0) continue;
+        const int h = U.hz;
+        const int q_row0 = __ldg(a.cu_q + U.b) + kBM * U.tile;
+        const int kv_row0 = __ldg(a.cu_k + U.b);
+        const int qb = qi % NQ;
+        if (!wait_bar(bar(QEMPTY + qb), ((qi / NQ) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(QFULL + qb), C::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(sQ + qb * C::Q_BYTES + c * (kBM * 128), &tm_q, bar(QFULL + qb), 64 * c, h,
+                      q_row0);
+        ++qi;
+        for (int n = 0; n < U.n; ++n) {
+          const int s = kvi % NS;
+          if (!wait_bar(bar(KVEMPTY + s), ((kvi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
+          const int row = kv_row0 + BN * n;
+          mbar_arrive_expect_tx(bar(KFULL + s), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            tma_load_3d(sK + s * C::KV_BYTES + c * (BN * 128), &tm_k, bar(KFULL + s), 64 * c, h, row);
+          mbar_arrive_expect_tx(bar(VFULL + s), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            tma_load_3d(sV + s * C::KV_BYTES + c * (BN * 128), &tm_v, bar(VFULL + s), 64 * c, h, row);
+          ++kvi;
+        }
+      }
+      // let the last copies land before the block may exit
+      for (uint32_t i = qi > NQ ? qi - NQ : 0; i < qi; ++i)
+        wait_bar(bar(QFULL + i % NQ), (i / NQ) & 1, drain, 0x0f1);
+      for (uint32_t i = kvi > NS ? kvi - NS : 0; i < kvi; ++i) {
+        wait_bar(bar(KFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
+        wait_bar(bar(VFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS = tmem + COL_S, tO = tmem + COL_O, tP = tmem + COL_P;
+      struct Pend {
+        int valid, s, b, first, last;
+        uint32_t kvi, g, oi;
+      } pv{0, 0, 0, 0, 0, 0, 0, 0};
+      auto issue_pv = [&](const Pend& p) -> bool {
+        if (!wait_bar(bar(VFULL + p.s), (p.kvi / NS) & 1, wc, 0x101)) return false;
+        if (!wait_bar(bar(PFULL + p.b), (p.g >> 1) & 1, wc, 0x102)) return false;
+        if (p.first && !wait_bar(bar(OEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
+        tc_fence_after();
+        const uint32_t vt = sV + p.s * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tO, tP + p.b * (BN / 2) + kk * 8, desc_mnmajor<BN>(vt, kk, 0), IDESC_PV,
+                 (!p.first || kk > 0) ? 1u : 0u);
+        mma_commit(bar(KVEMPTY + p.s));
+        if (p.last) mma_commit(bar(OFULL));
+        return true;
+      };
+      uint32_t qi = 0, kvi = 0, g = 0, oi = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const Unit U = load_unit(a.units, u);
+        if (U.n <= 0) continue;
+        const int qb = qi % NQ;
+        if (!wait_bar(bar(QFULL + qb), (qi / NQ) & 1, wc, 0x104)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qt = sQ + qb * C::Q_BYTES;
+        for (int n = 0; n < U.n; ++n) {
+          const int s = kvi % NS, b = g & 1;
+          if (!wait_bar(bar(KFULL + s), (kvi / NS) & 1, wc, 0x105)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kt = sK + s * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS + b * BN, desc_kmajor<kBM>(qt, kk), desc_kmajor<BN>(kt, kk), IDESC_S,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(bar(SFULL + b));
+          if (n == U.n - 1) mma_commit(bar(QEMPTY + qb));
+          if (pv.valid && !issue_pv(pv)) { ok = false; break; }
+          pv = Pend{1, s, b, n == 0, n == U.n - 1, kvi, g, oi};
+          ++kvi;
+          ++g;
+        }
+        ++qi;
+        ++oi;
+      }
+      if (ok && pv.valid) issue_pv(pv);
+      mma_commit(bar(DRAIN));
+      wait_bar(bar(DRAIN), 0, drain, 0x1ff);
+    }
+  } else {
+    // ------------------------------------------------------------ SiLU + epilogue
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + COL_S + lane_off, tO = tmem + COL_O + lane_off,
+                   tP = tmem + COL_P + lane_off;
+    const float half_alpha = 0.5f * a.alpha;
+    uint32_t g = 0, oi = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const Unit U = load_unit(a.units, u);
+      const int h = U.hz;
+      const int q0 = __ldg(a.cu_q + U.b);
+      const int Lq = __ldg(a.cu_q + U.b + 1) - q0;
+      const int Lk = __ldg(a.cu_k + U.b + 1) - __ldg(a.cu_k + U.b);
+      const int i = kBM * U.tile + r;
+      const int64_t grow = static_cast<int64_t>(q0) + i;
+      const bool row_ok = i < Lq && grow < a.total_q;
+      char* orow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh) * 2;
+      if (U.n <= 0) {
+        if (row_ok)
+          for (int c = 0; c < D / 32; ++c) store_zero32(orow + c * 64);
+        continue;
+      }
+      for (int n = 0; n < U.n; ++n) {
+        const int sb = g & 1;
+        if (!wait_bar_warp(bar(SFULL + sb), (g >> 1) & 1, wc, 0x201)) { ok = false; break; }
+        tc_fence_after();
+        const int j0 = BN * n;
+        const bool need_mask = (a.causal && j0 + BN - 1 > kBM * U.tile) || (j0 + BN > Lk);
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tS + sb * BN + 32 * c, x);
+          uint32_t p[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float h0 = __uint_as_float(x[2 * e]) * half_alpha;
+            const float h1 = __uint_as_float(x[2 * e + 1]) * half_alpha;
+            float p0 = fmaf(h0, tanh_approx(h0), h0);
+            float p1 = fmaf(h1, tanh_approx(h1), h1);
+            if (need_mask) {
+              const int j = j0 + 32 * c + 2 * e;
+              if (!(j < Lk && (!a.causal || j <= i))) p0 = 0.f;
+              if (!(j + 1 < Lk && (!a.causal || j + 1 <= i))) p1 = 0.f;
+            }
+            p[e] = pack2<BF16>(p0, p1);
+          }
+          tmem_st16(tP + sb * (BN / 2) + 16 * c, p);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(PFULL + sb));
+        ++g;
+      }
+      if (!ok) break;
+      if (!wait_bar_warp(bar(OFULL), oi & 1, wc, 0x202)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tO + 32 * c, x);
+        if (row_ok) store_row32<BF16>(orow + c * 64, x, a.inv_L);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(OEMPTY));
+      ++oi;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(int grid, cudaStream_t st, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const AttnArgs& a) {
+  auto kern = hstu_fwd_kernel<D, BF16>;
+  static bool attr_set = false;  // benign race: setting the attribute twice is harmless
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FwdCfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, kAttnThreads, FwdCfg<D>::SMEM, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a) {
+  switch (D) {
+    case 64: return bf16 ? launch_fwd_t<64, true>(grid, st, tq, tk, tv, a)
+                         : launch_fwd_t<64, false>(grid, st, tq, tk, tv, a);
+    case 128: return bf16 ? launch_fwd_t<128, true>(grid, st, tq, tk, tv, a)
+                          : launch_fwd_t<128, false>(grid, st, tq, tk, tv, a);
+    case 256: return bf16 ? launch_fwd_t<256, true>(grid, st, tq, tk, tv, a)
+                          : launch_fwd_t<256, false>(grid, st, tq, tk, tv, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace hstu

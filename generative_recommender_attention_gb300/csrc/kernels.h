@@ -1,0 +1,114 @@
+// Internal interface between the host library and the device kernels:
+// tile configurations, argument blocks and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace hstu {
+
+constexpr int kSchedThreads = 1024;
+constexpr int kAttnThreads = 192;   // warp 0: TMA, warp 1: MMA, warps 2-5: SiLU/epilogue
+constexpr int kTmemCols = 512;
+
+// Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
+// address slot, the abort flags, and slack to align the tiles to 1024 bytes.
+constexpr int kCtlBytes = 1024;
+constexpr int kAlignSlack = 1024;
+
+struct SchedArgs {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int B, H, causal;
+  int bn_a, cmax_a, cap_a;   // list A: query tiles, inner tiles of bn_a keys
+  int4* units_a;
+  int bq_b, split_b, cmax_b, cap_b;  // list B: key tiles, inner tiles of bq_b queries
+  int4* units_b;
+  int* header;
+};
+
+struct AttnArgs {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int64_t total_q, total_k;
+  int H;
+  int causal;
+  float alpha;
+  float inv_L;          // 1 / L_scale
+  int* header;          // workspace header
+  const int4* units;    // work list walked by this kernel
+  int units_slot;       // header word holding its length
+  uint64_t timeout_ns;  // limit of every barrier wait
+  void* o0;             // fwd: out, dq kernel: dq, dkdv kernel: dv
+  int64_t o0_st, o0_sh;
+  void* o1;             // dkdv kernel: dk
+  int64_t o1_st, o1_sh;
+};
+
+// ------------------------------------------------------------ forward config
+template <int D>
+struct FwdCfg {
+  static constexpr int BN = D == 256 ? 64 : 128;     // keys per inner tile
+  static constexpr int NQ = D == 256 ? 1 : 2;        // Q buffers
+  static constexpr int NS = D == 64 ? 4 : 2;         // K/V stages
+  static constexpr int Q_BYTES = kBM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int TILE_BYTES = NQ * Q_BYTES + 2 * NS * KV_BYTES;
+  static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
+};
+
+// ------------------------------------------------------------ dQ config
+template <int D>
+struct DqCfg {
+  static constexpr int BN = D == 256 ? 64 : 128;
+  static constexpr int NQ = D == 64 ? 2 : 1;         // (Q, dO) buffers
+  static constexpr int NS = D == 64 ? 4 : (D == 128 ? 2 : 1);
+  static constexpr int Q_BYTES = kBM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + 2 * NS * KV_BYTES;
+  static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
+};
+
+// ------------------------------------------------------------ dK/dV config
+template <int D>
+struct DkdvCfg {
+  static constexpr int BQ = 64;                      // queries per inner tile
+  static constexpr int DH = D == 256 ? 128 : D;      // dK/dV columns per unit
+  static constexpr int SPLIT = D / DH;
+  static constexpr int NKV = D == 64 ? 2 : 1;        // stationary (K, V) buffers
+  static constexpr int NS = D == 64 ? 6 : (D == 128 ? 4 : 1);
+  static constexpr int KV_BYTES = kBM * D * 2;
+  static constexpr int Q_BYTES = BQ * D * 2;
+  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES;
+  static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
+};
+
+static_assert(FwdCfg<128>::SMEM <= 232448, "smem");
+static_assert(DqCfg<128>::SMEM <= 232448, "smem");
+static_assert(DkdvCfg<128>::SMEM <= 232448, "smem");
+static_assert(FwdCfg<256>::SMEM <= 232448 && DqCfg<256>::SMEM <= 232448 &&
+                  DkdvCfg<256>::SMEM <= 232448,
+              "smem");
+static_assert(FwdCfg<64>::SMEM <= 232448 && DqCfg<64>::SMEM <= 232448 &&
+                  DkdvCfg<64>::SMEM <= 232448,
+              "smem");
+
+__global__ void hstu_sched_kernel(SchedArgs a);
+
+// Launchers: return cudaErrorInvalidValue for a head_dim outside {64,128,256}.
+// Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (q/do: 128-row
+// box, k/v: BN-row box); dkdv (k/v: 128-row box, q/do: BQ-row box).
+cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a);
+cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+                      const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const AttnArgs& a);
+cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
+                        const AttnArgs& a);
+cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace hstu

@@ -1,0 +1,169 @@
+// Device-side tile scheduler.  Reads cu_seqlens on the device (the host
+// never sees their values) and writes work lists sorted by cost, longest
+// first, so a persistent kernel that walks the list in order balances ragged
+// sequences.  One block per list:
+//   list A: query tiles of 128 rows; cost = number of key tiles of `bn_a`
+//           rows the tile needs (causal tiles only need keys up to their
+//           last row);
+//   list B: key tiles of 128 rows; cost = number of query tiles of `bq_b`
+//           rows that can see the tile; each key tile is emitted once per head
+//           and per D split.
+// Units with cost 0 are kept (their rows must be written as zeros) and sort
+// last.  Order inside one cost bucket is whatever the atomics give; it only
+// changes timing, never results.
+#include "kernels.h"
+
+namespace hstu {
+
+namespace {
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void seq_lengths(const SchedArgs& a, int b, int& Lq, int& Lk) {
+  Lq = max(0, __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b));
+  Lk = max(0, __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b));
+}
+
+// Cost of query tile t (list A).
+__device__ __forceinline__ int cost_a(const SchedArgs& a, int t, int Lq, int Lk) {
+  if (a.causal) {
+    int nk = min(min(kBM * (t + 1), Lq), Lk);
+    return ceil_div(nk, a.bn_a);
+  }
+  return ceil_div(Lk, a.bn_a);
+}
+
+// Cost of key tile s (list B).
+__device__ __forceinline__ int cost_b(const SchedArgs& a, int s, int Lq) {
+  int nq = ceil_div(Lq, a.bq_b);
+  int m0 = a.causal ? (kBM * s) / a.bq_b : 0;
+  return max(0, nq - m0);
+}
+
+// Exclusive prefix sum over 1024 threads; returns this thread's offset and
+// writes the block total.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[31];
+  __syncthreads();
+  return before;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) {
+  extern __shared__ int hist[];
+  const bool list_b = blockIdx.x == 1;
+  const int cmax = list_b ? a.cmax_b : a.cmax_a;
+  const int cap = list_b ? a.cap_b : a.cap_a;
+  int4* units = list_b ? a.units_b : a.units_a;
+  const int per_tile = list_b ? a.H * a.split_b : a.H;
+  const int nb = cmax + 1;
+  const int tid = threadIdx.x;
+
+  if (!list_b && tid == 0) {
+    a.header[kHdrStatus] = 0;
+    a.header[kHdrWhere] = 0;
+    if (gridDim.x == 1) a.header[kHdrOverflow + 1] = 0;
+  }
+  if (tid == 0) a.header[kHdrOverflow + (list_b ? 1 : 0)] = 0;
+
+  for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+
+  // pass 1: histogram of costs
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    int Lq, Lk;
+    seq_lengths(a, b, Lq, Lk);
+    if (list_b) {
+      int nt = ceil_div(Lk, kBM);
+      for (int s = 0; s < nt; ++s) atomicAdd(&hist[min(cost_b(a, s, Lq), cmax)], per_tile);
+    } else {
+      int nt = ceil_div(Lq, kBM);
+      for (int t = 0; t < nt; ++t) atomicAdd(&hist[min(cost_a(a, t, Lq, Lk), cmax)], per_tile);
+    }
+  }
+  __syncthreads();
+
+  // pass 2: exclusive scan over costs in descending order (rank 0 = cmax)
+  const int chunk = (nb + blockDim.x - 1) / blockDim.x;
+  const int r0 = min(nb, tid * chunk), r1 = min(nb, r0 + chunk);
+  int local = 0;
+  for (int r = r0; r < r1; ++r) local += hist[cmax - r];
+  int total;
+  int run = block_exclusive_scan(local, &total);
+  for (int r = r0; r < r1; ++r) {
+    int c = cmax - r;
+    int h = hist[c];
+    hist[c] = run;
+    run += h;
+  }
+  __syncthreads();
+
+  // pass 3: emit units at their bucket cursors
+  int overflow = 0;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    int Lq, Lk;
+    seq_lengths(a, b, Lq, Lk);
+    int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
+    for (int t = 0; t < nt; ++t) {
+      int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
+      int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
+      for (int e = 0; e < per_tile; ++e) {
+        if (pos + e < cap) {
+          units[pos + e] = make_int4(b, t, e, cost);
+        } else {
+          overflow = 1;
+        }
+      }
+    }
+  }
+  if (overflow) atomicExch(a.header + kHdrOverflow + (list_b ? 1 : 0), 1);
+  if (tid == 0) a.header[list_b ? kHdrUnitsB : kHdrUnitsA] = min(total, cap);
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait must
+// give up after `timeout_ns`, record the timeout in the header and return.
+__global__ void hstu_selftest_timeout_kernel(int* header, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flags[2];
+  if (threadIdx.x == 0) {
+    header[kHdrStatus] = 0;
+    header[kHdrWhere] = 0;
+    header[kHdrOverflow] = 0;
+    header[kHdrOverflow + 1] = 0;
+    mbar_init(smem_u32(&bar), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+    const WaitCtl wc{header, flags, timeout_ns};
+    wait_bar(smem_u32(&bar), 0, wc, 0x7e5);
+  }
+}
+
+cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st) {
+  hstu_selftest_timeout_kernel<<<1, 32, 0, st>>>(header, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace hstu

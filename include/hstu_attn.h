@@ -1,0 +1,160 @@
+/*
+ * hstu_attn.h: C ABI of the GB300 (sm_103a) HSTU attention library.
+ *
+ * Operation ("HSTU Attention (Blackwell SM100/SM103)", section Overview):
+ * for every packed sequence and head h,
+ *     S_h = alpha * Q_h K_h^T
+ *     A_h = (1 / L_scale) * (M (.) SiLU(S_h))
+ *     O_h = A_h V_h
+ * with no row softmax; the heads' outputs are concatenated.  The backward
+ * returns dQ, dK, dV from dO (same page, section "High-level functions"):
+ *     dV = A^T dO,   dS = M (.) (dO V^T) (.) SiLU'(S) / L_scale,
+ *     dQ = alpha dS K,   dK = alpha dS^T Q.
+ *
+ * Layout (same page, section "Tensor layout"): packed variable-length THD
+ * tensors.  q, dO, out, dq are (T_q, H, D); k, v, dk, dv are (T_k, H, D);
+ * all share one dtype, FP16 or BF16.  cu_seqlens_q / cu_seqlens_k are int32
+ * (B + 1,) cumulative lengths starting at 0 that delimit each sequence.
+ * Q, K and V have the same number of heads (MHA only: no GQA/MQA).
+ *
+ * Mask (same page, section "Mask support"): causal = window (-1, 0), the
+ * top-left aligned diagonal with the diagonal kept (key j valid iff j <= i,
+ * indices local to the sequence); full = window (-1, -1).  Keys outside the
+ * sequence never count.  A query row with no valid key gets a zero output and
+ * a zero dQ; a key that no query sees gets zero dK and dV (same page, section
+ * "Mask support": keyless rows are written as zeros, no output memset needed).
+ *
+ * Ownership and calling rules, common to every entry point:
+ *  - The caller owns every buffer.  The library never allocates device or
+ *    host memory and keeps no per-call state outside the caller's workspace.
+ *  - All tensor pointers and cu_seqlens are DEVICE pointers.  Their values
+ *    (cu_seqlens) are trusted and never copied to the host (same page,
+ *    section "Tensor layout").  Work is enqueued asynchronously on `stream`.
+ *  - Outputs are overwritten; every logical output element is written.
+ *  - Each tensor is described by a base pointer and two element strides
+ *    (token, head); the last (D) dimension is contiguous.  Base pointers and
+ *    both strides (in bytes) must be multiples of 16 (the page requires
+ *    16-byte aligned bases; the strides feed the tensor-memory-access unit).
+ *    A tensor's strides must not map two logical elements to one address.
+ *    Storage spans of distinct tensors are not compared: outputs must not
+ *    overlap live inputs.  dk and dv may be disjoint views of one packed KV
+ *    allocation (same page, section "High-level functions").
+ *  - Return codes: HSTU_OK, or an error with nothing enqueued (argument
+ *    errors) or with a launch error (HSTU_ERR_CUDA).
+ */
+#ifndef HSTU_ATTN_H_
+#define HSTU_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HSTU_OK = 0,
+  HSTU_ERR_INVALID_ARG = 1,    /* bad sizes, null pointers, max_seqlen_q > max_seqlen_k,
+                                  scaling_seqlen < 0, non-finite alpha, overlapping strides,
+                                  workspace too small */
+  HSTU_ERR_UNSUPPORTED = 2,    /* head_dim or dtype outside the built set, device not sm_103 */
+  HSTU_ERR_MISALIGNED = 3,     /* base pointer or stride not a multiple of 16 bytes */
+  HSTU_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+  HSTU_ERR_DEVICE_TIMEOUT = 5  /* a kernel wait ran past its limit (read back by
+                                  hstu_attn_last_device_status) */
+} hstu_status_t;
+
+typedef enum { HSTU_FP16 = 0, HSTU_BF16 = 1 } hstu_dtype_t;
+
+/* Read-only THD tensor: element (t, h, d) is at ptr[t*stride_t + h*stride_h + d]. */
+typedef struct {
+  const void* ptr;
+  int64_t stride_t;
+  int64_t stride_h;
+} hstu_cten_t;
+
+/* Writable THD tensor, same addressing. */
+typedef struct {
+  void* ptr;
+  int64_t stride_t;
+  int64_t stride_h;
+} hstu_ten_t;
+
+/*
+ * Device workspace size, in bytes, that hstu_attn_fwd (is_bwd = 0) or
+ * hstu_attn_bwd (is_bwd = 1) needs for these sizes.  The workspace holds the
+ * device-built tile schedule and a status word; it must be 256-byte aligned
+ * and may be reused by later calls on the same stream.  Returns 0 for invalid
+ * sizes.
+ */
+size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
+                                int32_t num_heads, int32_t head_dim, int32_t is_bwd);
+
+/*
+ * Forward: out = HSTU-MHA(q, k, v) (page "HSTU Attention (Blackwell
+ * SM100/SM103)", sections Overview and "High-level functions").
+ *   q, out: (total_q, num_heads, head_dim); k, v: (total_k, num_heads, head_dim).
+ *   batch B >= 0; cu_seqlens_q/k: device int32 (B+1,), cu[0] = 0,
+ *     cu_seqlens_q[B] <= total_q, cu_seqlens_k[B] <= total_k.
+ *   max_seqlen_q <= max_seqlen_k, each >= the longest sequence on its side.
+ *   alpha: score scale, finite.  scaling_seqlen: L_scale; 0 selects
+ *     max_seqlen_q, negative is an error (the page requires it positive).
+ *   causal: 1 = window (-1, 0), 0 = window (-1, -1).
+ *   head_dim in {64, 128, 256}; dtype FP16 or BF16.
+ * B == 0 or total_q == 0 is a no-op returning HSTU_OK.
+ */
+hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k,
+                            int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                            int32_t scaling_seqlen, int32_t causal, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Backward: (dq, dk, dv) from dout (page "HSTU Attention (Blackwell
+ * SM100/SM103)", section "High-level functions").  Arguments as for the
+ * forward, which must have used the same alpha, scaling_seqlen, mask and
+ * sequence metadata.  dout, dq: (total_q, H, D); dk, dv: (total_k, H, D).
+ * No forward output or statistic is needed: S is recomputed.  dQ is reduced
+ * without atomics, so results do not depend on scheduling.
+ */
+hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                            hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k,
+                            int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                            int32_t scaling_seqlen, int32_t causal, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* hstu_attn_status_string(hstu_status_t status);
+
+/*
+ * Synchronizes `stream` and returns the device-side status that the last
+ * call using `workspace` recorded: HSTU_OK, or HSTU_ERR_DEVICE_TIMEOUT when a
+ * kernel gave up a wait (it then wrote no further output and exited).
+ * For tests and debugging; costs a stream synchronization.
+ */
+hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one block that waits on
+ * a barrier nothing will ever complete, with a limit of `timeout_us`
+ * microseconds (1..10,000,000).  The kernel records HSTU_ERR_DEVICE_TIMEOUT in
+ * `workspace` and returns; no fault, no hang.  Read the result with
+ * hstu_attn_last_device_status.  workspace: >= 256 bytes, device.
+ */
+hstu_status_t hstu_attn_selftest_timeout(void* workspace, uint32_t timeout_us,
+                                         cudaStream_t stream);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int32_t hstu_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSTU_ATTN_H_ */

@@ -1,0 +1,166 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/hstu_attn.h declares, sizes its workspace, and rejects bad arguments
+on the host before anything is launched (those paths make no CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from generative_recommender_attention_gb300 import _lib as L
+from generative_recommender_attention_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hstu_attn.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hstu_attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(L.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_symbols_have_c_linkage():
+    out = os.popen(f"nm -D --defined-only {L.library_path()}").read()
+    names = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in names, name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.hstu_attn_version() == 100
+    for code in range(6):
+        assert lib.hstu_attn_status_string(code)
+    assert lib.hstu_attn_status_string(5) == b"device wait timed out"
+
+
+def test_workspace_size(lib):
+    ws = lib.hstu_attn_workspace_size
+    # header + 16 bytes per unit, units <= H * (ceil(T/128) + B), 256-aligned
+    assert ws(4, 309, 309, 2, 64, 0) == (256 + 16 * 2 * (3 + 4) + 255) // 256 * 256
+    fwd = ws(32, 20480, 20480, 4, 128, 0)
+    bwd = ws(32, 20480, 20480, 4, 128, 1)
+    assert bwd == ((256 + 16 * 4 * (160 + 32) * 2) + 255) // 256 * 256 and fwd < bwd
+    # D = 256 splits dK/dV into two column halves: twice the key-side units
+    assert ws(16, 65536, 65536, 2, 256, 1) == 256 + 16 * 2 * (512 + 16) * 3
+    assert ws(1, 10, 10, 1, 96, 0) == 0        # unsupported head_dim
+    assert ws(-1, 10, 10, 1, 64, 0) == 0
+    assert ws(1, 10, 10, 0, 64, 0) == 0
+
+
+def _call_fwd(lib, **over):
+    """hstu_attn_fwd with fake (never dereferenced) device pointers."""
+    a = dict(q=(0x10000, 256, 64), k=(0x20000, 256, 64), v=(0x30000, 256, 64),
+             out=(0x40000, 256, 64), cu_q=0x50000, cu_k=0x60000, batch=2, total_q=100,
+             total_k=100, H=4, D=64, dtype=L.HSTU_BF16, max_q=60, max_k=60, alpha=0.125,
+             scaling=0, causal=1, ws=0x70000, ws_bytes=1 << 20, stream=None)
+    a.update(over)
+    return lib.hstu_attn_fwd(L.CTen(*a["q"]), L.CTen(*a["k"]), L.CTen(*a["v"]),
+                             L.Ten(*a["out"]), a["cu_q"], a["cu_k"], a["batch"], a["total_q"],
+                             a["total_k"], a["H"], a["D"], a["dtype"], a["max_q"], a["max_k"],
+                             a["alpha"], a["scaling"], a["causal"], a["ws"], a["ws_bytes"],
+                             a["stream"])
+
+
+def test_fwd_argument_errors(lib):
+    assert _call_fwd(lib, D=96) == UNSUPPORTED
+    assert _call_fwd(lib, D=32) == UNSUPPORTED
+    assert _call_fwd(lib, dtype=7) == UNSUPPORTED
+    assert _call_fwd(lib, max_q=61, max_k=60) == INVALID          # max_seqlen_q > max_seqlen_k
+    assert _call_fwd(lib, scaling=-1) == INVALID                 # scaling_seqlen must be > 0
+    assert _call_fwd(lib, alpha=float("nan")) == INVALID
+    assert _call_fwd(lib, alpha=float("inf")) == INVALID
+    assert _call_fwd(lib, batch=-1) == INVALID
+    assert _call_fwd(lib, H=0) == INVALID
+    assert _call_fwd(lib, total_q=-5) == INVALID
+    assert _call_fwd(lib, cu_q=None) == INVALID
+    assert _call_fwd(lib, q=(0, 256, 64)) == INVALID              # null with rows
+    assert _call_fwd(lib, q=(0x10008, 256, 64)) == MISALIGNED     # base not 16-byte aligned
+    assert _call_fwd(lib, k=(0x20000, 260, 64)) == MISALIGNED     # stride 520 bytes
+    assert _call_fwd(lib, v=(0x30000, 256, 36)) == MISALIGNED     # head stride 72 bytes
+    assert _call_fwd(lib, out=(0x40000, 256, 32)) == INVALID      # heads overlap (32 < 64)
+    assert _call_fwd(lib, out=(0x40000, 64, 64)) == INVALID       # tokens overlap heads
+    assert _call_fwd(lib, out=(0x40000, -256, 64)) == INVALID
+    assert _call_fwd(lib, ws=None) == INVALID                     # workspace required
+    assert _call_fwd(lib, ws_bytes=16) == INVALID                 # workspace too small
+    assert _call_fwd(lib, ws=0x70010) == MISALIGNED               # workspace 256-aligned
+    assert _call_fwd(lib, max_q=0, max_k=0, scaling=0) == INVALID  # L_scale would be 0
+
+
+def test_fwd_empty_problems_are_noops(lib):
+    # nothing to compute: returns before touching the device
+    assert _call_fwd(lib, batch=0) == OK
+    assert _call_fwd(lib, total_q=0, q=(0, 256, 64), out=(0, 256, 64)) == OK
+
+
+def test_non_contiguous_layouts_accepted_by_validation(lib):
+    # (T, H, 2D) packed KV buffer: k and v are disjoint views with stride_t = 2*H*D
+    from generative_recommender_attention_gb300._lib import CTen  # noqa: F401
+    st = lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 0)
+    assert st > 0
+    # validation of a padded layout passes (the call then fails only for lack
+    # of a device, which the CPU test does not reach: batch = 0 short-cuts)
+    assert _call_fwd(lib, k=(0x20000, 512, 128), v=(0x20080, 512, 128), batch=0) == OK
+
+
+def _call_bwd(lib, **over):
+    t = (0x10000, 256, 64)
+    a = dict(do=t, q=t, k=t, v=t, dq=(0x80000, 256, 64), dk=(0x90000, 256, 64),
+             dv=(0xA0000, 256, 64), batch=2, total_q=100, total_k=100, D=64, max_q=60,
+             max_k=60, scaling=0, ws_bytes=1 << 20)
+    a.update(over)
+    return lib.hstu_attn_bwd(L.CTen(*a["do"]), L.CTen(*a["q"]), L.CTen(*a["k"]), L.CTen(*a["v"]),
+                             L.Ten(*a["dq"]), L.Ten(*a["dk"]), L.Ten(*a["dv"]), 0x50000, 0x60000,
+                             a["batch"], a["total_q"], a["total_k"], 4, a["D"], L.HSTU_FP16,
+                             a["max_q"], a["max_k"], 0.5, a["scaling"], 0, 0x70000,
+                             a["ws_bytes"], None)
+
+
+def test_bwd_argument_errors(lib):
+    assert _call_bwd(lib, D=48) == UNSUPPORTED
+    assert _call_bwd(lib, max_q=70) == INVALID
+    assert _call_bwd(lib, scaling=-3) == INVALID
+    assert _call_bwd(lib, dk=(0x90004, 256, 64)) == MISALIGNED
+    assert _call_bwd(lib, dv=(0xA0000, 8, 64)) == INVALID
+    assert _call_bwd(lib, ws_bytes=100) == INVALID
+    assert _call_bwd(lib, batch=0) == OK
+
+
+def test_selftest_argument_errors(lib):
+    assert lib.hstu_attn_selftest_timeout(None, 1000, None) == INVALID
+    assert lib.hstu_attn_selftest_timeout(0x70000, 0, None) == INVALID
+    assert lib.hstu_attn_selftest_timeout(0x70000, 20_000_000, None) == INVALID
+    assert lib.hstu_attn_selftest_timeout(0x70008, 1000, None) == MISALIGNED
+    assert lib.hstu_attn_last_device_status(None, None) == INVALID
+
+
+def test_binding_rejects_bad_tensors_on_cpu():
+    import torch
+    import generative_recommender_attention_gb300 as g
+    q = torch.zeros(8, 2, 64, dtype=torch.float32)
+    cu = torch.tensor([0, 8], dtype=torch.int32)
+    with pytest.raises(TypeError):
+        g.hstu_attn_fwd(q, q, q, cu, cu, 8, 8)
+    with pytest.raises(NotImplementedError):
+        g._causal(True, (4, 0))
+    with pytest.raises(ValueError):
+        g._scaling(-2)
+    assert g._causal(False, (-1, 0)) is True and g._causal(True, (-1, -1)) is False

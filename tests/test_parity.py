@@ -1,0 +1,160 @@
+"""GPU parity: the CUDA path (called through the C ABI via the binding)
+against the fp64 oracle on the same bf16/fp16 inputs, element by element.
+
+Tolerances: forward max-abs error <= 1e-2 * max|O_ref|, each gradient
+<= 2e-2 * max|grad_ref| (see hstu_testlib)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from generative_recommender_attention_gb300 import workloads
+import generative_recommender_attention_gb300 as hstu
+
+from hstu_testlib import (TOL_BWD, TOL_FWD, check, full_compare, gpu_fwd_bwd,
+                          sampled_compare, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _ws(name):
+    return workloads.WORKLOADS[name]
+
+
+# ------------------------------------------------------------------ workloads
+def test_tiny_workload_full():
+    w = _ws("tiny")
+    x = workloads.make_inputs(w, seed=0)
+    full_compare(x, w.scaling_seqlen, w.causal, w.alpha)
+
+
+@pytest.mark.parametrize("name", ["recsys", "long", "skewed", "full"])
+def test_workload_full_size_sampled(name):
+    w = _ws(name)
+    x = workloads.make_inputs(w, seed=0)
+    sampled_compare(x, w.scaling_seqlen, w.causal, w.alpha, n_random=96)
+
+
+# ------------------------------------------------------------------ medium, every variant
+MEDIUM_LENS = [300, 1, 129, 517, 0, 64, 256]
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("causal", [True, False])
+def test_medium_every_variant(D, dtype, causal):
+    x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, D, dtype, seed=D + int(causal))
+    alpha = 1.0 / math.sqrt(D)
+    full_compare(x, None, causal, alpha)
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("causal", [True, False])
+def test_unequal_q_and_k_lengths(causal):
+    # per sequence Lq <= Lk, and one sequence with Lq > Lk (max_q <= max_k still)
+    lq = [100, 250, 7, 300]
+    lk = [180, 250, 40, 200]
+    x = workloads.random_inputs(lq, lk, 2, 64, torch.bfloat16, seed=3)
+    x["max_seqlen_k"] = max(max(lk), x["max_seqlen_q"])
+    full_compare(x, 96, causal, 0.2)
+
+
+def test_sequences_without_keys_get_zero_rows():
+    lq = [50, 130, 20]
+    lk = [60, 0, 140]
+    x = workloads.random_inputs(lq, lk, 2, 128, torch.bfloat16, seed=4)
+    res = full_compare(x, None, True, 0.1)
+    xd = to_dev(x)
+    o, dq, _, _ = gpu_fwd_bwd(xd, None, True, 0.1)
+    assert torch.all(o[50:180] == 0) and torch.all(dq[50:180] == 0)
+    assert res["o"][1] > 0
+
+
+def test_length_one_and_empty_sequences():
+    lens = [1, 0, 1, 1, 0, 2, 1]
+    x = workloads.random_inputs(lens, lens, 3, 64, torch.float16, seed=5)
+    full_compare(x, 4, True, 0.3)
+
+
+def test_single_long_sequence_ragged_tail():
+    lens = [1000]
+    x = workloads.random_inputs(lens, lens, 1, 128, torch.bfloat16, seed=6)
+    full_compare(x, None, True, 1.0 / math.sqrt(128))
+
+
+def test_explicit_scaling_and_negative_alpha():
+    lens = [200, 77]
+    x = workloads.random_inputs(lens, lens, 2, 64, torch.bfloat16, seed=7)
+    full_compare(x, 1000, True, -0.15)
+
+
+def test_strided_views_and_packed_kv_gradients():
+    """q/k/v as views of one packed (T, 3, H, D) buffer, dk/dv as disjoint
+    views of one packed (T, H, 2D) buffer, out with a padded token stride."""
+    lens = [140, 260, 33]
+    T, H, D = sum(lens), 2, 64
+    g = torch.Generator().manual_seed(8)
+    qkv = torch.randn(T, 3, H, D, generator=g).to(torch.bfloat16)
+    do = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    cu = workloads.cu_seqlens(lens)
+    x = {"q": qkv[:, 0], "k": qkv[:, 1], "v": qkv[:, 2], "do": do, "cu_seqlens_q": cu,
+         "cu_seqlens_k": cu.clone(), "max_seqlen_q": max(lens), "max_seqlen_k": max(lens)}
+    qkv_d = qkv.cuda()
+    xd = {"q": qkv_d[:, 0], "k": qkv_d[:, 1], "v": qkv_d[:, 2], "do": do.cuda(),
+          "cu_seqlens_q": cu.cuda(), "cu_seqlens_k": cu.cuda(),
+          "max_seqlen_q": max(lens), "max_seqlen_k": max(lens)}
+    out_buf = torch.full((T, H, D + 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    kv_grad = torch.full((T, H, 2 * D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o, dq, dk, dv = gpu_fwd_bwd(xd, None, True, 0.125,
+                                fwd={"out": out_buf[:, :, :D]},
+                                bwd={"dk": kv_grad[:, :, :D], "dv": kv_grad[:, :, D:]})
+    assert o.data_ptr() == out_buf.data_ptr()
+    L = float(max(lens))
+    ro = oracle.fwd(x["q"], x["k"], x["v"], cu, cu, 0.125, L, True)
+    rdq, rdk, rdv = oracle.bwd(do, x["q"], x["k"], x["v"], cu, cu, 0.125, L, True)
+    check("O", o, ro, TOL_FWD)
+    check("dQ", dq, rdq, TOL_BWD)
+    check("dK", kv_grad[:, :, :D], rdk, TOL_BWD)
+    check("dV", kv_grad[:, :, D:], rdv, TOL_BWD)
+    assert torch.isnan(out_buf[:, :, D:].float()).all()   # padding untouched
+
+
+def test_backward_is_deterministic():
+    w = _ws("recsys")
+    x = workloads.make_inputs(w, seed=1, lengths=[700, 256, 1024, 300])
+    xd = to_dev(x)
+    a = gpu_fwd_bwd(xd, None, True, w.alpha)
+    b = gpu_fwd_bwd(xd, None, True, w.alpha)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_outputs_fully_overwritten():
+    lens = [129, 64, 300]
+    x = workloads.random_inputs(lens, lens, 2, 128, torch.float16, seed=9)
+    xd = to_dev(x)
+    T = sum(lens)
+    nan = lambda: torch.full((T, 2, 128), float("nan"), dtype=torch.float16, device="cuda")  # noqa
+    o, dq, dk, dv = gpu_fwd_bwd(xd, None, False, 0.09, fwd={"out": nan()},
+                                bwd={"dq": nan(), "dk": nan(), "dv": nan()})
+    for t in (o, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+
+
+def test_device_status_ok_after_calls():
+    lens = [300, 20]
+    x = workloads.random_inputs(lens, lens, 2, 64, torch.bfloat16, seed=10)
+    xd = to_dev(x)
+    ws = torch.empty(hstu.workspace_size(2, 320, 320, 2, 64, True), dtype=torch.uint8,
+                     device="cuda")
+    hstu.hstu_attn_bwd(xd["do"], xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"],
+                       xd["cu_seqlens_k"], 300, 300, workspace=ws)
+    assert hstu.last_device_status(ws) == 0
