@@ -1,0 +1,349 @@
+#!/usr/bin/env python3
+"""Benchmark: HSTU attention forward + backward throughput on one GB300.
+
+A step is one forward and one backward pass (all hot-path kernels: tile
+scheduler, forward, dQ, dK/dV) over one batch of the recommender-training
+workload: B = 32 sequences with lengths uniform in [256, 1024], H = 4,
+D = 128, bf16 q/k/v/dO ~ N(0, 1), alpha = 1/sqrt(128), L_scale = max_seqlen,
+causal.  Inputs are synthetic (seed 0) and resident in HBM before timing.
+
+The metric counts algorithmic tensor FLOPs only, causal-aware:
+N = H * sum_b L_b (L_b + 1) / 2 attended pairs; forward 4 D N, backward
+10 D N (S recompute, dO V^T, dV, dQ, dK); recomputation beyond that (S and
+dP in both backward kernels) is not credited.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HSTU attn fwd+bwd TFLOP/s (varlen causal bf16) and % of GB300 dense BF16 peak"
+WORKLOAD = "recsys"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def pairs(lengths, H, causal):
+    if causal:
+        return H * sum(L * (L + 1) // 2 for L in lengths)
+    return H * sum(L * L for L in lengths)
+
+
+def workload_config(w, lengths):
+    d = w.describe()
+    d["T"] = int(sum(lengths))
+    d["max_seqlen"] = int(max(lengths))
+    d["N_pairs"] = int(pairs(lengths, w.heads, w.causal))
+    return d
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(x, w, budget_s: float, start: int = 0):
+    """Times the fp64 oracle fwd+bwd on whole sequences (all heads) of the
+    workload, one after another from `start`, until `budget_s` is spent.
+    Returns (flops, seconds, n_sequences, threads)."""
+    import numpy as np
+    import oracle
+    threads = oracle.threads(os.cpu_count() or 1)
+    cu = x["cu_seqlens_q"].tolist()
+    B = len(cu) - 1
+    L_scale = oracle.resolve_scaling(w.scaling_seqlen, x["max_seqlen_q"])
+    D = w.head_dim
+    flops, secs, n = 0.0, 0.0, 0
+    b = start
+    while n < B and (n == 0 or secs < budget_s):
+        s0, s1 = cu[b], cu[b + 1]
+        sub = {k: x[k][s0:s1].double().numpy() for k in ("q", "k", "v", "do")}
+        c1 = np.array([0, s1 - s0], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.fwd(sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, w.causal, threads)
+        oracle.bwd(sub["do"], sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, w.causal,
+                   threads)
+        secs += time.perf_counter() - t0
+        flops += 14.0 * D * pairs([s1 - s0], w.heads, w.causal)
+        n += 1
+        b = (b + 1) % B
+    return flops, secs, n, threads
+
+
+def run_reference(args, w):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    import torch
+    from generative_recommender_attention_gb300 import workloads
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    x = workloads.make_inputs(w, seed=0)
+    per_step = []
+    flops_tot = 0.0
+    n_seq = 0
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        f, s, n, threads = oracle_sample(x, w, 0.0, start=i % w.batch)  # one sequence per step
+        if i >= args.warmup:
+            per_step.append(s)
+            flops_tot += f
+            n_seq += n
+    secs = sum(per_step)
+    value = flops_tot / secs / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, x["lengths"]),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_seq} whole sequences (all heads, fwd+bwd), one per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    from generative_recommender_attention_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import generative_recommender_attention_gb300 as hstu
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    x = workloads.make_inputs(w, seed=0)
+    lengths = x["lengths"]
+    B, T, H, D = w.batch, sum(lengths), w.heads, w.head_dim
+    N = pairs(lengths, H, w.causal)
+    flops_step = 14.0 * D * N
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    o = torch.empty_like(d["q"])
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    ws_f = torch.empty(hstu.workspace_size(B, T, T, H, D, False), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(hstu.workspace_size(B, T, T, H, D, True), dtype=torch.uint8, device=dev)
+    kw = dict(scaling_seqlen=w.scaling_seqlen, causal=w.causal, alpha=w.alpha)
+    mq, mk = x["max_seqlen_q"], x["max_seqlen_k"]
+    flush = None if args.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)]
+          for _ in range(args.warmup + args.steps)]
+    for row in ev:
+        for e in row:
+            e.record()   # creates the events before they are handed to the library
+    torch.cuda.synchronize()
+
+    def step(evs):
+        hstu.hstu_attn_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], mq, mk,
+                           out=o, workspace=ws_f, events=evs[0:3], **kw)
+        hstu.hstu_attn_bwd(d["do"], d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"],
+                           mq, mk, dq=dq, dk=dk, dv=dv, workspace=ws_b, events=evs[3:7], **kw)
+
+    for i in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/hstu_clocks.csv")
+    wall0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        if flush is not None:
+            flush.zero_()
+        step(ev[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    assert hstu.last_device_status(ws_b) == 0 and hstu.last_device_status(ws_f) == 0
+
+    timed = ev[args.warmup:]
+    t_sched_f = [r[0].elapsed_time(r[1]) for r in timed]
+    t_fwd = [r[1].elapsed_time(r[2]) for r in timed]
+    t_sched_b = [r[3].elapsed_time(r[4]) for r in timed]
+    t_dq = [r[4].elapsed_time(r[5]) for r in timed]
+    t_dkdv = [r[5].elapsed_time(r[6]) for r in timed]
+    t_step = [r[0].elapsed_time(r[2]) + r[3].elapsed_time(r[6]) for r in timed]
+    ms_total = sum(t_step)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+
+    # per-kernel live timings and algorithmic FLOPs per launch
+    mean = lambda a: sum(a) / len(a)  # noqa: E731
+    kernels = {
+        "hstu_fwd_kernel": (4.0 * D * N, mean(t_fwd)),
+        "hstu_bwd_dq_kernel": (6.0 * D * N, mean(t_dq)),
+        "hstu_bwd_dkdv_kernel": (8.0 * D * N, mean(t_dkdv)),
+    }
+    dom = max(kernels, key=lambda k: kernels[k][1])
+    f_dom, ms_dom = kernels[dom]
+    achieved = f_dom / (ms_dom * 1e-3) / 1e12
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            traffic = json.load(open(tfile)).get(dom)
+        except Exception:
+            traffic = None
+
+    # end to end through the public API: pinned host inputs in, outputs back
+    pin = {k: x[k].pin_memory() for k in ("q", "k", "v", "do", "cu_seqlens_q", "cu_seqlens_k")}
+    host_out = [torch.empty(x["q"].shape, dtype=x["q"].dtype).pin_memory() for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_ms = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 20))
+    for i in range(n_e2e + 2):
+        if flush is not None:
+            flush.zero_()
+        e0.record()
+        g = {k: v.to(dev, non_blocking=True) for k, v in pin.items()}
+        oo = hstu.hstu_attn_fwd(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_k"], mq,
+                                mk, workspace=ws_f, **kw)
+        gq, gk, gv = hstu.hstu_attn_bwd(g["do"], g["q"], g["k"], g["v"], g["cu_seqlens_q"],
+                                        g["cu_seqlens_k"], mq, mk, workspace=ws_b, **kw)
+        for hsrc, dst in zip((oo, gq, gk, gv), host_out):
+            dst.copy_(hsrc, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = world * flops_step / (mean(e2e_ms) * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "pct_of_dense_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
+        "pct_of_sustained_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
+        "config": dict(workload_config(w, lengths),
+                       l2="flushed between steps (256 MiB write)" if flush is not None else "not flushed",
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       flops_per_step=flops_step, peaks_source=pk["source"]),
+        "per_kernel_ms": {"sched_fwd": mean(t_sched_f), "fwd": mean(t_fwd),
+                          "sched_bwd": mean(t_sched_b), "bwd_dq": mean(t_dq),
+                          "bwd_dkdv": mean(t_dkdv)},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops_sustained"], "traffic": traffic,
+                     "peak_kind": "bf16 sustained (kernel timed inside a long step loop)"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": len(e2e_ms)},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_loop": wall,
+    }
+
+    if rank == 0:
+        f, s, n, threads = oracle_sample(x, w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"first {n} of {B} sequences, all heads, fwd+bwd (fp64)"}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

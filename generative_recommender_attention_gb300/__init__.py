@@ -94,6 +94,15 @@ def _workspace(workspace, nbytes, device):
     return workspace
 
 
+def _event_array(events):
+    import ctypes
+    handles = [e.cuda_event for e in events]   # torch creates the event lazily
+    if any(h == 0 for h in handles):
+        raise ValueError("events must have been created on the device (record them once first)")
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    return arr, len(handles)
+
+
 def _stream(device):
     import torch
     return torch.cuda.current_stream(device).cuda_stream
@@ -101,12 +110,15 @@ def _stream(device):
 
 def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                   scaling_seqlen: Optional[int] = None, causal: bool = True,
-                  alpha: float = 1.0, out=None, workspace=None, window_size=None):
+                  alpha: float = 1.0, out=None, workspace=None, window_size=None,
+                  events=None):
     """Forward HSTU attention; returns ``out`` of shape ``q.shape``.
 
     q: (T_q, H, D); k, v: (T_k, H, D); fp16 or bf16 on a CUDA device.
     cu_seqlens_q/k: int32 (B + 1,) on the same device (values are trusted and
     never copied to the host).  ``out`` may be supplied (overwritten).
+    ``events``: optional list of 3 torch.cuda.Event recorded before the
+    scheduler, after it and after the forward kernel (profiling).
     """
     import torch
     lib = library()
@@ -122,11 +134,15 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     _check_thd("out", out, T_q, H, D, q.dtype, dev)
     causal = _causal(causal, window_size)
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, False), dev)
-    st = lib.hstu_attn_fwd(_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
-                           cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
-                           int(max_seqlen_q), int(max_seqlen_k), float(alpha),
-                           _scaling(scaling_seqlen), int(causal), ws.data_ptr(),
-                           ws.numel(), _stream(dev))
+    args = (_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
+            cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q), int(max_seqlen_q),
+            int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen), int(causal),
+            ws.data_ptr(), ws.numel(), _stream(dev))
+    if events is None:
+        st = lib.hstu_attn_fwd(*args)
+    else:
+        arr, n = _event_array(events)
+        st = lib.hstu_attn_fwd_profiled(*args, arr, n)
     if st != 0:
         raise HstuError(st)
     return out
@@ -135,12 +151,14 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
 def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, scaling_seqlen: Optional[int] = None,
                   causal: bool = True, alpha: float = 1.0, dq=None, dk=None, dv=None,
-                  workspace=None, window_size=None) -> Tuple:
+                  workspace=None, window_size=None, events=None) -> Tuple:
     """Backward HSTU attention; returns ``(dq, dk, dv)``.
 
     Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
     ``dq``/``dk``/``dv`` may be supplied (overwritten); dk and dv may be
-    disjoint views of one packed KV buffer.
+    disjoint views of one packed KV buffer.  ``events``: optional list of 4
+    torch.cuda.Event (before the scheduler, after it, after the dQ kernel,
+    after the dK/dV kernel).
     """
     import torch
     lib = library()
@@ -163,11 +181,15 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
     causal = _causal(causal, window_size)
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, True), dev)
-    st = lib.hstu_attn_bwd(_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk),
-                           _ten(dv), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q,
-                           T_k, H, D, _dtype_code(q), int(max_seqlen_q), int(max_seqlen_k),
-                           float(alpha), _scaling(scaling_seqlen), int(causal), ws.data_ptr(),
-                           ws.numel(), _stream(dev))
+    args = (_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk), _ten(dv),
+            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
+            int(max_seqlen_q), int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen),
+            int(causal), ws.data_ptr(), ws.numel(), _stream(dev))
+    if events is None:
+        st = lib.hstu_attn_bwd(*args)
+    else:
+        arr, n = _event_array(events)
+        st = lib.hstu_attn_bwd_profiled(*args, arr, n)
     if st != 0:
         raise HstuError(st)
     return dq, dk, dv

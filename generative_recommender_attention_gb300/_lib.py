@@ -21,7 +21,8 @@ STATUS = {0: "HSTU_OK", 1: "HSTU_ERR_INVALID_ARG", 2: "HSTU_ERR_UNSUPPORTED",
           3: "HSTU_ERR_MISALIGNED", 4: "HSTU_ERR_CUDA", 5: "HSTU_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/hstu_attn.h declares.
-EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_workspace_size",
+EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_attn_bwd_profiled",
+           "hstu_attn_workspace_size",
            "hstu_attn_status_string", "hstu_attn_last_device_status",
            "hstu_attn_selftest_timeout", "hstu_attn_version")
 
@@ -61,6 +62,10 @@ def _declare(lib):
     lib.hstu_attn_fwd.restype = ctypes.c_int
     lib.hstu_attn_bwd.argtypes = [CTen, CTen, CTen, CTen, Ten, Ten, Ten] + scal
     lib.hstu_attn_bwd.restype = ctypes.c_int
+    lib.hstu_attn_fwd_profiled.argtypes = lib.hstu_attn_fwd.argtypes + [P, i32]
+    lib.hstu_attn_fwd_profiled.restype = ctypes.c_int
+    lib.hstu_attn_bwd_profiled.argtypes = lib.hstu_attn_bwd.argtypes + [P, i32]
+    lib.hstu_attn_bwd_profiled.restype = ctypes.c_int
     lib.hstu_attn_workspace_size.argtypes = [i32, i64, i64, i32, i32, i32]
     lib.hstu_attn_workspace_size.restype = S
     lib.hstu_attn_status_string.argtypes = [ctypes.c_int]

@@ -184,13 +184,25 @@ size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
   return (bytes + 255) & ~size_t(255);
 }
 
-hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
-                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
-                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
-                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
-                            int32_t causal, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Records events[i] on `stream` when a profiling caller supplied them.
+struct EventMarks {
+  cudaEvent_t* ev;
+  int n;
+  bool mark(int i, cudaStream_t st) const {
+    return ev == nullptr || i >= n || cudaEventRecord(ev[i], st) == cudaSuccess;
+  }
+};
+
+hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                       int64_t total_q, int64_t total_k, int32_t num_heads, int32_t head_dim,
+                       hstu_dtype_t dtype, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                       float alpha, int32_t scaling_seqlen, int32_t causal, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
@@ -229,8 +241,10 @@ hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_te
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
   sa.header = header;
+  if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   hstu_sched_kernel<<<1, kSchedThreads, sched_bytes, stream>>>(sa);
   if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
   a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
@@ -239,17 +253,17 @@ hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_te
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
   const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
   if (launch_fwd(D, c.bf16, grid, stream, tq, tk, tv, a) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
 }
 
-hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
-                            hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
-                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
-                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
-                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
-                            int32_t causal, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                       hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv, const int32_t* cu_seqlens_q,
+                       const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q,
+                       int64_t total_k, int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                       int32_t scaling_seqlen, int32_t causal, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
@@ -301,8 +315,10 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
+  if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   hstu_sched_kernel<<<2, kSchedThreads, sched_bytes, stream>>>(sa);
   if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
   a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
@@ -316,6 +332,7 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
     if (launch_dq(D, c.bf16, grid, stream, m_q128, m_do128, m_kbn, m_vbn, aq) != cudaSuccess)
       return HSTU_ERR_CUDA;
   }
+  if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
   if (total_k > 0) {
     AttnArgs ak = a;
     ak.units = unitsB; ak.units_slot = kHdrUnitsB;
@@ -325,7 +342,66 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
     if (launch_dkdv(D, c.bf16, grid, stream, m_k128, m_v128, m_q64, m_do64, ak) != cudaSuccess)
       return HSTU_ERR_CUDA;
   }
+  if (!em.mark(3, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
+                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  workspace, workspace_bytes, stream, EventMarks{nullptr, 0});
+}
+
+hstu_status_t hstu_attn_fwd_profiled(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream,
+                                     cudaEvent_t* events, int32_t n_events) {
+  if (events == nullptr || n_events < 0) return HSTU_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  workspace, workspace_bytes, stream, EventMarks{events, n_events});
+}
+
+hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                            hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                            int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+                            int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
+                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
+                  causal, workspace, workspace_bytes, stream, EventMarks{nullptr, 0});
+}
+
+hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k,
+                                     hstu_cten_t v, hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream,
+                                     cudaEvent_t* events, int32_t n_events) {
+  if (events == nullptr || n_events < 0) return HSTU_ERR_INVALID_ARG;
+  return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
+                  causal, workspace, workspace_bytes, stream, EventMarks{events, n_events});
 }
 
 hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t stream) {

@@ -12,7 +12,8 @@
 // dK += dS^T Q with the A operand read from TMEM.  No atomics.
 //   warp 0      TMA: K and V per unit, Q and dO per step.
 //   warp 1      tcgen05 issuer.
-//   warps 2-5   one key row each.
+//   warps 2-9   row work, two warps per TMEM lane quarter (one per column
+//               half of each query tile).
 // TMEM: S^T | dP^T | dV | dK | A^T x2 | dS^T x2.
 #include "kernels.h"
 
@@ -61,10 +62,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(QFULL + i), 1); mbar_init(bar(DOFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
     }
     mbar_init(bar(STFULL), 1);
-    mbar_init(bar(ASFULL), 128);
-    mbar_init(bar(ASFULL + 1), 128);
+    mbar_init(bar(ASFULL), kRowThreads);
+    mbar_init(bar(ASFULL + 1), kRowThreads);
     mbar_init(bar(ACCFULL), 1);
-    mbar_init(bar(ACCEMPTY), 128);
+    mbar_init(bar(ACCEMPTY), kRowThreads);
     mbar_init(bar(DRAIN), 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -204,13 +205,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ A^T, dS^T + epilogue
-    const int wq = warp & 3;
+    // Eight warps: warp w owns TMEM lane quarter w % 4 (32 key rows) and one
+    // half of the query columns of each S^T / dP^T tile (and of dK / dV).
+    constexpr int CPW = BQ / 2;
+    static_assert(CPW == 32, "one 32-column batch per warp");
+    const int wq = warp & 3, hc = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tST = tmem + COL_ST + lane_off, tDPT = tmem + COL_DPT + lane_off,
+    const uint32_t tST = tmem + COL_ST + lane_off + hc * CPW, tDPT = tmem + COL_DPT + lane_off + hc * CPW,
                    tDV = tmem + COL_DV + lane_off, tDK = tmem + COL_DK + lane_off,
-                   tAT = tmem + COL_AT + lane_off, tDST = tmem + COL_DST + lane_off;
-    const float alpha = a.alpha;
+                   tAT = tmem + COL_AT + lane_off + hc * (CPW / 2),
+                   tDST = tmem + COL_DST + lane_off + hc * (CPW / 2);
+    const float half_alpha = 0.5f * a.alpha;
+    const float dk_scale = 0.5f * a.alpha * a.inv_L;  // dS^T is stored doubled
     uint32_t g = 0, oi = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
@@ -221,49 +228,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int k0 = __ldg(a.cu_k + U.b);
       const int Lk = __ldg(a.cu_k + U.b + 1) - k0;
       const int j = kBM * U.tile + r;
+      const int j_warp_last = kBM * U.tile + wq * 32 + 31;
       const int64_t grow = static_cast<int64_t>(k0) + j;
       const bool row_ok = j < Lk && grow < a.total_k;
-      const int64_t col0 = static_cast<int64_t>(half) * DH;
+      const int64_t col0 = static_cast<int64_t>(half) * DH + hc * (DH / 2);
       char* dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + col0) * 2;
       char* dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + static_cast<int64_t>(h) * a.o1_sh + col0) * 2;
       if (U.n <= 0) {
         if (row_ok)
-          for (int c = 0; c < DH / 32; ++c) { store_zero32(dvrow + c * 64); store_zero32(dkrow + c * 64); }
+          for (int c = 0; c < DH / 64; ++c) { store_zero32(dvrow + c * 64); store_zero32(dkrow + c * 64); }
         continue;
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
-      const int j_last = kBM * U.tile + kBM - 1;
+      const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
       for (int m = 0; m < U.n; ++m) {
         const int b = g & 1;
         if (!wait_bar_warp(bar(STFULL), g & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
-        const int i0 = BQ * (m0 + m);
-        const bool need_mask = (i0 + BQ > Lq) || (kBM * U.tile + kBM > Lk) || (a.causal && j_last > i0);
+        const int ic = BQ * (m0 + m) + hc * CPW;  // first query of this warp's columns
+        const bool need_mask = (ic + CPW > Lq) || (a.causal && j_warp_last > ic);
+        uint32_t xs[32], xp[32];
+        tmem_ld32x2(tST, tDPT, xs, xp);
+        uint32_t pa[16], pd[16];
 #pragma unroll
-        for (int c = 0; c < BQ / 32; ++c) {
-          uint32_t xs[32], xp[32];
-          tmem_ld32x2(tST + 32 * c, tDPT + 32 * c, xs, xp);
-          uint32_t pa[16], pd2[16];
+        for (int e = 0; e < 16; ++e) {
+          float av[2], dv[2];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float av[2], dv[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const float x = __uint_as_float(xs[2 * e + t]) * alpha;
-              const float sg = sigmoid_fast(x);
-              av[t] = x * sg;
-              dv[t] = __uint_as_float(xp[2 * e + t]) * (sg * fmaf(x, 1.f - sg, 1.f));
-              if (need_mask) {
-                const int i = i0 + 32 * c + 2 * e + t;
-                if (!(i < Lq && j < Lk && (!a.causal || j <= i))) { av[t] = 0.f; dv[t] = 0.f; }
-              }
+          for (int t2 = 0; t2 < 2; ++t2) {
+            float sv = __uint_as_float(xs[2 * e + t2]), pv = __uint_as_float(xp[2 * e + t2]);
+            if (need_mask) {
+              const int i = ic + 2 * e + t2;
+              if (i < lo || i >= Lq) { sv = 0.f; pv = 0.f; }
             }
-            pa[e] = pack2<BF16>(av[0], av[1]);
-            pd2[e] = pack2<BF16>(dv[0], dv[1]);
+            const float hh = sv * half_alpha;
+            const float tt = tanh_approx(hh);
+            av[t2] = fmaf(hh, tt, hh);     // SiLU(x)
+            dv[t2] = dsilu2(hh, tt, pv);   // 2 dP^T SiLU'(x)
           }
-          tmem_st16(tAT + b * (BQ / 2) + 16 * c, pa);
-          tmem_st16(tDST + b * (BQ / 2) + 16 * c, pd2);
+          pa[e] = pack2<BF16>(av[0], av[1]);
+          pd[e] = pack2<BF16>(dv[0], dv[1]);
         }
+        tmem_st16(tAT + b * (BQ / 2), pa);
+        tmem_st16(tDST + b * (BQ / 2), pd);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(ASFULL + b));
@@ -273,16 +279,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int c = 0; c < DH / 64; ++c) {
         uint32_t x[32];
-        tmem_ld32(tDV + 32 * c, x);
+        tmem_ld32(tDV + hc * (DH / 2) + 32 * c, x);
         if (row_ok) store_row32<BF16>(dvrow + c * 64, x, a.inv_L);
       }
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int c = 0; c < DH / 64; ++c) {
         uint32_t x[32];
-        tmem_ld32(tDK + 32 * c, x);
-        if (row_ok) store_row32<BF16>(dkrow + c * 64, x, alpha * a.inv_L);
+        tmem_ld32(tDK + hc * (DH / 2) + 32 * c, x);
+        if (row_ok) store_row32<BF16>(dkrow + c * 64, x, dk_scale);
       }
       tc_fence_before();
       mbar_arrive(bar(ACCEMPTY));

@@ -9,7 +9,8 @@
 // once in the fp32 epilogue.
 //   warp 0      TMA: Q and dO per unit, K and V per step.
 //   warp 1      tcgen05 issuer.
-//   warps 2-5   one row each: SiLU' and mask, then the dQ epilogue.
+//   warps 2-9   row work (two warps per TMEM lane quarter, one per column
+//               half): SiLU' and mask, then the dQ epilogue.
 // TMEM: S | dP | dQ | dS0, dS1.
 #include "kernels.h"
 
@@ -24,8 +25,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = DqCfg<D>;
-  constexpr int BN = C::BN, NQ = C::NQ, NS = C::NS, KCH = D / 64;
-  constexpr bool SERIAL = NS == 1;  // one K/V stage: accumulate before the next S
+  constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
+  static_assert(NK >= 2, "the next S is issued before the pending dQ += dS K");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_DQ = idesc_f16(BF16, kBM, D, false, true);
   constexpr uint32_t COL_S = 0, COL_DP = BN, COL_DQ = 2 * BN, COL_DS = 2 * BN + D;
@@ -36,13 +37,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sQ = base;                        // NQ x (Q, dO)
-  const uint32_t sK = sQ + 2 * NQ * C::Q_BYTES;    // NS x K
-  const uint32_t sV = sK + NS * C::KV_BYTES;       // NS x V
+  const uint32_t sK = sQ + 2 * NQ * C::Q_BYTES;    // NK x K
+  const uint32_t sV = sK + NK * C::KV_BYTES;       // NV x V
 
   enum {
-    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, VFULL = KFULL + NS,
-    KVEMPTY = VFULL + NS, SPFULL = KVEMPTY + NS, DSFULL = SPFULL + 1, DQFULL = DSFULL + 2,
-    DQEMPTY = DQFULL + 1, DRAIN = DQEMPTY + 1, NBARS = DRAIN + 1
+    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, KEMPTY = KFULL + NK,
+    VFULL = KEMPTY + NK, VEMPTY = VFULL + NV, SPFULL = VEMPTY + NV, DSFULL = SPFULL + 1,
+    DQFULL = DSFULL + 2, DQEMPTY = DQFULL + 1, DRAIN = DQEMPTY + 1, NBARS = DRAIN + 1
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
@@ -52,14 +53,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(KFULL + i), 1); mbar_init(bar(VFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1);
-    }
+    for (int i = 0; i < NK; ++i) { mbar_init(bar(KFULL + i), 1); mbar_init(bar(KEMPTY + i), 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
     mbar_init(bar(SPFULL), 1);
-    mbar_init(bar(DSFULL), 128);
-    mbar_init(bar(DSFULL + 1), 128);
+    mbar_init(bar(DSFULL), kRowThreads);
+    mbar_init(bar(DSFULL + 1), kRowThreads);
     mbar_init(bar(DQFULL), 1);
-    mbar_init(bar(DQEMPTY), 128);
+    mbar_init(bar(DQEMPTY), kRowThreads);
     mbar_init(bar(DRAIN), 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -81,7 +81,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t qi = 0, kvi = 0;
+      uint32_t qi = 0, ki = 0, vi = 0;
+      auto load_kv = [&](const CUtensorMap* map, uint32_t base_s, int nst, uint32_t& cnt,
+                         int full, int empty, int row, int h, int where) -> bool {
+        const int s = cnt % nst;
+        if (!wait_bar(bar(empty + s), ((cnt / nst) & 1) ^ 1, wc, where)) return false;
+        mbar_arrive_expect_tx(bar(full + s), C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(base_s + s * C::KV_BYTES + c * (BN * 128), map, bar(full + s), 64 * c, h, row);
+        ++cnt;
+        return true;
+      };
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const Unit U = load_unit(a.units, u);
@@ -100,50 +111,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         ++qi;
         for (int n = 0; n < U.n; ++n) {
-          const int s = kvi % NS;
-          if (!wait_bar(bar(KVEMPTY + s), ((kvi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           const int row = kv_row0 + BN * n;
-          mbar_arrive_expect_tx(bar(KFULL + s), C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sK + s * C::KV_BYTES + c * (BN * 128), &tm_k, bar(KFULL + s), 64 * c, h, row);
-          mbar_arrive_expect_tx(bar(VFULL + s), C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sV + s * C::KV_BYTES + c * (BN * 128), &tm_v, bar(VFULL + s), 64 * c, h, row);
-          ++kvi;
+          if (!load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, row, h, 0x002) ||
+              !load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, row, h, 0x003)) {
+            ok = false;
+            break;
+          }
         }
       }
       for (uint32_t i = qi > NQ ? qi - NQ : 0; i < qi; ++i)
         wait_bar(bar(QFULL + i % NQ), (i / NQ) & 1, drain, 0x0f1);
-      for (uint32_t i = kvi > NS ? kvi - NS : 0; i < kvi; ++i) {
-        wait_bar(bar(KFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
-        wait_bar(bar(VFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
-      }
+      for (uint32_t i = ki > NK ? ki - NK : 0; i < ki; ++i)
+        wait_bar(bar(KFULL + i % NK), (i / NK) & 1, drain, 0x0f2);
+      for (uint32_t i = vi > NV ? vi - NV : 0; i < vi; ++i)
+        wait_bar(bar(VFULL + i % NV), (i / NV) & 1, drain, 0x0f3);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Step n: [wait dS_{n-1}] S_n, dP_n, then the pending dQ += dS_{n-1} K_{n-1}.
     if (lane == 0) {
       const uint32_t tS = tmem + COL_S, tDP = tmem + COL_DP, tDQ = tmem + COL_DQ,
                      tDS = tmem + COL_DS;
       struct Pend {
-        int valid, s, b, first, last, qb;
+        int valid, ks, b, first, last;
         uint32_t g, oi;
-      } pd{0, 0, 0, 0, 0, 0, 0, 0};
+      } pd{0, 0, 0, 0, 0, 0, 0};
       // dQ += dS_g K_g (the step's dS has been waited for already)
       auto issue_dq = [&](const Pend& p) -> bool {
         if (p.first && !wait_bar(bar(DQEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
         tc_fence_after();
-        const uint32_t kt = sK + p.s * C::KV_BYTES;
+        const uint32_t kt = sK + p.ks * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tDQ, tDS + p.b * (BN / 2) + kk * 8, desc_mnmajor<BN>(kt, kk, 0), IDESC_DQ,
                  (!p.first || kk > 0) ? 1u : 0u);
-        mma_commit(bar(KVEMPTY + p.s));
+        mma_commit(bar(KEMPTY + p.ks));
         if (p.last) mma_commit(bar(DQFULL));
         return true;
       };
-      uint32_t qi = 0, kvi = 0, g = 0, oi = 0;
+      uint32_t qi = 0, ki = 0, vi = 0, g = 0, oi = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const Unit U = load_unit(a.units, u);
@@ -153,40 +159,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         const uint32_t qt = sQ + qb * 2 * C::Q_BYTES, dot = qt + C::Q_BYTES;
         for (int n = 0; n < U.n; ++n) {
-          const int s = kvi % NS, b = g & 1;
+          const int ks = ki % NK, vs = vi % NV, b = g & 1;
           // S and dP of the previous step must have been read before they are overwritten
           if (pd.valid) {
             if (!wait_bar(bar(DSFULL + pd.b), (pd.g >> 1) & 1, wc, 0x105)) { ok = false; break; }
           }
-          if (!wait_bar(bar(KFULL + s), (kvi / NS) & 1, wc, 0x106)) { ok = false; break; }
+          if (!wait_bar(bar(KFULL + ks), (ki / NK) & 1, wc, 0x106)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sK + s * C::KV_BYTES, vt = sV + s * C::KV_BYTES;
+          const uint32_t kt = sK + ks * C::KV_BYTES, vt = sV + vs * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tS, desc_kmajor<kBM>(qt, kk), desc_kmajor<BN>(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
-          if (!wait_bar(bar(VFULL + s), (kvi / NS) & 1, wc, 0x107)) { ok = false; break; }
+          if (!wait_bar(bar(VFULL + vs), (vi / NV) & 1, wc, 0x107)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tDP, desc_kmajor<kBM>(dot, kk), desc_kmajor<BN>(vt, kk), IDESC_S, kk > 0 ? 1u : 0u);
           mma_commit(bar(SPFULL));
+          mma_commit(bar(VEMPTY + vs));
           if (n == U.n - 1) mma_commit(bar(QEMPTY + qb));
-          Pend cur{1, s, b, n == 0, n == U.n - 1, qb, g, oi};
-          if (SERIAL) {
-            // single K/V stage: the accumulation must free it before the next load
-            if (!wait_bar(bar(DSFULL + b), (g >> 1) & 1, wc, 0x108)) { ok = false; break; }
-            if (!issue_dq(cur)) { ok = false; break; }
-          } else {
-            if (pd.valid && !issue_dq(pd)) { ok = false; break; }
-            pd = cur;
-          }
-          ++kvi;
+          if (pd.valid && !issue_dq(pd)) { ok = false; break; }
+          pd = Pend{1, ks, b, n == 0, n == U.n - 1, g, oi};
+          ++ki;
+          ++vi;
           ++g;
         }
         ++qi;
         ++oi;
       }
-      if (!SERIAL && ok && pd.valid) {
+      if (ok && pd.valid) {
         if (wait_bar(bar(DSFULL + pd.b), (pd.g >> 1) & 1, wc, 0x109)) issue_dq(pd);
       }
       mma_commit(bar(DRAIN));
@@ -194,13 +195,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ SiLU' + epilogue
-    const int wq = warp & 3;
+    // Eight warps: warp w owns TMEM lane quarter w % 4 and one half of the key
+    // columns of each S / dP tile (and of the dQ columns).
+    constexpr int CPW = BN / 2;
+    const int wq = warp & 3, hc = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + COL_S + lane_off, tDP = tmem + COL_DP + lane_off,
-                   tDQ = tmem + COL_DQ + lane_off, tDS = tmem + COL_DS + lane_off;
-    const float alpha = a.alpha;
-    const float out_scale = a.alpha * a.inv_L;
+    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tDP = tmem + COL_DP + lane_off + hc * CPW,
+                   tDQ = tmem + COL_DQ + lane_off, tDS = tmem + COL_DS + lane_off + hc * (CPW / 2);
+    const float half_alpha = 0.5f * a.alpha;
+    const float out_scale = 0.5f * a.alpha * a.inv_L;  // dS is stored doubled
     uint32_t g = 0, oi = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
@@ -210,42 +214,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int Lq = __ldg(a.cu_q + U.b + 1) - q0;
       const int Lk = __ldg(a.cu_k + U.b + 1) - __ldg(a.cu_k + U.b);
       const int i = kBM * U.tile + r;
+      const int i_warp = kBM * U.tile + wq * 32;
       const int64_t grow = static_cast<int64_t>(q0) + i;
       const bool row_ok = i < Lq && grow < a.total_q;
-      char* orow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh) * 2;
+      char* orow = static_cast<char*>(a.o0) +
+                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + hc * (D / 2)) * 2;
       if (U.n <= 0) {
         if (row_ok)
-          for (int c = 0; c < D / 32; ++c) store_zero32(orow + c * 64);
+          for (int c = 0; c < D / 64; ++c) store_zero32(orow + c * 64);
         continue;
       }
+      const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
       for (int n = 0; n < U.n; ++n) {
         const int b = g & 1;
         if (!wait_bar_warp(bar(SPFULL), g & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
-        const int j0 = BN * n;
-        const bool need_mask = (a.causal && j0 + BN - 1 > kBM * U.tile) || (j0 + BN > Lk);
+        const int jc = BN * n + hc * CPW;
+        const bool need_mask = (a.causal && jc + CPW - 1 > i_warp) || (jc + CPW > Lk);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int sc = 0; sc < CPW / 32; ++sc) {
           uint32_t xs[32], xp[32];
-          tmem_ld32x2(tS + 32 * c, tDP + 32 * c, xs, xp);
+          tmem_ld32x2(tS + 32 * sc, tDP + 32 * sc, xs, xp);
           uint32_t d[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float ds[2];
+            float v[2];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const float x = __uint_as_float(xs[2 * e + t]) * alpha;
-              const float sg = sigmoid_fast(x);
-              const float dsilu = sg * fmaf(x, 1.f - sg, 1.f);
-              ds[t] = __uint_as_float(xp[2 * e + t]) * dsilu;
-              if (need_mask) {
-                const int j = j0 + 32 * c + 2 * e + t;
-                if (!(j < Lk && (!a.causal || j <= i))) ds[t] = 0.f;
-              }
+            for (int t2 = 0; t2 < 2; ++t2) {
+              float sv = __uint_as_float(xs[2 * e + t2]), pv = __uint_as_float(xp[2 * e + t2]);
+              if (need_mask && jc + 32 * sc + 2 * e + t2 >= lim) { sv = 0.f; pv = 0.f; }
+              const float hh = sv * half_alpha;
+              v[t2] = dsilu2(hh, tanh_approx(hh), pv);
             }
-            d[e] = pack2<BF16>(ds[0], ds[1]);
+            d[e] = pack2<BF16>(v[0], v[1]);
           }
-          tmem_st16(tDS + b * (BN / 2) + 16 * c, d);
+          tmem_st16(tDS + b * (BN / 2) + 16 * sc, d);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -256,9 +259,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!wait_bar_warp(bar(DQFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t x[32];
-        tmem_ld32(tDQ + 32 * c, x);
+        tmem_ld32(tDQ + hc * (D / 2) + 32 * c, x);
         if (row_ok) store_row32<BF16>(orow + c * 64, x, out_scale);
       }
       tc_fence_before();

@@ -116,6 +116,33 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
   return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
 }
 
+// TMEM column batches of compile-time width: N in {32, 64} loads, {16, 32} stores.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 64) tmem_ld64(taddr, r);
+  else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 32) tmem_st32(taddr, r);
+  else tmem_st16(taddr, r);
+}
+
+// SiLU of two scaled scores, rounded and packed: h = x/2, SiLU(x) = h + h tanh(h).
+template <bool BF16>
+__device__ __forceinline__ uint32_t silu_pair(uint32_t s0, uint32_t s1, float half_alpha) {
+  const float h0 = __uint_as_float(s0) * half_alpha;
+  const float h1 = __uint_as_float(s1) * half_alpha;
+  return pack2<BF16>(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
+}
+
+// Twice the score gradient of one element: with h = x/2 and t = tanh(h),
+// SiLU'(x) = sigmoid(x) (1 + x (1 - sigmoid(x))) = (1 + t)(1 + h (1 - t)) / 2,
+// so 2 dP SiLU'(x) = dP (1 + t)(1 + h (1 - t)); the 1/2 goes to the epilogue.
+__device__ __forceinline__ float dsilu2(float h, float t, float dp) {
+  return dp * (1.f + t) * fmaf(h, 1.f - t, 1.f);
+}
+
 // Store 32 fp32 values (one TMEM chunk of one row) as 32 16-bit elements,
 // scaled by `scale`, with four 16-byte stores.
 template <bool BF16>

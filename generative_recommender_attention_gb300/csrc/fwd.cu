@@ -6,8 +6,9 @@
 //   warp 0      TMA producer: Q tile per unit, K/V tiles per inner step.
 //   warp 1      tcgen05 issuer: S = Q K^T into TMEM (double buffered), then
 //               O += P V with P read straight from TMEM.
-//   warps 2-5   one row each: tcgen05.ld S, alpha scale, SiLU, mask, round to
-//               16 bits, tcgen05.st P; per unit, the epilogue O * (1/L_scale)
+//   warps 2-9   row work, two warps per TMEM lane quarter (one per column
+//               half): tcgen05.ld S, alpha scale, SiLU, mask, round to 16
+//               bits, tcgen05.st P; per unit, the epilogue O * (1/L_scale)
 //               with predicated row stores.
 // No softmax, so no running max or rescale: O simply accumulates in TMEM.
 // Causal units only visit key tiles up to their last row (the scheduler's
@@ -26,7 +27,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = FwdCfg<D>;
-  constexpr int BN = C::BN, NQ = C::NQ, NS = C::NS, KCH = D / 64;
+  constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_PV = idesc_f16(BF16, kBM, D, false, true);
   // TMEM columns: S0, S1 | O | P0, P1 (16-bit P packed two per column)
@@ -39,12 +40,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sK = sQ + NQ * C::Q_BYTES;
-  const uint32_t sV = sK + NS * C::KV_BYTES;
+  const uint32_t sV = sK + NK * C::KV_BYTES;
 
   enum {
-    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, VFULL = KFULL + NS,
-    KVEMPTY = VFULL + NS, SFULL = KVEMPTY + NS, PFULL = SFULL + 2, OFULL = PFULL + 2,
-    OEMPTY = OFULL + 1, DRAIN = OEMPTY + 1, NBARS = DRAIN + 1
+    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, KEMPTY = KFULL + NK,
+    VFULL = KEMPTY + NK, VEMPTY = VFULL + NV, SFULL = VEMPTY + NV, PFULL = SFULL + 2,
+    OFULL = PFULL + 2, OEMPTY = OFULL + 1, DRAIN = OEMPTY + 1, NBARS = DRAIN + 1
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
@@ -54,12 +55,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(KFULL + i), 1); mbar_init(bar(VFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) { mbar_init(bar(SFULL + i), 1); mbar_init(bar(PFULL + i), 128); }
+    for (int i = 0; i < NK; ++i) { mbar_init(bar(KFULL + i), 1); mbar_init(bar(KEMPTY + i), 1); }
+    for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(SFULL + i), 1); mbar_init(bar(PFULL + i), kRowThreads); }
     mbar_init(bar(OFULL), 1);
-    mbar_init(bar(OEMPTY), 128);
+    mbar_init(bar(OEMPTY), kRowThreads);
     mbar_init(bar(DRAIN), 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -79,8 +79,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per unit: Q, K_0, then K_{n+1} ahead of V_n, so K runs one step ahead.
     if (lane == 0) {
-      uint32_t qi = 0, kvi = 0;
+      uint32_t qi = 0, ki = 0, vi = 0;
+      auto load_kv = [&](const CUtensorMap* map, uint32_t base_s, int nst, uint32_t& cnt,
+                         int full, int empty, int row, int h, int where) -> bool {
+        const int s = cnt % nst;
+        if (!wait_bar(bar(empty + s), ((cnt / nst) & 1) ^ 1, wc, where)) return false;
+        mbar_arrive_expect_tx(bar(full + s), C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < KCH; ++c)
+          tma_load_3d(base_s + s * C::KV_BYTES + c * (BN * 128), map, bar(full + s), 64 * c, h, row);
+        ++cnt;
+        return true;
+      };
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const Unit U = load_unit(a.units, u);
@@ -96,52 +108,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(sQ + qb * C::Q_BYTES + c * (kBM * 128), &tm_q, bar(QFULL + qb), 64 * c, h,
                       q_row0);
         ++qi;
+        if (!load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, kv_row0, h, 0x002)) { ok = false; break; }
         for (int n = 0; n < U.n; ++n) {
-          const int s = kvi % NS;
-          if (!wait_bar(bar(KVEMPTY + s), ((kvi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
-          const int row = kv_row0 + BN * n;
-          mbar_arrive_expect_tx(bar(KFULL + s), C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sK + s * C::KV_BYTES + c * (BN * 128), &tm_k, bar(KFULL + s), 64 * c, h, row);
-          mbar_arrive_expect_tx(bar(VFULL + s), C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sV + s * C::KV_BYTES + c * (BN * 128), &tm_v, bar(VFULL + s), 64 * c, h, row);
-          ++kvi;
+          if (n + 1 < U.n &&
+              !load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, kv_row0 + BN * (n + 1), h, 0x002)) {
+            ok = false;
+            break;
+          }
+          if (!load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, kv_row0 + BN * n, h, 0x003)) {
+            ok = false;
+            break;
+          }
         }
       }
       // let the last copies land before the block may exit
       for (uint32_t i = qi > NQ ? qi - NQ : 0; i < qi; ++i)
         wait_bar(bar(QFULL + i % NQ), (i / NQ) & 1, drain, 0x0f1);
-      for (uint32_t i = kvi > NS ? kvi - NS : 0; i < kvi; ++i) {
-        wait_bar(bar(KFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
-        wait_bar(bar(VFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
-      }
+      for (uint32_t i = ki > NK ? ki - NK : 0; i < ki; ++i)
+        wait_bar(bar(KFULL + i % NK), (i / NK) & 1, drain, 0x0f2);
+      for (uint32_t i = vi > NV ? vi - NV : 0; i < vi; ++i)
+        wait_bar(bar(VFULL + i % NV), (i / NV) & 1, drain, 0x0f3);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t tS = tmem + COL_S, tO = tmem + COL_O, tP = tmem + COL_P;
       struct Pend {
-        int valid, s, b, first, last;
-        uint32_t kvi, g, oi;
+        int valid, vs, b, first, last;
+        uint32_t vi, g, oi;
       } pv{0, 0, 0, 0, 0, 0, 0, 0};
       auto issue_pv = [&](const Pend& p) -> bool {
-        if (!wait_bar(bar(VFULL + p.s), (p.kvi / NS) & 1, wc, 0x101)) return false;
+        if (!wait_bar(bar(VFULL + p.vs), (p.vi / NV) & 1, wc, 0x101)) return false;
         if (!wait_bar(bar(PFULL + p.b), (p.g >> 1) & 1, wc, 0x102)) return false;
         if (p.first && !wait_bar(bar(OEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
         tc_fence_after();
-        const uint32_t vt = sV + p.s * C::KV_BYTES;
+        const uint32_t vt = sV + p.vs * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tO, tP + p.b * (BN / 2) + kk * 8, desc_mnmajor<BN>(vt, kk, 0), IDESC_PV,
                  (!p.first || kk > 0) ? 1u : 0u);
-        mma_commit(bar(KVEMPTY + p.s));
+        mma_commit(bar(VEMPTY + p.vs));
         if (p.last) mma_commit(bar(OFULL));
         return true;
       };
-      uint32_t qi = 0, kvi = 0, g = 0, oi = 0;
+      uint32_t qi = 0, ki = 0, vi = 0, g = 0, oi = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const Unit U = load_unit(a.units, u);
@@ -151,19 +161,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         const uint32_t qt = sQ + qb * C::Q_BYTES;
         for (int n = 0; n < U.n; ++n) {
-          const int s = kvi % NS, b = g & 1;
-          if (!wait_bar(bar(KFULL + s), (kvi / NS) & 1, wc, 0x105)) { ok = false; break; }
+          const int ks = ki % NK, b = g & 1;
+          if (!wait_bar(bar(KFULL + ks), (ki / NK) & 1, wc, 0x105)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sK + s * C::KV_BYTES;
+          const uint32_t kt = sK + ks * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tS + b * BN, desc_kmajor<kBM>(qt, kk), desc_kmajor<BN>(kt, kk), IDESC_S,
                    kk > 0 ? 1u : 0u);
           mma_commit(bar(SFULL + b));
+          mma_commit(bar(KEMPTY + ks));
           if (n == U.n - 1) mma_commit(bar(QEMPTY + qb));
           if (pv.valid && !issue_pv(pv)) { ok = false; break; }
-          pv = Pend{1, s, b, n == 0, n == U.n - 1, kvi, g, oi};
-          ++kvi;
+          pv = Pend{1, static_cast<int>(vi % NV), b, n == 0, n == U.n - 1, vi, g, oi};
+          ++ki;
+          ++vi;
           ++g;
         }
         ++qi;
@@ -175,11 +187,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ SiLU + epilogue
-    const int wq = warp & 3;
+    // Eight warps: warp w owns TMEM lane quarter w % 4 (its 32 rows) and one
+    // half of the key columns of each S tile (and of the O columns).
+    constexpr int CPW = BN / 2;
+    const int wq = warp & 3, hc = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + COL_S + lane_off, tO = tmem + COL_O + lane_off,
-                   tP = tmem + COL_P + lane_off;
+    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tO = tmem + COL_O + lane_off,
+                   tP = tmem + COL_P + lane_off + hc * (CPW / 2);
     const float half_alpha = 0.5f * a.alpha;
     uint32_t g = 0, oi = 0;
     bool ok = true;
@@ -190,40 +205,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int Lq = __ldg(a.cu_q + U.b + 1) - q0;
       const int Lk = __ldg(a.cu_k + U.b + 1) - __ldg(a.cu_k + U.b);
       const int i = kBM * U.tile + r;
+      const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
       const int64_t grow = static_cast<int64_t>(q0) + i;
       const bool row_ok = i < Lq && grow < a.total_q;
-      char* orow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh) * 2;
+      char* orow = static_cast<char*>(a.o0) +
+                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + hc * (D / 2)) * 2;
       if (U.n <= 0) {
         if (row_ok)
-          for (int c = 0; c < D / 32; ++c) store_zero32(orow + c * 64);
+          for (int c = 0; c < D / 64; ++c) store_zero32(orow + c * 64);
         continue;
       }
       for (int n = 0; n < U.n; ++n) {
         const int sb = g & 1;
         if (!wait_bar_warp(bar(SFULL + sb), (g >> 1) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
-        const int j0 = BN * n;
-        const bool need_mask = (a.causal && j0 + BN - 1 > kBM * U.tile) || (j0 + BN > Lk);
+        const int jc = BN * n + hc * CPW;  // first key of this warp's columns
+        const bool need_mask = (a.causal && jc + CPW - 1 > i_warp) || (jc + CPW > Lk);
+        uint32_t x[CPW];
+        tmem_ld_n<CPW>(tS + sb * BN, x);
+        uint32_t p[CPW / 2];
+        if (!need_mask) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tS + sb * BN + 32 * c, x);
-          uint32_t p[16];
+          for (int e = 0; e < CPW / 2; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
+        } else {
+          const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float h0 = __uint_as_float(x[2 * e]) * half_alpha;
-            const float h1 = __uint_as_float(x[2 * e + 1]) * half_alpha;
-            float p0 = fmaf(h0, tanh_approx(h0), h0);
-            float p1 = fmaf(h1, tanh_approx(h1), h1);
-            if (need_mask) {
-              const int j = j0 + 32 * c + 2 * e;
-              if (!(j < Lk && (!a.causal || j <= i))) p0 = 0.f;
-              if (!(j + 1 < Lk && (!a.causal || j + 1 <= i))) p1 = 0.f;
-            }
-            p[e] = pack2<BF16>(p0, p1);
+          for (int e = 0; e < CPW / 2; ++e) {
+            const int j = jc + 2 * e;
+            const uint32_t s0 = j < lim ? x[2 * e] : 0u;          // SiLU(0) = 0
+            const uint32_t s1 = j + 1 < lim ? x[2 * e + 1] : 0u;
+            p[e] = silu_pair<BF16>(s0, s1, half_alpha);
           }
-          tmem_st16(tP + sb * (BN / 2) + 16 * c, p);
         }
+        tmem_st_n<CPW / 2>(tP + sb * (BN / 2), p);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(PFULL + sb));
@@ -233,9 +247,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!wait_bar_warp(bar(OFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t x[32];
-        tmem_ld32(tO + 32 * c, x);
+        tmem_ld32(tO + hc * (D / 2) + 32 * c, x);
         if (row_ok) store_row32<BF16>(orow + c * 64, x, a.inv_L);
       }
       tc_fence_before();

@@ -11,7 +11,8 @@
 namespace hstu {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kAttnThreads = 192;   // warp 0: TMA, warp 1: MMA, warps 2-5: SiLU/epilogue
+constexpr int kAttnThreads = 320;   // warp 0: TMA, warp 1: MMA, warps 2-9: row work
+constexpr int kRowThreads = 256;    // two warps per TMEM lane quarter, one per column half
 constexpr int kTmemCols = 512;
 
 // Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
@@ -49,26 +50,31 @@ struct AttnArgs {
 };
 
 // ------------------------------------------------------------ forward config
+// Separate K and V rings: a K stage frees as soon as S = Q K^T completes, a V
+// stage only after O += P V, so K runs further ahead.
 template <int D>
 struct FwdCfg {
   static constexpr int BN = D == 256 ? 64 : 128;     // keys per inner tile
   static constexpr int NQ = D == 256 ? 1 : 2;        // Q buffers
-  static constexpr int NS = D == 64 ? 4 : 2;         // K/V stages
+  static constexpr int NK = D == 64 ? 6 : 3;         // K stages
+  static constexpr int NV = D == 64 ? 4 : 2;         // V stages
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int TILE_BYTES = NQ * Q_BYTES + 2 * NS * KV_BYTES;
+  static constexpr int TILE_BYTES = NQ * Q_BYTES + (NK + NV) * KV_BYTES;
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
 };
 
 // ------------------------------------------------------------ dQ config
+// K is read by S = Q K^T and by dQ += dS K (freed last); V only by dP = dO V^T.
 template <int D>
 struct DqCfg {
   static constexpr int BN = D == 256 ? 64 : 128;
   static constexpr int NQ = D == 64 ? 2 : 1;         // (Q, dO) buffers
-  static constexpr int NS = D == 64 ? 4 : (D == 128 ? 2 : 1);
+  static constexpr int NK = D == 64 ? 5 : (D == 128 ? 3 : 2);
+  static constexpr int NV = D == 64 ? 3 : (D == 128 ? 2 : 1);
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + 2 * NS * KV_BYTES;
+  static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + (NK + NV) * KV_BYTES;
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
 };
 

@@ -129,6 +129,35 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
                             int32_t scaling_seqlen, int32_t causal, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Profiling variants: identical to hstu_attn_fwd / hstu_attn_bwd (same
+ * arguments, results and errors), and they additionally record the first
+ * `n_events` of these caller-created CUDA events on `stream`:
+ *   forward:  events[0] before the scheduler launch, events[1] after it,
+ *             events[2] after the forward kernel;
+ *   backward: events[0] before the scheduler launch, events[1] after it,
+ *             events[2] after the dQ kernel, events[3] after the dK/dV kernel.
+ * Elapsed times between consecutive events are per-kernel device times.
+ * events must be non-null (HSTU_ERR_INVALID_ARG otherwise).
+ */
+hstu_status_t hstu_attn_fwd_profiled(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream,
+                                     cudaEvent_t* events, int32_t n_events);
+hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k,
+                                     hstu_cten_t v, hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                     int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                     int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream,
+                                     cudaEvent_t* events, int32_t n_events);
+
 /* Static text for a status code. */
 const char* hstu_attn_status_string(hstu_status_t status);
 
