@@ -24,7 +24,7 @@ STATUS = {0: "HSTU_OK", 1: "HSTU_ERR_INVALID_ARG", 2: "HSTU_ERR_UNSUPPORTED",
 EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_attn_bwd_profiled",
            "hstu_attn_workspace_size",
            "hstu_attn_status_string", "hstu_attn_last_device_status",
-           "hstu_attn_selftest_timeout", "hstu_attn_version")
+           "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc")
 
 
 class CTen(ctypes.Structure):
@@ -74,6 +74,8 @@ def _declare(lib):
     lib.hstu_attn_last_device_status.restype = ctypes.c_int
     lib.hstu_attn_selftest_timeout.argtypes = [P, ctypes.c_uint32, P]
     lib.hstu_attn_selftest_timeout.restype = ctypes.c_int
+    lib.hstu_attn_fwd_noalloc.argtypes = [CTen, CTen, CTen, Ten] + scal[:13] + [P]
+    lib.hstu_attn_fwd_noalloc.restype = ctypes.c_int
     lib.hstu_attn_version.argtypes = []
     lib.hstu_attn_version.restype = i32
 

@@ -425,3 +425,54 @@ hstu_status_t hstu_attn_selftest_timeout(void* workspace, uint32_t timeout_us, c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation forward
+// Some callers cannot allocate device memory when they call us: for example a
+// plugin inside an inference engine whose execute hook only receives buffers
+// the engine planned in advance, or a service that fixes its device-memory
+// budget at start-up and forbids allocation afterwards.  Such a caller cannot
+// provide the workspace hstu_attn_fwd asks for.  This variant keeps that
+// workspace (the tile schedule and the status words) in a fixed-size array
+// in the library's own device memory instead; every GPU that loads the
+// library holds one such array until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB: up to 65,520 work units
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (host code may not use the symbol's name as a device pointer).
+bool noalloc_scratch(void** out) {
+  static void* ptr[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return false;
+    ptr[dev] = p;
+  }
+  *out = ptr[dev];
+  return true;
+}
+
+}  // namespace
+
+extern "C" hstu_status_t hstu_attn_fwd_noalloc(
+    hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q, int64_t total_k,
+    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+    int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen, int32_t causal,
+    cudaStream_t stream) {
+  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim, 0);
+  if (need == 0) return supported_dim(head_dim) ? HSTU_ERR_INVALID_ARG : HSTU_ERR_UNSUPPORTED;
+  if (need > kNoAllocScratchBytes) return HSTU_ERR_INVALID_ARG;  // schedule would not fit
+  void* scratch = nullptr;
+  if (!noalloc_scratch(&scratch)) return HSTU_ERR_CUDA;
+  // The scheduler kernel rewrites the header and the whole work list at the
+  // start of every call, so nothing in the array has to be cleared first.
+  return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  scratch, kNoAllocScratchBytes, stream, EventMarks{nullptr, 0});
+}

@@ -158,6 +158,33 @@ hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_
                                      size_t workspace_bytes, cudaStream_t stream,
                                      cudaEvent_t* events, int32_t n_events);
 
+/*
+ * Forward without a workspace argument; it allocates nothing.  The pages
+ * have no counterpart: it exists for callers that cannot allocate device
+ * memory when they call in (e.g. a plugin of an inference engine whose
+ * execute hook only gets buffers planned ahead, or a service that fixes its
+ * memory budget at start-up) and so cannot pass the workspace hstu_attn_fwd
+ * needs.  Arguments and results are those of hstu_attn_fwd; the caller still
+ * passes every input and output.
+ *
+ * The schedule lives in a 1 MiB array in the library's own device memory
+ * (one per GPU that loads the library, held until exit).  Problems whose
+ * schedule exceeds it, hstu_attn_workspace_size(..., is_bwd = 0) > 1 MiB,
+ * i.e. more than 65,520 work units (num_heads * (ceil(total_q / 128) + batch)),
+ * return HSTU_ERR_INVALID_ARG.  The first call on a device looks the array's
+ * address up (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the one array and each
+ * call rewrites it from the start, so calls that can overlap on the GPU (for
+ * example on two streams) race: serialize them.  Uses no cudaMalloc, no
+ * cudaFree and no allocating library routine.
+ */
+hstu_status_t hstu_attn_fwd_noalloc(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t batch, int64_t total_q, int64_t total_k,
+                                    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                    int32_t scaling_seqlen, int32_t causal, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* hstu_attn_status_string(hstu_status_t status);
 
