@@ -72,7 +72,7 @@ class ClockSampler:
             self.f = open(path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}", "--format=csv,noheader",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -171,8 +171,8 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
@@ -214,23 +214,21 @@ def main():
     mq, mk = x["max_seqlen_q"], x["max_seqlen_k"]
     flush = None if args.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)]
-          for _ in range(args.warmup + args.steps)]
-    for row in ev:
-        for e in row:
-            e.record()   # creates the events before they are handed to the library
-    torch.cuda.synchronize()
-
-    def step(evs):
+    def step(evs=None):
         hstu.hstu_attn_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], mq, mk,
-                           out=o, workspace=ws_f, events=evs[0:3], **kw)
+                           out=o, workspace=ws_f, events=None if evs is None else evs[0:3], **kw)
         hstu.hstu_attn_bwd(d["do"], d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"],
-                           mq, mk, dq=dq, dk=dk, dv=dv, workspace=ws_b, events=evs[3:7], **kw)
+                           mq, mk, dq=dq, dk=dk, dv=dv, workspace=ws_b,
+                           events=None if evs is None else evs[3:7], **kw)
 
+    # Timed region: whole steps between two events each; no events between the
+    # kernels, so each grid may launch while its predecessor drains.
+    e_beg = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.warmup):
         if flush is not None:
             flush.zero_()
-        step(ev[i])
+        step()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -238,24 +236,39 @@ def main():
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
         if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/hstu_clocks.csv")
     wall0 = time.perf_counter()
-    for i in range(args.warmup, args.warmup + args.steps):
+    for i in range(args.steps):
         if flush is not None:
             flush.zero_()
-        step(ev[i])
+        e_beg[i].record()
+        step()
+        e_end[i].record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
     assert hstu.last_device_status(ws_b) == 0 and hstu.last_device_status(ws_f) == 0
+    t_step = [b.elapsed_time(e) for b, e in zip(e_beg, e_end)]
 
-    timed = ev[args.warmup:]
+    # Per-kernel pass: events between the kernels (one launch each, in
+    # sequence), for the roofline of the dominant kernel.
+    n_prof = max(3, min(args.steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_prof + 1)]
+    for row in ev:
+        for e in row:
+            e.record()   # creates the events before they are handed to the library
+    torch.cuda.synchronize()
+    for row in ev:
+        if flush is not None:
+            flush.zero_()
+        step(row)
+    torch.cuda.synchronize()
+    timed = ev[1:]
     t_sched_f = [r[0].elapsed_time(r[1]) for r in timed]
     t_fwd = [r[1].elapsed_time(r[2]) for r in timed]
     t_sched_b = [r[3].elapsed_time(r[4]) for r in timed]
     t_dq = [r[4].elapsed_time(r[5]) for r in timed]
     t_dkdv = [r[5].elapsed_time(r[6]) for r in timed]
-    t_step = [r[0].elapsed_time(r[2]) + r[3].elapsed_time(r[6]) for r in timed]
     ms_total = sum(t_step)
     if dist is not None:
         t = torch.tensor([ms_total], device=dev)
@@ -321,7 +334,11 @@ def main():
                        flops_per_step=flops_step, peaks_source=pk["source"]),
         "per_kernel_ms": {"sched_fwd": mean(t_sched_f), "fwd": mean(t_fwd),
                           "sched_bwd": mean(t_sched_b), "bwd_dq": mean(t_dq),
-                          "bwd_dkdv": mean(t_dkdv)},
+                          "bwd_dkdv": mean(t_dkdv),
+                          "sum": mean([a + b + c + e + f for a, b, c, e, f in
+                                       zip(t_sched_f, t_fwd, t_sched_b, t_dq, t_dkdv)]),
+                          "steps": len(timed),
+                          "note": "second pass with events between kernels (no launch overlap)"},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops_sustained"], "traffic": traffic,

@@ -192,6 +192,9 @@ namespace {
 struct EventMarks {
   cudaEvent_t* ev;
   int n;
+  // Events between the kernels would serialise them: chain the grids with
+  // programmatic dependent launch only when no events are recorded.
+  bool pdl() const { return ev == nullptr; }
   bool mark(int i, cudaStream_t st) const {
     return ev == nullptr || i >= n || cudaEventRecord(ev[i], st) == cudaSuccess;
   }
@@ -249,10 +252,12 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   AttnArgs a{};
   a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
-  a.units = units; a.units_slot = kHdrUnitsA; a.timeout_ns = kWaitTimeoutNs;
+  a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
+  a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
   const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-  if (launch_fwd(D, c.bf16, grid, stream, tq, tk, tv, a) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (launch_fwd(D, c.bf16, grid, stream, em.pdl(), tq, tk, tv, a) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
 }
@@ -283,7 +288,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
-  const int BN = bn_for(D);
+  const int BN = DqCfg<64>::BN;  // dQ kernel key tile (same for every D)
   const int BQ = DkdvCfg<64>::BQ;
   const int split = D == 256 ? 2 : 1;
   const int64_t capA = cap_a(batch, total_q, H);
@@ -326,20 +331,25 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   a.timeout_ns = kWaitTimeoutNs;
   if (total_q > 0) {
     AttnArgs aq = a;
-    aq.units = unitsA; aq.units_slot = kHdrUnitsA;
+    aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA; aq.pdl_wait = 1;
     aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
     const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-    if (launch_dq(D, c.bf16, grid, stream, m_q128, m_do128, m_kbn, m_vbn, aq) != cudaSuccess)
+    if (launch_dq(D, c.bf16, grid, stream, em.pdl(), m_q128, m_do128, m_kbn, m_vbn, aq) !=
+        cudaSuccess)
       return HSTU_ERR_CUDA;
   }
   if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
   if (total_k > 0) {
     AttnArgs ak = a;
-    ak.units = unitsB; ak.units_slot = kHdrUnitsB;
+    ak.units = unitsB; ak.units_slot = kHdrUnitsB; ak.next_slot = kHdrNextB;
+    // Beside a running dQ grid (which already waited for the scheduler) the
+    // dK/dV grid needs no wait before it starts; alone, it waits first.
+    ak.pdl_wait = total_q > 0 ? 2 : 1;
     ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
     ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
     const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capB));
-    if (launch_dkdv(D, c.bf16, grid, stream, m_k128, m_v128, m_q64, m_do64, ak) != cudaSuccess)
+    if (launch_dkdv(D, c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64, ak) !=
+        cudaSuccess)
       return HSTU_ERR_CUDA;
   }
   if (!em.mark(3, stream)) return HSTU_ERR_CUDA;
@@ -411,7 +421,7 @@ hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t s
       cudaStreamSynchronize(stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   if (h[kHdrStatus] != 0) return static_cast<hstu_status_t>(h[kHdrStatus]);
-  if (h[kHdrOverflow] != 0 || h[kHdrOverflow + 1] != 0) return HSTU_ERR_INVALID_ARG;
+  if (h[kHdrOverflow] != 0 || h[kHdrOverflowB] != 0) return HSTU_ERR_INVALID_ARG;
   return HSTU_OK;
 }
 

@@ -19,7 +19,10 @@ enum HeaderWord : int {
   kHdrUnitsA = 1,     // number of units in list A
   kHdrUnitsB = 2,     // number of units in list B
   kHdrWhere = 3,      // which wait gave up (role * 256 + barrier id), for debugging
-  kHdrOverflow = 4,   // units dropped because the metadata exceeded the totals
+  kHdrOverflow = 4,   // units dropped because the metadata exceeded the totals (list A)
+  kHdrOverflowB = 5,  // same, list B
+  kHdrNextA = 6,      // next unclaimed unit of list A (atomic counter)
+  kHdrNextB = 7,      // next unclaimed unit of list B
 };
 constexpr int kHeaderBytes = 256;
 constexpr int kStatusTimeout = 5;     // == HSTU_ERR_DEVICE_TIMEOUT
@@ -52,17 +55,21 @@ struct WaitCtl {
   uint64_t timeout_ns;
 };
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c,
-                                       int where) {
+// The slow path takes its controls by value so that nothing is spilled to
+// the stack (local memory misses a nearly cache-less L1 when shared memory
+// takes the whole carve-out).
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, int* status,
+                                              volatile int* abort_flag, uint64_t timeout_ns,
+                                              int where) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u) {
-      if (*c.abort_flag) return false;
-      if (globaltimer_ns() - t0 > c.timeout_ns) {
-        *c.abort_flag = 1;
-        atomicCAS(c.status + kHdrStatus, 0, kStatusTimeout);
-        atomicExch(c.status + kHdrWhere, where);
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicCAS(status + kHdrStatus, 0, kStatusTimeout);
+        atomicExch(status + kHdrWhere, where);
         return false;
       }
     }
@@ -72,8 +79,31 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                          int where) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, c, where);
+  return wait_slow(bar, parity, c.status, c.abort_flag, c.timeout_ns, where);
 }
+
+// Work-unit record plus the packed-sequence offsets and lengths it needs,
+// loaded together so a role can prefetch the next unit while it works on
+// the current one (the loads are independent global reads).
+struct UnitInfo {
+  int b, tile, hz, n;
+  int q0, Lq, k0, Lk;
+};
+
+__device__ __forceinline__ UnitInfo load_unit_info(const int4* units, const int32_t* cu_q,
+                                                   const int32_t* cu_k, int u, int n_units) {
+  UnitInfo r{0, 0, 0, -1, 0, 0, 0, 0};  // n = -1: no more units
+  if (u < n_units) {
+    const int4 v = units[u];
+    r.b = v.x; r.tile = v.y; r.hz = v.z; r.n = v.w;
+    r.q0 = cu_q[v.x];
+    r.Lq = cu_q[v.x + 1] - r.q0;
+    r.k0 = cu_k[v.x];
+    r.Lk = cu_k[v.x + 1] - r.k0;
+  }
+  return r;
+}
+
 
 // Warp-uniform wait for the four row warps: lane 0 polls with the bounded
 // wait and broadcasts the outcome, so a give-up never splits a warp in front
@@ -90,6 +120,59 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     }
   }
   return ok;
+}
+
+// ---------------------------------------------------------------- dynamic units
+// The producer thread claims units from the work list with an atomic counter
+// (so a CTA that finishes early takes the next unit, longest first) and hands
+// each one to the MMA thread and the row warps through a small ring in
+// shared memory.  An entry with n = -1 ends the stream.
+constexpr int kUnitRing = 4;
+constexpr int kUnitConsumers = 9;  // the MMA thread + one arrival per row warp (8)
+
+struct UnitQueue {
+  UnitInfo* ring;       // kUnitRing entries in shared memory
+  uint32_t full, empty; // first barrier of each kUnitRing-long barrier array
+};
+
+// Producer: publish unit k (waits until consumers released the slot's last use).
+__device__ __forceinline__ bool unit_push(const UnitQueue& q, uint32_t k, const UnitInfo& u,
+                                          const WaitCtl& wc) {
+  const uint32_t s = k % kUnitRing;
+  if (!wait_bar(q.empty + 8 * s, ((k / kUnitRing) & 1) ^ 1, wc, 0x00a)) return false;
+  q.ring[s] = u;
+  mbar_arrive(q.full + 8 * s);
+  return true;
+}
+
+// Single consumer thread (the MMA issuer).
+__device__ __forceinline__ bool unit_pop(const UnitQueue& q, uint32_t k, UnitInfo& u,
+                                         const WaitCtl& wc) {
+  const uint32_t s = k % kUnitRing;
+  if (!wait_bar(q.full + 8 * s, (k / kUnitRing) & 1, wc, 0x10a)) return false;
+  u = q.ring[s];
+  mbar_arrive(q.empty + 8 * s);
+  return true;
+}
+
+// Whole row warp (warp-uniform); lane 0 releases the slot for the warp.
+__device__ __forceinline__ bool unit_pop_warp(const UnitQueue& q, uint32_t k, UnitInfo& u,
+                                              const WaitCtl& wc) {
+  const uint32_t s = k % kUnitRing;
+  if (!wait_bar_warp(q.full + 8 * s, (k / kUnitRing) & 1, wc, 0x20a)) return false;
+  u = q.ring[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(q.empty + 8 * s);
+  return true;
+}
+
+// Programmatic dependent launch: wait for the grid this one depends on (its
+// writes become visible), and let the next dependent grid start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- conversion
@@ -139,8 +222,31 @@ __device__ __forceinline__ uint32_t silu_pair(uint32_t s0, uint32_t s1, float ha
 // Twice the score gradient of one element: with h = x/2 and t = tanh(h),
 // SiLU'(x) = sigmoid(x) (1 + x (1 - sigmoid(x))) = (1 + t)(1 + h (1 - t)) / 2,
 // so 2 dP SiLU'(x) = dP (1 + t)(1 + h (1 - t)); the 1/2 goes to the epilogue.
+// Equivalently 2 SiLU'(x) = 1 + t + h (1 - t^2): three FMAs.
 __device__ __forceinline__ float dsilu2(float h, float t, float dp) {
-  return dp * (1.f + t) * fmaf(h, 1.f - t, 1.f);
+  const float a = fmaf(-t, t, 1.f);  // 1 - t^2
+  const float v = fmaf(h, a, t);     // t + h (1 - t^2)
+  return fmaf(dp, v, dp);            // dp (1 + v)
+}
+
+// dS pair (doubled) from raw scores s and dP of two elements; a masked
+// element enters as s = dP = 0 and leaves as exactly 0.
+template <bool BF16>
+__device__ __forceinline__ uint32_t ds_pair(uint32_t s0, uint32_t s1, uint32_t p0, uint32_t p1,
+                                            float half_alpha) {
+  const float h0 = __uint_as_float(s0) * half_alpha, h1 = __uint_as_float(s1) * half_alpha;
+  return pack2<BF16>(dsilu2(h0, tanh_approx(h0), __uint_as_float(p0)),
+                     dsilu2(h1, tanh_approx(h1), __uint_as_float(p1)));
+}
+
+// A^T pair (SiLU) and dS^T pair (doubled) of two elements sharing one tanh each.
+template <bool BF16>
+__device__ __forceinline__ void a_ds_pair(uint32_t s0, uint32_t s1, uint32_t p0, uint32_t p1,
+                                          float half_alpha, uint32_t& a, uint32_t& d) {
+  const float h0 = __uint_as_float(s0) * half_alpha, h1 = __uint_as_float(s1) * half_alpha;
+  const float t0 = tanh_approx(h0), t1 = tanh_approx(h1);
+  a = pack2<BF16>(fmaf(h0, t0, h0), fmaf(h1, t1, h1));
+  d = pack2<BF16>(dsilu2(h0, t0, __uint_as_float(p0)), dsilu2(h1, t1, __uint_as_float(p1)));
 }
 
 // Store 32 fp32 values (one TMEM chunk of one row) as 32 16-bit elements,
@@ -169,22 +275,26 @@ __device__ __forceinline__ void store_zero32(void* dst) {
 // K-major operand descriptor: tile of ROWS rows by D columns, stored as D/64
 // chunks of [ROWS][64] 16-bit elements with the 128-byte swizzle (the TMA box
 // layout).  kk selects the 16-element K step.
+// `base` is kdesc(tile).
+__device__ __forceinline__ SDesc kdesc(uint32_t tile) { return sdesc_split(tile, 16, 1024); }
 template <int ROWS>
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
-  const uint32_t addr = tile + static_cast<uint32_t>(kk >> 2) * (ROWS * 128) +
-                        static_cast<uint32_t>(kk & 3) * 32;
-  return sdesc_sw128(addr, 16, 1024);
+__device__ __forceinline__ SDesc desc_kmajor(SDesc base, int kk) {
+  return sdesc_add(base, static_cast<uint32_t>(kk >> 2) * (ROWS * 128) +
+                             static_cast<uint32_t>(kk & 3) * 32);
 }
 
 // MN-major B operand read from the same tile layout: K runs down the ROWS
 // (16 rows per step kk), N runs along the columns starting at column n0
 // (a multiple of 64); 64-column chunks are ROWS*128 bytes apart (LBO) and
-// 8-row groups 1024 bytes apart (SBO).
+// 8-row groups 1024 bytes apart (SBO).  `base` is mndesc<ROWS>(tile).
 template <int ROWS>
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, int n0) {
-  const uint32_t addr = tile + static_cast<uint32_t>(n0 >> 6) * (ROWS * 128) +
-                        static_cast<uint32_t>(kk) * 2048;
-  return sdesc_sw128(addr, ROWS * 128, 1024);
+__device__ __forceinline__ SDesc mndesc(uint32_t tile) {
+  return sdesc_split(tile, ROWS * 128, 1024);
+}
+template <int ROWS>
+__device__ __forceinline__ SDesc desc_mnmajor(SDesc base, int kk, int n0) {
+  return sdesc_add(base, static_cast<uint32_t>(n0 >> 6) * (ROWS * 128) +
+                             static_cast<uint32_t>(kk) * 2048);
 }
 
 }  // namespace hstu

@@ -3,18 +3,29 @@
 //
 // Persistent, warp-specialised kernel; one CTA per SM walks the longest-first
 // list of 128-row query tiles written by the scheduler kernel.
-//   warp 0      TMA producer: Q tile per unit, K/V tiles per inner step.
-//   warp 1      tcgen05 issuer: S = Q K^T into TMEM (double buffered), then
-//               O += P V with P read straight from TMEM.
+//   warp 0      TMA producer: Q tile per unit, K_{n+1} ahead of V_n.
+//   warp 1      tcgen05 issuer.  S tiles live in three TMEM buffers and run
+//               two steps ahead: S_{g+2} = Q K^T is queued before
+//               O += P_g V_g, so the tensor pipe has independent work while
+//               the row warps turn S_g into P_g.
 //   warps 2-9   row work, two warps per TMEM lane quarter (one per column
 //               half): tcgen05.ld S, alpha scale, SiLU, mask, round to 16
-//               bits, tcgen05.st P; per unit, the epilogue O * (1/L_scale)
-//               with predicated row stores.
+//               bits, tcgen05.st P in place over the S columns the warp just
+//               read; per unit, the epilogue O * (1/L_scale) with predicated
+//               row stores.
 // No softmax, so no running max or rescale: O simply accumulates in TMEM.
 // Causal units only visit key tiles up to their last row (the scheduler's
 // cost); masked entries are set to exactly 0, never -inf, since SiLU(-inf)
 // is NaN.  Rows of a tile past the sequence end are computed but not stored;
 // keys past it are masked, and past the tensor end TMA fills zeros.
+//
+// K_g and S_g share ring slot g % 3: S_g completing frees K_g, so the producer
+// waits on the S barrier instead of a separate K-empty barrier.
+//
+// P overwrites its own S buffer, which S_{g+3} overwrites again.  S_{g+3} is
+// issued by the same thread after O += P_g V_g, and tcgen05.mma operations
+// from one thread execute in issue order, so P_g is consumed before it is
+// overwritten.
 #include "kernels.h"
 
 namespace hstu {
@@ -28,11 +39,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = FwdCfg<D>;
   constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
+  constexpr int NSB = 3;        // S buffers in TMEM
+  constexpr int LA = NSB - 1;   // S tiles issued ahead of their P V
+  constexpr int CPW = BN / 2;   // S columns per row warp
+  static_assert(NK == NSB, "K slot g % NSB is freed by the S_g barrier");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_PV = idesc_f16(BF16, kBM, D, false, true);
-  // TMEM columns: S0, S1 | O | P0, P1 (16-bit P packed two per column)
-  constexpr uint32_t COL_S = 0, COL_O = 2 * BN, COL_P = 2 * BN + D;
-  static_assert(COL_P + BN <= kTmemCols, "TMEM budget");
+  // TMEM columns: S0 | S1 | S2 | O.  P_g is packed two per column into the
+  // first half of each warp's own S columns.
+  constexpr uint32_t COL_S = 0, COL_O = NSB * BN;
+  static_assert(COL_O + D <= kTmemCols, "TMEM budget");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -43,10 +59,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sV = sK + NK * C::KV_BYTES;
 
   enum {
-    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, KEMPTY = KFULL + NK,
-    VFULL = KEMPTY + NK, VEMPTY = VFULL + NV, SFULL = VEMPTY + NV, PFULL = SFULL + 2,
-    OFULL = PFULL + 2, OEMPTY = OFULL + 1, DRAIN = OEMPTY + 1, NBARS = DRAIN + 1
+    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ,
+    VFULL = KFULL + NK, VEMPTY = VFULL + NV, SFULL = VEMPTY + NV, PFULL = SFULL + NSB,
+    OFULL = PFULL + NSB, OEMPTY = OFULL + 1, UFULL = OEMPTY + 1, UEMPTY = UFULL + kUnitRing,
+    DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
   };
+  // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
+  static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0] abort, [1] 0
@@ -55,11 +74,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
-    for (int i = 0; i < NK; ++i) { mbar_init(bar(KFULL + i), 1); mbar_init(bar(KEMPTY + i), 1); }
+    for (int i = 0; i < NK; ++i) mbar_init(bar(KFULL + i), 1);
     for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(bar(SFULL + i), 1); mbar_init(bar(PFULL + i), kRowThreads); }
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(bar(SFULL + i), 1);
+      mbar_init(bar(PFULL + i), kRowThreads);
+    }
     mbar_init(bar(OFULL), 1);
     mbar_init(bar(OEMPTY), kRowThreads);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(bar(UFULL + i), 1);
+      mbar_init(bar(UEMPTY + i), kUnitConsumers);
+    }
     mbar_init(bar(DRAIN), 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -75,7 +101,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{a.header, flags, a.timeout_ns};
   const WaitCtl drain{a.header, flags + 1, a.timeout_ns};
+  // everything below reads what earlier grids wrote (work list, inputs)
+  if (a.pdl_wait == 1) grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int n_units = *reinterpret_cast<volatile int*>(a.header + a.units_slot);
+  const UnitQueue uq{reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4)), bar(UFULL), bar(UEMPTY)};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -94,12 +124,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         return true;
       };
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit U = load_unit(a.units, u);
+      // claim units one ahead: the next claim overlaps this unit's loads
+      UnitInfo nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1),
+                                   n_units);
+      for (uint32_t uk = 0; ok; ++uk) {
+        const UnitInfo U = nx;
+        if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
+        if (U.n < 0) break;
+        nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz;
-        const int q_row0 = __ldg(a.cu_q + U.b) + kBM * U.tile;
-        const int kv_row0 = __ldg(a.cu_k + U.b);
+        const int q_row0 = U.q0 + kBM * U.tile;
+        const int kv_row0 = U.k0;
         const int qb = qi % NQ;
         if (!wait_bar(bar(QEMPTY + qb), ((qi / NQ) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(QFULL + qb), C::Q_BYTES);
@@ -108,10 +144,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(sQ + qb * C::Q_BYTES + c * (kBM * 128), &tm_q, bar(QFULL + qb), 64 * c, h,
                       q_row0);
         ++qi;
-        if (!load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, kv_row0, h, 0x002)) { ok = false; break; }
+        if (!load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, kv_row0, h, 0x002)) { ok = false; break; }
         for (int n = 0; n < U.n; ++n) {
           if (n + 1 < U.n &&
-              !load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, kv_row0 + BN * (n + 1), h, 0x002)) {
+              !load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, kv_row0 + BN * (n + 1), h, 0x002)) {
             ok = false;
             break;
           }
@@ -131,49 +167,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One flat stream of steps g over all of this CTA's units.  Issue order:
+    // S_{g}, then O += P_{g-LA} V_{g-LA}.
     if (lane == 0) {
-      const uint32_t tS = tmem + COL_S, tO = tmem + COL_O, tP = tmem + COL_P;
-      struct Pend {
-        int valid, vs, b, first, last;
-        uint32_t vi, g, oi;
-      } pv{0, 0, 0, 0, 0, 0, 0, 0};
-      auto issue_pv = [&](const Pend& p) -> bool {
-        if (!wait_bar(bar(VFULL + p.vs), (p.vi / NV) & 1, wc, 0x101)) return false;
-        if (!wait_bar(bar(PFULL + p.b), (p.g >> 1) & 1, wc, 0x102)) return false;
+      const uint32_t tO = tmem + COL_O;
+      struct Step {
+        uint32_t g, vi, oi;
+        int first, last;
+      };
+      static_assert(LA == 2, "two pending steps kept in registers");
+      Step p0{}, p1{};
+      int npend = 0;
+      auto issue_pv = [&](const Step& p) -> bool {
+        const int vs = p.vi % NV, sb = p.g % NSB;
+        if (!wait_bar(bar(VFULL + vs), (p.vi / NV) & 1, wc, 0x101)) return false;
+        if (!wait_bar(bar(PFULL + sb), (p.g / NSB) & 1, wc, 0x102)) return false;
         if (p.first && !wait_bar(bar(OEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
         tc_fence_after();
-        const uint32_t vt = sV + p.vs * C::KV_BYTES;
+        const SDesc vd = mndesc<BN>(sV + vs * C::KV_BYTES);
+        const uint32_t tP = tmem + COL_S + sb * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tO, tP + p.b * (BN / 2) + kk * 8, desc_mnmajor<BN>(vt, kk, 0), IDESC_PV,
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const int key = 16 * kk;  // P of keys [key, key+16) sits in the producing warp's columns
+          const uint32_t col = (key / CPW) * CPW + (key % CPW) / 2;
+          mma_ts(tO, tP + col, desc_mnmajor<BN>(vd, kk, 0), IDESC_PV,
                  (!p.first || kk > 0) ? 1u : 0u);
-        mma_commit(bar(VEMPTY + p.vs));
+        }
+        mma_commit(bar(VEMPTY + vs));
         if (p.last) mma_commit(bar(OFULL));
         return true;
       };
       uint32_t qi = 0, ki = 0, vi = 0, g = 0, oi = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit U = load_unit(a.units, u);
-        if (U.n <= 0) continue;
+      for (uint32_t uk = 0; ok; ++uk) {
+        UnitInfo U;
+        if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
+        if (U.n < 0) break;
+        const int un = U.n;
+        if (un <= 0) continue;
         const int qb = qi % NQ;
         if (!wait_bar(bar(QFULL + qb), (qi / NQ) & 1, wc, 0x104)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t qt = sQ + qb * C::Q_BYTES;
-        for (int n = 0; n < U.n; ++n) {
-          const int ks = ki % NK, b = g & 1;
+        const SDesc qd = kdesc(sQ + qb * C::Q_BYTES);
+        for (int n = 0; n < un; ++n) {
+          const int ks = ki % NK, sb = g % NSB;
           if (!wait_bar(bar(KFULL + ks), (ki / NK) & 1, wc, 0x105)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kt = sK + ks * C::KV_BYTES;
+          const SDesc kd = kdesc(sK + ks * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tS + b * BN, desc_kmajor<kBM>(qt, kk), desc_kmajor<BN>(kt, kk), IDESC_S,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(bar(SFULL + b));
-          mma_commit(bar(KEMPTY + ks));
-          if (n == U.n - 1) mma_commit(bar(QEMPTY + qb));
-          if (pv.valid && !issue_pv(pv)) { ok = false; break; }
-          pv = Pend{1, static_cast<int>(vi % NV), b, n == 0, n == U.n - 1, vi, g, oi};
+            mma_ss(tmem + COL_S + sb * BN, desc_kmajor<kBM>(qd, kk), desc_kmajor<BN>(kd, kk),
+                   IDESC_S, kk > 0 ? 1u : 0u);
+          mma_commit(bar(SFULL + sb));  // also frees K slot ks == sb
+          if (n == un - 1) mma_commit(bar(QEMPTY + qb));
+          const Step cur{g, vi, oi, n == 0, n == un - 1};
+          if (npend == LA) {
+            if (!issue_pv(p0)) { ok = false; break; }
+            p0 = p1;
+            p1 = cur;
+          } else if (npend == 1) {
+            p1 = cur;
+            npend = 2;
+          } else {
+            p0 = cur;
+            npend = 1;
+          }
           ++ki;
           ++vi;
           ++g;
@@ -181,7 +239,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++qi;
         ++oi;
       }
-      if (ok && pv.valid) issue_pv(pv);
+      if (ok && npend >= 1) ok = issue_pv(p0);
+      if (ok && npend == 2) ok = issue_pv(p1);
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
     }
@@ -189,21 +248,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ SiLU + epilogue
     // Eight warps: warp w owns TMEM lane quarter w % 4 (its 32 rows) and one
     // half of the key columns of each S tile (and of the O columns).
-    constexpr int CPW = BN / 2;
     const int wq = warp & 3, hc = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tO = tmem + COL_O + lane_off,
-                   tP = tmem + COL_P + lane_off + hc * (CPW / 2);
+    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tO = tmem + COL_O + lane_off;
     const float half_alpha = 0.5f * a.alpha;
     uint32_t g = 0, oi = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const Unit U = load_unit(a.units, u);
+    for (uint32_t uk = 0; ok; ++uk) {
+      UnitInfo U;
+      if (!unit_pop_warp(uq, uk, U, wc)) { ok = false; break; }
+      if (U.n < 0) break;
       const int h = U.hz;
-      const int q0 = __ldg(a.cu_q + U.b);
-      const int Lq = __ldg(a.cu_q + U.b + 1) - q0;
-      const int Lk = __ldg(a.cu_k + U.b + 1) - __ldg(a.cu_k + U.b);
+      const int q0 = U.q0, Lq = U.Lq, Lk = U.Lk;
       const int i = kBM * U.tile + r;
       const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
       const int64_t grow = static_cast<int64_t>(q0) + i;
@@ -216,8 +273,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         continue;
       }
       for (int n = 0; n < U.n; ++n) {
-        const int sb = g & 1;
-        if (!wait_bar_warp(bar(SFULL + sb), (g >> 1) & 1, wc, 0x201)) { ok = false; break; }
+        const int sb = g % NSB;
+        if (!wait_bar_warp(bar(SFULL + sb), (g / NSB) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
         const int jc = BN * n + hc * CPW;  // first key of this warp's columns
         const bool need_mask = (a.causal && jc + CPW - 1 > i_warp) || (jc + CPW > Lk);
@@ -237,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             p[e] = silu_pair<BF16>(s0, s1, half_alpha);
           }
         }
-        tmem_st_n<CPW / 2>(tP + sb * (BN / 2), p);
+        tmem_st_n<CPW / 2>(tS + sb * BN, p);  // in place over this warp's S columns
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(PFULL + sb));
@@ -267,7 +324,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 template <int D, bool BF16>
-cudaError_t launch_fwd_t(int grid, cudaStream_t st, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_fwd_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const AttnArgs& a) {
   auto kern = hstu_fwd_kernel<D, BF16>;
   static bool attr_set = false;  // benign race: setting the attribute twice is harmless
@@ -277,21 +334,20 @@ cudaError_t launch_fwd_t(int grid, cudaStream_t st, const CUtensorMap& tq, const
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, kAttnThreads, FwdCfg<D>::SMEM, st>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return launch_attn(kern, grid, FwdCfg<D>::SMEM, st, pdl, tq, tk, tv, a);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a) {
   switch (D) {
-    case 64: return bf16 ? launch_fwd_t<64, true>(grid, st, tq, tk, tv, a)
-                         : launch_fwd_t<64, false>(grid, st, tq, tk, tv, a);
-    case 128: return bf16 ? launch_fwd_t<128, true>(grid, st, tq, tk, tv, a)
-                          : launch_fwd_t<128, false>(grid, st, tq, tk, tv, a);
-    case 256: return bf16 ? launch_fwd_t<256, true>(grid, st, tq, tk, tv, a)
-                          : launch_fwd_t<256, false>(grid, st, tq, tk, tv, a);
+    case 64: return bf16 ? launch_fwd_t<64, true>(grid, st, pdl, tq, tk, tv, a)
+                         : launch_fwd_t<64, false>(grid, st, pdl, tq, tk, tv, a);
+    case 128: return bf16 ? launch_fwd_t<128, true>(grid, st, pdl, tq, tk, tv, a)
+                          : launch_fwd_t<128, false>(grid, st, pdl, tq, tk, tv, a);
+    case 256: return bf16 ? launch_fwd_t<256, true>(grid, st, pdl, tq, tk, tv, a)
+                          : launch_fwd_t<256, false>(grid, st, pdl, tq, tk, tv, a);
     default: return cudaErrorInvalidValue;
   }
 }

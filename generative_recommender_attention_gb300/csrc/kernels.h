@@ -43,6 +43,8 @@ struct AttnArgs {
   const int4* units;    // work list walked by this kernel
   int units_slot;       // header word holding its length
   uint64_t timeout_ns;  // limit of every barrier wait
+  int next_slot;        // header word counting units claimed so far
+  int pdl_wait;         // 0: none, 1: wait for the previous grid first, 2: only before exit
   void* o0;             // fwd: out, dq kernel: dq, dkdv kernel: dv
   int64_t o0_st, o0_sh;
   void* o1;             // dkdv kernel: dk
@@ -56,8 +58,8 @@ template <int D>
 struct FwdCfg {
   static constexpr int BN = D == 256 ? 64 : 128;     // keys per inner tile
   static constexpr int NQ = D == 256 ? 1 : 2;        // Q buffers
-  static constexpr int NK = D == 64 ? 6 : 3;         // K stages
-  static constexpr int NV = D == 64 ? 4 : 2;         // V stages
+  static constexpr int NK = 3;                       // K stages (one per S buffer)
+  static constexpr int NV = D == 64 ? 6 : 2;         // V stages
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int TILE_BYTES = NQ * Q_BYTES + (NK + NV) * KV_BYTES;
@@ -66,12 +68,13 @@ struct FwdCfg {
 
 // ------------------------------------------------------------ dQ config
 // K is read by S = Q K^T and by dQ += dS K (freed last); V only by dP = dO V^T.
+// 64-key steps so that S and dP fit twice in TMEM next to dQ.
 template <int D>
 struct DqCfg {
-  static constexpr int BN = D == 256 ? 64 : 128;
+  static constexpr int BN = 64;
   static constexpr int NQ = D == 64 ? 2 : 1;         // (Q, dO) buffers
-  static constexpr int NK = D == 64 ? 5 : (D == 128 ? 3 : 2);
-  static constexpr int NV = D == 64 ? 3 : (D == 128 ? 2 : 1);
+  static constexpr int NK = D == 64 ? 6 : (D == 128 ? 5 : 2);
+  static constexpr int NV = D == 64 ? 6 : (D == 128 ? 5 : 1);
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + (NK + NV) * KV_BYTES;
@@ -85,7 +88,7 @@ struct DkdvCfg {
   static constexpr int DH = D == 256 ? 128 : D;      // dK/dV columns per unit
   static constexpr int SPLIT = D / DH;
   static constexpr int NKV = D == 64 ? 2 : 1;        // stationary (K, V) buffers
-  static constexpr int NS = D == 64 ? 6 : (D == 128 ? 4 : 1);
+  static constexpr int NS = D == 64 ? 6 : (D == 128 ? 5 : 1);
   static constexpr int KV_BYTES = kBM * D * 2;
   static constexpr int Q_BYTES = BQ * D * 2;
   static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES;
@@ -107,12 +110,32 @@ __global__ void hstu_sched_kernel(SchedArgs a);
 // Launchers: return cudaErrorInvalidValue for a head_dim outside {64,128,256}.
 // Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (q/do: 128-row
 // box, k/v: BN-row box); dkdv (k/v: 128-row box, q/do: BQ-row box).
-cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+// Launch of a persistent attention kernel.  With `pdl` the grid may start
+// while the previous grid in the stream is still running (programmatic
+// dependent launch); the kernel orders itself with griddepcontrol.wait as
+// AttnArgs::pdl_wait says.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_attn(void (*kern)(KArgs...), int grid, int smem, cudaStream_t st,
+                               bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a);
-cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tq,
+cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
                       const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
                       const AttnArgs& a);
-cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, const CUtensorMap& tk,
+cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const AttnArgs& a);
 cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st);

@@ -81,12 +81,20 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   const int nb = cmax + 1;
   const int tid = threadIdx.x;
 
+  // the attention grid queued behind this one may start its prologue now
+  if (tid == 0) grid_launch_dependents();
   if (!list_b && tid == 0) {
     a.header[kHdrStatus] = 0;
     a.header[kHdrWhere] = 0;
-    if (gridDim.x == 1) a.header[kHdrOverflow + 1] = 0;
+    if (gridDim.x == 1) {
+      a.header[kHdrOverflowB] = 0;
+      a.header[kHdrNextB] = 0;
+    }
   }
-  if (tid == 0) a.header[kHdrOverflow + (list_b ? 1 : 0)] = 0;
+  if (tid == 0) {
+    a.header[list_b ? kHdrOverflowB : kHdrOverflow] = 0;
+    a.header[list_b ? kHdrNextB : kHdrNextA] = 0;
+  }
 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
       }
     }
   }
-  if (overflow) atomicExch(a.header + kHdrOverflow + (list_b ? 1 : 0), 1);
+  if (overflow) atomicExch(a.header + (list_b ? kHdrOverflowB : kHdrOverflow), 1);
   if (tid == 0) a.header[list_b ? kHdrUnitsB : kHdrUnitsA] = min(total, cap);
 }
 
@@ -151,7 +159,7 @@ __global__ void hstu_selftest_timeout_kernel(int* header, uint64_t timeout_ns) {
     header[kHdrStatus] = 0;
     header[kHdrWhere] = 0;
     header[kHdrOverflow] = 0;
-    header[kHdrOverflow + 1] = 0;
+    header[kHdrOverflowB] = 0;
     mbar_init(smem_u32(&bar), 1);
     flags[0] = 0;
     flags[1] = 0;
