@@ -288,8 +288,8 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
-  const int BN = DqCfg<64>::BN;  // dQ kernel key tile (same for every D)
-  const int BQ = DkdvCfg<64>::BQ;
+  const int BN = D == 256 ? DqCfg<256>::BN : DqCfg<128>::BN;  // dQ kernel key tile
+  const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;  // dK/dV query tile
   const int split = D == 256 ? 2 : 1;
   const int64_t capA = cap_a(batch, total_q, H);
   const int64_t capB = cap_b(batch, total_k, H, D);

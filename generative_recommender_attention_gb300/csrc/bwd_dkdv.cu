@@ -5,22 +5,26 @@
 //
 // Key-stationary: each CTA owns a 128-row key tile (and, for D = 256, one
 // 128-column half of dK/dV, so the accumulators fit in TMEM) and walks the
-// 64-row query tiles that can see it.  Per step it recomputes S^T = K Q^T and
+// query tiles that can see it.  Per step it recomputes S^T = K Q^T and
 // dP^T = V dO^T into TMEM, forms A^T = M (.) SiLU(alpha S^T) and
 // dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
-// element), stores both to TMEM as 16-bit, and accumulates dV += A^T dO and
-// dK += dS^T Q with the A operand read from TMEM.  No atomics.
-//   warp 0      TMA: K and V per unit, Q and dO per step.
-//   warp 1      tcgen05 issuer.  S^T and dP^T are double-buffered and run one
-//               step ahead of the dV / dK accumulation, so the tensor pipe has
-//               work while the row warps form A^T and dS^T.
-//   warps 2-9   row work, two warps per TMEM lane quarter (one per column
-//               half of each query tile).
-// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK [| A^T0 | A^T1 | dS^T0 | dS^T1].
-// When the separate A^T / dS^T buffers do not fit (D >= 128) they are written
-// in place over the S^T / dP^T columns their warp just read; S^T_{g+2}
-// (issued after the step-g accumulation by the same thread, in order)
-// overwrites them only after they are consumed.
+// element), and accumulates dV += A^T dO and dK += dS^T Q.  No atomics.
+//   warp 0       TMA: K and V per unit, Q and dO per step (one barrier).
+//   warp 1       tcgen05 issuer.  Per step g: S^T_g (once the row warps have
+//                loaded S^T_{g-1}), dK += dS^T_{g-1} Q_{g-1}, dP^T_g, then
+//                dV += A^T_{g-1} dO_{g-1}.
+//   warps 2-17   row work, four warps per TMEM lane quarter (one per quarter
+//                of the query columns): dS^T first (it gates dP^T_{g+1}),
+//                then A^T.
+// TMEM: S^T | dP^T | dV | dK.  dS^T is written in place over the dP^T
+// columns its warp just read (the TMEM A operand of dK += dS^T Q); A^T goes
+// to a shared-memory tile in the 128-byte-swizzled K-major layout (the A
+// operand of dV += A^T dO).  S^T is released as soon as it is loaded, so
+// S^T_{g+1} runs on the tensor pipe while the row warps work on step g.
+// dP^T_{g+1} follows dK += dS^T_g Q_g from the same thread, and tcgen05.mma
+// operations from one thread execute in issue order, so dS^T_g is consumed
+// before it is overwritten; dV, which reads only shared memory, is issued
+// after dP^T_{g+1} so it stays off that chain.
 #include "kernels.h"
 
 namespace hstu {
@@ -28,7 +32,7 @@ namespace hstu {
 namespace {
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, 1)
     hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q,
@@ -36,21 +40,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using C = DkdvCfg<D>;
   constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV, NS = C::NS;
   constexpr int KCH = D / 64;
-  constexpr int CPW = BQ / 2;
-  static_assert(CPW == 32, "one 32-column batch per row warp");
+  constexpr int RW = kRowWarps16;
+  constexpr int CW = BQ / 4;   // query columns per row warp
+  constexpr int DW = DH / 4;   // dK / dV columns per row warp
   constexpr bool SERIAL = NS == 1;  // one Q/dO stage: accumulate before the next S^T
-  constexpr bool ALIAS = 4 * BQ + 2 * DH + 2 * BQ > kTmemCols;
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BQ, false, false);
   constexpr uint32_t IDESC_ACC = idesc_f16(BF16, kBM, DH, false, true);
-  constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH,
-                     COL_AT = 4 * BQ + 2 * DH, COL_DST = COL_AT + BQ;
-  static_assert(COL_DK + DH + (ALIAS ? 0 : 2 * BQ) <= kTmemCols, "TMEM budget");
-  // A^T / dS^T of step g: separate buffers of BQ/2 packed columns, or the
-  // first half of each row warp's own S^T / dP^T columns.
-  constexpr uint32_t P_BUF = ALIAS ? BQ : BQ / 2;
-  constexpr uint32_t P_HALF = ALIAS ? CPW : CPW / 2;
-  constexpr uint32_t A_BASE = ALIAS ? COL_ST : COL_AT;
-  constexpr uint32_t D_BASE = ALIAS ? COL_DPT : COL_DST;
+  constexpr uint32_t COL_ST = 0, COL_DPT = BQ, COL_DV = 2 * BQ, COL_DK = 2 * BQ + DH;
+  static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
+  static_assert(C::SMEM <= 232448, "shared memory budget");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -59,12 +57,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sKV = base;                          // NKV x (K, V)
   const uint32_t sQ = sKV + 2 * NKV * C::KV_BYTES;    // NS x Q
   const uint32_t sDO = sQ + NS * C::Q_BYTES;          // NS x dO
+  const uint32_t sP = sDO + NS * C::Q_BYTES;          // A^T tile
 
   enum {
-    KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, DOFULL = QFULL + NS,
-    QEMPTY = DOFULL + NS, STFULL = QEMPTY + NS, ASFULL = STFULL + 2, ACCFULL = ASFULL + 2,
-    ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1, UEMPTY = UFULL + kUnitRing,
-    DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
+    KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
+    STFULL = QEMPTY + NS, SEMPTY = STFULL + 1, DSFULL = SEMPTY + 1, PFULL = DSFULL + 1,
+    PEMPTY = PFULL + 1, ACCFULL = PEMPTY + 1, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
+    UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
   static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
@@ -76,18 +75,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NKV; ++i) { mbar_init(bar(KVFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1); }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(QFULL + i), 1); mbar_init(bar(DOFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(STFULL + i), 1);
-      mbar_init(bar(ASFULL + i), kRowThreads);
-    }
+    for (int i = 0; i < NS; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
+    mbar_init(bar(STFULL), 1);
+    mbar_init(bar(SEMPTY), RW);
+    mbar_init(bar(DSFULL), RW);
+    mbar_init(bar(PFULL), RW);
+    mbar_init(bar(PEMPTY), 1);
     mbar_init(bar(ACCFULL), 1);
-    mbar_init(bar(ACCEMPTY), kRowThreads);
+    mbar_init(bar(ACCEMPTY), RW);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
-      mbar_init(bar(UEMPTY + i), kUnitConsumers);
+      mbar_init(bar(UEMPTY + i), 1 + RW);
     }
     mbar_init(bar(DRAIN), 1);
     flags[0] = 0;
@@ -143,56 +141,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int s = qi % NS;
           if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           const int row = q_seq0 + BQ * (m0 + m);
-          mbar_arrive_expect_tx(bar(QFULL + s), C::Q_BYTES);
+          mbar_arrive_expect_tx(bar(QFULL + s), 2 * C::Q_BYTES);
 #pragma unroll
-          for (int c = 0; c < KCH; ++c)
+          for (int c = 0; c < KCH; ++c) {
             tma_load_3d(sQ + s * C::Q_BYTES + c * (BQ * 128), &tm_q, bar(QFULL + s), 64 * c, h, row);
-          mbar_arrive_expect_tx(bar(DOFULL + s), C::Q_BYTES);
-#pragma unroll
-          for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(DOFULL + s), 64 * c, h, row);
+            tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(QFULL + s), 64 * c, h, row);
+          }
           ++qi;
         }
       }
       for (uint32_t i = kvi > NKV ? kvi - NKV : 0; i < kvi; ++i)
         wait_bar(bar(KVFULL + i % NKV), (i / NKV) & 1, drain, 0x0f1);
-      for (uint32_t i = qi > NS ? qi - NS : 0; i < qi; ++i) {
+      for (uint32_t i = qi > NS ? qi - NS : 0; i < qi; ++i)
         wait_bar(bar(QFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
-        wait_bar(bar(DOFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Flat stream of steps g: S^T_g, dP^T_g, then the step g-1 accumulation.
+    // Waits on TMA-filled stages need no tcgen05 fence; waits on the row
+    // warps' TMEM accesses do.
     if (lane == 0) {
       const uint32_t tDV = tmem + COL_DV, tDK = tmem + COL_DK;
+      const SDesc pdesc = kdesc(sP);
       struct Pend {
         int valid, s, first, last, half;
         uint32_t g, oi;
       } pd{0, 0, 0, 0, 0, 0, 0};
-      // dV += A^T dO, dK += dS^T Q over the step's queries, once A^T / dS^T exist
-      auto issue_acc = [&](const Pend& p) -> bool {
-        const int b = p.g & 1;
-        if (!wait_bar(bar(ASFULL + b), (p.g >> 1) & 1, wc, 0x105)) return false;
+      // dK += dS^T Q over the step's queries, once dS^T is in TMEM
+      auto issue_dk = [&](const Pend& p) -> bool {
+        if (!wait_bar(bar(DSFULL), p.g & 1, wc, 0x105)) return false;
         if (p.first && !wait_bar(bar(ACCEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
         tc_fence_after();
-        const SDesc qd = mndesc<BQ>(sQ + p.s * C::Q_BYTES), dod = mndesc<BQ>(sDO + p.s * C::Q_BYTES);
+        const SDesc qd = mndesc<BQ>(sQ + p.s * C::Q_BYTES);
         const int n0 = p.half * DH;
-        const uint32_t tAT = tmem + A_BASE + b * P_BUF, tDST = tmem + D_BASE + b * P_BUF;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
+          // dS^T of queries [16 kk, 16 kk + 16) sits packed in the first half
+          // of its row warp's own dP^T columns
           const int q = 16 * kk;
-          const uint32_t col = (q / CPW) * P_HALF + (q % CPW) / 2;
-          mma_ts(tDV, tAT + col, desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC,
+          const uint32_t col = (q / CW) * CW + (q % CW) / 2;
+          mma_ts(tDK, tmem + COL_DPT + col, desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC,
                  (!p.first || kk > 0) ? 1u : 0u);
         }
+        return true;
+      };
+      // dV += A^T dO once A^T is in shared memory (ACCEMPTY was waited for by
+      // the dK half of the same step); frees the A^T tile and the Q/dO stage
+      auto issue_dv = [&](const Pend& p) -> bool {
+        if (!wait_bar(bar(PFULL), p.g & 1, wc, 0x109)) return false;
+        const SDesc dod = mndesc<BQ>(sDO + p.s * C::Q_BYTES);
+        const int n0 = p.half * DH;
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const int q = 16 * kk;
-          const uint32_t col = (q / CPW) * P_HALF + (q % CPW) / 2;
-          mma_ts(tDK, tDST + col, desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC,
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ss(tDV, desc_kmajor<kBM>(pdesc, kk), desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC,
                  (!p.first || kk > 0) ? 1u : 0u);
-        }
+        mma_commit(bar(PEMPTY));
         mma_commit(bar(QEMPTY + p.s));
         if (p.last) mma_commit(bar(ACCFULL));
         return true;
@@ -207,31 +209,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int half = U.hz % SPLIT;
         const int kb = kvi % NKV;
         if (!wait_bar(bar(KVFULL + kb), (kvi / NKV) & 1, wc, 0x104)) { ok = false; break; }
-        tc_fence_after();
         const SDesc kd = kdesc(sKV + kb * 2 * C::KV_BYTES);
         const SDesc vd = kdesc(sKV + kb * 2 * C::KV_BYTES + C::KV_BYTES);
         for (int m = 0; m < U.n; ++m) {
-          const int s = qi % NS, b = g & 1;
+          const int s = qi % NS;
           if (!wait_bar(bar(QFULL + s), (qi / NS) & 1, wc, 0x106)) { ok = false; break; }
-          tc_fence_after();
+          // S^T is single-buffered: the row warps must have loaded step g-1
+          if (g > 0) {
+            if (!wait_bar(bar(SEMPTY), (g - 1) & 1, wc, 0x108)) { ok = false; break; }
+            tc_fence_after();
+          }
           const SDesc qd = kdesc(sQ + s * C::Q_BYTES), dod = kdesc(sDO + s * C::Q_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_ST + b * BQ, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          if (!wait_bar(bar(DOFULL + s), (qi / NS) & 1, wc, 0x107)) { ok = false; break; }
-          tc_fence_after();
+            mma_ss(tmem + COL_ST, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk), IDESC_S,
+                   kk > 0 ? 1u : 0u);
+          // dK of step g-1 reads dS^T_{g-1} from the dP^T columns: before dP^T_g
+          if (!SERIAL && pd.valid && !issue_dk(pd)) { ok = false; break; }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_DPT + b * BQ, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          mma_commit(bar(STFULL + b));
+            mma_ss(tmem + COL_DPT, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk), IDESC_S,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(bar(STFULL));
           if (m == U.n - 1) mma_commit(bar(KVEMPTY + kb));
-          Pend cur{1, s, m == 0, m == U.n - 1, half, g, oi};
+          if (!SERIAL && pd.valid && !issue_dv(pd)) { ok = false; break; }
+          const Pend cur{1, s, m == 0, m == U.n - 1, half, g, oi};
           if (SERIAL) {
-            if (!issue_acc(cur)) { ok = false; break; }
+            if (!issue_dk(cur) || !issue_dv(cur)) { ok = false; break; }
           } else {
-            if (pd.valid && !issue_acc(pd)) { ok = false; break; }
             pd = cur;
           }
           ++qi;
@@ -240,21 +245,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++kvi;
         ++oi;
       }
-      if (!SERIAL && ok && pd.valid) issue_acc(pd);
+      if (!SERIAL && ok && pd.valid) ok = issue_dk(pd) && issue_dv(pd);
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
     }
   } else {
     // ------------------------------------------------------------ A^T, dS^T + epilogue
-    // Eight warps: warp w owns TMEM lane quarter w % 4 (32 key rows) and one
-    // half of the query columns of each S^T / dP^T tile (and of dK / dV).
-    const int wq = warp & 3, hc = (warp - 2) >> 2;
+    // Sixteen warps: warp w owns TMEM lane quarter w % 4 (32 key rows) and one
+    // quarter of the query columns of each S^T / dP^T tile (and of dK / dV).
+    const int wq = warp & 3, cg = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tST = tmem + COL_ST + lane_off + hc * CPW, tDPT = tmem + COL_DPT + lane_off + hc * CPW,
-                   tDV = tmem + COL_DV + lane_off, tDK = tmem + COL_DK + lane_off,
-                   tAT = tmem + A_BASE + lane_off + hc * P_HALF,
-                   tDST = tmem + D_BASE + lane_off + hc * P_HALF;
+    const uint32_t tST = tmem + COL_ST + lane_off + cg * CW,
+                   tDPT = tmem + COL_DPT + lane_off + cg * CW,
+                   tDV = tmem + COL_DV + lane_off + cg * DW, tDK = tmem + COL_DK + lane_off + cg * DW;
+    // A^T row r, queries [cg CW, cg CW + CW): 64-query chunk, 16-byte units
+    // within the 128-byte row, XOR-swizzled by r % 8
+    const int q_first = cg * CW;
+    const uint32_t p_row = sP + (q_first / 64) * (kBM * 128) + r * 128;
+    const int u0 = (q_first % 64) / 8;
     const float half_alpha = 0.5f * a.alpha;
     const float dk_scale = 0.5f * a.alpha * a.inv_L;  // dS^T is stored doubled
     uint32_t g = 0, oi = 0;
@@ -269,63 +278,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int j_warp_last = kBM * U.tile + wq * 32 + 31;
       const int64_t grow = static_cast<int64_t>(k0) + j;
       const bool row_ok = j < Lk && grow < a.total_k;
-      const int64_t col0 = static_cast<int64_t>(half) * DH + hc * (DH / 2);
+      const int64_t col0 = static_cast<int64_t>(half) * DH + cg * DW;
       char* dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + col0) * 2;
       char* dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + static_cast<int64_t>(h) * a.o1_sh + col0) * 2;
       if (U.n <= 0) {
-        if (row_ok)
-          for (int c = 0; c < DH / 64; ++c) { store_zero32(dvrow + c * 64); store_zero32(dkrow + c * 64); }
+        if (row_ok) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
         continue;
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
       const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
       for (int m = 0; m < U.n; ++m) {
-        const int b = g & 1;
-        if (!wait_bar_warp(bar(STFULL + b), (g >> 1) & 1, wc, 0x201)) { ok = false; break; }
+        if (!wait_bar_warp(bar(STFULL), g & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
-        const int ic = BQ * (m0 + m) + hc * CPW;  // first query of this warp's columns
-        const bool need_mask = (ic + CPW > Lq) || (a.causal && j_warp_last > ic);
-        uint32_t xs[32], xp[32];
-        tmem_ld32x2(tST + b * BQ, tDPT + b * BQ, xs, xp);
-        uint32_t pa[16], pd[16];
+        const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
+        const bool need_mask = (ic + CW > Lq) || (a.causal && j_warp_last > ic);
+        uint32_t xs[CW], xp[CW];
+        tmem_ld_x2<CW>(tST, tDPT, xs, xp);
+        warp_arrive(bar(SEMPTY));  // S^T of this step is in registers
+        uint32_t pa[CW / 2], pd[CW / 2];
         if (!need_mask) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < CW / 2; ++e)
             a_ds_pair<BF16>(xs[2 * e], xs[2 * e + 1], xp[2 * e], xp[2 * e + 1], half_alpha, pa[e],
                             pd[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < CW / 2; ++e) {
             const int i = ic + 2 * e;
             const bool v0 = i >= lo && i < Lq, v1 = i + 1 >= lo && i + 1 < Lq;
             a_ds_pair<BF16>(v0 ? xs[2 * e] : 0u, v1 ? xs[2 * e + 1] : 0u, v0 ? xp[2 * e] : 0u,
                             v1 ? xp[2 * e + 1] : 0u, half_alpha, pa[e], pd[e]);
           }
         }
-        tmem_st16(tAT + b * P_BUF, pa);
-        tmem_st16(tDST + b * P_BUF, pd);
+        // dS^T first: it gates dK += dS^T Q and hence dP^T of the next step
+        tmem_st_w<CW / 2>(tDPT, pd);
         tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(ASFULL + b));
+        warp_arrive(bar(DSFULL));
+        // the A^T tile is free once the step g-1 dV accumulation has read it
+        if (g > 0 && !wait_bar_warp(bar(PEMPTY), (g - 1) & 1, wc, 0x203)) { ok = false; break; }
+#pragma unroll
+        for (int v = 0; v < CW / 8; ++v)
+          st_shared_v4(p_row + (((u0 + v) ^ (r & 7)) << 4), pa[4 * v], pa[4 * v + 1], pa[4 * v + 2],
+                       pa[4 * v + 3]);
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        warp_arrive(bar(PFULL));
         ++g;
       }
       if (!ok) break;
       if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
+      if constexpr (DW <= 32) {
+        uint32_t x[DW];
+        tmem_ld_w<DW>(tDV, x);
+        if (row_ok) store_row_n<DW, BF16>(dvrow, x, a.inv_L);
+        tmem_ld_w<DW>(tDK, x);
+        if (row_ok) store_row_n<DW, BF16>(dkrow, x, dk_scale);
+      } else {
 #pragma unroll 1
-      for (int c = 0; c < DH / 64; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tDV + hc * (DH / 2) + 32 * c, x);
-        if (row_ok) store_row32<BF16>(dvrow + c * 64, x, a.inv_L);
+        for (int c = 0; c < DW / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tDV + 32 * c, x);
+          if (row_ok) store_row_n<32, BF16>(dvrow + c * 64, x, a.inv_L);
+          tmem_ld32(tDK + 32 * c, x);
+          if (row_ok) store_row_n<32, BF16>(dkrow + c * 64, x, dk_scale);
+        }
       }
-#pragma unroll 1
-      for (int c = 0; c < DH / 64; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tDK + hc * (DH / 2) + 32 * c, x);
-        if (row_ok) store_row32<BF16>(dkrow + c * 64, x, dk_scale);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(ACCEMPTY));
+      warp_arrive(bar(ACCEMPTY));
       ++oi;
     }
   }
@@ -352,7 +370,7 @@ cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, a);
+  return launch_attn(kern, grid, kWideThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, a);
 }
 
 }  // namespace

@@ -3,21 +3,26 @@
 // (Blackwell SM100/SM103)", Overview equations).
 //
 // Query-stationary and atomic-free: each 128-row query tile is owned by one
-// CTA, which recomputes S = Q K^T and dP = dO V^T per 64-key step, forms
+// CTA, which recomputes S = Q K^T and dP = dO V^T per key step, forms
 // dS = M (.) dP (.) SiLU'(alpha S) in registers, stores it to TMEM as 16-bit,
 // and accumulates dQ += dS K in TMEM.  The alpha/L_scale factor is applied
 // once in the fp32 epilogue.
-//   warp 0      TMA: Q and dO per unit, K and V per step.
-//   warp 1      tcgen05 issuer.  S and dP are double-buffered in TMEM and run
-//               one step ahead: S_{g+1}, dP_{g+1} are queued before
-//               dQ += dS_g K_g, so the tensor pipe has work while the row
-//               warps form dS_g.
-//   warps 2-9   row work (two warps per TMEM lane quarter, one per column
-//               half): SiLU' and mask, then the dQ epilogue.
-// TMEM: S0 | S1 | dP0 | dP1 | dQ | dS0 | dS1.  At D = 256 there is no room
-// for separate dS buffers; dS_g is then written in place over the S_g
-// columns its warp just read, and S_{g+2} (issued after dQ += dS_g K_g by
-// the same thread, in order) overwrites it only after it is consumed.
+//   warp 0       TMA: Q and dO per unit, K and V per step (one barrier per
+//                step for both).
+//   warp 1       tcgen05 issuer of S_g and dP_g (once the row warps have loaded
+//                S_{g-1} and dP_{g-1}).
+//   warp 18      tcgen05 issuer of dQ += dS_g K_g (once dS_g is written).
+//   warps 2-17   row work, four warps per TMEM lane quarter (one per quarter
+//                of the key columns): load S and dP, release them (and the V
+//                stage), SiLU' and mask, store dS; then the dQ epilogue.
+// TMEM: S | dP | dQ | dS0 | dS1.
+//
+// A tcgen05.mma costs about 47 cycles of tensor-pipe intake whatever its size
+// (M = 128) and the pipe queues only about one instruction ahead, so 128-key
+// steps keep every instruction at N >= 128 (D = 256 uses 64-key steps to fit
+// TMEM) and each issuing thread does little besides issuing: two issuers keep
+// their barrier waits off each other's stream; releases that need no tensor
+// ordering are signalled by a row warp.
 #include "kernels.h"
 
 namespace hstu {
@@ -25,26 +30,24 @@ namespace hstu {
 namespace {
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     hstu_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = DqCfg<D>;
   constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
-  constexpr int CPW = BN / 2;  // key columns per row warp
-  static_assert(CPW == 32, "one 32-column batch per row warp");
-  static_assert(NK >= 2, "the next S is issued before the pending dQ += dS K");
-  constexpr bool DS_ALIAS = 4 * BN + D + BN > kTmemCols;
+  constexpr int NF = NK < NV ? NK : NV;  // step barriers (K and V land on one)
+  constexpr int RW = kRowWarps16;
+  constexpr int CW = BN / 4;   // key columns per row warp
+  constexpr int DW = D / 4;    // dQ columns per row warp
+  constexpr int MMA_B = 2 + RW;  // warp of the dQ issuer
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_DQ = idesc_f16(BF16, kBM, D, false, true);
-  constexpr uint32_t COL_S = 0, COL_DP = 2 * BN, COL_DQ = 4 * BN, COL_DS = 4 * BN + D;
-  static_assert(COL_DQ + D + (DS_ALIAS ? 0 : BN) <= kTmemCols, "TMEM budget");
-  // dS_g columns: a separate buffer of BN/2 packed columns, or the first
-  // half of each row warp's own S columns.
-  constexpr uint32_t DS_BUF = DS_ALIAS ? BN : BN / 2;         // stride between the two buffers
-  constexpr uint32_t DS_HALF = DS_ALIAS ? CPW : CPW / 2;      // offset of column half 1
-  constexpr uint32_t DS_BASE = DS_ALIAS ? COL_S : COL_DS;
+  constexpr uint32_t COL_S = 0, COL_DP = BN, COL_DQ = 2 * BN, COL_DS = 2 * BN + D;
+  constexpr uint32_t DS_BUF = BN / 2;  // packed dS columns per buffer
+  static_assert(COL_DS + 2 * DS_BUF <= kTmemCols, "TMEM budget");
+  static_assert(C::SMEM <= 232448, "shared memory budget");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -55,10 +58,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t sV = sK + NK * C::KV_BYTES;       // NV x V
 
   enum {
-    QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ, KEMPTY = KFULL + NK,
-    VFULL = KEMPTY + NK, VEMPTY = VFULL + NV, SPFULL = VEMPTY + NV, DSFULL = SPFULL + 2,
-    DQFULL = DSFULL + 2, DQEMPTY = DQFULL + 1, UFULL = DQEMPTY + 1, UEMPTY = UFULL + kUnitRing,
-    DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
+    QFULL = 0, QEMPTY = QFULL + NQ, FULL = QEMPTY + NQ, KEMPTY = FULL + NF,
+    VEMPTY = KEMPTY + NK, SPFULL = VEMPTY + NV, SPEMPTY = SPFULL + 1, DSFULL = SPEMPTY + 1,
+    DSEMPTY = DSFULL + 2, DQFULL = DSEMPTY + 2, DQEMPTY = DQFULL + 1, UFULL = DQEMPTY + 1,
+    UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
   static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
@@ -70,19 +73,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
-    for (int i = 0; i < NK; ++i) { mbar_init(bar(KFULL + i), 1); mbar_init(bar(KEMPTY + i), 1); }
-    for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(SPFULL + i), 1);
-      mbar_init(bar(DSFULL + i), kRowThreads);
-    }
+    for (int i = 0; i < NF; ++i) mbar_init(bar(FULL + i), 1);
+    for (int i = 0; i < NK; ++i) mbar_init(bar(KEMPTY + i), 1);
+    for (int i = 0; i < NV; ++i) mbar_init(bar(VEMPTY + i), 1);
+    mbar_init(bar(SPFULL), 1);
+    mbar_init(bar(SPEMPTY), RW);
+    for (int i = 0; i < 2; ++i) { mbar_init(bar(DSFULL + i), RW); mbar_init(bar(DSEMPTY + i), 1); }
     mbar_init(bar(DQFULL), 1);
-    mbar_init(bar(DQEMPTY), kRowThreads);
+    mbar_init(bar(DQEMPTY), RW);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
-      mbar_init(bar(UEMPTY + i), kUnitConsumers);
+      mbar_init(bar(UEMPTY + i), 2 + RW);
     }
     mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(DRAIN + 1), 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -107,18 +111,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t qi = 0, ki = 0, vi = 0;
-      auto load_kv = [&](const CUtensorMap* map, uint32_t base_s, int nst, uint32_t& cnt,
-                         int full, int empty, int row, int h, int where) -> bool {
-        const int s = cnt % nst;
-        if (!wait_bar(bar(empty + s), ((cnt / nst) & 1) ^ 1, wc, where)) return false;
-        mbar_arrive_expect_tx(bar(full + s), C::KV_BYTES);
-#pragma unroll
-        for (int c = 0; c < KCH; ++c)
-          tma_load_3d(base_s + s * C::KV_BYTES + c * (BN * 128), map, bar(full + s), 64 * c, h, row);
-        ++cnt;
-        return true;
-      };
+      uint32_t qi = 0, g = 0;
       bool ok = true;
       // claim units one ahead: the next claim overlaps this unit's loads
       UnitInfo nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1),
@@ -142,51 +135,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(dot + c * (kBM * 128), &tm_do, bar(QFULL + qb), 64 * c, h, q_row0);
         }
         ++qi;
-        for (int n = 0; n < U.n; ++n) {
-          const int row = kv_row0 + BN * n;
-          if (!load_kv(&tm_k, sK, NK, ki, KFULL, KEMPTY, row, h, 0x002) ||
-              !load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, row, h, 0x003)) {
+        for (int n = 0; n < U.n; ++n, ++g) {
+          const int ks = g % NK, vs = g % NV, f = g % NF;
+          if (!wait_bar(bar(KEMPTY + ks), ((g / NK) & 1) ^ 1, wc, 0x002) ||
+              !wait_bar(bar(VEMPTY + vs), ((g / NV) & 1) ^ 1, wc, 0x003)) {
             ok = false;
             break;
+          }
+          const int row = kv_row0 + BN * n;
+          mbar_arrive_expect_tx(bar(FULL + f), 2 * C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < KCH; ++c) {
+            tma_load_3d(sK + ks * C::KV_BYTES + c * (BN * 128), &tm_k, bar(FULL + f), 64 * c, h, row);
+            tma_load_3d(sV + vs * C::KV_BYTES + c * (BN * 128), &tm_v, bar(FULL + f), 64 * c, h, row);
           }
         }
       }
       for (uint32_t i = qi > NQ ? qi - NQ : 0; i < qi; ++i)
         wait_bar(bar(QFULL + i % NQ), (i / NQ) & 1, drain, 0x0f1);
-      for (uint32_t i = ki > NK ? ki - NK : 0; i < ki; ++i)
-        wait_bar(bar(KFULL + i % NK), (i / NK) & 1, drain, 0x0f2);
-      for (uint32_t i = vi > NV ? vi - NV : 0; i < vi; ++i)
-        wait_bar(bar(VFULL + i % NV), (i / NV) & 1, drain, 0x0f3);
+      for (uint32_t i = g > NF ? g - NF : 0; i < g; ++i)
+        wait_bar(bar(FULL + i % NF), (i / NF) & 1, drain, 0x0f2);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Flat stream of steps g: S_g, dP_g, then dQ += dS_{g-1} K_{g-1}.
+    // ------------------------------------------------------------ S / dP issuer
+    // Waits on TMA-filled stages need no tcgen05 fence (the async proxy both
+    // writes and reads them); waits on the row warps' TMEM accesses do.
     if (lane == 0) {
-      const uint32_t tDQ = tmem + COL_DQ;
-      struct Pend {
-        int valid, ks, first, last;
-        uint32_t g, oi;
-      } pd{0, 0, 0, 0, 0, 0};
-      // dQ += dS_g K_g once the row warps have written dS_g
-      auto issue_dq = [&](const Pend& p) -> bool {
-        const int b = p.g & 1;
-        if (!wait_bar(bar(DSFULL + b), (p.g >> 1) & 1, wc, 0x105)) return false;
-        if (p.first && !wait_bar(bar(DQEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
-        tc_fence_after();
-        const SDesc kd = mndesc<BN>(sK + p.ks * C::KV_BYTES);
-        const uint32_t tDS = tmem + DS_BASE + b * DS_BUF;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const int key = 16 * kk;
-          const uint32_t col = (key / CPW) * DS_HALF + (key % CPW) / 2;
-          mma_ts(tDQ, tDS + col, desc_mnmajor<BN>(kd, kk, 0), IDESC_DQ,
-                 (!p.first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(KEMPTY + p.ks));
-        if (p.last) mma_commit(bar(DQFULL));
-        return true;
-      };
-      uint32_t qi = 0, ki = 0, vi = 0, g = 0, oi = 0;
+      uint32_t qi = 0, g = 0;
       bool ok = true;
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U;
@@ -195,55 +170,78 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (U.n <= 0) continue;
         const int qb = qi % NQ;
         if (!wait_bar(bar(QFULL + qb), (qi / NQ) & 1, wc, 0x104)) { ok = false; break; }
-        tc_fence_after();
         const SDesc qd = kdesc(sQ + qb * 2 * C::Q_BYTES);
         const SDesc dod = kdesc(sQ + qb * 2 * C::Q_BYTES + C::Q_BYTES);
-        for (int n = 0; n < U.n; ++n) {
-          const int ks = ki % NK, vs = vi % NV, b = g & 1;
-          // buffer b last held step g-2, whose dS was waited for (and, when
-          // aliased, consumed by dQ) before step g-1's dQ was issued
-          if (!wait_bar(bar(KFULL + ks), (ki / NK) & 1, wc, 0x106)) { ok = false; break; }
-          tc_fence_after();
-          const SDesc kd = kdesc(sK + ks * C::KV_BYTES);
+        for (int n = 0; n < U.n; ++n, ++g) {
+          if (!wait_bar(bar(FULL + g % NF), (g / NF) & 1, wc, 0x106)) { ok = false; break; }
+          // S and dP are single-buffered: the row warps must have loaded step g-1
+          if (g > 0) {
+            if (!wait_bar(bar(SPEMPTY), (g - 1) & 1, wc, 0x108)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const SDesc kd = kdesc(sK + (g % NK) * C::KV_BYTES);
+          const SDesc vd = kdesc(sV + (g % NV) * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_S + b * BN, desc_kmajor<kBM>(qd, kk), desc_kmajor<BN>(kd, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          if (!wait_bar(bar(VFULL + vs), (vi / NV) & 1, wc, 0x107)) { ok = false; break; }
-          tc_fence_after();
-          const SDesc vd = kdesc(sV + vs * C::KV_BYTES);
+            mma_ss(tmem + COL_S, desc_kmajor<kBM>(qd, kk), desc_kmajor<BN>(kd, kk), IDESC_S,
+                   kk > 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_DP + b * BN, desc_kmajor<kBM>(dod, kk), desc_kmajor<BN>(vd, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          mma_commit(bar(SPFULL + b));
-          mma_commit(bar(VEMPTY + vs));
-          if (n == U.n - 1) mma_commit(bar(QEMPTY + qb));
-          if (pd.valid && !issue_dq(pd)) { ok = false; break; }
-          pd = Pend{1, ks, n == 0, n == U.n - 1, g, oi};
-          ++ki;
-          ++vi;
-          ++g;
+            mma_ss(tmem + COL_DP, desc_kmajor<kBM>(dod, kk), desc_kmajor<BN>(vd, kk), IDESC_S,
+                   kk > 0 ? 1u : 0u);
+          mma_commit(bar(SPFULL));
         }
         ++qi;
-        ++oi;
       }
-      if (ok && pd.valid) issue_dq(pd);
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
     }
+  } else if (warp == MMA_B) {
+    // ------------------------------------------------------------ dQ issuer
+    if (lane == 0) {
+      const uint32_t tDQ = tmem + COL_DQ;
+      uint32_t g = 0, oi = 0;
+      bool ok = true;
+      for (uint32_t uk = 0; ok; ++uk) {
+        UnitInfo U;
+        if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
+        if (U.n < 0) break;
+        if (U.n <= 0) continue;
+        for (int n = 0; n < U.n; ++n, ++g) {
+          const int b = g & 1;
+          if (!wait_bar(bar(DSFULL + b), (g >> 1) & 1, wc, 0x105)) { ok = false; break; }
+          if (n == 0 && !wait_bar(bar(DQEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
+          tc_fence_after();
+          const int ks = g % NK;
+          const SDesc kd = mndesc<BN>(sK + ks * C::KV_BYTES);
+          const uint32_t tDS = tmem + COL_DS + b * DS_BUF;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tDQ, tDS + 8 * kk, desc_mnmajor<BN>(kd, kk, 0), IDESC_DQ,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(KEMPTY + ks));
+          mma_commit(bar(DSEMPTY + b));
+          if (n == U.n - 1) mma_commit(bar(DQFULL));
+        }
+        ++oi;
+      }
+      mma_commit(bar(DRAIN + 1));
+      wait_bar(bar(DRAIN + 1), 0, drain, 0x1fe);
+    }
   } else {
     // ------------------------------------------------------------ SiLU' + epilogue
-    // Eight warps: warp w owns TMEM lane quarter w % 4 and one half of the key
-    // columns of each S / dP tile (and of the dQ columns).
-    const int wq = warp & 3, hc = (warp - 2) >> 2;
+    // Sixteen warps: warp w owns TMEM lane quarter w % 4 (its 32 rows) and one
+    // quarter of the key columns of each S / dP tile (and of the dQ columns).
+    const int wq = warp & 3, cg = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
+    const bool releaser = warp == 2 && lane == 0;  // frees the V and Q stages
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tDP = tmem + COL_DP + lane_off + hc * CPW,
-                   tDQ = tmem + COL_DQ + lane_off, tDS = tmem + DS_BASE + lane_off + hc * DS_HALF;
+    const uint32_t tS = tmem + COL_S + lane_off + cg * CW, tDP = tmem + COL_DP + lane_off + cg * CW,
+                   tDQ = tmem + COL_DQ + lane_off + cg * DW,
+                   tDS = tmem + COL_DS + lane_off + cg * (CW / 2);
     const float half_alpha = 0.5f * a.alpha;
     const float out_scale = 0.5f * a.alpha * a.inv_L;  // dS is stored doubled
-    uint32_t g = 0, oi = 0;
+    uint32_t g = 0, oi = 0, qi = 0;
     bool ok = true;
     for (uint32_t uk = 0; ok; ++uk) {
       UnitInfo U;
@@ -256,53 +254,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int64_t grow = static_cast<int64_t>(q0) + i;
       const bool row_ok = i < Lq && grow < a.total_q;
       char* orow = static_cast<char*>(a.o0) +
-                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + hc * (D / 2)) * 2;
+                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + cg * DW) * 2;
       if (U.n <= 0) {
-        if (row_ok)
-          for (int c = 0; c < D / 64; ++c) store_zero32(orow + c * 64);
+        if (row_ok) store_zero_n<DW>(orow);
         continue;
       }
+      const int qb = qi % NQ;
       const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
-      for (int n = 0; n < U.n; ++n) {
+      for (int n = 0; n < U.n; ++n, ++g) {
         const int b = g & 1;
-        if (!wait_bar_warp(bar(SPFULL + b), (g >> 1) & 1, wc, 0x201)) { ok = false; break; }
+        if (!wait_bar_warp(bar(SPFULL), g & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
-        const int jc = BN * n + hc * CPW;
-        const bool need_mask = (a.causal && jc + CPW - 1 > i_warp) || (jc + CPW > Lk);
-        uint32_t xs[CPW], xp[CPW];
-        tmem_ld32x2(tS + b * BN, tDP + b * BN, xs, xp);
-        uint32_t d[CPW / 2];
+        uint32_t xs[CW], xp[CW];
+        tmem_ld_x2<CW>(tS, tDP, xs, xp);
+        warp_arrive(bar(SPEMPTY));  // S and dP of this step are in registers
+        if (releaser) {
+          // S_g and dP_g are complete: V_g and (after the last step) Q, dO are unused
+          mbar_arrive(bar(VEMPTY + g % NV));
+          if (n == U.n - 1) mbar_arrive(bar(QEMPTY + qb));
+        }
+        const int jc = BN * n + cg * CW;
+        const bool need_mask = (a.causal && jc + CW - 1 > i_warp) || (jc + CW > Lk);
+        uint32_t d[CW / 2];
         if (!need_mask) {
 #pragma unroll
-          for (int e = 0; e < CPW / 2; ++e)
+          for (int e = 0; e < CW / 2; ++e)
             d[e] = ds_pair<BF16>(xs[2 * e], xs[2 * e + 1], xp[2 * e], xp[2 * e + 1], half_alpha);
         } else {
 #pragma unroll
-          for (int e = 0; e < CPW / 2; ++e) {
+          for (int e = 0; e < CW / 2; ++e) {
             const int j = jc + 2 * e;
             const bool v0 = j < lim, v1 = j + 1 < lim;
             d[e] = ds_pair<BF16>(v0 ? xs[2 * e] : 0u, v1 ? xs[2 * e + 1] : 0u, v0 ? xp[2 * e] : 0u,
                                  v1 ? xp[2 * e + 1] : 0u, half_alpha);
           }
         }
-        tmem_st16(tDS + b * DS_BUF, d);
+        // dS buffer b last held step g-2: free once dQ += dS_{g-2} K_{g-2} ran
+        if (g >= 2 && !wait_bar_warp(bar(DSEMPTY + b), ((g >> 1) - 1) & 1, wc, 0x203)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st_w<CW / 2>(tDS + b * DS_BUF, d);
         tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(DSFULL + b));
-        ++g;
+        warp_arrive(bar(DSFULL + b));
       }
       if (!ok) break;
       if (!wait_bar_warp(bar(DQFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
+      if constexpr (DW <= 32) {
+        uint32_t x[DW];
+        tmem_ld_w<DW>(tDQ, x);
+        if (row_ok) store_row_n<DW, BF16>(orow, x, out_scale);
+      } else {
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tDQ + hc * (D / 2) + 32 * c, x);
-        if (row_ok) store_row32<BF16>(orow + c * 64, x, out_scale);
+        for (int c = 0; c < DW / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tDQ + 32 * c, x);
+          if (row_ok) store_row_n<32, BF16>(orow + c * 64, x, out_scale);
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(DQEMPTY));
+      warp_arrive(bar(DQEMPTY));
       ++oi;
+      ++qi;
     }
   }
 
@@ -325,7 +339,7 @@ cudaError_t launch_dq_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, DqCfg<D>::SMEM, st, pdl, tq, tdo, tk, tv, a);
+  return launch_attn(kern, grid, kDqThreads, DqCfg<D>::SMEM, st, pdl, tq, tdo, tk, tv, a);
 }
 
 }  // namespace

@@ -272,6 +272,61 @@ __device__ __forceinline__ void store_zero32(void* dst) {
   for (int v = 0; v < 4; ++v) p[v] = z;
 }
 
+// Compile-time-width variants used by the 16-row-warp kernels.
+template <int N>
+__device__ __forceinline__ void tmem_ld_x2(uint32_t ta, uint32_t tb, uint32_t (&a)[N],
+                                           uint32_t (&b)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) tmem_ld32x2(ta, tb, a, b);
+  else tmem_ld16x2(ta, tb, a, b);
+}
+template <int N>
+__device__ __forceinline__ void tmem_ld_w(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) tmem_ld32(taddr, r);
+  else tmem_ld16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_w(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+  if constexpr (N == 32) tmem_st32(taddr, r);
+  else if constexpr (N == 16) tmem_st16(taddr, r);
+  else tmem_st8(taddr, r);
+}
+
+// N fp32 values (N a multiple of 8) scaled, rounded to 16 bits and stored
+// with 16-byte writes; dst is 16-byte aligned.
+template <int N, bool BF16>
+__device__ __forceinline__ void store_row_n(void* dst, const uint32_t (&x)[N], float scale) {
+  static_assert(N % 8 == 0, "whole 16-byte groups");
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < N / 8; ++v) {
+    uint4 w;
+    w.x = pack2<BF16>(__uint_as_float(x[8 * v + 0]) * scale, __uint_as_float(x[8 * v + 1]) * scale);
+    w.y = pack2<BF16>(__uint_as_float(x[8 * v + 2]) * scale, __uint_as_float(x[8 * v + 3]) * scale);
+    w.z = pack2<BF16>(__uint_as_float(x[8 * v + 4]) * scale, __uint_as_float(x[8 * v + 5]) * scale);
+    w.w = pack2<BF16>(__uint_as_float(x[8 * v + 6]) * scale, __uint_as_float(x[8 * v + 7]) * scale);
+    p[v] = w;
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_zero_n(void* dst) {
+  static_assert(N % 8 == 0, "whole 16-byte groups");
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int v = 0; v < N / 8; ++v) p[v] = z;
+}
+
+// Row-warp barrier arrival: every lane's TMEM accesses are complete (waited
+// for by the caller), then one arrival per warp.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // K-major operand descriptor: tile of ROWS rows by D columns, stored as D/64
 // chunks of [ROWS][64] 16-bit elements with the 128-byte swizzle (the TMA box
 // layout).  kk selects the 16-element K step.

@@ -334,7 +334,7 @@ cudaError_t launch_fwd_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap&
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, FwdCfg<D>::SMEM, st, pdl, tq, tk, tv, a);
+  return launch_attn(kern, grid, kAttnThreads, FwdCfg<D>::SMEM, st, pdl, tq, tk, tv, a);
 }
 
 }  // namespace

@@ -13,6 +13,13 @@ namespace hstu {
 constexpr int kSchedThreads = 1024;
 constexpr int kAttnThreads = 320;   // warp 0: TMA, warp 1: MMA, warps 2-9: row work
 constexpr int kRowThreads = 256;    // two warps per TMEM lane quarter, one per column half
+// Backward kernels: warp 0 TMA, warp 1 MMA, warps 2-17 row work (four warps
+// per TMEM lane quarter, one per quarter of the columns).
+constexpr int kRowWarps16 = 16;
+constexpr int kWideThreads = 64 + 32 * kRowWarps16;
+// dQ kernel: one more warp (18) issues the dQ accumulation MMAs, so the two
+// MMA streams wait on their own barriers without stalling each other.
+constexpr int kDqThreads = kWideThreads + 32;
 constexpr int kTmemCols = 512;
 
 // Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
@@ -68,13 +75,15 @@ struct FwdCfg {
 
 // ------------------------------------------------------------ dQ config
 // K is read by S = Q K^T and by dQ += dS K (freed last); V only by dP = dO V^T.
-// 64-key steps so that S and dP fit twice in TMEM next to dQ.
+// 128-key steps (64 at D = 256) so every MMA but the D = 256 S and dP has
+// N >= 128; S and dP are single-buffered (the row warps release them as soon
+// as they are loaded), dS is double-buffered.
 template <int D>
 struct DqCfg {
-  static constexpr int BN = 64;
+  static constexpr int BN = D == 256 ? 64 : 128;
   static constexpr int NQ = D == 64 ? 2 : 1;         // (Q, dO) buffers
-  static constexpr int NK = D == 64 ? 6 : (D == 128 ? 5 : 2);
-  static constexpr int NV = D == 64 ? 6 : (D == 128 ? 5 : 1);
+  static constexpr int NK = D == 64 ? 5 : (D == 128 ? 3 : 2);
+  static constexpr int NV = D == 64 ? 5 : (D == 128 ? 2 : 1);
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + (NK + NV) * KV_BYTES;
@@ -82,16 +91,20 @@ struct DqCfg {
 };
 
 // ------------------------------------------------------------ dK/dV config
+// 128-query steps (64 at D = 256) so S^T and dP^T are N = 128 MMAs.  A^T goes
+// to a shared-memory tile (the A operand of dV += A^T dO), dS^T stays in TMEM
+// in place over dP^T (the A operand of dK += dS^T Q).
 template <int D>
 struct DkdvCfg {
-  static constexpr int BQ = 64;                      // queries per inner tile
+  static constexpr int BQ = D == 256 ? 64 : 128;     // queries per inner tile
   static constexpr int DH = D == 256 ? 128 : D;      // dK/dV columns per unit
   static constexpr int SPLIT = D / DH;
   static constexpr int NKV = D == 64 ? 2 : 1;        // stationary (K, V) buffers
-  static constexpr int NS = D == 64 ? 6 : (D == 128 ? 5 : 1);
+  static constexpr int NS = D == 64 ? 3 : (D == 128 ? 2 : 1);
   static constexpr int KV_BYTES = kBM * D * 2;
   static constexpr int Q_BYTES = BQ * D * 2;
-  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES;
+  static constexpr int P_BYTES = kBM * BQ * 2;       // A^T staging tile
+  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES + P_BYTES;
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
 };
 
@@ -115,11 +128,11 @@ __global__ void hstu_sched_kernel(SchedArgs a);
 // dependent launch); the kernel orders itself with griddepcontrol.wait as
 // AttnArgs::pdl_wait says.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_attn(void (*kern)(KArgs...), int grid, int smem, cudaStream_t st,
-                               bool pdl, Args&&... args) {
+inline cudaError_t launch_attn(void (*kern)(KArgs...), int grid, int threads, int smem,
+                               cudaStream_t st, bool pdl, Args&&... args) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
