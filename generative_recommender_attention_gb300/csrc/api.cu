@@ -179,8 +179,9 @@ size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
                                 int32_t num_heads, int32_t head_dim, int32_t is_bwd) {
   if (batch < 0 || total_q < 0 || total_k < 0 || num_heads <= 0 || !supported_dim(head_dim))
     return 0;
-  size_t bytes = kHeaderBytes + 16 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
-  if (is_bwd) bytes += 16 * static_cast<size_t>(cap_b(batch, total_k, num_heads, head_dim));
+  // a unit record is two int4 (32 bytes)
+  size_t bytes = kHeaderBytes + 32 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
+  if (is_bwd) bytes += 32 * static_cast<size_t>(cap_b(batch, total_k, num_heads, head_dim));
   return (bytes + 255) & ~size_t(255);
 }
 
@@ -245,12 +246,11 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
   sa.header = header;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
-  hstu_sched_kernel<<<1, kSchedThreads, sched_bytes, stream>>>(sa);
-  if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  if (launch_sched(1, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
-  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
+  a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
@@ -314,19 +314,18 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
 
   int* header = static_cast<int*>(workspace);
   int4* unitsA = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
-  int4* unitsB = unitsA + capA;
+  int4* unitsB = unitsA + 2 * capA;  // two int4 per unit
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
-  hstu_sched_kernel<<<2, kSchedThreads, sched_bytes, stream>>>(sa);
-  if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  if (launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
-  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k; a.total_q = total_q; a.total_k = total_k;
+  a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.timeout_ns = kWaitTimeoutNs;
   if (total_q > 0) {
@@ -447,7 +446,7 @@ hstu_status_t hstu_attn_selftest_timeout(void* workspace, uint32_t timeout_us, c
 // library holds one such array until the process exits.
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB: up to 65,520 work units
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB: up to 65,528 work units
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device, looked up once

@@ -114,14 +114,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       uint32_t kvi = 0, qi = 0;
       bool ok = true;
-      // claim units one ahead: the next claim overlaps this unit's loads
-      UnitInfo nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1),
-                                   n_units);
+      int prev_n = kPrefetch;  // steps of the previous unit (the first unit is not warmed)
+      auto prefetch_qdo = [&](int h, int row) {
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) {
+          tma_prefetch_3d(&tm_q, 64 * c, h, row);
+          tma_prefetch_3d(&tm_do, 64 * c, h, row);
+        }
+      };
+      // units are claimed one ahead: the next claim overlaps this unit's loads
+      // the first unit of each CTA is its own index; later ones come from the counter
+      UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         const UnitInfo U = nx;
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1), n_units);
+        nx = load_unit_info(a.units, gridDim.x + atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz / SPLIT;
         const int k_row0 = U.k0 + kBM * U.tile;
@@ -137,7 +145,29 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tma_load_3d(vt + c * (kBM * 128), &tm_v, bar(KVFULL + kb), 64 * c, h, k_row0);
         }
         ++kvi;
+        // L2 warm-up runs kPrefetch steps ahead of the loads along the flat
+        // stream (this unit's later Q/dO tiles, then the next unit's K, V and
+        // first Q/dO tiles); what a short previous unit could not cover is
+        // issued here.
+        if (prev_n < kPrefetch)
+          for (int m = 0; m < min(U.n, kPrefetch - prev_n); ++m) prefetch_qdo(h, q_seq0 + BQ * (m0 + m));
+        prev_n = U.n;
         for (int m = 0; m < U.n; ++m) {
+          const int t = m + kPrefetch;
+          if (t < U.n) {
+            prefetch_qdo(h, q_seq0 + BQ * (m0 + t));
+          } else if (t - U.n < nx.n) {
+            const int nh = nx.hz / SPLIT;
+            if (t == U.n) {
+#pragma unroll
+              for (int c = 0; c < KCH; ++c) {
+                tma_prefetch_3d(&tm_k, 64 * c, nh, nx.k0 + kBM * nx.tile);
+                tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
+              }
+            }
+            const int nm0 = a.causal ? (kBM * nx.tile) / BQ : 0;
+            prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
+          }
           const int s = qi % NS;
           if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           const int row = q_seq0 + BQ * (m0 + m);

@@ -113,14 +113,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0) {
       uint32_t qi = 0, g = 0;
       bool ok = true;
-      // claim units one ahead: the next claim overlaps this unit's loads
-      UnitInfo nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1),
-                                   n_units);
+      auto prefetch_kv = [&](int h, int row) {
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) {
+          tma_prefetch_3d(&tm_k, 64 * c, h, row);
+          tma_prefetch_3d(&tm_v, 64 * c, h, row);
+        }
+      };
+      int prev_n = kPrefetch;  // steps of the previous unit (the first unit is not warmed)
+      // units are claimed one ahead: the next claim overlaps this unit's loads
+      // the first unit of each CTA is its own index; later ones come from the counter
+      UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         const UnitInfo U = nx;
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1), n_units);
+        nx = load_unit_info(a.units, gridDim.x + atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz;
         const int q_row0 = U.q0 + kBM * U.tile;
@@ -135,7 +143,27 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tma_load_3d(dot + c * (kBM * 128), &tm_do, bar(QFULL + qb), 64 * c, h, q_row0);
         }
         ++qi;
+        // L2 warm-up runs kPrefetch steps ahead of the loads along the flat
+        // stream (this unit's later K/V tiles, then the next unit's Q, dO and
+        // first K/V tiles); what a short previous unit could not cover is
+        // issued here.
+        if (prev_n < kPrefetch)
+          for (int m = 0; m < min(U.n, kPrefetch - prev_n); ++m) prefetch_kv(h, kv_row0 + BN * m);
+        prev_n = U.n;
         for (int n = 0; n < U.n; ++n, ++g) {
+          const int t = n + kPrefetch;
+          if (t < U.n) {
+            prefetch_kv(h, kv_row0 + BN * t);
+          } else if (t - U.n < nx.n) {
+            if (t == U.n) {
+#pragma unroll
+              for (int c = 0; c < KCH; ++c) {
+                tma_prefetch_3d(&tm_q, 64 * c, nx.hz, nx.q0 + kBM * nx.tile);
+                tma_prefetch_3d(&tm_do, 64 * c, nx.hz, nx.q0 + kBM * nx.tile);
+              }
+            }
+            prefetch_kv(nx.hz, nx.k0 + BN * (t - U.n));
+          }
           const int ks = g % NK, vs = g % NV, f = g % NF;
           if (!wait_bar(bar(KEMPTY + ks), ((g / NK) & 1) ^ 1, wc, 0x002) ||
               !wait_bar(bar(VEMPTY + vs), ((g / NV) & 1) ^ 1, wc, 0x003)) {

@@ -90,20 +90,15 @@ struct UnitInfo {
   int q0, Lq, k0, Lk;
 };
 
-__device__ __forceinline__ UnitInfo load_unit_info(const int4* units, const int32_t* cu_q,
-                                                   const int32_t* cu_k, int u, int n_units) {
+__device__ __forceinline__ UnitInfo load_unit_info(const int4* units, int u, int n_units) {
   UnitInfo r{0, 0, 0, -1, 0, 0, 0, 0};  // n = -1: no more units
   if (u < n_units) {
-    const int4 v = units[u];
+    const int4 v = units[2 * u], w = units[2 * u + 1];
     r.b = v.x; r.tile = v.y; r.hz = v.z; r.n = v.w;
-    r.q0 = cu_q[v.x];
-    r.Lq = cu_q[v.x + 1] - r.q0;
-    r.k0 = cu_k[v.x];
-    r.Lk = cu_k[v.x + 1] - r.k0;
+    r.q0 = w.x; r.Lq = w.y; r.k0 = w.z; r.Lk = w.w;
   }
   return r;
 }
-
 
 // Warp-uniform wait for the four row warps: lane 0 polls with the bounded
 // wait and broadcasts the outcome, so a give-up never splits a warp in front

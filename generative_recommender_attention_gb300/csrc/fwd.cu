@@ -3,7 +3,8 @@
 //
 // Persistent, warp-specialised kernel; one CTA per SM walks the longest-first
 // list of 128-row query tiles written by the scheduler kernel.
-//   warp 0      TMA producer: Q tile per unit, K_{n+1} ahead of V_n.
+//   warp 0      TMA producer: Q tile per unit, K_g ahead of V_{g-2}, one
+//               flat stream across units.
 //   warp 1      tcgen05 issuer.  S tiles live in three TMEM buffers and run
 //               two steps ahead: S_{g+2} = Q K^T is queued before
 //               O += P_g V_g, so the tensor pipe has independent work while
@@ -109,7 +110,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per unit: Q, K_0, then K_{n+1} ahead of V_n, so K runs one step ahead.
+    // One flat stream over all of this CTA's units, in the order the MMA
+    // thread consumes it: Q of a unit before its first K, and K_g before
+    // V_{g-LA} (the MMA issues S_g before O += P_{g-LA} V_{g-LA}).  The next
+    // unit's Q and first K tiles therefore go out before this unit's last V
+    // tiles, so a unit boundary does not wait for a fresh load.
     if (lane == 0) {
       uint32_t qi = 0, ki = 0, vi = 0;
       auto load_kv = [&](const CUtensorMap* map, uint32_t base_s, int nst, uint32_t& cnt,
@@ -123,15 +128,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++cnt;
         return true;
       };
+      auto prefetch_kv = [&](int h, int row) {
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) {
+          tma_prefetch_3d(&tm_k, 64 * c, h, row);
+          tma_prefetch_3d(&tm_v, 64 * c, h, row);
+        }
+      };
+      auto prefetch_q = [&](const UnitInfo& u) {
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) tma_prefetch_3d(&tm_q, 64 * c, u.hz, u.q0 + kBM * u.tile);
+      };
+      int prev_n = kPrefetch;  // steps of the previous unit (the first unit is not warmed)
+      // V loads not yet issued (at most LA of them): key row and head
+      static_assert(LA == 2, "two deferred V loads kept in registers");
+      int v_row0 = 0, v_h0 = 0, v_row1 = 0, v_h1 = 0, nv = 0;
       bool ok = true;
-      // claim units one ahead: the next claim overlaps this unit's loads
-      UnitInfo nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1),
-                                   n_units);
+      // units are claimed one ahead: the next claim overlaps this unit's loads
+      // the first unit of each CTA is its own index; later ones come from the counter
+      UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         const UnitInfo U = nx;
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        nx = load_unit_info(a.units, a.cu_q, a.cu_k, atomicAdd(a.header + a.next_slot, 1), n_units);
+        nx = load_unit_info(a.units, gridDim.x + atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz;
         const int q_row0 = U.q0 + kBM * U.tile;
@@ -144,19 +164,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(sQ + qb * C::Q_BYTES + c * (kBM * 128), &tm_q, bar(QFULL + qb), 64 * c, h,
                       q_row0);
         ++qi;
-        if (!load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, kv_row0, h, 0x002)) { ok = false; break; }
+        // L2 warm-up runs kPrefetch steps ahead of the loads along the flat
+        // stream (this unit's later K/V tiles, then the next unit's Q and
+        // first K/V tiles); what a short previous unit could not cover is
+        // issued here.
+        if (prev_n < kPrefetch)
+          for (int m = 0; m < min(U.n, kPrefetch - prev_n); ++m) prefetch_kv(h, kv_row0 + BN * m);
+        prev_n = U.n;
         for (int n = 0; n < U.n; ++n) {
-          if (n + 1 < U.n &&
-              !load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, kv_row0 + BN * (n + 1), h, 0x002)) {
-            ok = false;
-            break;
+          const int row = kv_row0 + BN * n;
+          const int t = n + kPrefetch;
+          if (t < U.n) {
+            prefetch_kv(h, kv_row0 + BN * t);
+          } else if (t - U.n < nx.n) {
+            if (t == U.n) prefetch_q(nx);
+            prefetch_kv(nx.hz, nx.k0 + BN * (t - U.n));
           }
-          if (!load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, kv_row0 + BN * n, h, 0x003)) {
-            ok = false;
-            break;
+          if (!load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, row, h, 0x002)) { ok = false; break; }
+          if (nv == LA) {
+            if (!load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, v_row0, v_h0, 0x003)) { ok = false; break; }
+            v_row0 = v_row1; v_h0 = v_h1;
+            v_row1 = row; v_h1 = h;
+          } else if (nv == 1) {
+            v_row1 = row; v_h1 = h; nv = 2;
+          } else {
+            v_row0 = row; v_h0 = h; nv = 1;
           }
         }
       }
+      if (ok && nv >= 1) ok = load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, v_row0, v_h0, 0x003);
+      if (ok && nv == 2) ok = load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, v_row1, v_h1, 0x003);
       // let the last copies land before the block may exit
       for (uint32_t i = qi > NQ ? qi - NQ : 0; i < qi; ++i)
         wait_bar(bar(QFULL + i % NQ), (i / NQ) & 1, drain, 0x0f1);

@@ -26,6 +26,8 @@ constexpr int kTmemCols = 512;
 // address slot, the abort flags, and slack to align the tiles to 1024 bytes.
 constexpr int kCtlBytes = 1024;
 constexpr int kAlignSlack = 1024;
+// K/V steps warmed in L2 ahead of the TMA loads (and of the next unit).
+constexpr int kPrefetch = 4;
 
 struct SchedArgs {
   const int32_t* cu_q;
@@ -39,15 +41,13 @@ struct SchedArgs {
 };
 
 struct AttnArgs {
-  const int32_t* cu_q;
-  const int32_t* cu_k;
   int64_t total_q, total_k;
   int H;
   int causal;
   float alpha;
   float inv_L;          // 1 / L_scale
   int* header;          // workspace header
-  const int4* units;    // work list walked by this kernel
+  const int4* units;    // work list walked by this kernel (two int4 per unit)
   int units_slot;       // header word holding its length
   uint64_t timeout_ns;  // limit of every barrier wait
   int next_slot;        // header word counting units claimed so far
@@ -119,6 +119,8 @@ static_assert(FwdCfg<64>::SMEM <= 232448 && DqCfg<64>::SMEM <= 232448 &&
               "smem");
 
 __global__ void hstu_sched_kernel(SchedArgs a);
+// Scheduler launch: `lists` blocks (1: list A only, 2: lists A and B).
+cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a);
 
 // Launchers: return cudaErrorInvalidValue for a head_dim outside {64,128,256}.
 // Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (q/do: 128-row

@@ -8,8 +8,10 @@
 //   list B: key tiles of 128 rows; cost = number of query tiles of `bq_b`
 //           rows that can see the tile; each key tile is emitted once per head
 //           and per D split.
-// Units with cost 0 are kept (their rows must be written as zeros) and sort
-// last.  Order inside one cost bucket is whatever the atomics give; it only
+// Each unit record is two int4: {sequence, tile, head (x split), cost} and
+// {q offset, q length, k offset, k length}, so a consumer needs one round
+// trip to global memory per unit.  Units with cost 0 are kept (their rows
+// must be written as zeros) and sort last.  Order inside one cost bucket is whatever the atomics give; it only
 // changes timing, never results.
 #include "kernels.h"
 
@@ -79,8 +81,12 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   int4* units = list_b ? a.units_b : a.units_a;
   const int per_tile = list_b ? a.H * a.split_b : a.H;
   const int nb = cmax + 1;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = blockDim.x >> 5;
 
+  // Launched early behind the previous grid of the stream, which may still
+  // read this workspace: wait for it before writing anything.
+  grid_dependency_wait();
   // the attention grid queued behind this one may start its prologue now
   if (tid == 0) grid_launch_dependents();
   if (!list_b && tid == 0) {
@@ -99,16 +105,14 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
 
-  // pass 1: histogram of costs
-  for (int b = tid; b < a.B; b += blockDim.x) {
+  // pass 1: histogram of costs; a warp per sequence, a lane per tile
+  for (int b = warp; b < a.B; b += nwarps) {
     int Lq, Lk;
     seq_lengths(a, b, Lq, Lk);
-    if (list_b) {
-      int nt = ceil_div(Lk, kBM);
-      for (int s = 0; s < nt; ++s) atomicAdd(&hist[min(cost_b(a, s, Lq), cmax)], per_tile);
-    } else {
-      int nt = ceil_div(Lq, kBM);
-      for (int t = 0; t < nt; ++t) atomicAdd(&hist[min(cost_a(a, t, Lq, Lk), cmax)], per_tile);
+    const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
+    for (int t = lane; t < nt; t += 32) {
+      const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
+      atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
   __syncthreads();
@@ -128,18 +132,19 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
   __syncthreads();
 
-  // pass 3: emit units at their bucket cursors
+  // pass 3: emit complete unit records at their bucket cursors
   int overflow = 0;
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    int Lq, Lk;
-    seq_lengths(a, b, Lq, Lk);
-    int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
-    for (int t = 0; t < nt; ++t) {
-      int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
-      int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
+  for (int b = warp; b < a.B; b += nwarps) {
+    const int q0 = __ldg(a.cu_q + b), k0 = __ldg(a.cu_k + b);
+    const int Lq = max(0, __ldg(a.cu_q + b + 1) - q0), Lk = max(0, __ldg(a.cu_k + b + 1) - k0);
+    const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
+    for (int t = lane; t < nt; t += 32) {
+      const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
+      const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       for (int e = 0; e < per_tile; ++e) {
         if (pos + e < cap) {
-          units[pos + e] = make_int4(b, t, e, cost);
+          units[2 * (pos + e)] = make_int4(b, t, e, cost);
+          units[2 * (pos + e) + 1] = make_int4(q0, Lq, k0, Lk);
         } else {
           overflow = 1;
         }
@@ -148,6 +153,20 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
   if (overflow) atomicExch(a.header + (list_b ? kHdrOverflowB : kHdrOverflow), 1);
   if (tid == 0) a.header[list_b ? kHdrUnitsB : kHdrUnitsA] = min(total, cap);
+}
+
+cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(lists));
+  cfg.blockDim = dim3(kSchedThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, hstu_sched_kernel, a);
 }
 
 // One thread waits on a barrier that nothing completes; the bounded wait must

@@ -167,10 +167,10 @@ hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_
  * needs.  Arguments and results are those of hstu_attn_fwd; the caller still
  * passes every input and output.
  *
- * The schedule lives in a 1 MiB array in the library's own device memory
+ * The schedule lives in a 2 MiB array in the library's own device memory
  * (one per GPU that loads the library, held until exit).  Problems whose
- * schedule exceeds it, hstu_attn_workspace_size(..., is_bwd = 0) > 1 MiB,
- * i.e. more than 65,520 work units (num_heads * (ceil(total_q / 128) + batch)),
+ * schedule exceeds it, hstu_attn_workspace_size(..., is_bwd = 0) > 2 MiB,
+ * i.e. more than 65,528 work units (num_heads * (ceil(total_q / 128) + batch)),
  * return HSTU_ERR_INVALID_ARG.  The first call on a device looks the array's
  * address up (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture.  All calls share the one array and each

@@ -54,13 +54,13 @@ def test_version_and_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.hstu_attn_workspace_size
-    # header + 16 bytes per unit, units <= H * (ceil(T/128) + B), 256-aligned
-    assert ws(4, 309, 309, 2, 64, 0) == (256 + 16 * 2 * (3 + 4) + 255) // 256 * 256
+    # header + 32 bytes per unit record, units <= H * (ceil(T/128) + B), 256-aligned
+    assert ws(4, 309, 309, 2, 64, 0) == (256 + 32 * 2 * (3 + 4) + 255) // 256 * 256
     fwd = ws(32, 20480, 20480, 4, 128, 0)
     bwd = ws(32, 20480, 20480, 4, 128, 1)
-    assert bwd == ((256 + 16 * 4 * (160 + 32) * 2) + 255) // 256 * 256 and fwd < bwd
+    assert bwd == ((256 + 32 * 4 * (160 + 32) * 2) + 255) // 256 * 256 and fwd < bwd
     # D = 256 splits dK/dV into two column halves: twice the key-side units
-    assert ws(16, 65536, 65536, 2, 256, 1) == 256 + 16 * 2 * (512 + 16) * 3
+    assert ws(16, 65536, 65536, 2, 256, 1) == 256 + 32 * 2 * (512 + 16) * 3
     assert ws(1, 10, 10, 1, 96, 0) == 0        # unsupported head_dim
     assert ws(-1, 10, 10, 1, 64, 0) == 0
     assert ws(1, 10, 10, 0, 64, 0) == 0

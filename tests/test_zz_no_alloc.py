@@ -63,9 +63,9 @@ def test_noalloc_matches_regular_forward_twice(name):
 
 def test_noalloc_rejects_schedules_over_its_limit():
     lib = L.library()
-    # 65,521 work units: one more than the 1 MiB array holds; rejected on the host
+    # 65,529 work units: one more than the 2 MiB array holds; rejected on the host
     fake = L.CTen(0x1000, 64, 64)
     st = lib.hstu_attn_fwd_noalloc(fake, fake, fake, L.Ten(0x1000, 64, 64), 0x2000, 0x2000, 1,
-                                   128 * 65520, 128 * 65520, 1, 64, L.HSTU_BF16, 128, 128,
+                                   128 * 65528, 128 * 65528, 1, 64, L.HSTU_BF16, 128, 128,
                                    0.125, 0, 1, None)
     assert st == 1
