@@ -177,6 +177,9 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="run warm-up and timed steps only (no second pass, end-to-end, clocks or "
+                         "CPU baseline) and print no JSON line: for wrapping in a profiler")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -233,6 +236,14 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    if args.kernels_only:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        assert hstu.last_device_status(ws_b) == 0 and hstu.last_device_status(ws_f) == 0
+        return 0
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
         if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/hstu_clocks.csv")
     wall0 = time.perf_counter()
@@ -288,13 +299,15 @@ def main():
     dom = max(kernels, key=lambda k: kernels[k][1])
     f_dom, ms_dom = kernels[dom]
     achieved = f_dom / (ms_dom * 1e-3) / 1e12
+    # DRAM bytes of one launch of the dominant kernel, from the committed ncu
+    # summary of this workload (a line "traffic <kernel> <bytes>"), if any
     traffic = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    tfile = os.path.join(ROOT, "profiles", f"kernels_{w.name}_full.md")
     if os.path.exists(tfile):
-        try:
-            traffic = json.load(open(tfile)).get(dom)
-        except Exception:
-            traffic = None
+        for tline in open(tfile):
+            parts = tline.split()
+            if len(parts) == 3 and parts[0] == "traffic" and parts[1] == dom:
+                traffic = int(parts[2])
 
     # end to end through the public API: pinned host inputs in, outputs back
     pin = {k: x[k].pin_memory() for k in ("q", "k", "v", "do", "cu_seqlens_q", "cu_seqlens_k")}

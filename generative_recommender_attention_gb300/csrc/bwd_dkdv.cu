@@ -9,7 +9,8 @@
 // dP^T = V dO^T into TMEM, forms A^T = M (.) SiLU(alpha S^T) and
 // dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
 // element), and accumulates dV += A^T dO and dK += dS^T Q.  No atomics.
-//   warp 0       TMA: K and V per unit, Q and dO per step (one barrier).
+//   warp 0       TMA: K and V per unit, Q and dO per step (separate rings:
+//                Q is released after dK, dO after dV).
 //   warp 1       tcgen05 issuer.  Per step g: S^T_g (once the row warps have
 //                loaded S^T_{g-1}), dK += dS^T_{g-1} Q_{g-1}, dP^T_g, then
 //                dV += A^T_{g-1} dO_{g-1}.
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   enum {
     KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
-    STFULL = QEMPTY + NS, SEMPTY = STFULL + 1, DSFULL = SEMPTY + 1, PFULL = DSFULL + 1,
+    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, STFULL = DOEMPTY + NS, SEMPTY = STFULL + 1, DSFULL = SEMPTY + 1, PFULL = DSFULL + 1,
     PEMPTY = PFULL + 1, ACCFULL = PEMPTY + 1, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
     UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
   };
@@ -75,7 +76,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NKV; ++i) { mbar_init(bar(KVFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1); }
-    for (int i = 0; i < NS; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
+      mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 1);
+    }
     mbar_init(bar(STFULL), 1);
     mbar_init(bar(SEMPTY), RW);
     mbar_init(bar(DSFULL), RW);
@@ -169,21 +173,28 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
           }
           const int s = qi % NS;
-          if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           const int row = q_seq0 + BQ * (m0 + m);
-          mbar_arrive_expect_tx(bar(QFULL + s), 2 * C::Q_BYTES);
+          // Q_g is free after dK_g, dO_g only after dV_g: separate rings, so
+          // each reload starts as soon as its own tile is released
+          if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(QFULL + s), C::Q_BYTES);
 #pragma unroll
-          for (int c = 0; c < KCH; ++c) {
+          for (int c = 0; c < KCH; ++c)
             tma_load_3d(sQ + s * C::Q_BYTES + c * (BQ * 128), &tm_q, bar(QFULL + s), 64 * c, h, row);
-            tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(QFULL + s), 64 * c, h, row);
-          }
+          if (!wait_bar(bar(DOEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x004)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(DOFULL + s), C::Q_BYTES);
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(DOFULL + s), 64 * c, h, row);
           ++qi;
         }
       }
       for (uint32_t i = kvi > NKV ? kvi - NKV : 0; i < kvi; ++i)
         wait_bar(bar(KVFULL + i % NKV), (i / NKV) & 1, drain, 0x0f1);
-      for (uint32_t i = qi > NS ? qi - NS : 0; i < qi; ++i)
+      for (uint32_t i = qi > NS ? qi - NS : 0; i < qi; ++i) {
         wait_bar(bar(QFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
+        wait_bar(bar(DOFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -212,10 +223,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           mma_ts(tDK, tmem + COL_DPT + col, desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC,
                  (!p.first || kk > 0) ? 1u : 0u);
         }
+        mma_commit(bar(QEMPTY + p.s));
         return true;
       };
       // dV += A^T dO once A^T is in shared memory (ACCEMPTY was waited for by
-      // the dK half of the same step); frees the A^T tile and the Q/dO stage
+      // the dK half of the same step); frees the A^T tile and the dO stage
       auto issue_dv = [&](const Pend& p) -> bool {
         if (!wait_bar(bar(PFULL), p.g & 1, wc, 0x109)) return false;
         const SDesc dod = mndesc<BQ>(sDO + p.s * C::Q_BYTES);
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           mma_ss(tDV, desc_kmajor<kBM>(pdesc, kk), desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC,
                  (!p.first || kk > 0) ? 1u : 0u);
         mma_commit(bar(PEMPTY));
-        mma_commit(bar(QEMPTY + p.s));
+        mma_commit(bar(DOEMPTY + p.s));
         if (p.last) mma_commit(bar(ACCFULL));
         return true;
       };
@@ -256,6 +268,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                    kk > 0 ? 1u : 0u);
           // dK of step g-1 reads dS^T_{g-1} from the dP^T columns: before dP^T_g
           if (!SERIAL && pd.valid && !issue_dk(pd)) { ok = false; break; }
+          if (!wait_bar(bar(DOFULL + s), (qi / NS) & 1, wc, 0x107)) { ok = false; break; }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + COL_DPT, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk), IDESC_S,
