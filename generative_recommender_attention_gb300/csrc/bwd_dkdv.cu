@@ -5,27 +5,25 @@
 //
 // Key-stationary: each CTA owns a 128-row key tile (and, for D = 256, one
 // 128-column half of dK/dV, so the accumulators fit in TMEM) and walks the
-// query tiles that can see it.  Per step it recomputes S^T = K Q^T and
-// dP^T = V dO^T into TMEM, forms A^T = M (.) SiLU(alpha S^T) and
-// dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
-// element), and accumulates dV += A^T dO and dK += dS^T Q.  No atomics.
-//   warp 0       TMA: K and V per unit, Q and dO per step (separate rings:
-//                Q is released after dK, dO after dV).
-//   warp 1       tcgen05 issuer.  Per step g: S^T_g (once the row warps have
-//                loaded S^T_{g-1}), dK += dS^T_{g-1} Q_{g-1}, dP^T_g, then
-//                dV += A^T_{g-1} dO_{g-1}.
+// 64-row query tiles that can see it.  Per half-step h it recomputes
+// S^T = K Q^T and dP^T = V dO^T into TMEM, forms A^T = M (.) SiLU(alpha S^T)
+// and dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
+// element), writes both back in place as 16-bit, and accumulates
+// dV += A^T dO and dK += dS^T Q with the A operand read from TMEM.  No
+// atomics.
+//   warp 0       TMA: K and V per unit, Q and dO per half-step (separate
+//                rings: Q is released after dK, dO after dV).
+//   warp 1       tcgen05 issuer of S^T_h and dP^T_h into buffer h % 2, once
+//                the accumulation of step h-2 has consumed that buffer.
+//   warp 18      tcgen05 issuer of dV += A^T_h dO_h and dK += dS^T_h Q_h.
 //   warps 2-17   row work, four warps per TMEM lane quarter (one per quarter
-//                of the query columns): dS^T first (it gates dP^T_{g+1}),
-//                then A^T.
-// TMEM: S^T | dP^T | dV | dK.  dS^T is written in place over the dP^T
-// columns its warp just read (the TMEM A operand of dK += dS^T Q); A^T goes
-// to a shared-memory tile in the 128-byte-swizzled K-major layout (the A
-// operand of dV += A^T dO).  S^T is released as soon as it is loaded, so
-// S^T_{g+1} runs on the tensor pipe while the row warps work on step g.
-// dP^T_{g+1} follows dK += dS^T_g Q_g from the same thread, and tcgen05.mma
-// operations from one thread execute in issue order, so dS^T_g is consumed
-// before it is overwritten; dV, which reads only shared memory, is issued
-// after dP^T_{g+1} so it stays off that chain.
+//                of the query columns).
+// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  While the row warps work on
+// buffer h % 2 the tensor pipe runs the other buffer's S^T / dP^T and the
+// previous accumulation, so the row work stays off the tensor pipe's path.
+// The N = 64 S^T / dP^T MMAs run at about two thirds of the tensor rate; that
+// costs less than serialising the row work with 128-query steps, for which
+// TMEM has no room to double-buffer.
 #include "kernels.h"
 
 namespace hstu {
@@ -33,7 +31,7 @@ namespace hstu {
 namespace {
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kWideThreads, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q,
@@ -44,10 +42,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   constexpr int RW = kRowWarps16;
   constexpr int CW = BQ / 4;   // query columns per row warp
   constexpr int DW = DH / 4;   // dK / dV columns per row warp
-  constexpr bool SERIAL = NS == 1;  // one Q/dO stage: accumulate before the next S^T
+  constexpr int MMA_B = 2 + RW;  // warp of the accumulation issuer
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BQ, false, false);
   constexpr uint32_t IDESC_ACC = idesc_f16(BF16, kBM, DH, false, true);
-  constexpr uint32_t COL_ST = 0, COL_DPT = BQ, COL_DV = 2 * BQ, COL_DK = 2 * BQ + DH;
+  constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
   static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
   static_assert(C::SMEM <= 232448, "shared memory budget");
 
@@ -58,13 +56,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t sKV = base;                          // NKV x (K, V)
   const uint32_t sQ = sKV + 2 * NKV * C::KV_BYTES;    // NS x Q
   const uint32_t sDO = sQ + NS * C::Q_BYTES;          // NS x dO
-  const uint32_t sP = sDO + NS * C::Q_BYTES;          // A^T tile
 
   enum {
     KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
-    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, STFULL = DOEMPTY + NS, SEMPTY = STFULL + 1, DSFULL = SEMPTY + 1, PFULL = DSFULL + 1,
-    PEMPTY = PFULL + 1, ACCFULL = PEMPTY + 1, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
-    UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
+    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, STFULL = DOEMPTY + NS, ASFULL = STFULL + 2,
+    ACCDONE = ASFULL + 2, ACCFULL = ACCDONE + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
+    UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
   static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
@@ -80,18 +77,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
       mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 1);
     }
-    mbar_init(bar(STFULL), 1);
-    mbar_init(bar(SEMPTY), RW);
-    mbar_init(bar(DSFULL), RW);
-    mbar_init(bar(PFULL), RW);
-    mbar_init(bar(PEMPTY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(STFULL + i), 1);
+      mbar_init(bar(ASFULL + i), RW);
+      mbar_init(bar(ACCDONE + i), 1);
+    }
     mbar_init(bar(ACCFULL), 1);
     mbar_init(bar(ACCEMPTY), RW);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
-      mbar_init(bar(UEMPTY + i), 1 + RW);
+      mbar_init(bar(UEMPTY + i), 2 + RW);
     }
     mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(DRAIN + 1), 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -118,7 +116,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       uint32_t kvi = 0, qi = 0;
       bool ok = true;
-      int prev_n = kPrefetch;  // steps of the previous unit (the first unit is not warmed)
+      int prev_n = kPrefetchQ;  // steps of the previous unit (the first unit is not warmed)
       auto prefetch_qdo = [&](int h, int row) {
 #pragma unroll
         for (int c = 0; c < KCH; ++c) {
@@ -149,15 +147,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tma_load_3d(vt + c * (kBM * 128), &tm_v, bar(KVFULL + kb), 64 * c, h, k_row0);
         }
         ++kvi;
-        // L2 warm-up runs kPrefetch steps ahead of the loads along the flat
+        // L2 warm-up runs kPrefetchQ steps ahead of the loads along the flat
         // stream (this unit's later Q/dO tiles, then the next unit's K, V and
         // first Q/dO tiles); what a short previous unit could not cover is
         // issued here.
-        if (prev_n < kPrefetch)
-          for (int m = 0; m < min(U.n, kPrefetch - prev_n); ++m) prefetch_qdo(h, q_seq0 + BQ * (m0 + m));
+        if (prev_n < kPrefetchQ)
+          for (int m = 0; m < min(U.n, kPrefetchQ - prev_n); ++m) prefetch_qdo(h, q_seq0 + BQ * (m0 + m));
         prev_n = U.n;
         for (int m = 0; m < U.n; ++m) {
-          const int t = m + kPrefetch;
+          const int t = m + kPrefetchQ;
           if (t < U.n) {
             prefetch_qdo(h, q_seq0 + BQ * (m0 + t));
           } else if (t - U.n < nx.n) {
@@ -174,8 +172,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           }
           const int s = qi % NS;
           const int row = q_seq0 + BQ * (m0 + m);
-          // Q_g is free after dK_g, dO_g only after dV_g: separate rings, so
-          // each reload starts as soon as its own tile is released
           if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(QFULL + s), C::Q_BYTES);
 #pragma unroll
@@ -197,100 +193,84 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S^T / dP^T issuer
     // Waits on TMA-filled stages need no tcgen05 fence; waits on the row
-    // warps' TMEM accesses do.
+    // warps' or the other issuer's TMEM accesses do.
     if (lane == 0) {
-      const uint32_t tDV = tmem + COL_DV, tDK = tmem + COL_DK;
-      const SDesc pdesc = kdesc(sP);
-      struct Pend {
-        int valid, s, first, last, half;
-        uint32_t g, oi;
-      } pd{0, 0, 0, 0, 0, 0, 0};
-      // dK += dS^T Q over the step's queries, once dS^T is in TMEM
-      auto issue_dk = [&](const Pend& p) -> bool {
-        if (!wait_bar(bar(DSFULL), p.g & 1, wc, 0x105)) return false;
-        if (p.first && !wait_bar(bar(ACCEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
-        tc_fence_after();
-        const SDesc qd = mndesc<BQ>(sQ + p.s * C::Q_BYTES);
-        const int n0 = p.half * DH;
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          // dS^T of queries [16 kk, 16 kk + 16) sits packed in the first half
-          // of its row warp's own dP^T columns
-          const int q = 16 * kk;
-          const uint32_t col = (q / CW) * CW + (q % CW) / 2;
-          mma_ts(tDK, tmem + COL_DPT + col, desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC,
-                 (!p.first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(QEMPTY + p.s));
-        return true;
-      };
-      // dV += A^T dO once A^T is in shared memory (ACCEMPTY was waited for by
-      // the dK half of the same step); frees the A^T tile and the dO stage
-      auto issue_dv = [&](const Pend& p) -> bool {
-        if (!wait_bar(bar(PFULL), p.g & 1, wc, 0x109)) return false;
-        const SDesc dod = mndesc<BQ>(sDO + p.s * C::Q_BYTES);
-        const int n0 = p.half * DH;
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ss(tDV, desc_kmajor<kBM>(pdesc, kk), desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC,
-                 (!p.first || kk > 0) ? 1u : 0u);
-        mma_commit(bar(PEMPTY));
-        mma_commit(bar(DOEMPTY + p.s));
-        if (p.last) mma_commit(bar(ACCFULL));
-        return true;
-      };
-      uint32_t kvi = 0, qi = 0, g = 0, oi = 0;
+      uint32_t kvi = 0, h = 0;
       bool ok = true;
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U;
         if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
         if (U.n <= 0) continue;
-        const int half = U.hz % SPLIT;
         const int kb = kvi % NKV;
         if (!wait_bar(bar(KVFULL + kb), (kvi / NKV) & 1, wc, 0x104)) { ok = false; break; }
         const SDesc kd = kdesc(sKV + kb * 2 * C::KV_BYTES);
         const SDesc vd = kdesc(sKV + kb * 2 * C::KV_BYTES + C::KV_BYTES);
-        for (int m = 0; m < U.n; ++m) {
-          const int s = qi % NS;
-          if (!wait_bar(bar(QFULL + s), (qi / NS) & 1, wc, 0x106)) { ok = false; break; }
-          // S^T is single-buffered: the row warps must have loaded step g-1
-          if (g > 0) {
-            if (!wait_bar(bar(SEMPTY), (g - 1) & 1, wc, 0x108)) { ok = false; break; }
+        for (int m = 0; m < U.n; ++m, ++h) {
+          const int s = h % NS, b = h & 1;
+          if (!wait_bar(bar(QFULL + s), (h / NS) & 1, wc, 0x106)) { ok = false; break; }
+          // buffer b last held step h-2: free once its accumulation was issued
+          if (h >= 2) {
+            if (!wait_bar(bar(ACCDONE + b), ((h >> 1) - 1) & 1, wc, 0x108)) { ok = false; break; }
             tc_fence_after();
           }
           const SDesc qd = kdesc(sQ + s * C::Q_BYTES), dod = kdesc(sDO + s * C::Q_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_ST, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk), IDESC_S,
-                   kk > 0 ? 1u : 0u);
-          // dK of step g-1 reads dS^T_{g-1} from the dP^T columns: before dP^T_g
-          if (!SERIAL && pd.valid && !issue_dk(pd)) { ok = false; break; }
-          if (!wait_bar(bar(DOFULL + s), (qi / NS) & 1, wc, 0x107)) { ok = false; break; }
+            mma_ss(tmem + COL_ST + b * BQ, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk),
+                   IDESC_S, kk > 0 ? 1u : 0u);
+          if (!wait_bar(bar(DOFULL + s), (h / NS) & 1, wc, 0x107)) { ok = false; break; }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_DPT, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk), IDESC_S,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(bar(STFULL));
+            mma_ss(tmem + COL_DPT + b * BQ, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk),
+                   IDESC_S, kk > 0 ? 1u : 0u);
+          mma_commit(bar(STFULL + b));
           if (m == U.n - 1) mma_commit(bar(KVEMPTY + kb));
-          if (!SERIAL && pd.valid && !issue_dv(pd)) { ok = false; break; }
-          const Pend cur{1, s, m == 0, m == U.n - 1, half, g, oi};
-          if (SERIAL) {
-            if (!issue_dk(cur) || !issue_dv(cur)) { ok = false; break; }
-          } else {
-            pd = cur;
-          }
-          ++qi;
-          ++g;
         }
         ++kvi;
-        ++oi;
       }
-      if (!SERIAL && ok && pd.valid) ok = issue_dk(pd) && issue_dv(pd);
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
+    }
+  } else if (warp == MMA_B) {
+    // ------------------------------------------------------------ dV / dK issuer
+    if (lane == 0) {
+      const uint32_t tDV = tmem + COL_DV, tDK = tmem + COL_DK;
+      uint32_t h = 0, oi = 0;
+      bool ok = true;
+      for (uint32_t uk = 0; ok; ++uk) {
+        UnitInfo U;
+        if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
+        if (U.n < 0) break;
+        if (U.n <= 0) continue;
+        const int n0 = (U.hz % SPLIT) * DH;
+        for (int m = 0; m < U.n; ++m, ++h) {
+          const int s = h % NS, b = h & 1;
+          if (!wait_bar(bar(ASFULL + b), (h >> 1) & 1, wc, 0x105)) { ok = false; break; }
+          if (m == 0 && !wait_bar(bar(ACCEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
+          tc_fence_after();
+          const SDesc qd = mndesc<BQ>(sQ + s * C::Q_BYTES), dod = mndesc<BQ>(sDO + s * C::Q_BYTES);
+          // A^T / dS^T of queries [16 kk, 16 kk + 16) sit packed in the first
+          // half of their row warp's own CW columns
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(tDV, tmem + COL_ST + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
+                   desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(DOEMPTY + s));
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(tDK, tmem + COL_DPT + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
+                   desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(QEMPTY + s));
+          mma_commit(bar(ACCDONE + b));
+          if (m == U.n - 1) mma_commit(bar(ACCFULL));
+        }
+        ++oi;
+      }
+      mma_commit(bar(DRAIN + 1));
+      wait_bar(bar(DRAIN + 1), 0, drain, 0x1fe);
     }
   } else {
     // ------------------------------------------------------------ A^T, dS^T + epilogue
@@ -302,42 +282,38 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const uint32_t tST = tmem + COL_ST + lane_off + cg * CW,
                    tDPT = tmem + COL_DPT + lane_off + cg * CW,
                    tDV = tmem + COL_DV + lane_off + cg * DW, tDK = tmem + COL_DK + lane_off + cg * DW;
-    // A^T row r, queries [cg CW, cg CW + CW): 64-query chunk, 16-byte units
-    // within the 128-byte row, XOR-swizzled by r % 8
     const int q_first = cg * CW;
-    const uint32_t p_row = sP + (q_first / 64) * (kBM * 128) + r * 128;
-    const int u0 = (q_first % 64) / 8;
     const float half_alpha = 0.5f * a.alpha;
     const float dk_scale = 0.5f * a.alpha * a.inv_L;  // dS^T is stored doubled
-    uint32_t g = 0, oi = 0;
+    uint32_t h = 0, oi = 0;
     bool ok = true;
     for (uint32_t uk = 0; ok; ++uk) {
       UnitInfo U;
       if (!unit_pop_warp(uq, uk, U, wc)) { ok = false; break; }
       if (U.n < 0) break;
-      const int h = U.hz / SPLIT, half = U.hz % SPLIT;
+      const int hd = U.hz / SPLIT, half = U.hz % SPLIT;
       const int Lq = U.Lq, k0 = U.k0, Lk = U.Lk;
       const int j = kBM * U.tile + r;
       const int j_warp_last = kBM * U.tile + wq * 32 + 31;
       const int64_t grow = static_cast<int64_t>(k0) + j;
       const bool row_ok = j < Lk && grow < a.total_k;
       const int64_t col0 = static_cast<int64_t>(half) * DH + cg * DW;
-      char* dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + col0) * 2;
-      char* dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + static_cast<int64_t>(h) * a.o1_sh + col0) * 2;
+      char* dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(hd) * a.o0_sh + col0) * 2;
+      char* dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + static_cast<int64_t>(hd) * a.o1_sh + col0) * 2;
       if (U.n <= 0) {
         if (row_ok) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
         continue;
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
       const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
-      for (int m = 0; m < U.n; ++m) {
-        if (!wait_bar_warp(bar(STFULL), g & 1, wc, 0x201)) { ok = false; break; }
+      for (int m = 0; m < U.n; ++m, ++h) {
+        const int b = h & 1;
+        if (!wait_bar_warp(bar(STFULL + b), (h >> 1) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
         const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
         const bool need_mask = (ic + CW > Lq) || (a.causal && j_warp_last > ic);
         uint32_t xs[CW], xp[CW];
-        tmem_ld_x2<CW>(tST, tDPT, xs, xp);
-        warp_arrive(bar(SEMPTY));  // S^T of this step is in registers
+        tmem_ld_x2<CW>(tST + b * BQ, tDPT + b * BQ, xs, xp);
         uint32_t pa[CW / 2], pd[CW / 2];
         if (!need_mask) {
 #pragma unroll
@@ -353,19 +329,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                             v1 ? xp[2 * e + 1] : 0u, half_alpha, pa[e], pd[e]);
           }
         }
-        // dS^T first: it gates dK += dS^T Q and hence dP^T of the next step
-        tmem_st_w<CW / 2>(tDPT, pd);
+        tmem_st_w<CW / 2>(tST + b * BQ, pa);   // in place over this warp's S^T columns
+        tmem_st_w<CW / 2>(tDPT + b * BQ, pd);  // in place over this warp's dP^T columns
         tmem_st_wait();
-        warp_arrive(bar(DSFULL));
-        // the A^T tile is free once the step g-1 dV accumulation has read it
-        if (g > 0 && !wait_bar_warp(bar(PEMPTY), (g - 1) & 1, wc, 0x203)) { ok = false; break; }
-#pragma unroll
-        for (int v = 0; v < CW / 8; ++v)
-          st_shared_v4(p_row + (((u0 + v) ^ (r & 7)) << 4), pa[4 * v], pa[4 * v + 1], pa[4 * v + 2],
-                       pa[4 * v + 3]);
-        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-        warp_arrive(bar(PFULL));
-        ++g;
+        warp_arrive(bar(ASFULL + b));
       }
       if (!ok) break;
       if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) { ok = false; break; }
@@ -413,7 +380,7 @@ cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, kWideThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, a);
+  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, a);
 }
 
 }  // namespace

@@ -17,17 +17,20 @@ constexpr int kRowThreads = 256;    // two warps per TMEM lane quarter, one per 
 // per TMEM lane quarter, one per quarter of the columns).
 constexpr int kRowWarps16 = 16;
 constexpr int kWideThreads = 64 + 32 * kRowWarps16;
-// dQ kernel: one more warp (18) issues the dQ accumulation MMAs, so the two
-// MMA streams wait on their own barriers without stalling each other.
+// dQ and dK/dV kernels: one more warp (18) issues the accumulation MMAs, so
+// the two MMA streams wait on their own barriers without stalling each other.
 constexpr int kDqThreads = kWideThreads + 32;
+constexpr int kDkdvThreads = kWideThreads + 32;
 constexpr int kTmemCols = 512;
 
 // Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
 // address slot, the abort flags, and slack to align the tiles to 1024 bytes.
 constexpr int kCtlBytes = 1024;
 constexpr int kAlignSlack = 1024;
-// K/V steps warmed in L2 ahead of the TMA loads (and of the next unit).
+// K/V steps warmed in L2 ahead of the TMA loads (and of the next unit);
+// the dK/dV kernel's 64-query steps run twice as many Q/dO tiles ahead.
 constexpr int kPrefetch = 4;
+constexpr int kPrefetchQ = 8;
 
 struct SchedArgs {
   const int32_t* cu_q;
@@ -91,20 +94,19 @@ struct DqCfg {
 };
 
 // ------------------------------------------------------------ dK/dV config
-// 128-query steps (64 at D = 256) so S^T and dP^T are N = 128 MMAs.  A^T goes
-// to a shared-memory tile (the A operand of dV += A^T dO), dS^T stays in TMEM
-// in place over dP^T (the A operand of dK += dS^T Q).
+// 64-query half-steps: S^T and dP^T are double-buffered in TMEM next to the
+// dV and dK accumulators, A^T and dS^T are written in place over them.
+// Separate Q and dO rings (Q is released after dK, dO after dV).
 template <int D>
 struct DkdvCfg {
-  static constexpr int BQ = D == 256 ? 64 : 128;     // queries per inner tile
+  static constexpr int BQ = 64;                      // queries per inner tile
   static constexpr int DH = D == 256 ? 128 : D;      // dK/dV columns per unit
   static constexpr int SPLIT = D / DH;
-  static constexpr int NKV = D == 64 ? 2 : 1;        // stationary (K, V) buffers
-  static constexpr int NS = D == 64 ? 3 : (D == 128 ? 2 : 1);
+  static constexpr int NKV = D == 256 ? 1 : 2;       // stationary (K, V) buffers
+  static constexpr int NS = D == 64 ? 8 : (D == 128 ? 3 : 1);  // Q and dO stages each
   static constexpr int KV_BYTES = kBM * D * 2;
   static constexpr int Q_BYTES = BQ * D * 2;
-  static constexpr int P_BYTES = kBM * BQ * 2;       // A^T staging tile
-  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES + P_BYTES;
+  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES;
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
 };
 
