@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
   }
   if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
+  __syncwarp();  // thread 0's set-up above diverged warp 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -361,6 +362,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   // Started early beside the dQ grid: finish only after it, so that work
   // queued behind this grid also sees dQ complete.
   if (a.pdl_wait == 2) grid_dependency_wait();
+  // The role branches leave lanes of warps 0, 1 (and 18) on different paths;
+  // reconverge each warp so the aligned CTA barrier counts it exactly once
+  // (otherwise it can release before the row warps finish reading TMEM).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
   }
   if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
+  __syncwarp();  // thread 0's set-up above diverged warp 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -348,6 +349,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
   }
 
+  // The role branches leave lanes of warps 0, 1 (and 18) on different paths;
+  // reconverge each warp so the aligned CTA barrier counts it exactly once
+  // (otherwise it can release before the row warps finish reading TMEM).
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

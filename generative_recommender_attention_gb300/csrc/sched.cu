@@ -54,6 +54,7 @@ __device__ int block_exclusive_scan(int v, int* total) {
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_sums[warp] = x;
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
   if (warp == 0) {
     int w = warp_sums[lane];
@@ -64,9 +65,11 @@ __device__ int block_exclusive_scan(int v, int* total) {
     }
     warp_sums[lane] = w;
   }
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
   int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
   *total = warp_sums[31];
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
   return before;
 }
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
 
   // pass 1: histogram of costs; a warp per sequence, a lane per tile
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
       atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
 
   // pass 2: exclusive scan over costs in descending order (rank 0 = cmax)
@@ -130,6 +135,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     hist[c] = run;
     run += h;
   }
+  __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
 
   // pass 3: emit complete unit records at their bucket cursors
