@@ -106,13 +106,14 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample(x, w, budget_s: float, start: int = 0):
+def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0):
     """Times the fp64 oracle fwd+bwd on whole sequences (all heads) of the
-    workload, one after another from `start`, until `budget_s` is spent.
-    Returns (flops, seconds, n_sequences, threads)."""
+    workload, one after another from `start`, until `budget_s` is spent, on
+    `threads` host threads (0: all cores).  Returns (flops, seconds,
+    n_sequences, threads)."""
     import numpy as np
     import oracle
-    threads = oracle.threads(os.cpu_count() or 1)
+    threads = oracle.threads(threads if threads > 0 else (os.cpu_count() or 1))
     cu = x["cu_seqlens_q"].tolist()
     B = len(cu) - 1
     L_scale = oracle.resolve_scaling(w.scaling_seqlen, x["max_seqlen_q"])
@@ -208,6 +209,7 @@ def main():
     B, T, H, D = w.batch, sum(lengths), w.heads, w.head_dim
     N = pairs(lengths, H, w.causal)
     flops_step = 14.0 * D * N
+    bytes_step = 11.0 * T * H * D * 2  # fwd 4 T H D and bwd 7 T H D elements of 2 bytes
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     o = torch.empty_like(d["q"])
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
@@ -275,6 +277,17 @@ def main():
         step(row)
     torch.cuda.synchronize()
     timed = ev[1:]
+    # Informational: the same steps back to back without the L2 flush (as in
+    # consecutive training steps); not the headline value.
+    n_warm = max(3, min(args.steps, 200))
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step()
+    w0.record()
+    for _ in range(n_warm):
+        step()
+    w1.record()
+    torch.cuda.synchronize()
+    ms_warm = w0.elapsed_time(w1) / n_warm
     t_sched_f = [r[0].elapsed_time(r[1]) for r in timed]
     t_fwd = [r[1].elapsed_time(r[2]) for r in timed]
     t_sched_b = [r[3].elapsed_time(r[4]) for r in timed]
@@ -341,6 +354,12 @@ def main():
         "data": "synthetic",
         "pct_of_dense_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
         "pct_of_sustained_bf16_peak": 100.0 * value / world / pk["bf16_tflops_sustained"],
+        "ms_per_step_median": statistics.median(t_step),
+        "achieved_gbs": world * bytes_step / (ms_step * 1e-3) / 1e9,
+        "achieved_gbs_note": "algorithmic bytes (fwd reads q,k,v and writes o; bwd reads q,k,v,dO and "
+                             "writes dq,dk,dv) per step time, against %.1f GB/s measured HBM" % pk["hbm_gbs"],
+        "value_l2_warm": world * flops_step / (ms_warm * 1e-3) / 1e12,
+        "ms_per_step_l2_warm": ms_warm,
         "config": dict(workload_config(w, lengths),
                        l2="flushed between steps (256 MiB write)" if flush is not None else "not flushed",
                        parallelism="replicas" if world > 1 else "single GPU",
@@ -368,6 +387,9 @@ def main():
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"first {n} of {B} sequences, all heads, fwd+bwd (fp64)"}
+        f1, s1, n1, _ = oracle_sample(x, w, min(2.0, args.cpu_budget), threads=1)
+        line["cpu_baseline_one_core"] = {"value": f1 / s1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                         "sample": f"first {n1} sequences, all heads, fwd+bwd (fp64)"}
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()
