@@ -123,7 +123,6 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
 // each one to the MMA thread and the row warps through a small ring in
 // shared memory.  An entry with n = -1 ends the stream.
 constexpr int kUnitRing = 4;
-constexpr int kUnitConsumers = 9;  // the MMA thread + one arrival per row warp (8)
 
 struct UnitQueue {
   UnitInfo* ring;       // kUnitRing entries in shared memory

@@ -5,15 +5,22 @@
 // list of 128-row query tiles written by the scheduler kernel.
 //   warp 0      TMA producer: Q tile per unit, K_g ahead of V_{g-2}, one
 //               flat stream across units.
-//   warp 1      tcgen05 issuer.  S tiles live in three TMEM buffers and run
-//               two steps ahead: S_{g+2} = Q K^T is queued before
-//               O += P_g V_g, so the tensor pipe has independent work while
-//               the row warps turn S_g into P_g.
-//   warps 2-9   row work, two warps per TMEM lane quarter (one per column
-//               half): tcgen05.ld S, alpha scale, SiLU, mask, round to 16
-//               bits, tcgen05.st P in place over the S columns the warp just
-//               read; per unit, the epilogue O * (1/L_scale) with predicated
-//               row stores.
+//   warp 1      issues S_g = Q K_g^T into TMEM buffer g % 3 as soon as K_g has
+//               landed and O += P_{g-3} V_{g-3} has consumed that buffer.
+//   warp 14     issues O += P_g V_g as soon as P_g and V_g are ready.
+//               The tensor pipe queues only about one instruction ahead, so
+//               an issuing thread that stops to wait or to do bookkeeping
+//               leaves it idle; two issuers keep it fed while either waits,
+//               and S runs up to three steps ahead of P V.
+//   warps 2-9   SiLU row work, two warps per TMEM lane quarter taking
+//               alternate key steps (warps 2-5 even steps, 6-9 odd ones), so
+//               one warp's TMEM and barrier latencies overlap the other's
+//               MUFU work: tcgen05.ld S, alpha scale, SiLU, mask, round to 16
+//               bits, tcgen05.st P in place over the first half of the S
+//               columns.
+//   warps 10-13 O epilogue, one per lane quarter: O * (1/L_scale) with
+//               predicated row stores; O is released as soon as it is read,
+//               so the SiLU warps never stop at a unit boundary.
 // No softmax, so no running max or rescale: O simply accumulates in TMEM.
 // Causal units only visit key tiles up to their last row (the scheduler's
 // cost); masked entries are set to exactly 0, never -inf, since SiLU(-inf)
@@ -23,10 +30,9 @@
 // K_g and S_g share ring slot g % 3: S_g completing frees K_g, so the producer
 // waits on the S barrier instead of a separate K-empty barrier.
 //
-// P overwrites its own S buffer, which S_{g+3} overwrites again.  S_{g+3} is
-// issued by the same thread after O += P_g V_g, and tcgen05.mma operations
-// from one thread execute in issue order, so P_g is consumed before it is
-// overwritten.
+// P_g (16-bit, two per column) overwrites the first half of its own S
+// buffer, which S_{g+3} overwrites again; S_{g+3} is issued only after the
+// commit of O += P_g V_g has arrived on that buffer's PV-done barrier.
 #include "kernels.h"
 
 namespace hstu {
@@ -41,13 +47,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using C = FwdCfg<D>;
   constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
   constexpr int NSB = 3;        // S buffers in TMEM
-  constexpr int LA = NSB - 1;   // S tiles issued ahead of their P V
-  constexpr int CPW = BN / 2;   // S columns per row warp
+  constexpr int NCH = BN / 64;  // 64-column chunks of one S tile
   static_assert(NK == NSB, "K slot g % NSB is freed by the S_g barrier");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_PV = idesc_f16(BF16, kBM, D, false, true);
   // TMEM columns: S0 | S1 | S2 | O.  P_g is packed two per column into the
-  // first half of each warp's own S columns.
+  // first half of its S buffer.
   constexpr uint32_t COL_S = 0, COL_O = NSB * BN;
   static_assert(COL_O + D <= kTmemCols, "TMEM budget");
 
@@ -62,8 +67,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   enum {
     QFULL = 0, QEMPTY = QFULL + NQ, KFULL = QEMPTY + NQ,
     VFULL = KFULL + NK, VEMPTY = VFULL + NV, SFULL = VEMPTY + NV, PFULL = SFULL + NSB,
-    OFULL = PFULL + NSB, OEMPTY = OFULL + 1, UFULL = OEMPTY + 1, UEMPTY = UFULL + kUnitRing,
-    DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 1
+    PVDONE = PFULL + NSB, OFULL = PVDONE + NSB, OEMPTY = OFULL + 1, UFULL = OEMPTY + 1,
+    UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
   static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
@@ -79,15 +84,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(bar(SFULL + i), 1);
-      mbar_init(bar(PFULL + i), kRowThreads);
+      mbar_init(bar(PFULL + i), 4);  // one arrival per warp of the step's parity
+      mbar_init(bar(PVDONE + i), 1);
     }
     mbar_init(bar(OFULL), 1);
-    mbar_init(bar(OEMPTY), kRowThreads);
+    mbar_init(bar(OEMPTY), kFwdEpiWarps);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
-      mbar_init(bar(UEMPTY + i), kUnitConsumers);
+      mbar_init(bar(UEMPTY + i), 2 + kFwdRowWarps + kFwdEpiWarps);
     }
     mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(DRAIN + 1), 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
@@ -111,9 +118,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // One flat stream over all of this CTA's units, in the order the MMA
-    // thread consumes it: Q of a unit before its first K, and K_g before
-    // V_{g-LA} (the MMA issues S_g before O += P_{g-LA} V_{g-LA}).  The next
+    // One flat stream over all of this CTA's units: Q of a unit before its
+    // first K, and K_g before V_{g-LA} (S runs ahead of P V).  The next
     // unit's Q and first K tiles therefore go out before this unit's last V
     // tiles, so a unit boundary does not wait for a fresh load.
     if (lane == 0) {
@@ -129,20 +135,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++cnt;
         return true;
       };
-      auto prefetch_kv = [&](int h, int row) {
-#pragma unroll
-        for (int c = 0; c < KCH; ++c) {
-          tma_prefetch_3d(&tm_k, 64 * c, h, row);
-          tma_prefetch_3d(&tm_v, 64 * c, h, row);
-        }
-      };
-      auto prefetch_q = [&](const UnitInfo& u) {
-#pragma unroll
-        for (int c = 0; c < KCH; ++c) tma_prefetch_3d(&tm_q, 64 * c, u.hz, u.q0 + kBM * u.tile);
-      };
-      int prev_n = kPrefetch;  // steps of the previous unit (the first unit is not warmed)
       // V loads not yet issued (at most LA of them): key row and head
-      static_assert(LA == 2, "two deferred V loads kept in registers");
+      constexpr int LA = 2;
       int v_row0 = 0, v_h0 = 0, v_row1 = 0, v_h1 = 0, nv = 0;
       bool ok = true;
       // units are claimed one ahead: the next claim overlaps this unit's loads
@@ -165,22 +159,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(sQ + qb * C::Q_BYTES + c * (kBM * 128), &tm_q, bar(QFULL + qb), 64 * c, h,
                       q_row0);
         ++qi;
-        // L2 warm-up runs kPrefetch steps ahead of the loads along the flat
-        // stream (this unit's later K/V tiles, then the next unit's Q and
-        // first K/V tiles); what a short previous unit could not cover is
-        // issued here.
-        if (prev_n < kPrefetch)
-          for (int m = 0; m < min(U.n, kPrefetch - prev_n); ++m) prefetch_kv(h, kv_row0 + BN * m);
-        prev_n = U.n;
+        // No L2 warm-up here: measured, the extra prefetch requests slowed
+        // the forward's own tile loads more than they saved.
         for (int n = 0; n < U.n; ++n) {
           const int row = kv_row0 + BN * n;
-          const int t = n + kPrefetch;
-          if (t < U.n) {
-            prefetch_kv(h, kv_row0 + BN * t);
-          } else if (t - U.n < nx.n) {
-            if (t == U.n) prefetch_q(nx);
-            prefetch_kv(nx.hz, nx.k0 + BN * (t - U.n));
-          }
           if (!load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, row, h, 0x002)) { ok = false; break; }
           if (nv == LA) {
             if (!load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, v_row0, v_h0, 0x003)) { ok = false; break; }
@@ -204,38 +186,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         wait_bar(bar(VFULL + i % NV), (i / NV) & 1, drain, 0x0f3);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One flat stream of steps g over all of this CTA's units.  Issue order:
-    // S_{g}, then O += P_{g-LA} V_{g-LA}.
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      const uint32_t tO = tmem + COL_O;
-      struct Step {
-        uint32_t g, vi, oi;
-        int first, last;
-      };
-      static_assert(LA == 2, "two pending steps kept in registers");
-      Step p0{}, p1{};
-      int npend = 0;
-      auto issue_pv = [&](const Step& p) -> bool {
-        const int vs = p.vi % NV, sb = p.g % NSB;
-        if (!wait_bar(bar(VFULL + vs), (p.vi / NV) & 1, wc, 0x101)) return false;
-        if (!wait_bar(bar(PFULL + sb), (p.g / NSB) & 1, wc, 0x102)) return false;
-        if (p.first && !wait_bar(bar(OEMPTY), (p.oi & 1) ^ 1, wc, 0x103)) return false;
-        tc_fence_after();
-        const SDesc vd = mndesc<BN>(sV + vs * C::KV_BYTES);
-        const uint32_t tP = tmem + COL_S + sb * BN;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const int key = 16 * kk;  // P of keys [key, key+16) sits in the producing warp's columns
-          const uint32_t col = (key / CPW) * CPW + (key % CPW) / 2;
-          mma_ts(tO, tP + col, desc_mnmajor<BN>(vd, kk, 0), IDESC_PV,
-                 (!p.first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(VEMPTY + vs));
-        if (p.last) mma_commit(bar(OFULL));
-        return true;
-      };
-      uint32_t qi = 0, ki = 0, vi = 0, g = 0, oi = 0;
+      uint32_t qi = 0, ki = 0, g = 0;
       bool ok = true;
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U;
@@ -245,12 +198,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (un <= 0) continue;
         const int qb = qi % NQ;
         if (!wait_bar(bar(QFULL + qb), (qi / NQ) & 1, wc, 0x104)) { ok = false; break; }
-        tc_fence_after();
         const SDesc qd = kdesc(sQ + qb * C::Q_BYTES);
-        for (int n = 0; n < un; ++n) {
+        for (int n = 0; n < un; ++n, ++ki, ++g) {
           const int ks = ki % NK, sb = g % NSB;
           if (!wait_bar(bar(KFULL + ks), (ki / NK) & 1, wc, 0x105)) { ok = false; break; }
-          tc_fence_after();
+          // buffer sb last held P_{g-3}: O += P_{g-3} V_{g-3} must have read it
+          if (g >= NSB) {
+            if (!wait_bar(bar(PVDONE + sb), ((g / NSB) - 1) & 1, wc, 0x106)) { ok = false; break; }
+            tc_fence_after();
+          }
           const SDesc kd = kdesc(sK + ks * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
@@ -258,97 +214,129 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                    IDESC_S, kk > 0 ? 1u : 0u);
           mma_commit(bar(SFULL + sb));  // also frees K slot ks == sb
           if (n == un - 1) mma_commit(bar(QEMPTY + qb));
-          const Step cur{g, vi, oi, n == 0, n == un - 1};
-          if (npend == LA) {
-            if (!issue_pv(p0)) { ok = false; break; }
-            p0 = p1;
-            p1 = cur;
-          } else if (npend == 1) {
-            p1 = cur;
-            npend = 2;
-          } else {
-            p0 = cur;
-            npend = 1;
-          }
-          ++ki;
-          ++vi;
-          ++g;
         }
         ++qi;
-        ++oi;
       }
-      if (ok && npend >= 1) ok = issue_pv(p0);
-      if (ok && npend == 2) ok = issue_pv(p1);
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
     }
-  } else {
-    // ------------------------------------------------------------ SiLU + epilogue
-    // Eight warps: warp w owns TMEM lane quarter w % 4 (its 32 rows) and one
-    // half of the key columns of each S tile (and of the O columns).
-    const int wq = warp & 3, hc = (warp - 2) >> 2;
+  } else if (warp == kFwdPvWarp) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      const uint32_t tO = tmem + COL_O;
+      uint32_t vi = 0, g = 0, oi = 0;
+      bool ok = true;
+      for (uint32_t uk = 0; ok; ++uk) {
+        UnitInfo U;
+        if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
+        if (U.n < 0) break;
+        const int un = U.n;
+        if (un <= 0) continue;
+        for (int n = 0; n < un; ++n, ++vi, ++g) {
+          const int vs = vi % NV, sb = g % NSB;
+          if (!wait_bar(bar(VFULL + vs), (vi / NV) & 1, wc, 0x101)) { ok = false; break; }
+          if (!wait_bar(bar(PFULL + sb), (g / NSB) & 1, wc, 0x102)) { ok = false; break; }
+          if (n == 0 && !wait_bar(bar(OEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
+          tc_fence_after();
+          const SDesc vd = mndesc<BN>(sV + vs * C::KV_BYTES);
+          const uint32_t tP = tmem + COL_S + sb * BN;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)  // P of keys [16 kk, 16 kk + 16): columns 8 kk..
+            mma_ts(tO, tP + 8 * kk, desc_mnmajor<BN>(vd, kk, 0), IDESC_PV,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(VEMPTY + vs));
+          mma_commit(bar(PVDONE + sb));
+          if (n == un - 1) mma_commit(bar(OFULL));
+        }
+        ++oi;
+      }
+      mma_commit(bar(DRAIN + 1));
+      wait_bar(bar(DRAIN + 1), 0, drain, 0x1fe);
+    }
+  } else if (warp < 2 + kFwdRowWarps) {
+    // ------------------------------------------------------------ SiLU
+    // Warp w owns TMEM lane quarter w % 4 (its 32 rows) and the steps of
+    // parity par; it reads all BN columns of those S tiles in 64-column
+    // chunks and writes P over the first half of the buffer.
+    const int wq = warp & 3, par = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + COL_S + lane_off + hc * CPW, tO = tmem + COL_O + lane_off;
+    const uint32_t tS = tmem + COL_S + lane_off;
     const float half_alpha = 0.5f * a.alpha;
-    uint32_t g = 0, oi = 0;
+    uint32_t g = 0;
+    bool ok = true;
+    for (uint32_t uk = 0; ok; ++uk) {
+      UnitInfo U;
+      if (!unit_pop_warp(uq, uk, U, wc)) { ok = false; break; }
+      if (U.n < 0) break;
+      const int Lk = U.Lk;
+      const int i = kBM * U.tile + r;
+      const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
+      const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
+      for (int n = 0; n < U.n; ++n, ++g) {
+        if (static_cast<int>(g & 1) != par) continue;
+        const int sb = g % NSB;
+        if (!wait_bar_warp(bar(SFULL + sb), (g / NSB) & 1, wc, 0x201)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const int jc = BN * n + 64 * c;  // first key of this chunk
+          const bool need_mask = (a.causal && jc + 63 > i_warp) || (jc + 64 > Lk);
+          uint32_t x[64];
+          tmem_ld64(tS + sb * BN + 64 * c, x);
+          uint32_t p[32];
+          if (!need_mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = jc + 2 * e;
+              const uint32_t s0 = j < lim ? x[2 * e] : 0u;          // SiLU(0) = 0
+              const uint32_t s1 = j + 1 < lim ? x[2 * e + 1] : 0u;
+              p[e] = silu_pair<BF16>(s0, s1, half_alpha);
+            }
+          }
+          // columns [32 c, 32 c + 32) were read by this chunk or the one before
+          tmem_st32(tS + sb * BN + 32 * c, p);
+        }
+        tmem_st_wait();
+        warp_arrive(bar(PFULL + sb));
+      }
+    }
+  } else if (warp < kFwdPvWarp) {
+    // ------------------------------------------------------------ O epilogue
+    // Warp w owns TMEM lane quarter w % 4: it reads its 32 rows of O in
+    // 64-column chunks, releases O once every chunk is in registers or
+    // stored, and scales, rounds and stores the rows.
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t tO = tmem + COL_O + (static_cast<uint32_t>(wq * 32) << 16);
+    uint32_t oi = 0;
     bool ok = true;
     for (uint32_t uk = 0; ok; ++uk) {
       UnitInfo U;
       if (!unit_pop_warp(uq, uk, U, wc)) { ok = false; break; }
       if (U.n < 0) break;
       const int h = U.hz;
-      const int q0 = U.q0, Lq = U.Lq, Lk = U.Lk;
       const int i = kBM * U.tile + r;
-      const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
-      const int64_t grow = static_cast<int64_t>(q0) + i;
-      const bool row_ok = i < Lq && grow < a.total_q;
+      const int64_t grow = static_cast<int64_t>(U.q0) + i;
+      const bool row_ok = i < U.Lq && grow < a.total_q;
       char* orow = static_cast<char*>(a.o0) +
-                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh + hc * (D / 2)) * 2;
+                   (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh) * 2;
       if (U.n <= 0) {
-        if (row_ok)
-          for (int c = 0; c < D / 64; ++c) store_zero32(orow + c * 64);
+        if (row_ok) store_zero_n<D>(orow);
         continue;
       }
-      for (int n = 0; n < U.n; ++n) {
-        const int sb = g % NSB;
-        if (!wait_bar_warp(bar(SFULL + sb), (g / NSB) & 1, wc, 0x201)) { ok = false; break; }
-        tc_fence_after();
-        const int jc = BN * n + hc * CPW;  // first key of this warp's columns
-        const bool need_mask = (a.causal && jc + CPW - 1 > i_warp) || (jc + CPW > Lk);
-        uint32_t x[CPW];
-        tmem_ld_n<CPW>(tS + sb * BN, x);
-        uint32_t p[CPW / 2];
-        if (!need_mask) {
-#pragma unroll
-          for (int e = 0; e < CPW / 2; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
-        } else {
-          const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
-#pragma unroll
-          for (int e = 0; e < CPW / 2; ++e) {
-            const int j = jc + 2 * e;
-            const uint32_t s0 = j < lim ? x[2 * e] : 0u;          // SiLU(0) = 0
-            const uint32_t s1 = j + 1 < lim ? x[2 * e + 1] : 0u;
-            p[e] = silu_pair<BF16>(s0, s1, half_alpha);
-          }
-        }
-        tmem_st_n<CPW / 2>(tS + sb * BN, p);  // in place over this warp's S columns
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(PFULL + sb));
-        ++g;
-      }
-      if (!ok) break;
       if (!wait_bar_warp(bar(OFULL), oi & 1, wc, 0x202)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tO + hc * (D / 2) + 32 * c, x);
-        if (row_ok) store_row32<BF16>(orow + c * 64, x, a.inv_L);
+        uint32_t x[64];
+        tmem_ld64(tO + 64 * c, x);
+        if (c == D / 64 - 1) warp_arrive(bar(OEMPTY));  // every O column is read
+        if (row_ok) store_row_n<64, BF16>(orow + c * 128, x, a.inv_L);
       }
-      tc_fence_before();
-      mbar_arrive(bar(OEMPTY));
       ++oi;
     }
   }

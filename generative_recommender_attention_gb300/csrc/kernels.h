@@ -11,8 +11,13 @@
 namespace hstu {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kAttnThreads = 320;   // warp 0: TMA, warp 1: MMA, warps 2-9: row work
-constexpr int kRowThreads = 256;    // two warps per TMEM lane quarter, one per column half
+// Forward kernel: warp 0 TMA, warp 1 issues S = Q K^T, warps 2-9 SiLU row
+// work (two per TMEM lane quarter, taking alternate key steps), warps 10-13
+// O epilogue (one per lane quarter), warp 14 issues O += P V.
+constexpr int kFwdRowWarps = 8;
+constexpr int kFwdEpiWarps = 4;
+constexpr int kFwdPvWarp = 2 + kFwdRowWarps + kFwdEpiWarps;
+constexpr int kAttnThreads = 32 * (kFwdPvWarp + 1);
 // Backward kernels: warp 0 TMA, warp 1 MMA, warps 2-17 row work (four warps
 // per TMEM lane quarter, one per quarter of the columns).
 constexpr int kRowWarps16 = 16;
