@@ -133,7 +133,8 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     _check_thd("out", out, T_q, H, D, q.dtype, dev)
     causal = _causal(causal, window_size)
-    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, False), dev)
+    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
+                                              False), dev)
     args = (_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
             cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q), int(max_seqlen_q),
             int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen), int(causal),
@@ -157,8 +158,8 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
     ``dq``/``dk``/``dv`` may be supplied (overwritten); dk and dv may be
     disjoint views of one packed KV buffer.  ``events``: optional list of 4
-    torch.cuda.Event (before the scheduler, after it, after the dQ kernel,
-    after the dK/dV kernel).
+    torch.cuda.Event (before the scheduler, after it, after the dK/dV kernel,
+    after the dQ kernel).
     """
     import torch
     lib = library()
@@ -180,7 +181,8 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     _check_thd("dk", dk, T_k, H, D, q.dtype, dev)
     _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
     causal = _causal(causal, window_size)
-    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, True), dev)
+    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
+                                              True), dev)
     args = (_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk), _ten(dv),
             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
             int(max_seqlen_q), int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen),

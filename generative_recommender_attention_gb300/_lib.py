@@ -66,7 +66,7 @@ def _declare(lib):
     lib.hstu_attn_fwd_profiled.restype = ctypes.c_int
     lib.hstu_attn_bwd_profiled.argtypes = lib.hstu_attn_bwd.argtypes + [P, i32]
     lib.hstu_attn_bwd_profiled.restype = ctypes.c_int
-    lib.hstu_attn_workspace_size.argtypes = [i32, i64, i64, i32, i32, i32]
+    lib.hstu_attn_workspace_size.argtypes = [i32, i64, i64, i32, i32, i32, i32, i32]
     lib.hstu_attn_workspace_size.restype = S
     lib.hstu_attn_status_string.argtypes = [ctypes.c_int]
     lib.hstu_attn_status_string.restype = ctypes.c_char_p
@@ -96,9 +96,11 @@ def library():
         return _lib
 
 
-def workspace_size(batch, total_q, total_k, num_heads, head_dim, is_bwd) -> int:
+def workspace_size(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, max_seqlen_k,
+                   is_bwd) -> int:
     n = library().hstu_attn_workspace_size(int(batch), int(total_q), int(total_k),
-                                           int(num_heads), int(head_dim), int(bool(is_bwd)))
+                                           int(num_heads), int(head_dim), int(max_seqlen_q),
+                                           int(max_seqlen_k), int(bool(is_bwd)))
     if n == 0:
         raise ValueError("invalid sizes for hstu_attn_workspace_size")
     return int(n)

@@ -83,6 +83,24 @@ bool encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D, int64_
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the dS blocks: (64 queries, 128 keys, block), box of one
+// whole block, 128-byte swizzle.
+bool encode_ds(CUtensorMap* m, void* ptr, int64_t blocks, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDsQueries), static_cast<cuuint64_t>(kDsKeys),
+                        static_cast<cuuint64_t>(std::max<int64_t>(blocks, 1))};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDsQueries * 2),
+                           static_cast<cuuint64_t>(kDsBlockBytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kDsQueries), static_cast<cuuint32_t>(kDsKeys), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- validation
 bool supported_dim(int D) { return D == 64 || D == 128 || D == 256; }
 
@@ -142,6 +160,28 @@ int64_t cap_b(int32_t batch, int64_t total_k, int32_t H, int32_t D) {
 
 int bn_for(int D) { return D == 256 ? 64 : 128; }
 
+// Backward workspace: header | list A | list B | ds_base (B + 1 ints) | dS
+// blocks.  The dS capacity bounds sum_b H ceil(Lk_b/128) ceil(Lq_b/64) from
+// the sizes alone (every Lq_b <= max_seqlen_q), so the host never needs the
+// sequence lengths.
+struct BwdLayout {
+  size_t units_b, ds_base, ds, total;
+  int64_t ds_blocks;
+};
+
+bool bwd_layout(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_t D,
+                int32_t max_q, BwdLayout* L) {
+  const int64_t capA = cap_a(batch, total_q, H), capB = cap_b(batch, total_k, H, D);
+  L->units_b = kHeaderBytes + 32 * static_cast<size_t>(capA);
+  L->ds_base = L->units_b + 32 * static_cast<size_t>(capB);
+  L->ds = (L->ds_base + 4 * (static_cast<size_t>(batch) + 1) + 1023) & ~size_t(1023);
+  L->ds_blocks = static_cast<int64_t>(H) * cdiv(std::max<int32_t>(max_q, 0), kDsQueries) *
+                 (cdiv(total_k, kDsKeys) + batch);
+  if (L->ds_blocks > INT32_MAX) return false;  // block indices are int32 on the device
+  L->total = L->ds + static_cast<size_t>(L->ds_blocks) * kDsBlockBytes;
+  return true;
+}
+
 // Shared memory of the scheduler block: one int per cost bucket.
 bool sched_smem(int cmax, const DevInfo& dev, int* bytes) {
   const int b = (cmax + 1) * 4;
@@ -176,13 +216,19 @@ const char* hstu_attn_status_string(hstu_status_t s) {
 }
 
 size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
-                                int32_t num_heads, int32_t head_dim, int32_t is_bwd) {
-  if (batch < 0 || total_q < 0 || total_k < 0 || num_heads <= 0 || !supported_dim(head_dim))
+                                int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                int32_t max_seqlen_k, int32_t is_bwd) {
+  if (batch < 0 || total_q < 0 || total_k < 0 || num_heads <= 0 || !supported_dim(head_dim) ||
+      max_seqlen_q < 0 || max_seqlen_k < 0)
     return 0;
-  // a unit record is two int4 (32 bytes)
-  size_t bytes = kHeaderBytes + 32 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
-  if (is_bwd) bytes += 32 * static_cast<size_t>(cap_b(batch, total_k, num_heads, head_dim));
-  return (bytes + 255) & ~size_t(255);
+  if (!is_bwd) {
+    // a unit record is two int4 (32 bytes)
+    const size_t bytes = kHeaderBytes + 32 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
+    return (bytes + 255) & ~size_t(255);
+  }
+  BwdLayout L;
+  if (!bwd_layout(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, &L)) return 0;
+  return (L.total + 255) & ~size_t(255);
 }
 
 }  // extern "C"
@@ -217,7 +263,8 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   if ((s = check_tensor(v.ptr, v.stride_t, v.stride_h, total_k, H, D)) != HSTU_OK) return s;
   if ((s = check_tensor(out.ptr, out.stride_t, out.stride_h, total_q, H, D)) != HSTU_OK) return s;
   if (batch == 0 || total_q == 0) return HSTU_OK;
-  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, H, D, 0);
+  const size_t need =
+      hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
@@ -282,13 +329,16 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if ((s = check_tensor(dk.ptr, dk.stride_t, dk.stride_h, total_k, H, D)) != HSTU_OK) return s;
   if ((s = check_tensor(dv.ptr, dv.stride_t, dv.stride_h, total_k, H, D)) != HSTU_OK) return s;
   if (batch == 0 || (total_q == 0 && total_k == 0)) return HSTU_OK;
-  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, H, D, 1);
+  BwdLayout lay;
+  if (!bwd_layout(batch, total_q, total_k, H, D, max_seqlen_q, &lay)) return HSTU_ERR_UNSUPPORTED;
+  const size_t need =
+      hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 1);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
-  const int BN = D == 256 ? DqCfg<256>::BN : DqCfg<128>::BN;  // dQ kernel key tile
+  const int BN = kDsKeys;                                         // dQ kernel key tile
   const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;  // dK/dV query tile
   const int split = D == 256 ? 2 : 1;
   const int64_t capA = cap_a(batch, total_q, H);
@@ -301,25 +351,25 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   // Stand-ins for empty sides: valid maps that no unit ever reads through.
   const bool hq = total_q > 0, hk = total_k > 0;
   const hstu_cten_t qx = hq ? q : k, dox = hq ? dout : k, kx = hk ? k : q, vx = hk ? v : q;
-  CUtensorMap m_q128, m_do128, m_kbn, m_vbn, m_k128, m_v128, m_q64, m_do64;
-  if (!encode_thd(&m_q128, qx.ptr, total_q, H, D, qx.stride_t, qx.stride_h, kBM, c.bf16) ||
-      !encode_thd(&m_do128, dox.ptr, total_q, H, D, dox.stride_t, dox.stride_h, kBM, c.bf16) ||
-      !encode_thd(&m_kbn, kx.ptr, total_k, H, D, kx.stride_t, kx.stride_h, BN, c.bf16) ||
-      !encode_thd(&m_vbn, vx.ptr, total_k, H, D, vx.stride_t, vx.stride_h, BN, c.bf16) ||
-      !encode_thd(&m_k128, kx.ptr, total_k, H, D, kx.stride_t, kx.stride_h, kBM, c.bf16) ||
+  CUtensorMap m_k128, m_v128, m_q64, m_do64, m_ds;
+  char* ws = static_cast<char*>(workspace);
+  if (!encode_thd(&m_k128, kx.ptr, total_k, H, D, kx.stride_t, kx.stride_h, kBM, c.bf16) ||
       !encode_thd(&m_v128, vx.ptr, total_k, H, D, vx.stride_t, vx.stride_h, kBM, c.bf16) ||
       !encode_thd(&m_q64, qx.ptr, total_q, H, D, qx.stride_t, qx.stride_h, BQ, c.bf16) ||
-      !encode_thd(&m_do64, dox.ptr, total_q, H, D, dox.stride_t, dox.stride_h, BQ, c.bf16))
+      !encode_thd(&m_do64, dox.ptr, total_q, H, D, dox.stride_t, dox.stride_h, BQ, c.bf16) ||
+      !encode_ds(&m_ds, ws + lay.ds, lay.ds_blocks, c.bf16))
     return HSTU_ERR_CUDA;
 
-  int* header = static_cast<int*>(workspace);
-  int4* unitsA = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
-  int4* unitsB = unitsA + 2 * capA;  // two int4 per unit
+  int* header = reinterpret_cast<int*>(ws);
+  int4* unitsA = reinterpret_cast<int4*>(ws + kHeaderBytes);
+  int4* unitsB = reinterpret_cast<int4*>(ws + lay.units_b);
+  int* ds_base = reinterpret_cast<int*>(ws + lay.ds_base);
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
+  sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks);
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   if (launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
@@ -327,28 +377,26 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
-  a.timeout_ns = kWaitTimeoutNs;
-  if (total_q > 0) {
-    AttnArgs aq = a;
-    aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA; aq.pdl_wait = 1;
-    aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
-    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-    if (launch_dq(D, c.bf16, grid, stream, em.pdl(), m_q128, m_do128, m_kbn, m_vbn, aq) !=
-        cudaSuccess)
-      return HSTU_ERR_CUDA;
-  }
-  if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
+  a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
+  a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
+  // dK/dV first: it also stores the dS blocks that the dQ kernel reads
   if (total_k > 0) {
     AttnArgs ak = a;
     ak.units = unitsB; ak.units_slot = kHdrUnitsB; ak.next_slot = kHdrNextB;
-    // Beside a running dQ grid (which already waited for the scheduler) the
-    // dK/dV grid needs no wait before it starts; alone, it waits first.
-    ak.pdl_wait = total_q > 0 ? 2 : 1;
     ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
     ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
     const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capB));
     if (launch_dkdv(D, c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64, ak) !=
         cudaSuccess)
+      return HSTU_ERR_CUDA;
+  }
+  if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
+  if (total_q > 0) {
+    AttnArgs aq = a;
+    aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA;
+    aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
+    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
+    if (launch_dq(D, c.bf16, grid, stream, em.pdl(), m_ds, m_k128, aq) != cudaSuccess)
       return HSTU_ERR_CUDA;
   }
   if (!em.mark(3, stream)) return HSTU_ERR_CUDA;
@@ -474,7 +522,8 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(
     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
     int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen, int32_t causal,
     cudaStream_t stream) {
-  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim, 0);
+  const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim,
+                                               max_seqlen_q, max_seqlen_k, 0);
   if (need == 0) return supported_dim(head_dim) ? HSTU_ERR_INVALID_ARG : HSTU_ERR_UNSUPPORTED;
   if (need > kNoAllocScratchBytes) return HSTU_ERR_INVALID_ARG;  // schedule would not fit
   void* scratch = nullptr;

@@ -10,7 +10,9 @@
 // and dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
 // element), writes both back in place as 16-bit, and accumulates
 // dV += A^T dO and dK += dS^T Q with the A operand read from TMEM.  No
-// atomics.
+// atomics.  Each dS^T block (128 keys x 64 queries) is also stored to the
+// workspace, where the dQ kernel reads it for dQ = dS K; keys past the
+// sequence end store zeros there, so they add nothing to dQ.
 //   warp 0       TMA: K and V per unit, Q and dO per half-step (separate
 //                rings: Q is released after dK, dO after dV).
 //   warp 1       tcgen05 issuer of S^T_h and dP^T_h into buffer h % 2, once
@@ -48,6 +50,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
   static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
   static_assert(C::SMEM <= 232448, "shared memory budget");
+  static_assert(BQ == kDsQueries && kBM == kDsKeys && CW == 16, "one stored dS block per half-step");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -307,6 +310,18 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
       const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
+      // dS^T blocks of this key tile: one per half-step, stored by the D half 0
+      // unit; row r, this warp's 16 queries are 32 bytes at r * 128 + cg * 32
+      char* ds_row = nullptr;
+      if (half == 0) {
+        const int n_qb = (Lq + BQ - 1) / BQ;
+        const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
+        const int blk = b0 + hd * ((b1 - b0) / a.H) + ds_block_off(U.tile, n_qb, a.causal);
+        if (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap)  // else metadata overflow
+          ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(blk) * kDsBlockBytes + r * 128 +
+                   cg * 32;
+      }
+      const bool key_ok = j < Lk;
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
         if (!wait_bar_warp(bar(STFULL + b), (h >> 1) & 1, wc, 0x201)) { ok = false; break; }
@@ -332,6 +347,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         tmem_st_w<CW / 2>(tST + b * BQ, pa);   // in place over this warp's S^T columns
         tmem_st_w<CW / 2>(tDPT + b * BQ, pd);  // in place over this warp's dP^T columns
+        if (ds_row != nullptr) {
+          uint4* dst = reinterpret_cast<uint4*>(ds_row + static_cast<int64_t>(m) * kDsBlockBytes);
+          dst[0] = key_ok ? make_uint4(pd[0], pd[1], pd[2], pd[3]) : make_uint4(0, 0, 0, 0);
+          dst[1] = key_ok ? make_uint4(pd[4], pd[5], pd[6], pd[7]) : make_uint4(0, 0, 0, 0);
+        }
         tmem_st_wait();
         warp_arrive(bar(ASFULL + b));
       }
@@ -359,9 +379,6 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     }
   }
 
-  // Started early beside the dQ grid: finish only after it, so that work
-  // queued behind this grid also sees dQ complete.
-  if (a.pdl_wait == 2) grid_dependency_wait();
   // The role branches leave lanes of warps 0, 1 (and 18) on different paths;
   // reconverge each warp so the aligned CTA barrier counts it exactly once
   // (otherwise it can release before the row warps finish reading TMEM).

@@ -18,14 +18,16 @@ constexpr int kFwdRowWarps = 8;
 constexpr int kFwdEpiWarps = 4;
 constexpr int kFwdPvWarp = 2 + kFwdRowWarps + kFwdEpiWarps;
 constexpr int kAttnThreads = 32 * (kFwdPvWarp + 1);
-// Backward kernels: warp 0 TMA, warp 1 MMA, warps 2-17 row work (four warps
-// per TMEM lane quarter, one per quarter of the columns).
+// dK/dV kernel: warp 0 TMA, warp 1 MMA, warps 2-17 row work (four warps per
+// TMEM lane quarter, one per quarter of the columns), warp 18 issues the
+// accumulation MMAs, so the two MMA streams wait on their own barriers
+// without stalling each other.
 constexpr int kRowWarps16 = 16;
-constexpr int kWideThreads = 64 + 32 * kRowWarps16;
-// dQ and dK/dV kernels: one more warp (18) issues the accumulation MMAs, so
-// the two MMA streams wait on their own barriers without stalling each other.
-constexpr int kDqThreads = kWideThreads + 32;
-constexpr int kDkdvThreads = kWideThreads + 32;
+constexpr int kDkdvThreads = 64 + 32 * kRowWarps16 + 32;
+// dQ kernel (dQ = dS K from the stored dS blocks): warp 0 TMA, warp 1 MMA,
+// warps 2-5 epilogue (one per TMEM lane quarter).
+constexpr int kDqEpiWarps = 4;
+constexpr int kDqThreads = 64 + 32 * kDqEpiWarps;
 constexpr int kTmemCols = 512;
 
 // Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
@@ -46,7 +48,31 @@ struct SchedArgs {
   int bq_b, split_b, cmax_b, cap_b;  // list B: key tiles, inner tiles of bq_b queries
   int4* units_b;
   int* header;
+  int* ds_base;              // backward: (B + 1) first dS block of each sequence, or null
+  int ds_cap;                // backward: dS blocks the workspace holds
 };
+
+// ---------------------------------------------------------------- dS blocks
+// The backward stores dS (times 2, in the input dtype) as blocks of 128 keys
+// x 64 queries, key-major ([key][query], 128 bytes per key row), one block
+// per (sequence, head, key tile j, 64-query block m) that the mask leaves
+// non-empty.  Sequence b owns blocks [ds_base[b], ds_base[b+1]): H runs of
+// ds_blocks_head(...) blocks, head-major; inside a head, key tile j's blocks
+// start at ds_block_off(j, ...) and hold m = ds_m0(j) .. n_qb - 1 in order.
+constexpr int kDsKeys = 128, kDsQueries = 64;
+constexpr int kDsBlockBytes = kDsKeys * kDsQueries * 2;
+
+__host__ __device__ __forceinline__ int ds_m0(int j, int causal) { return causal ? 2 * j : 0; }
+// Blocks of key tiles 0 .. j-1 of one head (n_qb query blocks).
+__host__ __device__ __forceinline__ int ds_block_off(int j, int n_qb, int causal) {
+  if (!causal) return j * n_qb;
+  const int jj = j < (n_qb + 1) / 2 ? j : (n_qb + 1) / 2;  // later key tiles hold none
+  return jj * n_qb - jj * (jj - 1);
+}
+// Blocks of one head of a sequence with n_kt key tiles and n_qb query blocks.
+__host__ __device__ __forceinline__ int ds_blocks_head(int n_kt, int n_qb, int causal) {
+  return ds_block_off(n_kt, n_qb, causal);
+}
 
 struct AttnArgs {
   int64_t total_q, total_k;
@@ -64,6 +90,9 @@ struct AttnArgs {
   int64_t o0_st, o0_sh;
   void* o1;             // dkdv kernel: dk
   int64_t o1_st, o1_sh;
+  void* ds;             // backward: dS blocks (written by dK/dV, read by dQ)
+  const int* ds_base;   // backward: first dS block of each sequence (B + 1)
+  int ds_cap;           // backward: dS blocks the workspace holds
 };
 
 // ------------------------------------------------------------ forward config
@@ -82,19 +111,15 @@ struct FwdCfg {
 };
 
 // ------------------------------------------------------------ dQ config
-// K is read by S = Q K^T and by dQ += dS K (freed last); V only by dP = dO V^T.
-// 128-key steps (64 at D = 256) so every MMA but the D = 256 S and dP has
-// N >= 128; S and dP are single-buffered (the row warps release them as soon
-// as they are loaded), dS is double-buffered.
+// One stage: the two dS blocks of a 128-query tile against one 128-key tile
+// (2 x 16 KB), and that key tile (128 x D).
 template <int D>
 struct DqCfg {
-  static constexpr int BN = D == 256 ? 64 : 128;
-  static constexpr int NQ = D == 64 ? 2 : 1;         // (Q, dO) buffers
-  static constexpr int NK = D == 64 ? 5 : (D == 128 ? 3 : 2);
-  static constexpr int NV = D == 64 ? 5 : (D == 128 ? 2 : 1);
-  static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int TILE_BYTES = 2 * NQ * Q_BYTES + (NK + NV) * KV_BYTES;
+  static constexpr int NS = D == 64 ? 4 : (D == 128 ? 3 : 2);  // stages
+  static constexpr int A_BYTES = 2 * kDsBlockBytes;
+  static constexpr int K_BYTES = kDsKeys * D * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + K_BYTES;
+  static constexpr int TILE_BYTES = NS * STAGE_BYTES;
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
 };
 
@@ -130,8 +155,8 @@ __global__ void hstu_sched_kernel(SchedArgs a);
 cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a);
 
 // Launchers: return cudaErrorInvalidValue for a head_dim outside {64,128,256}.
-// Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (q/do: 128-row
-// box, k/v: BN-row box); dkdv (k/v: 128-row box, q/do: BQ-row box).
+// Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (dS blocks:
+// 64 x 128 box, k: 128-row box); dkdv (k/v: 128-row box, q/do: BQ-row box).
 // Launch of a persistent attention kernel.  With `pdl` the grid may start
 // while the previous grid in the stream is still running (programmatic
 // dependent launch); the kernel orders itself with griddepcontrol.wait as
@@ -154,9 +179,8 @@ inline cudaError_t launch_attn(void (*kern)(KArgs...), int grid, int threads, in
 
 cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a);
-cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
-                      const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const AttnArgs& a);
+cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tds,
+                      const CUtensorMap& tk, const AttnArgs& a);
 cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const AttnArgs& a);

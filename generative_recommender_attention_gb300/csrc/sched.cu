@@ -11,8 +11,10 @@
 // Each unit record is two int4: {sequence, tile, head (x split), cost} and
 // {q offset, q length, k offset, k length}, so a consumer needs one round
 // trip to global memory per unit.  Units with cost 0 are kept (their rows
-// must be written as zeros) and sort last.  Order inside one cost bucket is whatever the atomics give; it only
-// changes timing, never results.
+// must be written as zeros) and sort last.  Order inside one cost bucket is
+// whatever the atomics give; it only changes timing, never results.  For the
+// backward, the list-B block also writes ds_base: the first stored dS block
+// of every sequence (an exclusive scan of H * ds_blocks_head over them).
 #include "kernels.h"
 
 namespace hstu {
@@ -159,6 +161,31 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
   if (overflow) atomicExch(a.header + (list_b ? kHdrOverflowB : kHdrOverflow), 1);
   if (tid == 0) a.header[list_b ? kHdrUnitsB : kHdrUnitsA] = min(total, cap);
+
+  // pass 4 (backward, list-B block): first dS block of each sequence
+  if (list_b && a.ds_base != nullptr) {
+    auto blocks = [&](int b) {
+      int Lq, Lk;
+      seq_lengths(a, b, Lq, Lk);
+      return a.H * ds_blocks_head(ceil_div(Lk, kDsKeys), ceil_div(Lq, kDsQueries), a.causal);
+    };
+    const int per = (a.B + blockDim.x - 1) / blockDim.x;
+    const int s0 = min(a.B, tid * per), s1 = min(a.B, s0 + per);
+    int sum = 0;
+    for (int b = s0; b < s1; ++b) sum += blocks(b);
+    int all;
+    int run = block_exclusive_scan(sum, &all);
+    for (int b = s0; b < s1; ++b) {
+      a.ds_base[b] = run;
+      run += blocks(b);
+    }
+    if (tid == 0) {
+      a.ds_base[a.B] = all;
+      // sequences longer than the caller's max_seqlen_q: the blocks would not
+      // fit; the dK/dV kernel then skips the stores past the end
+      if (all > a.ds_cap || all < 0) atomicExch(a.header + kHdrOverflowB, 1);
+    }
+  }
 }
 
 cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a) {

@@ -83,13 +83,19 @@ typedef struct {
 
 /*
  * Device workspace size, in bytes, that hstu_attn_fwd (is_bwd = 0) or
- * hstu_attn_bwd (is_bwd = 1) needs for these sizes.  The workspace holds the
- * device-built tile schedule and a status word; it must be 256-byte aligned
- * and may be reused by later calls on the same stream.  Returns 0 for invalid
- * sizes.
+ * hstu_attn_bwd (is_bwd = 1) needs for these sizes; pass the same
+ * max_seqlen_q / max_seqlen_k as to the call.  The workspace holds the
+ * device-built tile schedule and status words, and for the backward the
+ * intermediate dS = M (.) (dO V^T) (.) SiLU'(S) in blocks of 128 keys x 64
+ * queries (16-bit), bounded from the sizes alone by
+ *     num_heads * ceil(max_seqlen_q / 64) * (ceil(total_k / 128) + batch)
+ * blocks of 16 KiB (the host never reads the sequence lengths).  It must be
+ * 256-byte aligned and may be reused by later calls on the same stream.
+ * Returns 0 for invalid sizes, or when the dS block count exceeds 2^31 - 1.
  */
 size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
-                                int32_t num_heads, int32_t head_dim, int32_t is_bwd);
+                                int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                int32_t max_seqlen_k, int32_t is_bwd);
 
 /*
  * Forward: out = HSTU-MHA(q, k, v) (page "HSTU Attention (Blackwell
@@ -117,8 +123,12 @@ hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_te
  * SM100/SM103)", section "High-level functions").  Arguments as for the
  * forward, which must have used the same alpha, scaling_seqlen, mask and
  * sequence metadata.  dout, dq: (total_q, H, D); dk, dv: (total_k, H, D).
- * No forward output or statistic is needed: S is recomputed.  dQ is reduced
- * without atomics, so results do not depend on scheduling.
+ * No forward output or statistic is needed: S is recomputed.  A key-stationary
+ * kernel forms dK, dV and the dS blocks (stored in the workspace); a second
+ * kernel reduces dQ = alpha dS K per query tile without atomics, so results
+ * do not depend on scheduling.  A sequence longer than max_seqlen_q makes the
+ * dS blocks overflow the workspace: the stores past its end are skipped and
+ * hstu_attn_last_device_status reports HSTU_ERR_INVALID_ARG.
  */
 hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
                             hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
@@ -136,7 +146,7 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
  *   forward:  events[0] before the scheduler launch, events[1] after it,
  *             events[2] after the forward kernel;
  *   backward: events[0] before the scheduler launch, events[1] after it,
- *             events[2] after the dQ kernel, events[3] after the dK/dV kernel.
+ *             events[2] after the dK/dV kernel, events[3] after the dQ kernel.
  * Elapsed times between consecutive events are per-kernel device times.
  * events must be non-null (HSTU_ERR_INVALID_ARG otherwise).
  */

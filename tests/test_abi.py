@@ -52,18 +52,36 @@ def test_version_and_status_strings(lib):
     assert lib.hstu_attn_status_string(5) == b"device wait timed out"
 
 
+def _bwd_bytes(B, Tq, Tk, H, D, max_q):
+    # header | list A | list B (unit records of 32 bytes, units <= H * (ceil(T/128) + B),
+    # twice on the key side for D = 256) | B + 1 block offsets | 1024-aligned dS blocks of
+    # 128 keys x 64 queries x 2 bytes, H * ceil(max_q / 64) * (ceil(Tk / 128) + B) of them
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+    capA = H * (cdiv(Tq, 128) + B)
+    capB = H * (2 if D == 256 else 1) * (cdiv(Tk, 128) + B)
+    ds = (256 + 32 * capA + 32 * capB + 4 * (B + 1) + 1023) // 1024 * 1024
+    total = ds + H * cdiv(max_q, 64) * (cdiv(Tk, 128) + B) * 128 * 64 * 2
+    return (total + 255) // 256 * 256
+
+
 def test_workspace_size(lib):
     ws = lib.hstu_attn_workspace_size
-    # header + 32 bytes per unit record, units <= H * (ceil(T/128) + B), 256-aligned
-    assert ws(4, 309, 309, 2, 64, 0) == (256 + 32 * 2 * (3 + 4) + 255) // 256 * 256
-    fwd = ws(32, 20480, 20480, 4, 128, 0)
-    bwd = ws(32, 20480, 20480, 4, 128, 1)
-    assert bwd == ((256 + 32 * 4 * (160 + 32) * 2) + 255) // 256 * 256 and fwd < bwd
-    # D = 256 splits dK/dV into two column halves: twice the key-side units
-    assert ws(16, 65536, 65536, 2, 256, 1) == 256 + 32 * 2 * (512 + 16) * 3
-    assert ws(1, 10, 10, 1, 96, 0) == 0        # unsupported head_dim
-    assert ws(-1, 10, 10, 1, 64, 0) == 0
-    assert ws(1, 10, 10, 0, 64, 0) == 0
+    # forward: header + 32 bytes per unit record, units <= H * (ceil(T/128) + B), 256-aligned
+    assert ws(4, 309, 309, 2, 64, 128, 128, 0) == (256 + 32 * 2 * (3 + 4) + 255) // 256 * 256
+    fwd = ws(32, 20480, 20480, 4, 128, 1024, 1024, 0)
+    bwd = ws(32, 20480, 20480, 4, 128, 1024, 1024, 1)
+    assert bwd == _bwd_bytes(32, 20480, 20480, 4, 128, 1024) and fwd < bwd
+    assert ws(16, 65536, 65536, 2, 256, 4096, 4096, 1) == _bwd_bytes(16, 65536, 65536, 2, 256, 4096)
+    assert ws(4, 309, 309, 2, 64, 128, 128, 1) == _bwd_bytes(4, 309, 309, 2, 64, 128)
+    # the dS bound grows with max_seqlen_q, not with max_seqlen_k
+    assert ws(4, 309, 309, 2, 64, 64, 128, 1) < ws(4, 309, 309, 2, 64, 128, 128, 1)
+    assert ws(4, 309, 309, 2, 64, 128, 256, 1) == ws(4, 309, 309, 2, 64, 128, 128, 1)
+    assert ws(1, 10, 10, 1, 96, 10, 10, 0) == 0        # unsupported head_dim
+    assert ws(-1, 10, 10, 1, 64, 10, 10, 0) == 0
+    assert ws(1, 10, 10, 0, 64, 10, 10, 0) == 0
+    assert ws(1, 10, 10, 1, 64, -1, 10, 1) == 0
+    # more than 2^31 - 1 dS blocks cannot be indexed
+    assert ws(1 << 20, 1 << 30, 1 << 30, 64, 64, 1 << 30, 1 << 30, 1) == 0
 
 
 def _call_fwd(lib, **over):
@@ -114,7 +132,7 @@ def test_fwd_empty_problems_are_noops(lib):
 def test_non_contiguous_layouts_accepted_by_validation(lib):
     # (T, H, 2D) packed KV buffer: k and v are disjoint views with stride_t = 2*H*D
     from generative_recommender_attention_gb300._lib import CTen  # noqa: F401
-    st = lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 0)
+    st = lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 60, 60, 0)
     assert st > 0
     # validation of a padded layout passes (the call then fails only for lack
     # of a device, which the CPU test does not reach: batch = 0 short-cuts)

@@ -153,7 +153,7 @@ def test_device_status_ok_after_calls():
     lens = [300, 20]
     x = workloads.random_inputs(lens, lens, 2, 64, torch.bfloat16, seed=10)
     xd = to_dev(x)
-    ws = torch.empty(hstu.workspace_size(2, 320, 320, 2, 64, True), dtype=torch.uint8,
+    ws = torch.empty(hstu.workspace_size(2, 320, 320, 2, 64, 300, 300, True), dtype=torch.uint8,
                      device="cuda")
     hstu.hstu_attn_bwd(xd["do"], xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"],
                        xd["cu_seqlens_k"], 300, 300, workspace=ws)
