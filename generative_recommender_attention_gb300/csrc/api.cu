@@ -83,16 +83,16 @@ bool encode_thd(CUtensorMap* m, const void* ptr, int64_t T, int H, int D, int64_
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the dS blocks: (64 queries, 128 keys, block), box of one
-// whole block, 128-byte swizzle.
+// 3-D map over the dS blocks: (128 keys, 64 queries, block), box of 64 keys
+// x 64 queries of one block, 128-byte swizzle.
 bool encode_ds(CUtensorMap* m, void* ptr, int64_t blocks, bool bf16) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDsQueries), static_cast<cuuint64_t>(kDsKeys),
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDsKeys), static_cast<cuuint64_t>(kDsQueries),
                         static_cast<cuuint64_t>(std::max<int64_t>(blocks, 1))};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDsQueries * 2),
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDsKeys * 2),
                            static_cast<cuuint64_t>(kDsBlockBytes)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kDsQueries), static_cast<cuuint32_t>(kDsKeys), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kDsQueries), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -10,19 +10,26 @@
 // and dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
 // element), writes both back in place as 16-bit, and accumulates
 // dV += A^T dO and dK += dS^T Q with the A operand read from TMEM.  No
-// atomics.  Each dS^T block (128 keys x 64 queries) is also stored to the
-// workspace, where the dQ kernel reads it for dQ = dS K; keys past the
-// sequence end store zeros there, so they add nothing to dQ.
+// atomics.  Each dS block (64 queries x 128 keys, query-major) is also
+// stored to the workspace, where the dQ kernel reads it for dQ = dS K; keys
+// past the sequence end store zeros there, so they add nothing to dQ.  A
+// thread holds one key row of dS^T; neighbouring lanes swap halves of their
+// packed pairs so that every 4-byte store writes two keys of one query and
+// a warp's store covers two contiguous 64-byte runs.
 //   warp 0       TMA: K and V per unit, Q and dO per half-step (separate
 //                rings: Q is released after dK, dO after dV).
-//   warp 1       tcgen05 issuer of S^T_h and dP^T_h into buffer h % 2, once
-//                the accumulation of step h-2 has consumed that buffer.
-//   warp 18      tcgen05 issuer of dV += A^T_h dO_h and dK += dS^T_h Q_h.
-//   warps 2-17   row work, four warps per TMEM lane quarter (one per quarter
-//                of the query columns).
-// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  While the row warps work on
-// buffer h % 2 the tensor pipe runs the other buffer's S^T / dP^T and the
-// previous accumulation, so the row work stays off the tensor pipe's path.
+//   warp 1       tcgen05 issuer of S^T_h into S^T buffer h % 2 once
+//                dV += A^T_{h-2} dO_{h-2} has consumed it, then of dP^T_h into
+//                dP^T buffer h % 2 once dK += dS^T_{h-2} Q_{h-2} has.
+//   warp 10      tcgen05 issuer of dV += A^T_h dO_h as soon as A^T_h is
+//                written, then of dK += dS^T_h Q_h as soon as dS^T_h is.
+//   warps 2-9    row work, two warps per TMEM lane quarter (one per half of
+//                the query columns): A^T_h from S^T_h as soon as S^T_h
+//                lands (so dV_h overlaps dP^T_h), then dS^T_h from dP^T_h.
+// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  Every buffer has its own
+// full / written / released barriers, so the two dependency chains
+// (S^T -> A^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T) run side by
+// side, two half-steps deep, and each step's row work overlaps MMAs.
 // The N = 64 S^T / dP^T MMAs run at about two thirds of the tensor rate; that
 // costs less than serialising the row work with 128-query steps, for which
 // TMEM has no room to double-buffer.
@@ -41,16 +48,18 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   using C = DkdvCfg<D>;
   constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV, NS = C::NS;
   constexpr int KCH = D / 64;
-  constexpr int RW = kRowWarps16;
-  constexpr int CW = BQ / 4;   // query columns per row warp
-  constexpr int DW = DH / 4;   // dK / dV columns per row warp
+  constexpr int RW = kDkdvRowWarps;
+  constexpr int WPQ = RW / 4;    // row warps per TMEM lane quarter
+  constexpr int CW = BQ / WPQ;   // query columns per row warp
+  constexpr int DW = DH / WPQ;  // dK / dV columns per row warp
   constexpr int MMA_B = 2 + RW;  // warp of the accumulation issuer
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BQ, false, false);
   constexpr uint32_t IDESC_ACC = idesc_f16(BF16, kBM, DH, false, true);
   constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
   static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
   static_assert(C::SMEM <= 232448, "shared memory budget");
-  static_assert(BQ == kDsQueries && kBM == kDsKeys && CW == 16, "one stored dS block per half-step");
+  static_assert(BQ == kDsQueries && kBM == kDsKeys && CW % 8 == 0 && CW <= 32,
+                "one stored dS block per half-step");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -62,8 +71,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   enum {
     KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
-    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, STFULL = DOEMPTY + NS, ASFULL = STFULL + 2,
-    ACCDONE = ASFULL + 2, ACCFULL = ACCDONE + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
+    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, SFULL = DOEMPTY + NS, PFULL = SFULL + 2,
+    AFULL = PFULL + 2, DSFULL = AFULL + 2, SDONE = DSFULL + 2, PDONE = SDONE + 2,
+    ACCFULL = PDONE + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
     UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
@@ -81,9 +91,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(STFULL + i), 1);
-      mbar_init(bar(ASFULL + i), RW);
-      mbar_init(bar(ACCDONE + i), 1);
+      mbar_init(bar(SFULL + i), 1);
+      mbar_init(bar(PFULL + i), 1);
+      mbar_init(bar(AFULL + i), RW);
+      mbar_init(bar(DSFULL + i), RW);
+      mbar_init(bar(SDONE + i), 1);
+      mbar_init(bar(PDONE + i), 1);
     }
     mbar_init(bar(ACCFULL), 1);
     mbar_init(bar(ACCEMPTY), RW);
@@ -215,9 +228,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         for (int m = 0; m < U.n; ++m, ++h) {
           const int s = h % NS, b = h & 1;
           if (!wait_bar(bar(QFULL + s), (h / NS) & 1, wc, 0x106)) { ok = false; break; }
-          // buffer b last held step h-2: free once its accumulation was issued
+          // the buffers last held step h-2: S^T is free once dV_{h-2} read
+          // A^T from it, dP^T once dK_{h-2} read dS^T
           if (h >= 2) {
-            if (!wait_bar(bar(ACCDONE + b), ((h >> 1) - 1) & 1, wc, 0x108)) { ok = false; break; }
+            if (!wait_bar(bar(SDONE + b), ((h >> 1) - 1) & 1, wc, 0x108)) { ok = false; break; }
             tc_fence_after();
           }
           const SDesc qd = kdesc(sQ + s * C::Q_BYTES), dod = kdesc(sDO + s * C::Q_BYTES);
@@ -225,12 +239,17 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + COL_ST + b * BQ, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk),
                    IDESC_S, kk > 0 ? 1u : 0u);
+          mma_commit(bar(SFULL + b));
           if (!wait_bar(bar(DOFULL + s), (h / NS) & 1, wc, 0x107)) { ok = false; break; }
+          if (h >= 2) {
+            if (!wait_bar(bar(PDONE + b), ((h >> 1) - 1) & 1, wc, 0x109)) { ok = false; break; }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + COL_DPT + b * BQ, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk),
                    IDESC_S, kk > 0 ? 1u : 0u);
-          mma_commit(bar(STFULL + b));
+          mma_commit(bar(PFULL + b));
           if (m == U.n - 1) mma_commit(bar(KVEMPTY + kb));
         }
         ++kvi;
@@ -252,7 +271,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int n0 = (U.hz % SPLIT) * DH;
         for (int m = 0; m < U.n; ++m, ++h) {
           const int s = h % NS, b = h & 1;
-          if (!wait_bar(bar(ASFULL + b), (h >> 1) & 1, wc, 0x105)) { ok = false; break; }
+          if (!wait_bar(bar(AFULL + b), (h >> 1) & 1, wc, 0x105)) { ok = false; break; }
           if (m == 0 && !wait_bar(bar(ACCEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
           tc_fence_after();
           const SDesc qd = mndesc<BQ>(sQ + s * C::Q_BYTES), dod = mndesc<BQ>(sDO + s * C::Q_BYTES);
@@ -263,12 +282,15 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             mma_ts(tDV, tmem + COL_ST + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
                    desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(DOEMPTY + s));
+          mma_commit(bar(SDONE + b));
+          if (!wait_bar(bar(DSFULL + b), (h >> 1) & 1, wc, 0x10a)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
             mma_ts(tDK, tmem + COL_DPT + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
                    desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(QEMPTY + s));
-          mma_commit(bar(ACCDONE + b));
+          mma_commit(bar(PDONE + b));
           if (m == U.n - 1) mma_commit(bar(ACCFULL));
         }
         ++oi;
@@ -278,8 +300,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ A^T, dS^T + epilogue
-    // Sixteen warps: warp w owns TMEM lane quarter w % 4 (32 key rows) and one
-    // quarter of the query columns of each S^T / dP^T tile (and of dK / dV).
+    // Warp w owns TMEM lane quarter w % 4 (32 key rows) and one share of the
+    // query columns of each S^T / dP^T tile (and of dK / dV).
     const int wq = warp & 3, cg = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -310,50 +332,82 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
       const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
-      // dS^T blocks of this key tile: one per half-step, stored by the D half 0
-      // unit; row r, this warp's 16 queries are 32 bytes at r * 128 + cg * 32
+      // dS blocks of this key tile: one per half-step, stored by the D half 0
+      // unit; this lane writes keys (r & ~1, r | 1) of query rows q, q + 2,
+      // ..., q = cg * CW + (r & 1), at q * 256 + (r & ~1) * 2
       char* ds_row = nullptr;
       if (half == 0) {
         const int n_qb = (Lq + BQ - 1) / BQ;
         const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
         const int blk = b0 + hd * ((b1 - b0) / a.H) + ds_block_off(U.tile, n_qb, a.causal);
         if (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap)  // else metadata overflow
-          ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(blk) * kDsBlockBytes + r * 128 +
-                   cg * 32;
+          ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(blk) * kDsBlockBytes +
+                   (cg * CW + (r & 1)) * (kDsKeys * 2) + (r & ~1) * 2;
       }
       const bool key_ok = j < Lk;
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
-        if (!wait_bar_warp(bar(STFULL + b), (h >> 1) & 1, wc, 0x201)) { ok = false; break; }
-        tc_fence_after();
         const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
         const bool need_mask = (ic + CW > Lq) || (a.causal && j_warp_last > ic);
-        uint32_t xs[CW], xp[CW];
-        tmem_ld_x2<CW>(tST + b * BQ, tDPT + b * BQ, xs, xp);
-        uint32_t pa[CW / 2], pd[CW / 2];
-        if (!need_mask) {
+        // masked queries of this warp's columns (bit e: query ic + e)
+        uint32_t valid = CW == 32 ? 0xffffffffu : (1u << CW) - 1u;
+        if (need_mask) {
+          valid = 0;
+#pragma unroll
+          for (int e = 0; e < CW; ++e) valid |= (ic + e >= lo && ic + e < Lq) ? (1u << e) : 0u;
+        }
+        // A^T = SiLU(alpha S^T) as soon as S^T lands; h and tanh(h) are kept
+        // for dS^T
+        if (!wait_bar_warp(bar(SFULL + b), (h >> 1) & 1, wc, 0x201)) { ok = false; break; }
+        tc_fence_after();
+        float hv[CW], tv[CW];
+        uint32_t pk[CW / 2];
+        {
+          uint32_t xs[CW];
+          tmem_ld_w<CW>(tST + b * BQ, xs);
+#pragma unroll
+          for (int e = 0; e < CW; ++e) {
+            hv[e] = ((valid >> e) & 1u) ? __uint_as_float(xs[e]) * half_alpha : 0.f;  // SiLU(0) = 0
+            tv[e] = tanh_approx(hv[e]);
+          }
 #pragma unroll
           for (int e = 0; e < CW / 2; ++e)
-            a_ds_pair<BF16>(xs[2 * e], xs[2 * e + 1], xp[2 * e], xp[2 * e + 1], half_alpha, pa[e],
-                            pd[e]);
-        } else {
+            pk[e] = pack2<BF16>(fmaf(hv[2 * e], tv[2 * e], hv[2 * e]),
+                                fmaf(hv[2 * e + 1], tv[2 * e + 1], hv[2 * e + 1]));
+        }
+        tmem_st_w<CW / 2>(tST + b * BQ, pk);   // in place over this warp's S^T columns
+        tmem_st_wait();
+        warp_arrive(bar(AFULL + b));
+        // dS^T = dP^T SiLU'(alpha S^T) (doubled), masked entries exactly 0
+        if (!wait_bar_warp(bar(PFULL + b), (h >> 1) & 1, wc, 0x203)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pd[CW / 2];
+        {
+          uint32_t xp[CW];
+          tmem_ld_w<CW>(tDPT + b * BQ, xp);
 #pragma unroll
           for (int e = 0; e < CW / 2; ++e) {
-            const int i = ic + 2 * e;
-            const bool v0 = i >= lo && i < Lq, v1 = i + 1 >= lo && i + 1 < Lq;
-            a_ds_pair<BF16>(v0 ? xs[2 * e] : 0u, v1 ? xs[2 * e + 1] : 0u, v0 ? xp[2 * e] : 0u,
-                            v1 ? xp[2 * e + 1] : 0u, half_alpha, pa[e], pd[e]);
+            const float d0 = ((valid >> (2 * e)) & 1u) ? __uint_as_float(xp[2 * e]) : 0.f;
+            const float d1 = ((valid >> (2 * e + 1)) & 1u) ? __uint_as_float(xp[2 * e + 1]) : 0.f;
+            pd[e] = pack2<BF16>(dsilu2(hv[2 * e], tv[2 * e], d0),
+                                dsilu2(hv[2 * e + 1], tv[2 * e + 1], d1));
           }
         }
-        tmem_st_w<CW / 2>(tST + b * BQ, pa);   // in place over this warp's S^T columns
         tmem_st_w<CW / 2>(tDPT + b * BQ, pd);  // in place over this warp's dP^T columns
         if (ds_row != nullptr) {
-          uint4* dst = reinterpret_cast<uint4*>(ds_row + static_cast<int64_t>(m) * kDsBlockBytes);
-          dst[0] = key_ok ? make_uint4(pd[0], pd[1], pd[2], pd[3]) : make_uint4(0, 0, 0, 0);
-          dst[1] = key_ok ? make_uint4(pd[4], pd[5], pd[6], pd[7]) : make_uint4(0, 0, 0, 0);
+          // pd[e] = (dS[q0 + 2e][r], dS[q0 + 2e + 1][r]); the even lane keeps
+          // query q0 + 2e for keys (r, r + 1), the odd lane query q0 + 2e + 1
+          uint32_t* dst = reinterpret_cast<uint32_t*>(ds_row + static_cast<int64_t>(m) * kDsBlockBytes);
+          const bool odd = (lane & 1) != 0;
+#pragma unroll
+          for (int e = 0; e < CW / 2; ++e) {
+            const uint32_t mine = key_ok ? pd[e] : 0u;
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            dst[e * kDsKeys] = __byte_perm(mine, other, odd ? 0x3276u : 0x5410u);
+          }
         }
         tmem_st_wait();
-        warp_arrive(bar(ASFULL + b));
+        warp_arrive(bar(DSFULL + b));
       }
       if (!ok) break;
       if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) { ok = false; break; }

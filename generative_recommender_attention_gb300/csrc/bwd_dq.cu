@@ -10,11 +10,11 @@
 // dS blocks and the matching key tile per 128-key step and accumulates dQ in
 // TMEM, so results do not depend on scheduling.
 //   warp 0      TMA: per step the two 64-query dS blocks (16 KB each) and
-//               the 128-key K tile into one ring stage.
-//   warp 1      tcgen05 issuer: dQ (+)= dS K, A = dS read M-major from the
-//               stored key-major blocks, B = K read N-major; two TMEM
-//               accumulators, so one unit's epilogue overlaps the next
-//               unit's MMAs.
+//               the 128-key K tile into one ring stage; the blocks land as
+//               rows 0-63 and 64-127 of one K-major 128 x 128 A tile.
+//   warp 1      tcgen05 issuer: dQ (+)= dS K, A = dS K-major, B = K read
+//               N-major; two TMEM accumulators, so one unit's epilogue
+//               overlaps the next unit's MMAs.
 //   warps 2-5   epilogue, one per TMEM lane quarter: dQ * alpha / (2 L_scale)
 //               with predicated row stores.
 // Rows of a tile past the sequence end (or a second dS block the sequence
@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   using C = DqCfg<D>;
   constexpr int NS = C::NS, KCH = D / 64;
   constexpr int NACC = 2;  // TMEM accumulators
-  constexpr uint32_t IDESC = idesc_f16(BF16, kBM, D, true, true);
+  constexpr uint32_t IDESC = idesc_f16(BF16, kBM, D, false, true);
   static_assert(NACC * D <= kTmemCols, "TMEM budget");
 
   extern __shared__ uint8_t smem_raw[];
@@ -109,8 +109,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!wait_bar(bar(EMPTY + s), ((g / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           const int blk = head_blk + ds_block_off(j, n_qb, a.causal) + 2 * i - ds_m0(j, a.causal);
           mbar_arrive_expect_tx(bar(FULL + s), bytes);
-          tma_load_3d(stage_a(s), &tm_ds, bar(FULL + s), 0, 0, blk);
-          if (second) tma_load_3d(stage_a(s) + kDsBlockBytes, &tm_ds, bar(FULL + s), 0, 0, blk + 1);
+          // A tile: 64-key chunk c of query rows 0-63 (block 2i) and 64-127 (2i + 1)
+#pragma unroll
+          for (int c = 0; c < kDsKeys / 64; ++c) {
+            tma_load_3d(stage_a(s) + c * (kBM * 128), &tm_ds, bar(FULL + s), 64 * c, 0, blk);
+            if (second)
+              tma_load_3d(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, &tm_ds, bar(FULL + s),
+                          64 * c, 0, blk + 1);
+          }
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
             tma_load_3d(stage_k(s) + c * (kDsKeys * 128), &tm_k, bar(FULL + s), 64 * c, h,
@@ -137,13 +143,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         for (int j = 0; j < U.n; ++j, ++g) {
           const int s = g % NS;
           if (!wait_bar(bar(FULL + s), (g / NS) & 1, wc, 0x106)) { ok = false; break; }
-          // A: dS, M = 128 queries in two 64-query chunks 16 KB apart, K = keys
-          // down the rows; B: K tile, N = D in 64-column chunks, K = keys.
-          const SDesc ad = mndesc<kDsKeys>(stage_a(s));
+          // A: dS, M = 128 query rows, K = keys in 64-key chunks 16 KB apart;
+          // B: K tile, N = D in 64-column chunks, K = keys down the rows.
+          const SDesc ad = kdesc(stage_a(s));
           const SDesc kd = mndesc<kDsKeys>(stage_k(s));
 #pragma unroll
           for (int kk = 0; kk < kDsKeys / 16; ++kk)
-            mma_ss(tAcc, desc_mnmajor<kDsKeys>(ad, kk, 0), desc_mnmajor<kDsKeys>(kd, kk, 0), IDESC,
+            mma_ss(tAcc, desc_kmajor<kBM>(ad, kk), desc_mnmajor<kDsKeys>(kd, kk, 0), IDESC,
                    (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(EMPTY + s));
         }

@@ -18,12 +18,13 @@ constexpr int kFwdRowWarps = 8;
 constexpr int kFwdEpiWarps = 4;
 constexpr int kFwdPvWarp = 2 + kFwdRowWarps + kFwdEpiWarps;
 constexpr int kAttnThreads = 32 * (kFwdPvWarp + 1);
-// dK/dV kernel: warp 0 TMA, warp 1 MMA, warps 2-17 row work (four warps per
-// TMEM lane quarter, one per quarter of the columns), warp 18 issues the
+// dK/dV kernel: warp 0 TMA, warp 1 MMA, warps 2-9 row work (two warps per
+// TMEM lane quarter, one per half of the columns), warp 10 issues the
 // accumulation MMAs, so the two MMA streams wait on their own barriers
-// without stalling each other.
-constexpr int kRowWarps16 = 16;
-constexpr int kDkdvThreads = 64 + 32 * kRowWarps16 + 32;
+// without stalling each other.  Few row warps per SM sub-partition leave
+// the issuing threads more of its issue slots.
+constexpr int kDkdvRowWarps = 8;
+constexpr int kDkdvThreads = 64 + 32 * kDkdvRowWarps + 32;
 // dQ kernel (dQ = dS K from the stored dS blocks): warp 0 TMA, warp 1 MMA,
 // warps 2-5 epilogue (one per TMEM lane quarter).
 constexpr int kDqEpiWarps = 4;
@@ -53,10 +54,10 @@ struct SchedArgs {
 };
 
 // ---------------------------------------------------------------- dS blocks
-// The backward stores dS (times 2, in the input dtype) as blocks of 128 keys
-// x 64 queries, key-major ([key][query], 128 bytes per key row), one block
-// per (sequence, head, key tile j, 64-query block m) that the mask leaves
-// non-empty.  Sequence b owns blocks [ds_base[b], ds_base[b+1]): H runs of
+// The backward stores dS (times 2, in the input dtype) as blocks of 64
+// queries x 128 keys, query-major ([query][key], 256 bytes per query row),
+// one block per (sequence, head, key tile j, 64-query block m) that the mask
+// leaves non-empty.  Sequence b owns blocks [ds_base[b], ds_base[b+1]): H runs of
 // ds_blocks_head(...) blocks, head-major; inside a head, key tile j's blocks
 // start at ds_block_off(j, ...) and hold m = ds_m0(j) .. n_qb - 1 in order.
 constexpr int kDsKeys = 128, kDsQueries = 64;
