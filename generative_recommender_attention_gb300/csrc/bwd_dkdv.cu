@@ -18,18 +18,20 @@
 // a warp's store covers two contiguous 64-byte runs.
 //   warp 0       TMA: K and V per unit, Q and dO per half-step (separate
 //                rings: Q is released after dK, dO after dV).
-//   warp 1       tcgen05 issuer of S^T_h into S^T buffer h % 2 once
-//                dV += A^T_{h-2} dO_{h-2} has consumed it, then of dP^T_h into
-//                dP^T buffer h % 2 once dK += dS^T_{h-2} Q_{h-2} has.
-//   warp 10      tcgen05 issuer of dV += A^T_h dO_h as soon as A^T_h is
-//                written, then of dK += dS^T_h Q_h as soon as dS^T_h is.
+//   warp 1       tcgen05 issuer of the dV chain: S^T_h into S^T buffer h % 2,
+//                and dV += A^T_h dO_h as soon as A^T_h is written, followed
+//                at once by S^T_{h+2} into the same buffer (MMAs from one
+//                thread execute in order, so S^T_{h+2} cannot overwrite A^T_h
+//                before dV_h has read it, and no release barrier is needed).
+//   warp 10      the same for the dK chain: dP^T_h, dK += dS^T_h Q_h,
+//                dP^T_{h+2}.
 //   warps 2-9    row work, two warps per TMEM lane quarter (one per half of
 //                the query columns): A^T_h from S^T_h as soon as S^T_h
 //                lands (so dV_h overlaps dP^T_h), then dS^T_h from dP^T_h.
-// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  Every buffer has its own
-// full / written / released barriers, so the two dependency chains
-// (S^T -> A^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T) run side by
-// side, two half-steps deep, and each step's row work overlaps MMAs.
+// TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  The two dependency chains
+// (S^T -> A^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T) run side by side,
+// two half-steps deep, one per issuing thread, so while one thread waits
+// for the row warps the other keeps the tensor pipe fed.
 // The N = 64 S^T / dP^T MMAs run at about two thirds of the tensor rate; that
 // costs less than serialising the row work with 128-query steps, for which
 // TMEM has no room to double-buffer.
@@ -52,7 +54,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   constexpr int WPQ = RW / 4;    // row warps per TMEM lane quarter
   constexpr int CW = BQ / WPQ;   // query columns per row warp
   constexpr int DW = DH / WPQ;  // dK / dV columns per row warp
-  constexpr int MMA_B = 2 + RW;  // warp of the accumulation issuer
+  constexpr int MMA_B = 2 + RW;  // warp of the dK chain's issuer
+  // Score tiles issued ahead of the accumulation that frees their buffer.
+  // Step h + LOOK needs a Q / dO stage that only step h + LOOK - NS releases,
+  // so LOOK < NS, or the two issuers could wait on each other.
+  constexpr int LOOK = NS >= 3 ? 2 : 1;
+  static_assert(LOOK < NS || NS == 1, "look-ahead must leave a free stage");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BQ, false, false);
   constexpr uint32_t IDESC_ACC = idesc_f16(BF16, kBM, DH, false, true);
   constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
@@ -72,8 +79,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   enum {
     KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
     DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, SFULL = DOEMPTY + NS, PFULL = SFULL + 2,
-    AFULL = PFULL + 2, DSFULL = AFULL + 2, SDONE = DSFULL + 2, PDONE = SDONE + 2,
-    ACCFULL = PDONE + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
+    AFULL = PFULL + 2, DSFULL = AFULL + 2,
+    ACCFULL = DSFULL + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
     UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
@@ -85,20 +92,20 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NKV; ++i) { mbar_init(bar(KVFULL + i), 1); mbar_init(bar(KVEMPTY + i), 1); }
+    // K / V and dO are released by both issuers, Q by the dK chain (dK_h is
+    // its last reader: the row warps read S^T_h before dS^T_h exists)
+    for (int i = 0; i < NKV; ++i) { mbar_init(bar(KVFULL + i), 1); mbar_init(bar(KVEMPTY + i), 2); }
     for (int i = 0; i < NS; ++i) {
       mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
-      mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 1);
+      mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SFULL + i), 1);
       mbar_init(bar(PFULL + i), 1);
       mbar_init(bar(AFULL + i), RW);
       mbar_init(bar(DSFULL + i), RW);
-      mbar_init(bar(SDONE + i), 1);
-      mbar_init(bar(PDONE + i), 1);
     }
-    mbar_init(bar(ACCFULL), 1);
+    mbar_init(bar(ACCFULL), 2);
     mbar_init(bar(ACCEMPTY), RW);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
@@ -209,94 +216,74 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         wait_bar(bar(DOFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ S^T / dP^T issuer
-    // Waits on TMA-filled stages need no tcgen05 fence; waits on the row
-    // warps' or the other issuer's TMEM accesses do.
+  } else if (warp == 1 || warp == MMA_B) {
+    // ------------------------------------------------------------ chain issuers
+    // Warp 1: S^T = K Q^T and dV += A^T dO.  Warp MMA_B: dP^T = V dO^T and
+    // dK += dS^T Q.  Waits on TMA-filled stages need no tcgen05 fence; waits
+    // on the row warps' TMEM writes do.
     if (lane == 0) {
-      uint32_t kvi = 0, h = 0;
+      const bool vchain = warp == 1;
+      // score MMA: A = K or V tile (K-major), B = Q or dO stage (K-major)
+      const int kv_off = vchain ? 0 : C::KV_BYTES;
+      const uint32_t sB = vchain ? sQ : sDO;
+      const int bfull = vchain ? QFULL : DOFULL;
+      const uint32_t tScore = tmem + (vchain ? COL_ST : COL_DPT);
+      const int score_full = vchain ? SFULL : PFULL;
+      // accumulation: A = the 16-bit operand written over the score buffer,
+      // B = dO or Q stage (MN-major), into dV or dK
+      const uint32_t sAccB = vchain ? sDO : sQ;
+      const int accbfull = vchain ? DOFULL : QFULL;
+      const int ready = vchain ? AFULL : DSFULL;
+      const uint32_t tAcc = tmem + (vchain ? COL_DV : COL_DK);
+      uint32_t kvi = 0, h = 0, oi = 0;
       bool ok = true;
+      auto score = [&](uint32_t hh, const SDesc& ad) -> bool {
+        const int s = hh % NS, b = hh & 1;
+        if (!wait_bar(bar(bfull + s), (hh / NS) & 1, wc, vchain ? 0x106 : 0x107)) return false;
+        const SDesc bd = kdesc(sB + s * C::Q_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tScore + b * BQ, desc_kmajor<kBM>(ad, kk), desc_kmajor<BQ>(bd, kk), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(bar(score_full + b));
+        if (!vchain) mma_commit(bar(DOEMPTY + s));  // dP^T is the dK chain's only dO reader
+        return true;
+      };
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U;
         if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
         if (U.n <= 0) continue;
         const int kb = kvi % NKV;
-        if (!wait_bar(bar(KVFULL + kb), (kvi / NKV) & 1, wc, 0x104)) { ok = false; break; }
-        const SDesc kd = kdesc(sKV + kb * 2 * C::KV_BYTES);
-        const SDesc vd = kdesc(sKV + kb * 2 * C::KV_BYTES + C::KV_BYTES);
-        for (int m = 0; m < U.n; ++m, ++h) {
-          const int s = h % NS, b = h & 1;
-          if (!wait_bar(bar(QFULL + s), (h / NS) & 1, wc, 0x106)) { ok = false; break; }
-          // the buffers last held step h-2: S^T is free once dV_{h-2} read
-          // A^T from it, dP^T once dK_{h-2} read dS^T
-          if (h >= 2) {
-            if (!wait_bar(bar(SDONE + b), ((h >> 1) - 1) & 1, wc, 0x108)) { ok = false; break; }
-            tc_fence_after();
-          }
-          const SDesc qd = kdesc(sQ + s * C::Q_BYTES), dod = kdesc(sDO + s * C::Q_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_ST + b * BQ, desc_kmajor<kBM>(kd, kk), desc_kmajor<BQ>(qd, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          mma_commit(bar(SFULL + b));
-          if (!wait_bar(bar(DOFULL + s), (h / NS) & 1, wc, 0x107)) { ok = false; break; }
-          if (h >= 2) {
-            if (!wait_bar(bar(PDONE + b), ((h >> 1) - 1) & 1, wc, 0x109)) { ok = false; break; }
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + COL_DPT + b * BQ, desc_kmajor<kBM>(vd, kk), desc_kmajor<BQ>(dod, kk),
-                   IDESC_S, kk > 0 ? 1u : 0u);
-          mma_commit(bar(PFULL + b));
-          if (m == U.n - 1) mma_commit(bar(KVEMPTY + kb));
-        }
-        ++kvi;
-      }
-      mma_commit(bar(DRAIN));
-      wait_bar(bar(DRAIN), 0, drain, 0x1ff);
-    }
-  } else if (warp == MMA_B) {
-    // ------------------------------------------------------------ dV / dK issuer
-    if (lane == 0) {
-      const uint32_t tDV = tmem + COL_DV, tDK = tmem + COL_DK;
-      uint32_t h = 0, oi = 0;
-      bool ok = true;
-      for (uint32_t uk = 0; ok; ++uk) {
-        UnitInfo U;
-        if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
-        if (U.n < 0) break;
-        if (U.n <= 0) continue;
         const int n0 = (U.hz % SPLIT) * DH;
-        for (int m = 0; m < U.n; ++m, ++h) {
+        if (!wait_bar(bar(KVFULL + kb), (kvi / NKV) & 1, wc, 0x104)) { ok = false; break; }
+        const SDesc ad = kdesc(sKV + kb * 2 * C::KV_BYTES + kv_off);
+        // the first LOOK score tiles of the unit; later ones follow the
+        // accumulation that frees their buffer
+        for (int m = 0; m < U.n && m < LOOK && ok; ++m) ok = score(h + m, ad);
+        for (int m = 0; m < U.n && ok; ++m, ++h) {
           const int s = h % NS, b = h & 1;
-          if (!wait_bar(bar(AFULL + b), (h >> 1) & 1, wc, 0x105)) { ok = false; break; }
+          if (!wait_bar(bar(ready + b), (h >> 1) & 1, wc, vchain ? 0x105 : 0x10a)) { ok = false; break; }
+          if (!wait_bar(bar(accbfull + s), (h / NS) & 1, wc, 0x10b)) { ok = false; break; }
           if (m == 0 && !wait_bar(bar(ACCEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
           tc_fence_after();
-          const SDesc qd = mndesc<BQ>(sQ + s * C::Q_BYTES), dod = mndesc<BQ>(sDO + s * C::Q_BYTES);
+          const SDesc bd = mndesc<BQ>(sAccB + s * C::Q_BYTES);
           // A^T / dS^T of queries [16 kk, 16 kk + 16) sit packed in the first
           // half of their row warp's own CW columns
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tDV, tmem + COL_ST + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
-                   desc_mnmajor<BQ>(dod, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(DOEMPTY + s));
-          mma_commit(bar(SDONE + b));
-          if (!wait_bar(bar(DSFULL + b), (h >> 1) & 1, wc, 0x10a)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tDK, tmem + COL_DPT + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
-                   desc_mnmajor<BQ>(qd, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(QEMPTY + s));
-          mma_commit(bar(PDONE + b));
+            mma_ts(tAcc, tScore + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
+                   desc_mnmajor<BQ>(bd, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar((vchain ? DOEMPTY : QEMPTY) + s));
           if (m == U.n - 1) mma_commit(bar(ACCFULL));
+          if (m + LOOK < U.n && !score(h + LOOK, ad)) { ok = false; break; }
         }
+        mma_commit(bar(KVEMPTY + kb));
+        ++kvi;
         ++oi;
       }
-      mma_commit(bar(DRAIN + 1));
-      wait_bar(bar(DRAIN + 1), 0, drain, 0x1fe);
+      mma_commit(bar(DRAIN + (vchain ? 0 : 1)));
+      wait_bar(bar(DRAIN + (vchain ? 0 : 1)), 0, drain, vchain ? 0x1ff : 0x1fe);
     }
   } else {
     // ------------------------------------------------------------ A^T, dS^T + epilogue
