@@ -182,9 +182,11 @@ bool bwd_layout(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int3
   return true;
 }
 
-// Shared memory of the scheduler block: one int per cost bucket.
-bool sched_smem(int cmax, const DevInfo& dev, int* bytes) {
-  const int b = (cmax + 1) * 4;
+// Shared memory of the scheduler block: one int per cost bucket, then (for
+// up to kSchedCacheSeqs sequences) one 16-byte record per sequence.
+bool sched_smem(int cmax, int batch, const DevInfo& dev, int* bytes, int* cache) {
+  *cache = batch <= kSchedCacheSeqs ? 1 : 0;
+  const int b = sched_hist_ints(cmax) * 4 + (*cache ? 16 * batch : 0);
   if (b > dev.max_smem_optin) return false;
   static bool set = false;
   if (b > 48 * 1024 && !set) {
@@ -273,8 +275,8 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   const int BN = bn_for(D);
   const int64_t capA = cap_a(batch, total_q, H);
   const int cmax = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
-  int sched_bytes;
-  if (!sched_smem(cmax, c.dev, &sched_bytes)) return HSTU_ERR_UNSUPPORTED;
+  int sched_bytes, sched_cache;
+  if (!sched_smem(cmax, batch, c.dev, &sched_bytes, &sched_cache)) return HSTU_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk, tv;
   const void* kptr = total_k > 0 ? k.ptr : q.ptr;  // stand-in, never read when total_k == 0
@@ -291,7 +293,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
-  sa.header = header;
+  sa.header = header; sa.cache_seqs = sched_cache;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   if (launch_sched(1, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
@@ -345,8 +347,9 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   const int64_t capB = cap_b(batch, total_k, H, D);
   const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
   const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));
-  int sched_bytes;
-  if (!sched_smem(std::max(cmaxA, cmaxB), c.dev, &sched_bytes)) return HSTU_ERR_UNSUPPORTED;
+  int sched_bytes, sched_cache;
+  if (!sched_smem(std::max(cmaxA, cmaxB), batch, c.dev, &sched_bytes, &sched_cache))
+    return HSTU_ERR_UNSUPPORTED;
 
   // Stand-ins for empty sides: valid maps that no unit ever reads through.
   const bool hq = total_q > 0, hk = total_k > 0;
@@ -369,7 +372,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
-  sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks);
+  sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks); sa.cache_seqs = sched_cache;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   if (launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;

@@ -11,6 +11,10 @@
 namespace hstu {
 
 constexpr int kSchedThreads = 1024;
+// Up to this many sequences the scheduler keeps every sequence's offsets and
+// lengths in shared memory (16 bytes each), read from cu_seqlens once.
+constexpr int kSchedCacheSeqs = 4096;
+__host__ __device__ constexpr int sched_hist_ints(int cmax) { return (cmax + 1 + 3) & ~3; }
 // Forward kernel: warp 0 TMA, warp 1 issues S = Q K^T, warps 2-9 SiLU row
 // work (two per TMEM lane quarter, taking alternate key steps), warps 10-13
 // O epilogue (one per lane quarter), warp 14 issues O += P V.
@@ -51,6 +55,7 @@ struct SchedArgs {
   int* header;
   int* ds_base;              // backward: (B + 1) first dS block of each sequence, or null
   int ds_cap;                // backward: dS blocks the workspace holds
+  int cache_seqs;            // 1: sequence records cached in shared memory
 };
 
 // ---------------------------------------------------------------- dS blocks

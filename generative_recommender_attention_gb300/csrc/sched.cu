@@ -23,9 +23,10 @@ namespace {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ void seq_lengths(const SchedArgs& a, int b, int& Lq, int& Lk) {
-  Lq = max(0, __ldg(a.cu_q + b + 1) - __ldg(a.cu_q + b));
-  Lk = max(0, __ldg(a.cu_k + b + 1) - __ldg(a.cu_k + b));
+// Sequence b as {q offset, q length, k offset, k length}, from cu_seqlens.
+__device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
+  const int q0 = __ldg(a.cu_q + b), k0 = __ldg(a.cu_k + b);
+  return make_int4(q0, max(0, __ldg(a.cu_q + b + 1) - q0), k0, max(0, __ldg(a.cu_k + b + 1) - k0));
 }
 
 // Cost of query tile t (list A).
@@ -42,6 +43,10 @@ __device__ __forceinline__ int cost_b(const SchedArgs& a, int s, int Lq) {
   int nq = ceil_div(Lq, a.bq_b);
   int m0 = a.causal ? (kBM * s) / a.bq_b : 0;
   return max(0, nq - m0);
+}
+
+__device__ __forceinline__ int list_cmax(const SchedArgs& a, bool list_b) {
+  return list_b ? a.cmax_b : a.cmax_a;
 }
 
 // Exclusive prefix sum over 1024 threads; returns this thread's offset and
@@ -79,7 +84,8 @@ __device__ int block_exclusive_scan(int v, int* total) {
 }  // namespace
 
 __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) {
-  extern __shared__ int hist[];
+  extern __shared__ int hist[];  // cost buckets, then the cached sequence records
+  int4* seqs = reinterpret_cast<int4*>(hist + sched_hist_ints(list_cmax(a, blockIdx.x == 1)));
   const bool list_b = blockIdx.x == 1;
   const int cmax = list_b ? a.cmax_b : a.cmax_a;
   const int cap = list_b ? a.cap_b : a.cap_a;
@@ -108,13 +114,17 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
+  // every pass reads the sequences: one coalesced read of cu_seqlens
+  if (a.cache_seqs)
+    for (int b = tid; b < a.B; b += blockDim.x) seqs[b] = seq_global(a, b);
+  auto seq = [&](int b) { return a.cache_seqs ? seqs[b] : seq_global(a, b); };
   __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
 
   // pass 1: histogram of costs; a warp per sequence, a lane per tile
   for (int b = warp; b < a.B; b += nwarps) {
-    int Lq, Lk;
-    seq_lengths(a, b, Lq, Lk);
+    const int4 sq = seq(b);
+    const int Lq = sq.y, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
       const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
@@ -143,8 +153,8 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   // pass 3: emit complete unit records at their bucket cursors
   int overflow = 0;
   for (int b = warp; b < a.B; b += nwarps) {
-    const int q0 = __ldg(a.cu_q + b), k0 = __ldg(a.cu_k + b);
-    const int Lq = max(0, __ldg(a.cu_q + b + 1) - q0), Lk = max(0, __ldg(a.cu_k + b + 1) - k0);
+    const int4 sq = seq(b);
+    const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
       const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
@@ -165,9 +175,8 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   // pass 4 (backward, list-B block): first dS block of each sequence
   if (list_b && a.ds_base != nullptr) {
     auto blocks = [&](int b) {
-      int Lq, Lk;
-      seq_lengths(a, b, Lq, Lk);
-      return a.H * ds_blocks_head(ceil_div(Lk, kDsKeys), ceil_div(Lq, kDsQueries), a.causal);
+      const int4 sq = seq(b);
+      return a.H * ds_blocks_head(ceil_div(sq.w, kDsKeys), ceil_div(sq.y, kDsQueries), a.causal);
     };
     const int per = (a.B + blockDim.x - 1) / blockDim.x;
     const int s0 = min(a.B, tid * per), s1 = min(a.B, s0 + per);
