@@ -182,3 +182,55 @@ def test_binding_rejects_bad_tensors_on_cpu():
     with pytest.raises(ValueError):
         g._scaling(-2)
     assert g._causal(False, (-1, 0)) is True and g._causal(True, (-1, -1)) is False
+
+
+def test_ds_block_layout_rule():
+    """The dS block layout of the backward workspace (kernels.h: ds_m0,
+    ds_block_off, ds_blocks_head; sched.cu: ds_base), restated and checked by
+    brute force on random ragged batches: every block the dK/dV kernel writes
+    has a unique index inside its sequence's range, the dQ kernel finds the
+    blocks it reads where they were written, and the host's size bound holds."""
+    import random
+
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+
+    def m0(j, causal):
+        return 2 * j if causal else 0
+
+    def off(j, nqb, causal):
+        if not causal:
+            return j * nqb
+        jj = min(j, (nqb + 1) // 2)
+        return jj * nqb - jj * (jj - 1)
+
+    rng = random.Random(7)
+    for _ in range(400):
+        causal = rng.random() < 0.5
+        B, H = rng.randint(1, 5), rng.randint(1, 3)
+        Lk = [rng.randint(0, 600) for _ in range(B)]
+        Lq = [rng.randint(0, l) if rng.random() < 0.3 else l for l in Lk]
+        base = [0]
+        for b in range(B):
+            base.append(base[-1] + H * off(cdiv(Lk[b], 128), cdiv(Lq[b], 64), causal))
+        written = {}
+        for b in range(B):
+            nqb, head_blocks = cdiv(Lq[b], 64), (base[b + 1] - base[b]) // H
+            for h in range(H):
+                for j in range(cdiv(Lk[b], 128)):
+                    first = base[b] + h * head_blocks + off(j, nqb, causal)
+                    for m in range(max(0, nqb - m0(j, causal))):   # the key tile's half-steps
+                        k = first + m
+                        assert base[b] <= k < base[b + 1] and k not in written
+                        written[k] = (b, h, j, m0(j, causal) + m)
+        assert len(written) == base[-1]
+        for b in range(B):
+            nqb, head_blocks = cdiv(Lq[b], 64), (base[b + 1] - base[b]) // H
+            for h in range(H):
+                for i in range(cdiv(Lq[b], 128)):
+                    n = cdiv(min(128 * (i + 1), Lq[b], Lk[b]), 128) if causal else cdiv(Lk[b], 128)
+                    for j in range(n):
+                        blk = base[b] + h * head_blocks + off(j, nqb, causal) + 2 * i - m0(j, causal)
+                        assert written[blk] == (b, h, j, 2 * i)
+                        if 2 * i + 1 < nqb:
+                            assert written[blk + 1] == (b, h, j, 2 * i + 1)
+        assert base[-1] <= H * cdiv(max(Lq), 64) * (cdiv(sum(Lk), 128) + B)

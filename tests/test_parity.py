@@ -158,3 +158,21 @@ def test_device_status_ok_after_calls():
     hstu.hstu_attn_bwd(xd["do"], xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"],
                        xd["cu_seqlens_k"], 300, 300, workspace=ws)
     assert hstu.last_device_status(ws) == 0
+
+
+def test_backward_reports_understated_max_seqlen():
+    # A sequence longer than max_seqlen_q makes the dS blocks outgrow the
+    # workspace, which is sized from max_seqlen_q: the stores past its end are
+    # skipped (nothing outside the workspace is written) and the device status
+    # reports an invalid argument.
+    lens = [700, 20]
+    x = workloads.random_inputs(lens, lens, 2, 64, torch.bfloat16, seed=11)
+    xd = to_dev(x)
+    n = hstu.workspace_size(2, 720, 720, 2, 64, 64, 64, True)
+    guard = 1 << 16
+    buf = torch.full((n + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = buf[guard:guard + n]
+    hstu.hstu_attn_bwd(xd["do"], xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"],
+                       xd["cu_seqlens_k"], 64, 64, workspace=ws)
+    assert hstu.last_device_status(ws) == 1   # HSTU_ERR_INVALID_ARG
+    assert torch.all(buf[:guard] == 0x5A) and torch.all(buf[guard + n:] == 0x5A)
