@@ -389,8 +389,12 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
     ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
     ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
     const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capB));
-    if (launch_dkdv(D, c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64, ak) !=
-        cudaSuccess)
+    CUtensorMap m_dk128, m_dv128;  // whole key tiles leave through TMA stores
+    if (!encode_thd(&m_dk128, dk.ptr, total_k, H, D, dk.stride_t, dk.stride_h, kBM, c.bf16) ||
+        !encode_thd(&m_dv128, dv.ptr, total_k, H, D, dv.stride_t, dv.stride_h, kBM, c.bf16))
+      return HSTU_ERR_CUDA;
+    if (launch_dkdv(D, c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64, m_dk128,
+                    m_dv128, ak) != cudaSuccess)
       return HSTU_ERR_CUDA;
   }
   if (!em.mark(2, stream)) return HSTU_ERR_CUDA;

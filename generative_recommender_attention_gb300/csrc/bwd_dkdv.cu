@@ -17,7 +17,8 @@
 // packed pairs so that every 4-byte store writes two keys of one query and
 // a warp's store covers two contiguous 64-byte runs.
 //   warp 0       TMA: K and V per unit, Q and dO per half-step (separate
-//                rings: Q is released after dK, dO after dV).
+//                rings: Q is released after dK, dO after dV); at D <= 128
+//                also the TMA stores of finished dK / dV tiles.
 //   warp 1       tcgen05 issuer of the dV chain: S^T_h into S^T buffer h % 2,
 //                and dV += A^T_h dO_h as soon as A^T_h is written, followed
 //                at once by S^T_{h+2} into the same buffer (MMAs from one
@@ -28,6 +29,14 @@
 //   warps 2-9    row work, two warps per TMEM lane quarter (one per half of
 //                the query columns): A^T_h from S^T_h as soon as S^T_h
 //                lands (so dV_h overlaps dP^T_h), then dS^T_h from dP^T_h.
+// Epilogue: once a unit's last MMAs complete, the row warps read dV and dK
+// from TMEM and release them at once.  At D <= 128 they write the two tiles
+// (scaled, 16-bit, in the TMA box layout) into the unit's own K / V buffer,
+// which no MMA reads any more, and the producer issues TMA stores of them
+// before it loads the unit after next into that buffer; per-row stores of
+// 64-byte pieces (one cache line per lane) kept the row warps from the next
+// unit for several thousand cycles.  Ragged last tiles and D = 256 (one
+// K/V buffer) keep the per-row stores.
 // TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  The two dependency chains
 // (S^T -> A^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T) run side by side,
 // two half-steps deep, one per issuing thread, so while one thread waits
@@ -41,12 +50,22 @@ namespace hstu {
 
 namespace {
 
+// A key tile whose 128 rows all belong to its sequence (and to the tensor)
+// can leave through a TMA store of the whole tile; a ragged last tile is
+// stored row by row, since the box would also cover the next sequence.
+__device__ __forceinline__ bool tile_full(const UnitInfo& U, int64_t total_k) {
+  const int end = kBM * (U.tile + 1);
+  return end <= U.Lk && static_cast<int64_t>(U.k0) + end <= total_k;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_do, const AttnArgs a) {
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk,
+                         const __grid_constant__ CUtensorMap tm_dv, const AttnArgs a) {
   using C = DkdvCfg<D>;
   constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV, NS = C::NS;
   constexpr int KCH = D / 64;
@@ -55,6 +74,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   constexpr int CW = BQ / WPQ;   // query columns per row warp
   constexpr int DW = DH / WPQ;  // dK / dV columns per row warp
   constexpr int MMA_B = 2 + RW;  // warp of the dK chain's issuer
+  // With two (K, V) buffers, a unit's dV / dK leave through its own K / V
+  // buffer: the row warps stage them there once the unit's MMAs are done,
+  // and the producer writes them out with TMA stores before it loads the
+  // unit after next into that buffer.
+  constexpr bool STAGE = NKV == 2;
+  static_assert(!STAGE || SPLIT == 1, "staging holds the whole dK / dV tile");
   // Score tiles issued ahead of the accumulation that frees their buffer.
   // Step h + LOOK needs a Q / dO stage that only step h + LOOK - NS releases,
   // so LOOK < NS, or the two issuers could wait on each other.
@@ -80,7 +105,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
     DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, SFULL = DOEMPTY + NS, PFULL = SFULL + 2,
     AFULL = PFULL + 2, DSFULL = AFULL + 2,
-    ACCFULL = DSFULL + 2, ACCEMPTY = ACCFULL + 1, UFULL = ACCEMPTY + 1,
+    ACCFULL = DSFULL + 2, ACCEMPTY = ACCFULL + 1, STAGED = ACCEMPTY + 1, UFULL = STAGED + 2,
     UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
@@ -107,6 +132,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     }
     mbar_init(bar(ACCFULL), 2);
     mbar_init(bar(ACCEMPTY), RW);
+    mbar_init(bar(STAGED), RW);
+    mbar_init(bar(STAGED + 1), RW);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(bar(UFULL + i), 1);
       mbar_init(bar(UEMPTY + i), 2 + RW);
@@ -120,6 +147,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
+    if (STAGE) { tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv); }
   }
   if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
   __syncwarp();  // thread 0's set-up above diverged warp 0
@@ -148,11 +176,40 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           tma_prefetch_3d(&tm_do, 64 * c, h, row);
         }
       };
+      // Staged output tiles of K/V buffers 0 and 1: first key row (-1: the
+      // row warps stored that unit row by row) and head.
+      int st_row0 = -1, st_hd0 = 0, st_row1 = -1, st_hd1 = 0;
+      // Writes out the dV / dK tiles that the u-th unit (with key steps)
+      // staged in its K/V buffer, and waits until TMA has read them.
+      auto store_staged = [&](uint32_t u, const WaitCtl& w) -> bool {
+        const int kb = static_cast<int>(u & 1u);
+        if (!wait_bar(bar(STAGED + kb), (u >> 1) & 1u, w, 0x005)) return false;
+        const int row = kb ? st_row1 : st_row0, hd = kb ? st_hd1 : st_hd0;
+        if (row >= 0) {
+          const uint32_t kt = sKV + kb * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
+#pragma unroll
+          for (int c = 0; c < KCH; ++c) {
+            tma_store_3d(&tm_dk, kt + c * (kBM * 128), 64 * c, hd, row);
+            tma_store_3d(&tm_dv, vt + c * (kBM * 128), 64 * c, hd, row);
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        return true;
+      };
       // units are claimed one ahead: the next claim overlaps this unit's loads
       // the first unit of each CTA is its own index; later ones come from the counter
       UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
-        const UnitInfo U = nx;
+        UnitInfo U = nx;
+        if (U.n > 0 && U.hz % SPLIT == 0) {
+          // first stored dS block of this key tile (D half 0 stores them);
+          // -1 when the metadata outgrew the workspace
+          const int n_qb = (U.Lq + BQ - 1) / BQ;
+          const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
+          const int blk = b0 + (U.hz / SPLIT) * ((b1 - b0) / a.H) + ds_block_off(U.tile, n_qb, a.causal);
+          U.ds = (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap) ? blk : -1;
+        }
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
         nx = load_unit_info(a.units, gridDim.x + atomicAdd(a.header + a.next_slot, 1), n_units);
@@ -162,7 +219,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int q_seq0 = U.q0;
         const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
         const int kb = kvi % NKV;
-        if (!wait_bar(bar(KVEMPTY + kb), ((kvi / NKV) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
+        if constexpr (STAGE) {
+          // buffer kb last held the unit before the previous one
+          if (kvi >= 2 && !store_staged(kvi - 2, wc)) { ok = false; break; }
+          const int row = tile_full(U, a.total_k) ? k_row0 : -1;
+          if (kb) { st_row1 = row; st_hd1 = h; } else { st_row0 = row; st_hd0 = h; }
+        } else {
+          if (!wait_bar(bar(KVEMPTY + kb), ((kvi / NKV) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
+        }
         mbar_arrive_expect_tx(bar(KVFULL + kb), 2 * C::KV_BYTES);
         const uint32_t kt = sKV + kb * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
 #pragma unroll
@@ -208,6 +272,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(DOFULL + s), 64 * c, h, row);
           ++qi;
         }
+      }
+      if constexpr (STAGE) {
+        if (ok)
+          for (uint32_t u = kvi > 2 ? kvi - 2 : 0; u < kvi; ++u)
+            if (!store_staged(u, wc)) break;
+        bulk_wait_all();  // the output writes are complete before the block exits
       }
       for (uint32_t i = kvi > NKV ? kvi - NKV : 0; i < kvi; ++i)
         wait_bar(bar(KVFULL + i % NKV), (i / NKV) & 1, drain, 0x0f1);
@@ -278,7 +348,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           if (m == U.n - 1) mma_commit(bar(ACCFULL));
           if (m + LOOK < U.n && !score(h + LOOK, ad)) { ok = false; break; }
         }
-        mma_commit(bar(KVEMPTY + kb));
+        if (!STAGE) mma_commit(bar(KVEMPTY + kb));  // staged: the epilogue frees it
         ++kvi;
         ++oi;
       }
@@ -300,21 +370,73 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const float dk_scale = 0.5f * a.alpha * a.inv_L;  // dS^T is stored doubled
     uint32_t h = 0, oi = 0;
     bool ok = true;
+    // this lane's dV / dK row pieces of unit V, for the per-row stores
+    // (formed only where they are used, so no pointer stays live across the
+    // steps); returns whether the row exists
+    auto out_rows = [&](const UnitInfo& V, char*& dvrow, char*& dkrow) -> bool {
+      const int jj = kBM * V.tile + r;
+      const int64_t grow = static_cast<int64_t>(V.k0) + jj;
+      const int64_t hd = V.hz / SPLIT;
+      const int64_t col0 = static_cast<int64_t>(V.hz % SPLIT) * DH + cg * DW;
+      dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + hd * a.o0_sh + col0) * 2;
+      dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + hd * a.o1_sh + col0) * 2;
+      return jj < V.Lk && grow < a.total_k;
+    };
+    // Epilogue of unit V (the oi-th unit with key steps): wait for its last
+    // MMAs, read dV and dK out of TMEM, release them, write them out.
+    auto epilogue = [&](const UnitInfo& V) -> bool {
+      if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) return false;
+      tc_fence_after();
+      const bool staged = STAGE && tile_full(V, a.total_k);
+      if (staged) {
+        // dV into the V half and dK into the K half of the unit's (K, V)
+        // buffer, which no MMA reads any more (ACCFULL covers them all)
+        const uint32_t kt = sKV + (oi & 1u) * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
+#pragma unroll
+        for (int c = 0; c < DW / 32; ++c) {
+          uint32_t xv[32], xk[32];
+          tmem_ld32x2(tDV + 32 * c, tDK + 32 * c, xv, xk);
+          stage_row32<BF16>(vt, r, cg * DW + 32 * c, xv, a.inv_L);
+          stage_row32<BF16>(kt, r, cg * DW + 32 * c, xk, dk_scale);
+        }
+      } else if constexpr (DW <= 32) {
+        char *dvrow, *dkrow;
+        const bool row_ok = out_rows(V, dvrow, dkrow);
+        uint32_t x[DW];
+        tmem_ld_w<DW>(tDV, x);
+        if (row_ok) store_row_n<DW, BF16>(dvrow, x, a.inv_L);
+        tmem_ld_w<DW>(tDK, x);
+        if (row_ok) store_row_n<DW, BF16>(dkrow, x, dk_scale);
+      } else {
+        char *dvrow, *dkrow;
+        const bool row_ok = out_rows(V, dvrow, dkrow);
+#pragma unroll 1
+        for (int c = 0; c < DW / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tDV + 32 * c, x);
+          if (row_ok) store_row_n<32, BF16>(dvrow + c * 64, x, a.inv_L);
+          tmem_ld32(tDK + 32 * c, x);
+          if (row_ok) store_row_n<32, BF16>(dkrow + c * 64, x, dk_scale);
+        }
+      }
+      warp_arrive(bar(ACCEMPTY));
+      if constexpr (STAGE) {
+        fence_proxy_async_smem();  // staged tiles become visible to the TMA store
+        warp_arrive(bar(STAGED + (oi & 1u)));
+      }
+      ++oi;
+      return true;
+    };
     for (uint32_t uk = 0; ok; ++uk) {
       UnitInfo U;
       if (!unit_pop_warp(uq, uk, U, wc)) { ok = false; break; }
       if (U.n < 0) break;
-      const int hd = U.hz / SPLIT, half = U.hz % SPLIT;
-      const int Lq = U.Lq, k0 = U.k0, Lk = U.Lk;
+      const int Lq = U.Lq, Lk = U.Lk;
       const int j = kBM * U.tile + r;
       const int j_warp_last = kBM * U.tile + wq * 32 + 31;
-      const int64_t grow = static_cast<int64_t>(k0) + j;
-      const bool row_ok = j < Lk && grow < a.total_k;
-      const int64_t col0 = static_cast<int64_t>(half) * DH + cg * DW;
-      char* dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + static_cast<int64_t>(hd) * a.o0_sh + col0) * 2;
-      char* dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + static_cast<int64_t>(hd) * a.o1_sh + col0) * 2;
-      if (U.n <= 0) {
-        if (row_ok) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
+      if (U.n <= 0) {  // no key steps: zeros, no TMEM
+        char *dvrow, *dkrow;
+        if (out_rows(U, dvrow, dkrow)) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
         continue;
       }
       const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
@@ -323,25 +445,22 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       // unit; this lane writes keys (r & ~1, r | 1) of query rows q, q + 2,
       // ..., q = cg * CW + (r & 1), at q * 256 + (r & ~1) * 2
       char* ds_row = nullptr;
-      if (half == 0) {
-        const int n_qb = (Lq + BQ - 1) / BQ;
-        const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
-        const int blk = b0 + hd * ((b1 - b0) / a.H) + ds_block_off(U.tile, n_qb, a.causal);
-        if (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap)  // else metadata overflow
-          ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(blk) * kDsBlockBytes +
-                   (cg * CW + (r & 1)) * (kDsKeys * 2) + (r & ~1) * 2;
-      }
+      if (U.ds >= 0)  // set by the producer for D half 0 when the blocks fit
+        ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(U.ds) * kDsBlockBytes +
+                 (cg * CW + (r & 1)) * (kDsKeys * 2) + (r & ~1) * 2;
       const bool key_ok = j < Lk;
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
         const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
         const bool need_mask = (ic + CW > Lq) || (a.causal && j_warp_last > ic);
-        // masked queries of this warp's columns (bit e: query ic + e)
+        // valid queries of this warp's columns (bit e: query ic + e), the run
+        // of bits [lo - ic, Lq - ic) clamped to [0, CW)
         uint32_t valid = CW == 32 ? 0xffffffffu : (1u << CW) - 1u;
         if (need_mask) {
-          valid = 0;
-#pragma unroll
-          for (int e = 0; e < CW; ++e) valid |= (ic + e >= lo && ic + e < Lq) ? (1u << e) : 0u;
+          const int e0 = min(max(lo - ic, 0), CW), e1 = min(max(Lq - ic, 0), CW);
+          const uint32_t below_e1 = e1 >= 32 ? 0xffffffffu : (1u << e1) - 1u;
+          const uint32_t below_e0 = e0 >= 32 ? 0xffffffffu : (1u << e0) - 1u;
+          valid = below_e1 & ~below_e0;
         }
         // A^T = SiLU(alpha S^T) as soon as S^T lands; h and tanh(h) are kept
         // for dS^T
@@ -397,26 +516,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         warp_arrive(bar(DSFULL + b));
       }
       if (!ok) break;
-      if (!wait_bar_warp(bar(ACCFULL), oi & 1, wc, 0x202)) { ok = false; break; }
-      tc_fence_after();
-      if constexpr (DW <= 32) {
-        uint32_t x[DW];
-        tmem_ld_w<DW>(tDV, x);
-        if (row_ok) store_row_n<DW, BF16>(dvrow, x, a.inv_L);
-        tmem_ld_w<DW>(tDK, x);
-        if (row_ok) store_row_n<DW, BF16>(dkrow, x, dk_scale);
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < DW / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tDV + 32 * c, x);
-          if (row_ok) store_row_n<32, BF16>(dvrow + c * 64, x, a.inv_L);
-          tmem_ld32(tDK + 32 * c, x);
-          if (row_ok) store_row_n<32, BF16>(dkrow + c * 64, x, dk_scale);
-        }
-      }
-      warp_arrive(bar(ACCEMPTY));
-      ++oi;
+      if (!epilogue(U)) { ok = false; break; }
     }
   }
 
@@ -434,7 +534,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
 template <int D, bool BF16>
 cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tq, const CUtensorMap& tdo, const AttnArgs& a) {
+                          const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                          const CUtensorMap& tdv, const AttnArgs& a) {
   auto kern = hstu_bwd_dkdv_kernel<D, BF16>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -443,21 +544,22 @@ cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, a);
+  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, tdk,
+                     tdv, a);
 }
 
 }  // namespace
 
 cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const AttnArgs& a) {
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, const AttnArgs& a) {
   switch (D) {
-    case 64: return bf16 ? launch_dkdv_t<64, true>(grid, st, pdl, tk, tv, tq, tdo, a)
-                         : launch_dkdv_t<64, false>(grid, st, pdl, tk, tv, tq, tdo, a);
-    case 128: return bf16 ? launch_dkdv_t<128, true>(grid, st, pdl, tk, tv, tq, tdo, a)
-                          : launch_dkdv_t<128, false>(grid, st, pdl, tk, tv, tq, tdo, a);
-    case 256: return bf16 ? launch_dkdv_t<256, true>(grid, st, pdl, tk, tv, tq, tdo, a)
-                          : launch_dkdv_t<256, false>(grid, st, pdl, tk, tv, tq, tdo, a);
+    case 64: return bf16 ? launch_dkdv_t<64, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
+                         : launch_dkdv_t<64, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
+    case 128: return bf16 ? launch_dkdv_t<128, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
+                          : launch_dkdv_t<128, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
+    case 256: return bf16 ? launch_dkdv_t<256, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
+                          : launch_dkdv_t<256, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
     default: return cudaErrorInvalidValue;
   }
 }

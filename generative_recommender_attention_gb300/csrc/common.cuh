@@ -85,13 +85,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
 // Work-unit record plus the packed-sequence offsets and lengths it needs,
 // loaded together so a role can prefetch the next unit while it works on
 // the current one (the loads are independent global reads).
+// `ds` is filled in by kernels that need it (dK/dV: the unit's first stored
+// dS block, -1 for none).
 struct UnitInfo {
   int b, tile, hz, n;
   int q0, Lq, k0, Lk;
+  int ds;
 };
 
 __device__ __forceinline__ UnitInfo load_unit_info(const int4* units, int u, int n_units) {
-  UnitInfo r{0, 0, 0, -1, 0, 0, 0, 0};  // n = -1: no more units
+  UnitInfo r{0, 0, 0, -1, 0, 0, 0, 0, -1};  // n = -1: no more units
   if (u < n_units) {
     const int4 v = units[2 * u], w = units[2 * u + 1];
     r.b = v.x; r.tile = v.y; r.hz = v.z; r.n = v.w;
@@ -304,6 +307,28 @@ __device__ __forceinline__ void store_row_n(void* dst, const uint32_t (&x)[N], f
     p[v] = w;
   }
 }
+// 32 fp32 values of row r (columns col .. col + 31, col a multiple of 32)
+// scaled, rounded to 16 bits and written into a shared-memory tile laid out
+// like the TMA box: 64-column chunks of [128 rows][128 bytes], 128-byte
+// swizzle (16-byte unit u of row r sits at unit u ^ (r & 7)), so a TMA store
+// of the tile writes the rows out and the eight lanes of each store phase hit
+// distinct banks.
+template <bool BF16>
+__device__ __forceinline__ void stage_row32(uint32_t tile, int r, int col, const uint32_t (&x)[32],
+                                            float scale) {
+  const uint32_t row_base = tile + static_cast<uint32_t>(col >> 6) * (kBM * 128) +
+                            static_cast<uint32_t>(r) * 128;
+  const int u0 = (col & 63) >> 3;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint32_t w0 = pack2<BF16>(__uint_as_float(x[8 * v + 0]) * scale, __uint_as_float(x[8 * v + 1]) * scale);
+    const uint32_t w1 = pack2<BF16>(__uint_as_float(x[8 * v + 2]) * scale, __uint_as_float(x[8 * v + 3]) * scale);
+    const uint32_t w2 = pack2<BF16>(__uint_as_float(x[8 * v + 4]) * scale, __uint_as_float(x[8 * v + 5]) * scale);
+    const uint32_t w3 = pack2<BF16>(__uint_as_float(x[8 * v + 6]) * scale, __uint_as_float(x[8 * v + 7]) * scale);
+    st_shared_v4(row_base + (static_cast<uint32_t>((u0 + v) ^ (r & 7)) << 4), w0, w1, w2, w3);
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void store_zero_n(void* dst) {
   static_assert(N % 8 == 0, "whole 16-byte groups");

@@ -162,7 +162,8 @@ cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const S
 
 // Launchers: return cudaErrorInvalidValue for a head_dim outside {64,128,256}.
 // Tensor maps: forward (q: 128-row box, k/v: BN-row box); dq (dS blocks:
-// 64 x 128 box, k: 128-row box); dkdv (k/v: 128-row box, q/do: BQ-row box).
+// 64 x 128 box, k: 128-row box); dkdv (k/v: 128-row box, q/do: BQ-row box,
+// dk/dv: 128-row box, written by TMA stores of whole key tiles).
 // Launch of a persistent attention kernel.  With `pdl` the grid may start
 // while the previous grid in the stream is still running (programmatic
 // dependent launch); the kernel orders itself with griddepcontrol.wait as
@@ -189,7 +190,7 @@ cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, con
                       const CUtensorMap& tk, const AttnArgs& a);
 cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
                         const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const AttnArgs& a);
+                        const CUtensorMap& tdk, const CUtensorMap& tdv, const AttnArgs& a);
 cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace hstu
