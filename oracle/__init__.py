@@ -13,7 +13,9 @@ used as a brute-force check on tiny inputs.
 Method ("HSTU Attention (Blackwell SM100/SM103)", Overview): per packed
 sequence and head, O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V, no softmax.
 ``scaling_seqlen`` None or 0 means max_seqlen_q (same page, Overview and
-"High-level functions").
+"High-level functions").  The mask argument ``causal`` of every entry point is
+either a bool (True: window (-1, 0), False: window (-1, -1)) or a window pair
+(left, right) as in the page's section "Mask support", -1 meaning unbounded.
 """
 from __future__ import annotations
 
@@ -58,7 +60,7 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        common = [i64, i64, i32, f64, f64, i32, P, P, i64]
+        common = [i64, i64, i32, f64, f64, i32, i32, P, P, i64]
         lib.hstu_oracle_fwd_rows.argtypes = [P, P, P, P, P] + common + [P, i32]
         lib.hstu_oracle_dq_rows.argtypes = [P, P, P, P, P, P] + common + [P, i32]
         lib.hstu_oracle_dkdv_rows.argtypes = [P, P, P, P, P, P] + common + [P, P, i32]
@@ -101,6 +103,16 @@ def resolve_scaling(scaling_seqlen, max_seqlen_q) -> float:
     return float(scaling_seqlen)
 
 
+def window(mask):
+    """(left, right) of a mask given as a bool (causal / full) or a pair."""
+    if isinstance(mask, (tuple, list)):
+        left, right = (int(x) for x in mask)
+        if left < -1 or right < -1:
+            raise ValueError("window bounds are -1 (none) or >= 0")
+        return left, right
+    return (-1, 0) if bool(mask) else (-1, -1)
+
+
 def _rows_all(T: int, H: int):
     tok = np.repeat(np.arange(T, dtype=np.int64), H)
     head = np.tile(np.arange(H, dtype=np.int64), T)
@@ -118,7 +130,7 @@ def fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
     out = np.zeros((tok.shape[0], D), dtype=np.float64)
     _load().hstu_oracle_fwd_rows(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), cq.shape[0] - 1, H, D,
-        float(alpha), float(L_scale), int(bool(causal)), _ptr(tok), _ptr(hd),
+        float(alpha), float(L_scale), *window(causal), _ptr(tok), _ptr(hd),
         tok.shape[0], _ptr(out), int(n_threads))
     return out
 
@@ -135,7 +147,7 @@ def dq_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
     _load().hstu_oracle_dq_rows(
         _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
         cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
-        int(bool(causal)), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(out),
+        *window(causal), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(out),
         int(n_threads))
     return out
 
@@ -153,7 +165,7 @@ def dkdv_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale,
     _load().hstu_oracle_dkdv_rows(
         _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
         cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
-        int(bool(causal)), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(dk),
+        *window(causal), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(dk),
         _ptr(dv), int(n_threads))
     return dk, dv
 

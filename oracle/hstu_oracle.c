@@ -16,12 +16,15 @@
  * delimited by cumulative lengths cu_seqlens (same page, section "Tensor
  * layout").  Indices i (query) and j (key) below are local to the sequence.
  *
- * Mask M (same page, section "Mask support"): window (-1, 0) is causal and
- * window (-1, -1) is full.  Causal is read as the top-left aligned diagonal,
- * key j valid iff j <= i, the diagonal itself kept (the cuDNN "Attention"
- * page, diagonal_alignment TOP_LEFT with right bound 0 is the standard causal
- * mask).  In every mode a key must also lie inside the sequence: j < Lk.
- * A masked score contributes exactly zero (M multiplies SiLU(S)).
+ * Mask M (same page, section "Mask support"): window_size = (left, right)
+ * is the token-window mask, -1 meaning no bound on that side: key j is valid
+ * for query i iff j >= i - left (when left >= 0) and j <= i + right (when
+ * right >= 0).  Window (-1, 0) is causal, (-1, -1) full, finite bounds the
+ * local / sliding window.  The window is read as aligned top-left, on the
+ * diagonal j = i (the cuDNN "Attention" page: diagonal_alignment TOP_LEFT
+ * with right bound 0 is the standard causal mask), with the diagonal kept.
+ * In every mode a key must also lie inside the sequence: j < Lk.  A masked
+ * score contributes exactly zero (M multiplies SiLU(S)).
  *
  * Backward: the pages give the API (section "High-level functions") but not
  * the formulas.  They follow from the forward equations by the chain rule:
@@ -58,9 +61,10 @@ static double silu_grad(double x) {
     return s * (1.0 + x * (1.0 - s));
 }
 
-static int mask_valid(int64_t i, int64_t j, int64_t Lk, int causal) {
+static int mask_valid(int64_t i, int64_t j, int64_t Lk, int left, int right) {
     if (j >= Lk) return 0;
-    if (causal && j > i) return 0;
+    if (left >= 0 && j < i - left) return 0;
+    if (right >= 0 && j > i + right) return 0;
     return 1;
 }
 
@@ -103,7 +107,7 @@ int hstu_oracle_threads(int threads) { return set_threads(threads); }
 int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
                          const int32_t *cu_q, const int32_t *cu_k, int64_t B,
                          int64_t H, int D, double alpha, double L_scale,
-                         int causal, const int64_t *tok, const int64_t *head,
+                         int left, int right, const int64_t *tok, const int64_t *head,
                          int64_t n, double *out, int threads) {
     set_threads(threads);
 #pragma omp parallel for schedule(dynamic, 4)
@@ -117,7 +121,7 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
         int64_t ok = cu_k[b], Lk = (int64_t)cu_k[b + 1] - cu_k[b];
         const double *qi = row(q, tok[r], h, H, D);
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!mask_valid(i, j, Lk, causal)) continue;
+            if (!mask_valid(i, j, Lk, left, right)) continue;
             const double *kj = row(k, ok + j, h, H, D);
             const double *vj = row(v, ok + j, h, H, D);
             double s = alpha * dot(qi, kj, D);
@@ -132,7 +136,7 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
 int hstu_oracle_dq_rows(const double *dout, const double *q, const double *k,
                         const double *v, const int32_t *cu_q,
                         const int32_t *cu_k, int64_t B, int64_t H, int D,
-                        double alpha, double L_scale, int causal,
+                        double alpha, double L_scale, int left, int right,
                         const int64_t *tok, const int64_t *head, int64_t n,
                         double *dq, int threads) {
     set_threads(threads);
@@ -148,7 +152,7 @@ int hstu_oracle_dq_rows(const double *dout, const double *q, const double *k,
         const double *qi = row(q, tok[r], h, H, D);
         const double *doi = row(dout, tok[r], h, H, D);
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!mask_valid(i, j, Lk, causal)) continue;
+            if (!mask_valid(i, j, Lk, left, right)) continue;
             const double *kj = row(k, ok + j, h, H, D);
             const double *vj = row(v, ok + j, h, H, D);
             double s = alpha * dot(qi, kj, D);
@@ -164,7 +168,7 @@ int hstu_oracle_dq_rows(const double *dout, const double *q, const double *k,
 int hstu_oracle_dkdv_rows(const double *dout, const double *q, const double *k,
                           const double *v, const int32_t *cu_q,
                           const int32_t *cu_k, int64_t B, int64_t H, int D,
-                          double alpha, double L_scale, int causal,
+                          double alpha, double L_scale, int left, int right,
                           const int64_t *tok, const int64_t *head, int64_t n,
                           double *dk, double *dv, int threads) {
     set_threads(threads);
@@ -182,7 +186,7 @@ int hstu_oracle_dkdv_rows(const double *dout, const double *q, const double *k,
         const double *kj = row(k, tok[r], h, H, D);
         const double *vj = row(v, tok[r], h, H, D);
         for (int64_t i = 0; i < Lq; ++i) {
-            if (!mask_valid(i, j, Lk, causal)) continue;
+            if (!mask_valid(i, j, Lk, left, right)) continue;
             const double *qi = row(q, oq + i, h, H, D);
             const double *doi = row(dout, oq + i, h, H, D);
             double s = alpha * dot(qi, kj, D);

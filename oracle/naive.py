@@ -8,8 +8,10 @@ the chain-rule backward, one scalar at a time, with Python floats and
 arithmetic, no C and nothing from the C oracle.
 
 Inputs are nested Python lists indexed [t][h][d]; cu_seqlens are lists of
-ints.  ``causal`` selects the top-left aligned causal mask (key j valid iff
-j <= i and j < Lk), else the full mask (j < Lk).
+ints.  ``causal`` is True for the top-left aligned causal mask (key j valid
+iff j <= i and j < Lk), False for the full mask (j < Lk), or a window pair
+(left, right): key j valid iff j < Lk, i - left <= j unless left == -1, and
+j <= i + right unless right == -1.
 """
 from __future__ import annotations
 
@@ -36,7 +38,14 @@ def _zeros(T, H, D):
 
 
 def _valid(i, j, Lk, causal):
-    return j < Lk and (not causal or j <= i)
+    if j >= Lk:
+        return False
+    if isinstance(causal, (tuple, list)):
+        left, right = causal
+        lo_ok = left == -1 or i - j <= left
+        hi_ok = right == -1 or j - i <= right
+        return lo_ok and hi_ok
+    return not causal or j <= i
 
 
 def forward(q, k, v, cu_q, cu_k, alpha, L_scale, causal):

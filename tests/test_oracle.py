@@ -14,7 +14,12 @@ to mathematics it does not share code with:
   packing invariance, head independence;
 * gradients: central finite differences of <dO, O>, and torch.autograd on a
   dense masked fp64 formulation built from torch primitives;
-* limits: no NaN at |score| = 1e4.
+* limits: no NaN at |score| = 1e4;
+* windows ("Mask support", window_size = (left, right)): brute force with
+  random windows, the degenerate windows that equal the causal and full
+  masks, the diagonal-only window (0, 0) in closed form, the band built with
+  numpy's tril/triu in the linear regime, band additivity, finite
+  differences and autograd with a band mask.
 
 Each pin is chosen so that a plausible mistake in the oracle (a dropped term,
 a wrong sign or index, a transposed operand, a wrong mask offset) fails it.
@@ -77,8 +82,11 @@ def test_hand_worked_example(case):
 # --------------------------------------------------------------------------
 # brute force vs pure-Python restatement
 # --------------------------------------------------------------------------
+WINDOWS = [(0, 0), (2, 1), (3, -1), (-1, 2), (1, 0), (0, 3)]
+
+
 @pytest.mark.parametrize("seed", range(6))
-@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("causal", [True, False] + WINDOWS)
 def test_brute_force_tiny(seed, causal):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 4))
@@ -143,6 +151,17 @@ def test_length_one_sequences():
 
 
 def _dense_mask(Lq, Lk, causal):
+    """Dense 0/1 mask: bool (causal / full) by index comparison; a window
+    (left, right) as a band from numpy's tril (j <= i + right) and triu
+    (j >= i - left)."""
+    if isinstance(causal, tuple):
+        left, right = causal
+        m = np.ones((Lq, Lk))
+        if right >= 0:
+            m = np.tril(m, right)
+        if left >= 0:
+            m = np.triu(m, -left)
+        return m
     i = np.arange(Lq)[:, None]
     j = np.arange(Lk)[None, :]
     m = j < Lk
@@ -207,7 +226,7 @@ def _aligned_inputs(lens, H, D, sign, seed):
     return {n: torch.tensor(a) for n, a in (("q", q), ("k", k), ("v", v), ("do", do))}, cu
 
 
-@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("causal", [True, False, (2, 1), (0, 0), (4, -1), (-1, 3)])
 def test_linear_regime_matches_matmul(causal):
     """Scores >= 40: sigma = 1 to fp64 precision, SiLU(x) = x and SiLU'(x) = 1,
     so HSTU is masked linear attention, computed here with numpy matmuls."""
@@ -327,7 +346,7 @@ def test_heads_independent():
 # --------------------------------------------------------------------------
 # gradients
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("causal", [True, False, (1, 1), (2, -1)])
 def test_finite_differences(causal):
     lens = [4, 3]
     lk = [5, 3]
@@ -366,7 +385,7 @@ def test_adjoint_identity_on_q():
     assert abs((fp - fm) / (2 * eps) - np.sum(dq * dQ.numpy())) < 1e-6
 
 
-@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("causal", [True, False, (2, 1), (0, 0), (-1, 2)])
 def test_torch_autograd_dense(causal):
     """Dense masked fp64 formulation built from torch primitives
     (torch.nn.functional.silu, matmul), differentiated by autograd."""
@@ -392,6 +411,67 @@ def test_torch_autograd_dense(causal):
         np.testing.assert_allclose(dq[cq[b]:cq[b + 1]], q.grad.numpy(), rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(dk[ck[b]:ck[b + 1]], k.grad.numpy(), rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(dv[ck[b]:ck[b + 1]], v.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# windows
+# --------------------------------------------------------------------------
+def test_degenerate_windows_equal_causal_and_full():
+    """(-1, 0) is causal and (-1, -1) full; bounds at least as long as every
+    sequence remove nothing on their side."""
+    lq, lk = [9, 1, 14, 0, 6], [9, 3, 16, 2, 6]
+    x = _rand(lq, lk, 2, 5, seed=41)
+    alpha, L = 0.8, 7.0
+    big = 40
+    pairs = [((-1, 0), True), ((-1, -1), False), ((big, 0), True), ((big, big), False),
+             ((big, -1), False), ((-1, big), False)]
+    for win, ref in pairs:
+        np.testing.assert_array_equal(_fwd(x, alpha, L, win), _fwd(x, alpha, L, ref))
+        for g, h in zip(_bwd(x, alpha, L, win), _bwd(x, alpha, L, ref)):
+            np.testing.assert_array_equal(g, h)
+
+
+def test_diagonal_window_closed_form():
+    """Window (0, 0) keeps only key j = i: O_i = SiLU(x_ii) v_i / L,
+    dV_i = SiLU(x_ii) dO_i / L, dQ_i = alpha SiLU'(x_ii) <dO_i, v_i> k_i / L,
+    dK_i = alpha SiLU'(x_ii) <dO_i, v_i> q_i / L (rows past the other side's
+    length get nothing)."""
+    lq, lk = [5, 7, 2], [6, 4, 2]
+    H, D = 2, 4
+    x = _rand(lq, lk, H, D, seed=42)
+    alpha, L = 1.1, 3.0
+    o = _fwd(x, alpha, L, (0, 0))
+    dq, dk, dv = _bwd(x, alpha, L, (0, 0))
+    cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_k"].tolist()
+    for b in range(len(lq)):
+        n = min(lq[b], lk[b])
+        qs, ks = slice(cq[b], cq[b] + n), slice(ck[b], ck[b] + n)
+        q, k, v, do = x["q"][qs].numpy(), x["k"][ks].numpy(), x["v"][ks].numpy(), x["do"][qs].numpy()
+        s = alpha * np.sum(q * k, axis=-1)
+        da = np.sum(do * v, axis=-1)
+        np.testing.assert_allclose(o[qs], _silu(s)[..., None] * v / L, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(dv[ks], _silu(s)[..., None] * do / L, rtol=1e-12, atol=1e-15)
+        g = alpha * _silu_grad(s) * da / L
+        np.testing.assert_allclose(dq[qs], g[..., None] * k, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(dk[ks], g[..., None] * q, rtol=1e-12, atol=1e-15)
+        assert np.all(o[cq[b] + n:cq[b + 1]] == 0) and np.all(dq[cq[b] + n:cq[b + 1]] == 0)
+        assert np.all(dk[ck[b] + n:ck[b + 1]] == 0) and np.all(dv[ck[b] + n:ck[b + 1]] == 0)
+
+
+@pytest.mark.parametrize("left,right", [(0, 2), (3, 1), (2, 4)])
+def test_band_additivity(left, right):
+    """Every output is a sum of per-pair terms over the valid pairs, so the
+    pairs that a right bound adds past the diagonal are the same with or
+    without a left bound: F(l, r) - F(l, 0) = F(-1, r) - F(-1, 0)."""
+    lens = [10, 13]
+    x = _rand(lens, lens, 2, 4, seed=43)
+    alpha, L = 0.6, 5.0
+    f = lambda w: [_fwd(x, alpha, L, w)] + list(_bwd(x, alpha, L, w))  # noqa: E731
+    a, b, c, d = f((left, right)), f((left, 0)), f((-1, right)), f((-1, 0))
+    for ta, tb, tc, td in zip(a, b, c, d):
+        np.testing.assert_allclose(ta - tb, tc - td, rtol=1e-11, atol=1e-13)
+    # and the band really excludes something on each side
+    assert np.abs(a[0] - f((-1, -1))[0]).max() > 1e-3
 
 
 # --------------------------------------------------------------------------
