@@ -26,6 +26,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -45,16 +47,29 @@ def peaks():
 
 
 def pairs(lengths, H, causal):
+    """Attended (query, key) pairs times heads; ``causal`` is a bool or a
+    (left, right) token window (-1: unbounded side), Lq = Lk per sequence."""
+    if isinstance(causal, tuple):
+        left, right = causal
+        n = 0
+        for L in lengths:
+            i = np.arange(L, dtype=np.int64)
+            lo = np.zeros(L, dtype=np.int64) if left < 0 else np.maximum(0, i - left)
+            hi = np.full(L, L - 1, dtype=np.int64) if right < 0 else np.minimum(L - 1, i + right)
+            n += int(np.maximum(0, hi - lo + 1).sum())
+        return H * n
     if causal:
         return H * sum(L * (L + 1) // 2 for L in lengths)
     return H * sum(L * L for L in lengths)
 
 
-def workload_config(w, lengths):
+def workload_config(w, lengths, mask=None):
     d = w.describe()
     d["T"] = int(sum(lengths))
     d["max_seqlen"] = int(max(lengths))
-    d["N_pairs"] = int(pairs(lengths, w.heads, w.causal))
+    if mask is not None and isinstance(mask, tuple):
+        d["mask"] = f"window {mask}"
+    d["N_pairs"] = int(pairs(lengths, w.heads, w.causal if mask is None else mask))
     return d
 
 
@@ -106,7 +121,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0):
+def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0, mask=None):
     """Times the fp64 oracle fwd+bwd on whole sequences (all heads) of the
     workload, one after another from `start`, until `budget_s` is spent, on
     `threads` host threads (0: all cores).  Returns (flops, seconds,
@@ -118,6 +133,7 @@ def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0):
     B = len(cu) - 1
     L_scale = oracle.resolve_scaling(w.scaling_seqlen, x["max_seqlen_q"])
     D = w.head_dim
+    mask = w.causal if mask is None else mask
     flops, secs, n = 0.0, 0.0, 0
     b = start
     while n < B and (n == 0 or secs < budget_s):
@@ -125,11 +141,11 @@ def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0):
         sub = {k: x[k][s0:s1].double().numpy() for k in ("q", "k", "v", "do")}
         c1 = np.array([0, s1 - s0], dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.fwd(sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, w.causal, threads)
-        oracle.bwd(sub["do"], sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, w.causal,
+        oracle.fwd(sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, mask, threads)
+        oracle.bwd(sub["do"], sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, mask,
                    threads)
         secs += time.perf_counter() - t0
-        flops += 14.0 * D * pairs([s1 - s0], w.heads, w.causal)
+        flops += 14.0 * D * pairs([s1 - s0], w.heads, mask)
         n += 1
         b = (b + 1) % B
     return flops, secs, n, threads
@@ -148,7 +164,8 @@ def run_reference(args, w):
     n_seq = 0
     threads = 1
     for i in range(args.warmup + args.steps):
-        f, s, n, threads = oracle_sample(x, w, 0.0, start=i % w.batch)  # one sequence per step
+        f, s, n, threads = oracle_sample(x, w, 0.0, start=i % w.batch,  # one sequence per step
+                                         mask=args.mask)
         if i >= args.warmup:
             per_step.append(s)
             flops_tot += f
@@ -159,7 +176,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, x["lengths"]),
+            "config": workload_config(w, x["lengths"], args.mask),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": f"{n_seq} whole sequences (all heads, fwd+bwd), one per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -176,6 +193,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--window", default=None,
+                    help="token window 'left,right' (-1: no bound) instead of the workload's "
+                         "causal / full mask")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step through the Python binding instead of replaying a "
@@ -186,6 +206,10 @@ def main():
                          "CPU baseline) and print no JSON line: for wrapping in a profiler")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.mask = None
+    if args.window:
+        left, right = (int(v) for v in args.window.split(","))
+        args.mask = (left, right)
 
     import torch
     from generative_recommender_attention_gb300 import workloads
@@ -210,7 +234,8 @@ def main():
     x = workloads.make_inputs(w, seed=0)
     lengths = x["lengths"]
     B, T, H, D = w.batch, sum(lengths), w.heads, w.head_dim
-    N = pairs(lengths, H, w.causal)
+    mask = w.causal if args.mask is None else args.mask
+    N = pairs(lengths, H, mask)
     flops_step = 14.0 * D * N
     bytes_step = 11.0 * T * H * D * 2  # fwd 4 T H D and bwd 7 T H D elements of 2 bytes
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
@@ -221,7 +246,11 @@ def main():
                        device=dev)
     ws_b = torch.empty(hstu.workspace_size(B, T, T, H, D, mq, mk, True), dtype=torch.uint8,
                        device=dev)
-    kw = dict(scaling_seqlen=w.scaling_seqlen, causal=w.causal, alpha=w.alpha)
+    kw = dict(scaling_seqlen=w.scaling_seqlen, alpha=w.alpha)
+    if args.mask is None:
+        kw["causal"] = w.causal
+    else:
+        kw["window_size"] = args.mask
     flush = None if args.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step(evs=None):
@@ -348,7 +377,7 @@ def main():
     # summary of this workload (a line "traffic <kernel> <bytes>"), if any
     traffic = None
     tfile = os.path.join(ROOT, "profiles", f"kernels_{w.name}_full.md")
-    if os.path.exists(tfile):
+    if os.path.exists(tfile) and args.mask is None:  # the summary covers the default mask
         for tline in open(tfile):
             parts = tline.split()
             if len(parts) == 3 and parts[0] == "traffic" and parts[1] == dom:
@@ -424,7 +453,7 @@ def main():
                              "writes dq,dk,dv) per step time, against %.1f GB/s measured HBM" % pk["hbm_gbs"],
         "value_l2_warm": world * flops_step / (ms_warm * 1e-3) / 1e12,
         "ms_per_step_l2_warm": ms_warm,
-        "config": dict(workload_config(w, lengths),
+        "config": dict(workload_config(w, lengths, args.mask),
                        l2="flushed between steps (256 MiB write)" if flush is not None else "not flushed",
                        launch=graph_note,
                        parallelism="replicas" if world > 1 else "single GPU",
@@ -450,11 +479,11 @@ def main():
     }
 
     if rank == 0:
-        f, s, n, threads = oracle_sample(x, w, args.cpu_budget)
+        f, s, n, threads = oracle_sample(x, w, args.cpu_budget, mask=args.mask)
         line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"first {n} of {B} sequences, all heads, fwd+bwd (fp64)"}
-        f1, s1, n1, _ = oracle_sample(x, w, min(2.0, args.cpu_budget), threads=1)
+        f1, s1, n1, _ = oracle_sample(x, w, min(2.0, args.cpu_budget), threads=1, mask=args.mask)
         line["cpu_baseline_one_core"] = {"value": f1 / s1 / 1e12, "unit": "TFLOP/s", "cores": 1,
                                          "sample": f"first {n1} sequences, all heads, fwd+bwd (fp64)"}
         print(json.dumps(line))

@@ -12,7 +12,9 @@ sequence and head, O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V, no softmax.
 ``hstu_attn_fwd`` / ``hstu_attn_bwd`` mirror the page's
 ``hstu_attention_forward`` / ``hstu_attention_backward`` ("High-level
 functions"): THD tensors, int32 cumulative lengths, ``scaling_seqlen=None``
-meaning ``max_seqlen_q``, ``window_size=(-1, 0)`` causal or ``(-1, -1)`` full.
+meaning ``max_seqlen_q``, ``window_size=(left, right)`` the token-window mask
+(-1: no bound on that side; ``(-1, 0)`` causal, ``(-1, -1)`` full); without
+``window_size`` the ``causal`` flag picks one of those two.
 """
 from __future__ import annotations
 
@@ -53,15 +55,15 @@ def _ten(t):
     return Ten(t.data_ptr(), t.stride(0), t.stride(1))
 
 
-def _causal(causal, window_size):
+def _window(causal, window_size):
+    """(left, right) of the mask: ``window_size`` when given, else causal
+    (-1, 0) or full (-1, -1)."""
     if window_size is None:
-        return bool(causal)
+        return (-1, 0) if bool(causal) else (-1, -1)
     w = tuple(int(x) for x in window_size)
-    if w == (-1, 0):
-        return True
-    if w == (-1, -1):
-        return False
-    raise NotImplementedError(f"window_size {w}: only (-1, 0) causal and (-1, -1) full are built")
+    if len(w) != 2 or w[0] < -1 or w[1] < -1:
+        raise ValueError(f"window_size {window_size}: two bounds, each -1 (none) or >= 0")
+    return w
 
 
 def _scaling(scaling_seqlen):
@@ -132,12 +134,12 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     _check_thd("out", out, T_q, H, D, q.dtype, dev)
-    causal = _causal(causal, window_size)
+    win = _window(causal, window_size)
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
                                               False), dev)
     args = (_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
             cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q), int(max_seqlen_q),
-            int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen), int(causal),
+            int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen), win[0], win[1],
             ws.data_ptr(), ws.numel(), _stream(dev))
     if events is None:
         st = lib.hstu_attn_fwd(*args)
@@ -180,13 +182,13 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     _check_thd("dq", dq, T_q, H, D, q.dtype, dev)
     _check_thd("dk", dk, T_k, H, D, q.dtype, dev)
     _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
-    causal = _causal(causal, window_size)
+    win = _window(causal, window_size)
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
                                               True), dev)
     args = (_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk), _ten(dv),
             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
             int(max_seqlen_q), int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen),
-            int(causal), ws.data_ptr(), ws.numel(), _stream(dev))
+            win[0], win[1], ws.data_ptr(), ws.numel(), _stream(dev))
     if events is None:
         st = lib.hstu_attn_bwd(*args)
     else:

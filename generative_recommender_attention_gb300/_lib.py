@@ -57,7 +57,8 @@ def library_path() -> str:
 def _declare(lib):
     i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     P, S = ctypes.c_void_p, ctypes.c_size_t
-    scal = [P, P, i32, i64, i64, i32, i32, ctypes.c_int, i32, i32, f32, i32, i32, P, S, P]
+    # ..., scaling_seqlen, window_left, window_right, workspace, bytes, stream
+    scal = [P, P, i32, i64, i64, i32, i32, ctypes.c_int, i32, i32, f32, i32, i32, i32, P, S, P]
     lib.hstu_attn_fwd.argtypes = [CTen, CTen, CTen, Ten] + scal
     lib.hstu_attn_fwd.restype = ctypes.c_int
     lib.hstu_attn_bwd.argtypes = [CTen, CTen, CTen, CTen, Ten, Ten, Ten] + scal
@@ -74,7 +75,7 @@ def _declare(lib):
     lib.hstu_attn_last_device_status.restype = ctypes.c_int
     lib.hstu_attn_selftest_timeout.argtypes = [P, ctypes.c_uint32, P]
     lib.hstu_attn_selftest_timeout.restype = ctypes.c_int
-    lib.hstu_attn_fwd_noalloc.argtypes = [CTen, CTen, CTen, Ten] + scal[:13] + [P]
+    lib.hstu_attn_fwd_noalloc.argtypes = [CTen, CTen, CTen, Ten] + scal[:14] + [P]
     lib.hstu_attn_fwd_noalloc.restype = ctypes.c_int
     lib.hstu_attn_version.argtypes = []
     lib.hstu_attn_version.restype = i32

@@ -129,11 +129,13 @@ struct Common {
   DevInfo dev;
   float inv_L;
   bool bf16;
+  Window win;
 };
 
 hstu_status_t check_common(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_t D,
                            hstu_dtype_t dtype, int32_t max_q, int32_t max_k, float alpha,
-                           int32_t scaling, const int32_t* cu_q, const int32_t* cu_k, Common* c) {
+                           int32_t scaling, int32_t wl, int32_t wr, const int32_t* cu_q,
+                           const int32_t* cu_k, Common* c) {
   if (batch < 0 || total_q < 0 || total_k < 0 || H <= 0 || max_q < 0 || max_k < 0)
     return HSTU_ERR_INVALID_ARG;
   if (total_q > INT32_MAX || total_k > INT32_MAX) return HSTU_ERR_INVALID_ARG;
@@ -142,11 +144,13 @@ hstu_status_t check_common(int32_t batch, int64_t total_q, int64_t total_k, int3
   if (max_q > max_k) return HSTU_ERR_INVALID_ARG;
   if (!std::isfinite(alpha)) return HSTU_ERR_INVALID_ARG;
   if (scaling < 0) return HSTU_ERR_INVALID_ARG;
+  if (wl < -1 || wr < -1) return HSTU_ERR_INVALID_ARG;  // -1: no bound on that side
   const int32_t L = scaling > 0 ? scaling : max_q;
   if (batch > 0 && total_q > 0 && L <= 0) return HSTU_ERR_INVALID_ARG;
   if (batch > 0 && (cu_q == nullptr || cu_k == nullptr)) return HSTU_ERR_INVALID_ARG;
   c->inv_L = L > 0 ? 1.0f / static_cast<float>(L) : 0.f;
   c->bf16 = dtype == HSTU_BF16;
+  c->win = Window{wl, wr};
   return HSTU_OK;
 }
 
@@ -253,11 +257,13 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
                        int64_t total_q, int64_t total_k, int32_t num_heads, int32_t head_dim,
                        hstu_dtype_t dtype, int32_t max_seqlen_q, int32_t max_seqlen_k,
-                       float alpha, int32_t scaling_seqlen, int32_t causal, void* workspace,
+                       float alpha, int32_t scaling_seqlen, int32_t window_left,
+                       int32_t window_right, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
-                                 max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
+                                 max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
+                                 cu_seqlens_q, cu_seqlens_k, &c);
   if (s != HSTU_OK) return s;
   const int H = num_heads, D = head_dim;
   if ((s = check_tensor(q.ptr, q.stride_t, q.stride_h, total_q, H, D)) != HSTU_OK) return s;
@@ -291,7 +297,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   int* header = static_cast<int*>(workspace);
   int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
   SchedArgs sa{};
-  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
+  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
   sa.header = header; sa.cache_seqs = sched_cache;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
@@ -300,7 +306,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
-  a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.H = H; a.win = c.win; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
@@ -316,11 +322,13 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
                        const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q,
                        int64_t total_k, int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                        int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                       int32_t scaling_seqlen, int32_t causal, void* workspace,
+                       int32_t scaling_seqlen, int32_t window_left, int32_t window_right,
+                       void* workspace,
                        size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
-                                 max_seqlen_k, alpha, scaling_seqlen, cu_seqlens_q, cu_seqlens_k, &c);
+                                 max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
+                                 cu_seqlens_q, cu_seqlens_k, &c);
   if (s != HSTU_OK) return s;
   const int H = num_heads, D = head_dim;
   if ((s = check_tensor(dout.ptr, dout.stride_t, dout.stride_h, total_q, H, D)) != HSTU_OK) return s;
@@ -368,7 +376,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   int4* unitsB = reinterpret_cast<int4*>(ws + lay.units_b);
   int* ds_base = reinterpret_cast<int*>(ws + lay.ds_base);
   SchedArgs sa{};
-  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.causal = causal ? 1 : 0;
+  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
@@ -379,7 +387,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
-  a.H = H; a.causal = causal ? 1 : 0; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.H = H; a.win = c.win; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
   // dK/dV first: it also stores the dS blocks that the dQ kernel reads
@@ -419,10 +427,12 @@ hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_te
                             int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
                             int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
                             int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
-                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            int32_t window_left, int32_t window_right, void* workspace,
+                            size_t workspace_bytes,
                             cudaStream_t stream) {
   return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
-                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, window_left,
+                  window_right,
                   workspace, workspace_bytes, stream, EventMarks{nullptr, 0});
 }
 
@@ -431,12 +441,15 @@ hstu_status_t hstu_attn_fwd_profiled(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v
                                      int32_t batch, int64_t total_q, int64_t total_k,
                                      int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     int32_t scaling_seqlen, int32_t window_left,
+                                     int32_t window_right,
+                       void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream,
                                      cudaEvent_t* events, int32_t n_events) {
   if (events == nullptr || n_events < 0) return HSTU_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
-                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, window_left,
+                  window_right,
                   workspace, workspace_bytes, stream, EventMarks{events, n_events});
 }
 
@@ -446,11 +459,13 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
                             int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
                             int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
                             int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
-                            int32_t causal, void* workspace, size_t workspace_bytes,
+                            int32_t window_left, int32_t window_right, void* workspace,
+                            size_t workspace_bytes,
                             cudaStream_t stream) {
   return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                   num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
-                  causal, workspace, workspace_bytes, stream, EventMarks{nullptr, 0});
+                  window_left, window_right, workspace, workspace_bytes, stream,
+                  EventMarks{nullptr, 0});
 }
 
 hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k,
@@ -459,13 +474,16 @@ hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_
                                      int32_t batch, int64_t total_q, int64_t total_k,
                                      int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     int32_t scaling_seqlen, int32_t window_left,
+                                     int32_t window_right,
+                       void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream,
                                      cudaEvent_t* events, int32_t n_events) {
   if (events == nullptr || n_events < 0) return HSTU_ERR_INVALID_ARG;
   return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
                   num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
-                  causal, workspace, workspace_bytes, stream, EventMarks{events, n_events});
+                  window_left, window_right, workspace, workspace_bytes, stream,
+                  EventMarks{events, n_events});
 }
 
 hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t stream) {
@@ -527,7 +545,8 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(
     hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out, const int32_t* cu_seqlens_q,
     const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q, int64_t total_k,
     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
-    int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen, int32_t causal,
+    int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen, int32_t window_left,
+    int32_t window_right,
     cudaStream_t stream) {
   const size_t need = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim,
                                                max_seqlen_q, max_seqlen_k, 0);
@@ -538,6 +557,7 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(
   // The scheduler kernel rewrites the header and the whole work list at the
   // start of every call, so nothing in the array has to be cleared first.
   return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
-                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, causal,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, window_left,
+                  window_right,
                   scratch, kNoAllocScratchBytes, stream, EventMarks{nullptr, 0});
 }

@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (U.n > 0 && U.hz % SPLIT == 0) {
           // first stored dS block of this key tile (D half 0 stores them);
           // -1 when the metadata outgrew the workspace
-          const int n_qb = (U.Lq + BQ - 1) / BQ;
           const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
-          const int blk = b0 + (U.hz / SPLIT) * ((b1 - b0) / a.H) + ds_block_off(U.tile, n_qb, a.causal);
+          const int blk = b0 + (U.hz / SPLIT) * ((b1 - b0) / a.H) +
+                          ds_block_off(U.tile, U.Lq, U.Lk, a.win);
           U.ds = (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap) ? blk : -1;
         }
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int h = U.hz / SPLIT;
         const int k_row0 = U.k0 + kBM * U.tile;
         const int q_seq0 = U.q0;
-        const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
+        int m0, nqt;  // the unit's query tiles: m0 .. m0 + U.n - 1
+        key_tile_queries(U.tile, U.Lq, U.Lk, a.win, BQ, m0, nqt);
         const int kb = kvi % NKV;
         if constexpr (STAGE) {
           // buffer kb last held the unit before the previous one
@@ -255,7 +256,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                 tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
               }
             }
-            const int nm0 = a.causal ? (kBM * nx.tile) / BQ : 0;
+            int nm0, nqt;
+            key_tile_queries(nx.tile, nx.Lq, nx.Lk, a.win, BQ, nm0, nqt);
             prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
           }
           const int s = qi % NS;
@@ -439,8 +441,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (out_rows(U, dvrow, dkrow)) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
         continue;
       }
-      const int m0 = a.causal ? (kBM * U.tile) / BQ : 0;
-      const int lo = a.causal ? j : 0;  // valid queries: lo <= i < Lq
+      int m0, nqt;  // the unit's query tiles: m0 .. m0 + U.n - 1
+      key_tile_queries(U.tile, Lq, Lk, a.win, BQ, m0, nqt);
+      // valid queries of this key row: lo <= i < hi; every key row of the
+      // warp is seen by queries [lo_all, hi_all)
+      const int lo = a.win.right < 0 ? 0 : j - a.win.right;
+      const int hi = a.win.left < 0 ? Lq : min(Lq, j + a.win.left + 1);
+      const int lo_all = a.win.right < 0 ? 0 : j_warp_last - a.win.right;
+      const int hi_all = a.win.left < 0 ? Lq : min(Lq, j_warp_last - 31 + a.win.left + 1);
       // dS blocks of this key tile: one per half-step, stored by the D half 0
       // unit; this lane writes keys (r & ~1, r | 1) of query rows q, q + 2,
       // ..., q = cg * CW + (r & 1), at q * 256 + (r & ~1) * 2
@@ -452,12 +460,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
         const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
-        const bool need_mask = (ic + CW > Lq) || (a.causal && j_warp_last > ic);
+        const bool need_mask = ic < lo_all || ic + CW > hi_all;
         // valid queries of this warp's columns (bit e: query ic + e), the run
-        // of bits [lo - ic, Lq - ic) clamped to [0, CW)
+        // of bits [lo - ic, hi - ic) clamped to [0, CW)
         uint32_t valid = CW == 32 ? 0xffffffffu : (1u << CW) - 1u;
         if (need_mask) {
-          const int e0 = min(max(lo - ic, 0), CW), e1 = min(max(Lq - ic, 0), CW);
+          const int e0 = min(max(lo - ic, 0), CW), e1 = min(max(hi - ic, 0), CW);
           const uint32_t below_e1 = e1 >= 32 ? 0xffffffffu : (1u << e1) - 1u;
           const uint32_t below_e0 = e0 >= 32 ? 0xffffffffu : (1u << e0) - 1u;
           valid = below_e1 & ~below_e0;

@@ -104,18 +104,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int head_blk = b0 + h * ((b1 - b0) / a.H);  // this head's first block
         const bool second = 2 * i + 1 < n_qb;            // the tile's upper 64 queries exist
         const uint32_t bytes = (second ? 2 : 1) * kDsBlockBytes + C::K_BYTES;
-        for (int j = 0; j < U.n; ++j, ++g) {
-          const int s = g % NS;
+        int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
+        query_tile_keys(i, U.Lq, U.Lk, a.win, kDsKeys, kt0, nkt);
+        int off = ds_block_off(kt0, U.Lq, U.Lk, a.win);  // blocks of the key tiles before
+        for (int jj = 0; jj < U.n; ++jj, ++g) {
+          const int s = g % NS, j = kt0 + jj;
           if (!wait_bar(bar(EMPTY + s), ((g / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
-          const int blk = head_blk + ds_block_off(j, n_qb, a.causal) + 2 * i - ds_m0(j, a.causal);
+          // query blocks 2i and 2i + 1 of key tile j; a block the window leaves
+          // empty was never stored and is read as zeros from an out-of-range
+          // block index (the TMA fill; the box still counts in full)
+          int m0, cnt;
+          ds_blocks_of(j, U.Lq, U.Lk, a.win, m0, cnt);
+          const int blk0 = (2 * i >= m0 && 2 * i < m0 + cnt) ? head_blk + off + 2 * i - m0 : -1;
+          const int blk1 =
+              (2 * i + 1 >= m0 && 2 * i + 1 < m0 + cnt) ? head_blk + off + 2 * i + 1 - m0 : -1;
+          off += cnt;
           mbar_arrive_expect_tx(bar(FULL + s), bytes);
           // A tile: 64-key chunk c of query rows 0-63 (block 2i) and 64-127 (2i + 1)
 #pragma unroll
           for (int c = 0; c < kDsKeys / 64; ++c) {
-            tma_load_3d(stage_a(s) + c * (kBM * 128), &tm_ds, bar(FULL + s), 64 * c, 0, blk);
+            tma_load_3d(stage_a(s) + c * (kBM * 128), &tm_ds, bar(FULL + s), 64 * c, 0, blk0);
             if (second)
               tma_load_3d(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, &tm_ds, bar(FULL + s),
-                          64 * c, 0, blk + 1);
+                          64 * c, 0, blk1);
           }
 #pragma unroll
           for (int c = 0; c < KCH; ++c)

@@ -22,9 +22,9 @@
 //               predicated row stores; O is released as soon as it is read,
 //               so the SiLU warps never stop at a unit boundary.
 // No softmax, so no running max or rescale: O simply accumulates in TMEM.
-// Causal units only visit key tiles up to their last row (the scheduler's
-// cost); masked entries are set to exactly 0, never -inf, since SiLU(-inf)
-// is NaN.  Rows of a tile past the sequence end are computed but not stored;
+// A unit only visits the key tiles its rows can see under the mask window
+// (causal: up to the last row; a left bound starts later); masked entries
+// are set to exactly 0, never -inf, since SiLU(-inf) is NaN.  Rows of a tile past the sequence end are computed but not stored;
 // keys past it are masked, and past the tensor end TMA fills zeros.
 //
 // K_g and S_g share ring slot g % 3: S_g completing frees K_g, so the producer
@@ -150,7 +150,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (U.n <= 0) continue;
         const int h = U.hz;
         const int q_row0 = U.q0 + kBM * U.tile;
-        const int kv_row0 = U.k0;
+        int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
+        query_tile_keys(U.tile, U.Lq, U.Lk, a.win, BN, kt0, nkt);
+        const int kv_row0 = U.k0 + BN * kt0;
         const int qb = qi % NQ;
         if (!wait_bar(bar(QEMPTY + qb), ((qi / NQ) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(QFULL + qb), C::Q_BYTES);
@@ -272,7 +274,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int Lk = U.Lk;
       const int i = kBM * U.tile + r;
       const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
-      const int lim = a.causal ? min(Lk, i + 1) : Lk;  // valid keys: j < lim
+      int kt0, nkt;
+      query_tile_keys(U.tile, U.Lq, Lk, a.win, BN, kt0, nkt);
+      // valid keys of this row: lo <= j < hi; every row of the warp sees
+      // [lo_all, hi_all)
+      const int lo = a.win.left < 0 ? 0 : i - a.win.left;
+      const int hi = a.win.right < 0 ? Lk : min(Lk, i + a.win.right + 1);
+      const int lo_all = a.win.left < 0 ? 0 : i_warp + 31 - a.win.left;
+      const int hi_all = a.win.right < 0 ? Lk : min(Lk, i_warp + a.win.right + 1);
       for (int n = 0; n < U.n; ++n, ++g) {
         if (static_cast<int>(g & 1) != par) continue;
         const int sb = g % NSB;
@@ -280,8 +289,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          const int jc = BN * n + 64 * c;  // first key of this chunk
-          const bool need_mask = (a.causal && jc + 63 > i_warp) || (jc + 64 > Lk);
+          const int jc = BN * (kt0 + n) + 64 * c;  // first key of this chunk
+          const bool need_mask = jc < lo_all || jc + 64 > hi_all;
           uint32_t x[64];
           tmem_ld64(tS + sb * BN + 64 * c, x);
           uint32_t p[32];
@@ -292,8 +301,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int j = jc + 2 * e;
-              const uint32_t s0 = j < lim ? x[2 * e] : 0u;          // SiLU(0) = 0
-              const uint32_t s1 = j + 1 < lim ? x[2 * e + 1] : 0u;
+              const uint32_t s0 = (j >= lo && j < hi) ? x[2 * e] : 0u;  // SiLU(0) = 0
+              const uint32_t s1 = (j + 1 >= lo && j + 1 < hi) ? x[2 * e + 1] : 0u;
               p[e] = silu_pair<BF16>(s0, s1, half_alpha);
             }
           }

@@ -44,10 +44,48 @@ constexpr int kAlignSlack = 1024;
 constexpr int kPrefetch = 4;
 constexpr int kPrefetchQ = 8;
 
+// ---------------------------------------------------------------- mask window
+// Token window ("HSTU Attention (Blackwell SM100/SM103)", section "Mask
+// support", window_size = (left, right)), -1 meaning no bound on that side:
+// key j is valid for query i (both local to the sequence) iff j < Lk,
+// j >= i - left when left >= 0, and j <= i + right when right >= 0.
+// (-1, 0) is causal, (-1, -1) full.
+struct Window {
+  int left, right;
+};
+__host__ __device__ constexpr int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int imax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr bool win_causal(Window w) { return w.left < 0 && w.right == 0; }
+__host__ __device__ constexpr bool win_full(Window w) { return w.left < 0 && w.right < 0; }
+
+// Keys a 128-row query tile t needs: inner key tiles of bn keys, the first
+// one `first` and `count` of them (0: the tile sees no key; its rows are
+// zeros).  Rows past Lq are not counted.
+__host__ __device__ inline void query_tile_keys(int t, int Lq, int Lk, Window w, int bn,
+                                                int& first, int& count) {
+  const int r0 = kBM * t, r1 = imin(kBM * t + kBM, Lq);           // rows [r0, r1)
+  const int j0 = w.left < 0 ? 0 : imax(0, r0 - w.left);           // keys [j0, j1)
+  const int j1 = w.right < 0 ? Lk : imin(Lk, r1 + w.right);
+  first = j0 / bn;
+  count = (r1 > r0 && j1 > j0) ? (j1 + bn - 1) / bn - first : 0;
+}
+
+// Queries a 128-key tile s is seen by: query blocks of bq rows, the first
+// one `first` and `count` of them.  Keys past Lk are not counted.
+__host__ __device__ inline void key_tile_queries(int s, int Lq, int Lk, Window w, int bq,
+                                                 int& first, int& count) {
+  const int c0 = kBM * s, c1 = imin(kBM * s + kBM, Lk);           // keys [c0, c1)
+  const int i0 = w.right < 0 ? 0 : imax(0, c0 - w.right);         // queries [i0, i1)
+  const int i1 = w.left < 0 ? Lq : imin(Lq, c1 + w.left);
+  first = i0 / bq;
+  count = (c1 > c0 && i1 > i0) ? (i1 + bq - 1) / bq - first : 0;
+}
+
 struct SchedArgs {
   const int32_t* cu_q;
   const int32_t* cu_k;
-  int B, H, causal;
+  int B, H;
+  Window win;
   int bn_a, cmax_a, cap_a;   // list A: query tiles, inner tiles of bn_a keys
   int4* units_a;
   int bq_b, split_b, cmax_b, cap_b;  // list B: key tiles, inner tiles of bq_b queries
@@ -61,29 +99,44 @@ struct SchedArgs {
 // ---------------------------------------------------------------- dS blocks
 // The backward stores dS (times 2, in the input dtype) as blocks of 64
 // queries x 128 keys, query-major ([query][key], 256 bytes per query row),
-// one block per (sequence, head, key tile j, 64-query block m) that the mask
-// leaves non-empty.  Sequence b owns blocks [ds_base[b], ds_base[b+1]): H runs of
-// ds_blocks_head(...) blocks, head-major; inside a head, key tile j's blocks
-// start at ds_block_off(j, ...) and hold m = ds_m0(j) .. n_qb - 1 in order.
+// one block per (sequence, head, key tile j, 64-query block m) with m among
+// the query blocks that can see key tile j (key_tile_queries).  Sequence b
+// owns blocks [ds_base[b], ds_base[b+1]): H runs of ds_blocks_head(...)
+// blocks, head-major; inside a head, key tile j's blocks start at
+// ds_block_off(j, ...) and hold its query blocks in order.
 constexpr int kDsKeys = 128, kDsQueries = 64;
 constexpr int kDsBlockBytes = kDsKeys * kDsQueries * 2;
 
-__host__ __device__ __forceinline__ int ds_m0(int j, int causal) { return causal ? 2 * j : 0; }
-// Blocks of key tiles 0 .. j-1 of one head (n_qb query blocks).
-__host__ __device__ __forceinline__ int ds_block_off(int j, int n_qb, int causal) {
-  if (!causal) return j * n_qb;
-  const int jj = j < (n_qb + 1) / 2 ? j : (n_qb + 1) / 2;  // later key tiles hold none
-  return jj * n_qb - jj * (jj - 1);
+// Stored blocks of key tile j: first query block and count.
+__host__ __device__ inline void ds_blocks_of(int j, int Lq, int Lk, Window w, int& m0, int& n) {
+  key_tile_queries(j, Lq, Lk, w, kDsQueries, m0, n);
 }
-// Blocks of one head of a sequence with n_kt key tiles and n_qb query blocks.
-__host__ __device__ __forceinline__ int ds_blocks_head(int n_kt, int n_qb, int causal) {
-  return ds_block_off(n_kt, n_qb, causal);
+// Blocks of key tiles 0 .. j-1 of one head (j at most the sequence's key
+// tiles).  Causal and full have closed forms; other windows sum the tiles.
+__host__ __device__ inline int ds_block_off(int j, int Lq, int Lk, Window w) {
+  const int n_qb = (Lq + kDsQueries - 1) / kDsQueries;
+  if (win_full(w)) return j * n_qb;
+  if (win_causal(w)) {  // key tile j holds n_qb - 2 j blocks while positive
+    const int jj = j < (n_qb + 1) / 2 ? j : (n_qb + 1) / 2;
+    return jj * n_qb - jj * (jj - 1);
+  }
+  int off = 0;
+  for (int t = 0; t < j; ++t) {
+    int m0, n;
+    ds_blocks_of(t, Lq, Lk, w, m0, n);
+    off += n;
+  }
+  return off;
+}
+// Blocks of one head of a sequence.
+__host__ __device__ inline int ds_blocks_head(int Lq, int Lk, Window w) {
+  return ds_block_off((Lk + kDsKeys - 1) / kDsKeys, Lq, Lk, w);
 }
 
 struct AttnArgs {
   int64_t total_q, total_k;
   int H;
-  int causal;
+  Window win;
   float alpha;
   float inv_L;          // 1 / L_scale
   int* header;          // workspace header

@@ -3,8 +3,9 @@
 // first, so a persistent kernel that walks the list in order balances ragged
 // sequences.  One block per list:
 //   list A: query tiles of 128 rows; cost = number of key tiles of `bn_a`
-//           rows the tile needs (causal tiles only need keys up to their
-//           last row);
+//           rows the tile needs (the mask window bounds its keys: causal
+//           tiles only need keys up to their last row, a left bound cuts
+//           keys before the first row);
 //   list B: key tiles of 128 rows; cost = number of query tiles of `bq_b`
 //           rows that can see the tile; each key tile is emitted once per head
 //           and per D split.
@@ -31,18 +32,16 @@ __device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
 
 // Cost of query tile t (list A).
 __device__ __forceinline__ int cost_a(const SchedArgs& a, int t, int Lq, int Lk) {
-  if (a.causal) {
-    int nk = min(min(kBM * (t + 1), Lq), Lk);
-    return ceil_div(nk, a.bn_a);
-  }
-  return ceil_div(Lk, a.bn_a);
+  int first, n;
+  query_tile_keys(t, Lq, Lk, a.win, a.bn_a, first, n);
+  return n;
 }
 
 // Cost of key tile s (list B).
-__device__ __forceinline__ int cost_b(const SchedArgs& a, int s, int Lq) {
-  int nq = ceil_div(Lq, a.bq_b);
-  int m0 = a.causal ? (kBM * s) / a.bq_b : 0;
-  return max(0, nq - m0);
+__device__ __forceinline__ int cost_b(const SchedArgs& a, int s, int Lq, int Lk) {
+  int first, n;
+  key_tile_queries(s, Lq, Lk, a.win, a.bq_b, first, n);
+  return n;
 }
 
 __device__ __forceinline__ int list_cmax(const SchedArgs& a, bool list_b) {
@@ -127,7 +126,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int Lq = sq.y, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
+      const int cost = list_b ? cost_b(a, t, Lq, Lk) : cost_a(a, t, Lq, Lk);
       atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
@@ -157,7 +156,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, t, Lq) : cost_a(a, t, Lq, Lk);
+      const int cost = list_b ? cost_b(a, t, Lq, Lk) : cost_a(a, t, Lq, Lk);
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       for (int e = 0; e < per_tile; ++e) {
         if (pos + e < cap) {
@@ -176,7 +175,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   if (list_b && a.ds_base != nullptr) {
     auto blocks = [&](int b) {
       const int4 sq = seq(b);
-      return a.H * ds_blocks_head(ceil_div(sq.w, kDsKeys), ceil_div(sq.y, kDsQueries), a.causal);
+      return a.H * ds_blocks_head(sq.y, sq.w, a.win);
     };
     const int per = (a.B + blockDim.x - 1) / blockDim.x;
     const int s0 = min(a.B, tid * per), s1 = min(a.B, s0 + per);

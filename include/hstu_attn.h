@@ -17,10 +17,13 @@
  * (B + 1,) cumulative lengths starting at 0 that delimit each sequence.
  * Q, K and V have the same number of heads (MHA only: no GQA/MQA).
  *
- * Mask (same page, section "Mask support"): causal = window (-1, 0), the
- * top-left aligned diagonal with the diagonal kept (key j valid iff j <= i,
- * indices local to the sequence); full = window (-1, -1).  Keys outside the
- * sequence never count.  A query row with no valid key gets a zero output and
+ * Mask (same page, section "Mask support"): the token window
+ * window_size = (window_left, window_right), -1 meaning no bound on that
+ * side.  Key j is valid for query i (indices local to the sequence) iff
+ * j >= i - window_left (when window_left >= 0) and j <= i + window_right
+ * (when window_right >= 0), aligned top-left on the diagonal j = i, which is
+ * kept.  Causal = window (-1, 0); full = window (-1, -1); finite bounds give
+ * the local / sliding window.  Keys outside the sequence never count.  A query row with no valid key gets a zero output and
  * a zero dQ; a key that no query sees gets zero dK and dV (same page, section
  * "Mask support": keyless rows are written as zeros, no output memset needed).
  *
@@ -56,8 +59,8 @@ extern "C" {
 typedef enum {
   HSTU_OK = 0,
   HSTU_ERR_INVALID_ARG = 1,    /* bad sizes, null pointers, max_seqlen_q > max_seqlen_k,
-                                  scaling_seqlen < 0, non-finite alpha, overlapping strides,
-                                  workspace too small */
+                                  scaling_seqlen < 0, non-finite alpha, a window bound
+                                  below -1, overlapping strides, workspace too small */
   HSTU_ERR_UNSUPPORTED = 2,    /* head_dim or dtype outside the built set, device not sm_103 */
   HSTU_ERR_MISALIGNED = 3,     /* base pointer or stride not a multiple of 16 bytes */
   HSTU_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
@@ -106,7 +109,8 @@ size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
  *   max_seqlen_q <= max_seqlen_k, each >= the longest sequence on its side.
  *   alpha: score scale, finite.  scaling_seqlen: L_scale; 0 selects
  *     max_seqlen_q, negative is an error (the page requires it positive).
- *   causal: 1 = window (-1, 0), 0 = window (-1, -1).
+ *   window_left, window_right: the mask window, each -1 (no bound) or >= 0;
+ *     (-1, 0) causal, (-1, -1) full; a bound below -1 is an error.
  *   head_dim in {64, 128, 256}; dtype FP16 or BF16.
  * B == 0 or total_q == 0 is a no-op returning HSTU_OK.
  */
@@ -115,8 +119,9 @@ hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_te
                             int32_t batch, int64_t total_q, int64_t total_k,
                             int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                             int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                            int32_t scaling_seqlen, int32_t causal, void* workspace,
-                            size_t workspace_bytes, cudaStream_t stream);
+                            int32_t scaling_seqlen, int32_t window_left,
+                            int32_t window_right, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /*
  * Backward: (dq, dk, dv) from dout (page "HSTU Attention (Blackwell
@@ -136,8 +141,9 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
                             int32_t batch, int64_t total_q, int64_t total_k,
                             int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                             int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                            int32_t scaling_seqlen, int32_t causal, void* workspace,
-                            size_t workspace_bytes, cudaStream_t stream);
+                            int32_t scaling_seqlen, int32_t window_left,
+                            int32_t window_right, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /*
  * Profiling variants: identical to hstu_attn_fwd / hstu_attn_bwd (same
@@ -155,7 +161,8 @@ hstu_status_t hstu_attn_fwd_profiled(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v
                                      int32_t batch, int64_t total_q, int64_t total_k,
                                      int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     int32_t scaling_seqlen, int32_t window_left,
+                                     int32_t window_right, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream,
                                      cudaEvent_t* events, int32_t n_events);
 hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k,
@@ -164,7 +171,8 @@ hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_
                                      int32_t batch, int64_t total_q, int64_t total_k,
                                      int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                                      int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                                     int32_t scaling_seqlen, int32_t causal, void* workspace,
+                                     int32_t scaling_seqlen, int32_t window_left,
+                                     int32_t window_right, void* workspace,
                                      size_t workspace_bytes, cudaStream_t stream,
                                      cudaEvent_t* events, int32_t n_events);
 
@@ -193,7 +201,8 @@ hstu_status_t hstu_attn_fwd_noalloc(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
                                     int32_t batch, int64_t total_q, int64_t total_k,
                                     int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
                                     int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
-                                    int32_t scaling_seqlen, int32_t causal, cudaStream_t stream);
+                                    int32_t scaling_seqlen, int32_t window_left,
+                                    int32_t window_right, cudaStream_t stream);
 
 /* Static text for a status code. */
 const char* hstu_attn_status_string(hstu_status_t status);

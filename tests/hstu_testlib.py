@@ -25,13 +25,20 @@ def to_dev(x, device="cuda"):
     return out
 
 
+def mask_kwargs(causal):
+    """Binding keywords of a mask given as a bool or a (left, right) window."""
+    if isinstance(causal, tuple):
+        return {"window_size": causal}
+    return {"causal": bool(causal)}
+
+
 def gpu_fwd_bwd(xd, scaling, causal, alpha, **kw):
     o = hstu.hstu_attn_fwd(xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"], xd["cu_seqlens_k"],
                            xd["max_seqlen_q"], xd["max_seqlen_k"], scaling_seqlen=scaling,
-                           causal=causal, alpha=alpha, **kw.get("fwd", {}))
+                           alpha=alpha, **mask_kwargs(causal), **kw.get("fwd", {}))
     dq, dk, dv = hstu.hstu_attn_bwd(xd["do"], xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"],
                                     xd["cu_seqlens_k"], xd["max_seqlen_q"], xd["max_seqlen_k"],
-                                    scaling_seqlen=scaling, causal=causal, alpha=alpha,
+                                    scaling_seqlen=scaling, alpha=alpha, **mask_kwargs(causal),
                                     **kw.get("bwd", {}))
     torch.cuda.synchronize()
     return o, dq, dk, dv

@@ -89,12 +89,12 @@ def _call_fwd(lib, **over):
     a = dict(q=(0x10000, 256, 64), k=(0x20000, 256, 64), v=(0x30000, 256, 64),
              out=(0x40000, 256, 64), cu_q=0x50000, cu_k=0x60000, batch=2, total_q=100,
              total_k=100, H=4, D=64, dtype=L.HSTU_BF16, max_q=60, max_k=60, alpha=0.125,
-             scaling=0, causal=1, ws=0x70000, ws_bytes=1 << 20, stream=None)
+             scaling=0, wl=-1, wr=0, ws=0x70000, ws_bytes=1 << 20, stream=None)
     a.update(over)
     return lib.hstu_attn_fwd(L.CTen(*a["q"]), L.CTen(*a["k"]), L.CTen(*a["v"]),
                              L.Ten(*a["out"]), a["cu_q"], a["cu_k"], a["batch"], a["total_q"],
                              a["total_k"], a["H"], a["D"], a["dtype"], a["max_q"], a["max_k"],
-                             a["alpha"], a["scaling"], a["causal"], a["ws"], a["ws_bytes"],
+                             a["alpha"], a["scaling"], a["wl"], a["wr"], a["ws"], a["ws_bytes"],
                              a["stream"])
 
 
@@ -108,6 +108,8 @@ def test_fwd_argument_errors(lib):
     assert _call_fwd(lib, alpha=float("inf")) == INVALID
     assert _call_fwd(lib, batch=-1) == INVALID
     assert _call_fwd(lib, H=0) == INVALID
+    assert _call_fwd(lib, wl=-2) == INVALID                      # window bounds are -1 or >= 0
+    assert _call_fwd(lib, wr=-5) == INVALID
     assert _call_fwd(lib, total_q=-5) == INVALID
     assert _call_fwd(lib, cu_q=None) == INVALID
     assert _call_fwd(lib, q=(0, 256, 64)) == INVALID              # null with rows
@@ -143,13 +145,13 @@ def _call_bwd(lib, **over):
     t = (0x10000, 256, 64)
     a = dict(do=t, q=t, k=t, v=t, dq=(0x80000, 256, 64), dk=(0x90000, 256, 64),
              dv=(0xA0000, 256, 64), batch=2, total_q=100, total_k=100, D=64, max_q=60,
-             max_k=60, scaling=0, ws_bytes=1 << 20)
+             max_k=60, scaling=0, wl=-1, wr=-1, ws_bytes=1 << 20)
     a.update(over)
     return lib.hstu_attn_bwd(L.CTen(*a["do"]), L.CTen(*a["q"]), L.CTen(*a["k"]), L.CTen(*a["v"]),
                              L.Ten(*a["dq"]), L.Ten(*a["dk"]), L.Ten(*a["dv"]), 0x50000, 0x60000,
                              a["batch"], a["total_q"], a["total_k"], 4, a["D"], L.HSTU_FP16,
-                             a["max_q"], a["max_k"], 0.5, a["scaling"], 0, 0x70000,
-                             a["ws_bytes"], None)
+                             a["max_q"], a["max_k"], 0.5, a["scaling"], a["wl"], a["wr"],
+                             0x70000, a["ws_bytes"], None)
 
 
 def test_bwd_argument_errors(lib):
@@ -159,7 +161,9 @@ def test_bwd_argument_errors(lib):
     assert _call_bwd(lib, dk=(0x90004, 256, 64)) == MISALIGNED
     assert _call_bwd(lib, dv=(0xA0000, 8, 64)) == INVALID
     assert _call_bwd(lib, ws_bytes=100) == INVALID
+    assert _call_bwd(lib, wl=-7) == INVALID
     assert _call_bwd(lib, batch=0) == OK
+    assert _call_bwd(lib, batch=0, wl=5, wr=3) == OK
 
 
 def test_selftest_argument_errors(lib):
@@ -177,60 +181,130 @@ def test_binding_rejects_bad_tensors_on_cpu():
     cu = torch.tensor([0, 8], dtype=torch.int32)
     with pytest.raises(TypeError):
         g.hstu_attn_fwd(q, q, q, cu, cu, 8, 8)
-    with pytest.raises(NotImplementedError):
-        g._causal(True, (4, 0))
+    with pytest.raises(ValueError):
+        g._window(True, (4, -3))
     with pytest.raises(ValueError):
         g._scaling(-2)
-    assert g._causal(False, (-1, 0)) is True and g._causal(True, (-1, -1)) is False
+    assert g._window(False, (-1, 0)) == (-1, 0) and g._window(True, (-1, -1)) == (-1, -1)
+    assert g._window(True, None) == (-1, 0) and g._window(False, None) == (-1, -1)
+    assert g._window(True, (16, 3)) == (16, 3)
+
+
+def _window_rules():
+    """The tile-range and dS-block rules of kernels.h (query_tile_keys,
+    key_tile_queries, ds_block_off), restated in Python."""
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+
+    def query_tile_keys(t, Lq, Lk, w, bn):
+        r0, r1 = 128 * t, min(128 * t + 128, Lq)
+        j0 = 0 if w[0] < 0 else max(0, r0 - w[0])
+        j1 = Lk if w[1] < 0 else min(Lk, r1 + w[1])
+        first = j0 // bn
+        return first, (cdiv(j1, bn) - first if r1 > r0 and j1 > j0 else 0)
+
+    def key_tile_queries(s, Lq, Lk, w, bq):
+        c0, c1 = 128 * s, min(128 * s + 128, Lk)
+        i0 = 0 if w[1] < 0 else max(0, c0 - w[1])
+        i1 = Lq if w[0] < 0 else min(Lq, c1 + w[0])
+        first = i0 // bq
+        return first, (cdiv(i1, bq) - first if c1 > c0 and i1 > i0 else 0)
+
+    def ds_block_off(j, Lq, Lk, w):
+        nqb = cdiv(Lq, 64)
+        if w == (-1, -1):
+            return j * nqb
+        if w == (-1, 0):
+            jj = min(j, (nqb + 1) // 2)
+            return jj * nqb - jj * (jj - 1)
+        return sum(key_tile_queries(t, Lq, Lk, w, 64)[1] for t in range(j))
+
+    return cdiv, query_tile_keys, key_tile_queries, ds_block_off
+
+
+def _valid(i, j, Lq, Lk, w):
+    return (i < Lq and j < Lk and (w[0] < 0 or j >= i - w[0])
+            and (w[1] < 0 or j <= i + w[1]))
+
+
+def test_tile_ranges_cover_exactly_the_valid_pairs():
+    """Brute force over the mask definition: the key tiles a query tile
+    visits, and the query blocks a key tile visits, are exactly those holding
+    at least one valid (query, key) pair, for random windows and ragged
+    lengths; the closed forms of ds_block_off equal the summed counts."""
+    import random
+    cdiv, qtk, ktq, off = _window_rules()
+    rng = random.Random(3)
+    for _ in range(300):
+        Lk = rng.randint(0, 700)
+        Lq = rng.randint(0, Lk)
+        w = rng.choice([(-1, 0), (-1, -1), (0, 0), (rng.randint(0, 300), rng.randint(-1, 200)),
+                        (rng.randint(-1, 300), rng.randint(0, 40)), (rng.randint(0, 90), -1)])
+        for bn in (64, 128):
+            for t in range(cdiv(Lq, 128)):
+                first, n = qtk(t, Lq, Lk, w, bn)
+                need = {j // bn for i in range(128 * t, min(128 * t + 128, Lq))
+                        for j in range(Lk) if _valid(i, j, Lq, Lk, w)}
+                assert set(range(first, first + n)) == need, (Lq, Lk, w, bn, t)
+        for s_ in range(cdiv(Lk, 128)):
+            first, n = ktq(s_, Lq, Lk, w, 64)
+            need = {i // 64 for j in range(128 * s_, min(128 * s_ + 128, Lk))
+                    for i in range(Lq) if _valid(i, j, Lq, Lk, w)}
+            assert set(range(first, first + n)) == need, (Lq, Lk, w, s_)
+        if w in ((-1, 0), (-1, -1)):
+            for j in range(cdiv(Lk, 128) + 1):
+                assert off(j, Lq, Lk, w) == sum(ktq(t, Lq, Lk, w, 64)[1] for t in range(j))
 
 
 def test_ds_block_layout_rule():
-    """The dS block layout of the backward workspace (kernels.h: ds_m0,
+    """The dS block layout of the backward workspace (kernels.h: ds_blocks_of,
     ds_block_off, ds_blocks_head; sched.cu: ds_base), restated and checked by
-    brute force on random ragged batches: every block the dK/dV kernel writes
-    has a unique index inside its sequence's range, the dQ kernel finds the
-    blocks it reads where they were written, and the host's size bound holds."""
+    brute force on random ragged batches and windows: every block the dK/dV
+    kernel writes has a unique index inside its sequence's range, the dQ
+    kernel finds each block it reads where it was written (and a block it
+    does not find holds no valid pair, so reading zeros there is exact), and
+    the host's size bound holds."""
     import random
-
-    cdiv = lambda a, b: -(-a // b)  # noqa: E731
-
-    def m0(j, causal):
-        return 2 * j if causal else 0
-
-    def off(j, nqb, causal):
-        if not causal:
-            return j * nqb
-        jj = min(j, (nqb + 1) // 2)
-        return jj * nqb - jj * (jj - 1)
-
+    cdiv, qtk, ktq, off = _window_rules()
     rng = random.Random(7)
-    for _ in range(400):
-        causal = rng.random() < 0.5
+    for _ in range(300):
+        w = rng.choice([(-1, 0), (-1, -1), (0, 0), (rng.randint(0, 300), rng.randint(-1, 200)),
+                        (rng.randint(-1, 300), rng.randint(0, 40))])
         B, H = rng.randint(1, 5), rng.randint(1, 3)
         Lk = [rng.randint(0, 600) for _ in range(B)]
         Lq = [rng.randint(0, l) if rng.random() < 0.3 else l for l in Lk]
         base = [0]
         for b in range(B):
-            base.append(base[-1] + H * off(cdiv(Lk[b], 128), cdiv(Lq[b], 64), causal))
+            base.append(base[-1] + H * off(cdiv(Lk[b], 128), Lq[b], Lk[b], w))
         written = {}
         for b in range(B):
-            nqb, head_blocks = cdiv(Lq[b], 64), (base[b + 1] - base[b]) // H
+            head_blocks = (base[b + 1] - base[b]) // H
             for h in range(H):
                 for j in range(cdiv(Lk[b], 128)):
-                    first = base[b] + h * head_blocks + off(j, nqb, causal)
-                    for m in range(max(0, nqb - m0(j, causal))):   # the key tile's half-steps
+                    first = base[b] + h * head_blocks + off(j, Lq[b], Lk[b], w)
+                    m0, n = ktq(j, Lq[b], Lk[b], w, 64)      # the key tile's half-steps
+                    for m in range(n):
                         k = first + m
                         assert base[b] <= k < base[b + 1] and k not in written
-                        written[k] = (b, h, j, m0(j, causal) + m)
+                        written[k] = (b, h, j, m0 + m)
         assert len(written) == base[-1]
         for b in range(B):
             nqb, head_blocks = cdiv(Lq[b], 64), (base[b + 1] - base[b]) // H
             for h in range(H):
                 for i in range(cdiv(Lq[b], 128)):
-                    n = cdiv(min(128 * (i + 1), Lq[b], Lk[b]), 128) if causal else cdiv(Lk[b], 128)
-                    for j in range(n):
-                        blk = base[b] + h * head_blocks + off(j, nqb, causal) + 2 * i - m0(j, causal)
-                        assert written[blk] == (b, h, j, 2 * i)
-                        if 2 * i + 1 < nqb:
-                            assert written[blk + 1] == (b, h, j, 2 * i + 1)
+                    kt0, n = qtk(i, Lq[b], Lk[b], w, 128)
+                    running = off(kt0, Lq[b], Lk[b], w)
+                    for j in range(kt0, kt0 + n):
+                        m0, cnt = ktq(j, Lq[b], Lk[b], w, 64)
+                        assert running == off(j, Lq[b], Lk[b], w)
+                        for m in (2 * i, 2 * i + 1):
+                            if m >= nqb:
+                                continue
+                            if m0 <= m < m0 + cnt:
+                                blk = base[b] + h * head_blocks + running + m - m0
+                                assert written[blk] == (b, h, j, m)
+                            else:   # never stored: must hold no valid pair
+                                assert not any(_valid(ii, jj, Lq[b], Lk[b], w)
+                                               for ii in range(64 * m, 64 * m + 64)
+                                               for jj in range(128 * j, 128 * j + 128))
+                        running += cnt
         assert base[-1] <= H * cdiv(max(Lq), 64) * (cdiv(sum(Lk), 128) + B)

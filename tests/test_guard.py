@@ -11,6 +11,8 @@ import torch
 from generative_recommender_attention_gb300 import workloads
 import generative_recommender_attention_gb300 as hstu
 
+from hstu_testlib import mask_kwargs
+
 pytestmark = pytest.mark.gpu
 
 SENT = -3072.0   # exactly representable in bf16 and fp16; no output reaches it
@@ -36,7 +38,8 @@ def _guarded(T, H, D, dtype, extra_rows=3, pad_h=8, pad_t=16, guard=64):
 
 
 @pytest.mark.parametrize("D,dtype,causal", [(64, torch.bfloat16, True), (128, torch.float16, False),
-                                            (256, torch.bfloat16, True)])
+                                            (256, torch.bfloat16, True),
+                                            (128, torch.bfloat16, (100, 20))])
 def test_no_write_outside_logical_outputs(D, dtype, causal):
     lens = [129, 1, 300, 0, 64]
     H = 2
@@ -48,10 +51,11 @@ def test_no_write_outside_logical_outputs(D, dtype, causal):
     pad = lambda t: torch.cat([t, torch.zeros(3, H, D, dtype=dtype, device="cuda")])  # noqa
     q, k, v, do = pad(dev["q"]), pad(dev["k"]), pad(dev["v"]), pad(dev["do"])
     bufs = [_guarded(T, H, D, dtype) for _ in range(4)]
+    mk = mask_kwargs(causal)
     o = hstu.hstu_attn_fwd(q, k, v, dev["cu_seqlens_q"], dev["cu_seqlens_k"], 300, 300,
-                           causal=causal, alpha=0.1, out=bufs[0][1])
+                           alpha=0.1, out=bufs[0][1], **mk)
     hstu.hstu_attn_bwd(do, q, k, v, dev["cu_seqlens_q"], dev["cu_seqlens_k"], 300, 300,
-                       causal=causal, alpha=0.1, dq=bufs[1][1], dk=bufs[2][1], dv=bufs[3][1])
+                       alpha=0.1, dq=bufs[1][1], dk=bufs[2][1], dv=bufs[3][1], **mk)
     torch.cuda.synchronize()
     for name, (buf, view, mask) in zip(("out", "dq", "dk", "dv"), bufs):
         outside = buf[~mask]

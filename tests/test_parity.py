@@ -56,6 +56,35 @@ def test_medium_every_variant(D, dtype, causal):
     full_compare(x, None, causal, alpha)
 
 
+# ------------------------------------------------------------------ windows
+# Local / sliding windows ("Mask support", window_size = (left, right)).
+WINDOWS = [(0, 0), (16, 0), (200, 40), (70, -1), (-1, 100), (129, 1), (1000, 0)]
+
+
+@pytest.mark.parametrize("D,dtype", [(64, torch.bfloat16), (128, torch.float16),
+                                     (256, torch.bfloat16)])
+@pytest.mark.parametrize("window", WINDOWS)
+def test_medium_windows(D, dtype, window):
+    x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, D, dtype, seed=D + window[0] + 7)
+    full_compare(x, None, window, 1.0 / math.sqrt(D))
+
+
+@pytest.mark.parametrize("window", [(256, 0), (64, 64)])
+def test_window_unequal_lengths(window):
+    lq = [100, 250, 7, 300, 513]
+    lk = [180, 250, 40, 200, 600]
+    x = workloads.random_inputs(lq, lk, 2, 128, torch.bfloat16, seed=13)
+    x["max_seqlen_k"] = max(max(lk), x["max_seqlen_q"])
+    full_compare(x, 96, window, 0.2)
+
+
+def test_window_recsys_sampled():
+    """The recsys workload's shapes with a 256-token look-back window."""
+    w = _ws("recsys")
+    x = workloads.make_inputs(w, seed=0)
+    sampled_compare(x, w.scaling_seqlen, (256, 0), w.alpha, n_random=96)
+
+
 # ------------------------------------------------------------------ edge cases
 @pytest.mark.parametrize("causal", [True, False])
 def test_unequal_q_and_k_lengths(causal):

@@ -36,7 +36,8 @@ def _noalloc(lib, x, out, causal, alpha, scaling):
     return lib.hstu_attn_fwd_noalloc(
         ten(x["q"]), ten(x["k"]), ten(x["v"]), L.Ten(out.data_ptr(), out.stride(0), out.stride(1)),
         x["cu_seqlens_q"].data_ptr(), x["cu_seqlens_k"].data_ptr(), B, T_q, x["k"].shape[0], H, D,
-        dt, x["max_seqlen_q"], x["max_seqlen_k"], float(alpha), int(scaling), int(causal),
+        dt, x["max_seqlen_q"], x["max_seqlen_k"], float(alpha), int(scaling), -1,
+        0 if causal else -1,
         torch.cuda.current_stream().cuda_stream)
 
 
@@ -67,5 +68,5 @@ def test_noalloc_rejects_schedules_over_its_limit():
     fake = L.CTen(0x1000, 64, 64)
     st = lib.hstu_attn_fwd_noalloc(fake, fake, fake, L.Ten(0x1000, 64, 64), 0x2000, 0x2000, 1,
                                    128 * 65528, 128 * 65528, 1, 64, L.HSTU_BF16, 128, 128,
-                                   0.125, 0, 1, None)
+                                   0.125, 0, -1, 0, None)
     assert st == 1
