@@ -102,7 +102,12 @@ bool encode_ds(CUtensorMap* m, void* ptr, int64_t blocks, bool bf16) {
 }
 
 // ---------------------------------------------------------------- validation
-bool supported_dim(int D) { return D == 64 || D == 128 || D == 256; }
+bool supported_dim(int D) { return D == 32 || D == 64 || D == 128 || D == 256; }
+// Head dim 32 runs through the D = 64 kernels: the tensor maps keep the true
+// head dim, the 64-wide boxes read its columns 32-63 as zeros (out-of-range
+// fill), which add nothing to any product, and the outputs are clipped to 32
+// columns.
+int kernel_dim(int D) { return D == 32 ? 64 : D; }
 
 // Checks one (T, H, D) tensor with element strides (st, sh, 1).
 hstu_status_t check_tensor(const void* ptr, int64_t st, int64_t sh, int64_t T, int H, int D) {
@@ -306,12 +311,12 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
-  a.H = H; a.win = c.win; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.H = H; a.win = c.win; a.d_out = D; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
   const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-  if (launch_fwd(D, c.bf16, grid, stream, em.pdl(), tq, tk, tv, a) != cudaSuccess)
+  if (launch_fwd(kernel_dim(D), c.bf16, grid, stream, em.pdl(), tq, tk, tv, a) != cudaSuccess)
     return HSTU_ERR_CUDA;
   if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
@@ -387,7 +392,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
-  a.H = H; a.win = c.win; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.H = H; a.win = c.win; a.d_out = D; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
   // dK/dV first: it also stores the dS blocks that the dQ kernel reads
@@ -401,7 +406,8 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
     if (!encode_thd(&m_dk128, dk.ptr, total_k, H, D, dk.stride_t, dk.stride_h, kBM, c.bf16) ||
         !encode_thd(&m_dv128, dv.ptr, total_k, H, D, dv.stride_t, dv.stride_h, kBM, c.bf16))
       return HSTU_ERR_CUDA;
-    if (launch_dkdv(D, c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64, m_dk128,
+    if (launch_dkdv(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64,
+                    m_dk128,
                     m_dv128, ak) != cudaSuccess)
       return HSTU_ERR_CUDA;
   }
@@ -411,7 +417,8 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
     aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA;
     aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
     const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-    if (launch_dq(D, c.bf16, grid, stream, em.pdl(), m_ds, m_k128, aq) != cudaSuccess)
+    if (launch_dq(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m_ds, m_k128, aq) !=
+        cudaSuccess)
       return HSTU_ERR_CUDA;
   }
   if (!em.mark(3, stream)) return HSTU_ERR_CUDA;

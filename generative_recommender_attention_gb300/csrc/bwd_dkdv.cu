@@ -382,7 +382,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int64_t col0 = static_cast<int64_t>(V.hz % SPLIT) * DH + cg * DW;
       dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + hd * a.o0_sh + col0) * 2;
       dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + hd * a.o1_sh + col0) * 2;
-      return jj < V.Lk && grow < a.total_k;
+      // columns past d_out (a zero-padded head dim 32) are not stored
+      return jj < V.Lk && grow < a.total_k && col0 < a.d_out;
     };
     // Epilogue of unit V (the oi-th unit with key steps): wait for its last
     // MMAs, read dV and dK out of TMEM, release them, write them out.

@@ -189,7 +189,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       char* orow = static_cast<char*>(a.o0) +
                    (grow * a.o0_st + static_cast<int64_t>(U.hz) * a.o0_sh) * 2;
       if (U.n <= 0) {
-        if (row_ok) store_zero_n<D>(orow);
+        if (row_ok) {
+          if (D == 64 && a.d_out == 32) store_zero_n<32>(orow);  // zero-padded head dim 32
+          else store_zero_n<D>(orow);
+        }
         continue;
       }
       const int ab = oi % NACC;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t x[32];
         tmem_ld32(tAcc + 32 * c, x);
         if (c == D / 32 - 1) warp_arrive(bar(ACCEMPTY + ab));  // every column is read
-        if (row_ok) store_row_n<32, BF16>(orow + c * 64, x, out_scale);
+        if (row_ok && 32 * c < a.d_out) store_row_n<32, BF16>(orow + c * 64, x, out_scale);
       }
       ++oi;
     }

@@ -329,6 +329,22 @@ __device__ __forceinline__ void stage_row32(uint32_t tile, int r, int col, const
   }
 }
 
+// The first N of M fp32 values, scaled, rounded and stored (N a multiple of 8).
+template <int N, int M, bool BF16>
+__device__ __forceinline__ void store_row_head(void* dst, const uint32_t (&x)[M], float scale) {
+  static_assert(N % 8 == 0 && N <= M, "whole 16-byte groups of the row");
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < N / 8; ++v) {
+    uint4 w;
+    w.x = pack2<BF16>(__uint_as_float(x[8 * v + 0]) * scale, __uint_as_float(x[8 * v + 1]) * scale);
+    w.y = pack2<BF16>(__uint_as_float(x[8 * v + 2]) * scale, __uint_as_float(x[8 * v + 3]) * scale);
+    w.z = pack2<BF16>(__uint_as_float(x[8 * v + 4]) * scale, __uint_as_float(x[8 * v + 5]) * scale);
+    w.w = pack2<BF16>(__uint_as_float(x[8 * v + 6]) * scale, __uint_as_float(x[8 * v + 7]) * scale);
+    p[v] = w;
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void store_zero_n(void* dst) {
   static_assert(N % 8 == 0, "whole 16-byte groups");

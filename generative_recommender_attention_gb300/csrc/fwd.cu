@@ -334,7 +334,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       char* orow = static_cast<char*>(a.o0) +
                    (grow * a.o0_st + static_cast<int64_t>(h) * a.o0_sh) * 2;
       if (U.n <= 0) {
-        if (row_ok) store_zero_n<D>(orow);
+        if (row_ok) {
+          if (D == 64 && a.d_out == 32) store_zero_n<32>(orow);  // zero-padded head dim 32
+          else store_zero_n<D>(orow);
+        }
         continue;
       }
       if (!wait_bar_warp(bar(OFULL), oi & 1, wc, 0x202)) { ok = false; break; }
@@ -344,7 +347,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t x[64];
         tmem_ld64(tO + 64 * c, x);
         if (c == D / 64 - 1) warp_arrive(bar(OEMPTY));  // every O column is read
-        if (row_ok) store_row_n<64, BF16>(orow + c * 128, x, a.inv_L);
+        if (row_ok) {
+          if (D == 64 && a.d_out == 32) store_row_head<32, 64, BF16>(orow, x, a.inv_L);
+          else store_row_n<64, BF16>(orow + c * 128, x, a.inv_L);
+        }
       }
       ++oi;
     }

@@ -111,7 +111,8 @@ size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
  *     max_seqlen_q, negative is an error (the page requires it positive).
  *   window_left, window_right: the mask window, each -1 (no bound) or >= 0;
  *     (-1, 0) causal, (-1, -1) full; a bound below -1 is an error.
- *   head_dim in {64, 128, 256}; dtype FP16 or BF16.
+ *   head_dim in {32, 64, 128, 256} (32 runs on the 64-wide kernels with the
+ *     head dimension zero-padded on chip); dtype FP16 or BF16.
  * B == 0 or total_q == 0 is a no-op returning HSTU_OK.
  */
 hstu_status_t hstu_attn_fwd(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,

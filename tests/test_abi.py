@@ -100,7 +100,7 @@ def _call_fwd(lib, **over):
 
 def test_fwd_argument_errors(lib):
     assert _call_fwd(lib, D=96) == UNSUPPORTED
-    assert _call_fwd(lib, D=32) == UNSUPPORTED
+    assert _call_fwd(lib, D=16) == UNSUPPORTED
     assert _call_fwd(lib, dtype=7) == UNSUPPORTED
     assert _call_fwd(lib, max_q=61, max_k=60) == INVALID          # max_seqlen_q > max_seqlen_k
     assert _call_fwd(lib, scaling=-1) == INVALID                 # scaling_seqlen must be > 0

@@ -39,7 +39,8 @@ def _guarded(T, H, D, dtype, extra_rows=3, pad_h=8, pad_t=16, guard=64):
 
 @pytest.mark.parametrize("D,dtype,causal", [(64, torch.bfloat16, True), (128, torch.float16, False),
                                             (256, torch.bfloat16, True),
-                                            (128, torch.bfloat16, (100, 20))])
+                                            (128, torch.bfloat16, (100, 20)),
+                                            (32, torch.float16, True)])
 def test_no_write_outside_logical_outputs(D, dtype, causal):
     lens = [129, 1, 300, 0, 64]
     H = 2

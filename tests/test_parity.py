@@ -47,7 +47,7 @@ def test_workload_full_size_sampled(name):
 MEDIUM_LENS = [300, 1, 129, 517, 0, 64, 256]
 
 
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("causal", [True, False])
 def test_medium_every_variant(D, dtype, causal):
@@ -61,8 +61,8 @@ def test_medium_every_variant(D, dtype, causal):
 WINDOWS = [(0, 0), (16, 0), (200, 40), (70, -1), (-1, 100), (129, 1), (1000, 0)]
 
 
-@pytest.mark.parametrize("D,dtype", [(64, torch.bfloat16), (128, torch.float16),
-                                     (256, torch.bfloat16)])
+@pytest.mark.parametrize("D,dtype", [(32, torch.float16), (64, torch.bfloat16),
+                                     (128, torch.float16), (256, torch.bfloat16)])
 @pytest.mark.parametrize("window", WINDOWS)
 def test_medium_windows(D, dtype, window):
     x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, D, dtype, seed=D + window[0] + 7)
