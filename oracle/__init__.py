@@ -179,6 +179,35 @@ def fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
                     causal, tok, hd, n_threads).reshape(T, H, D)
 
 
+def gather_paged(paged_kv, page_ids, page_indptrs, cu_seqlens_k):
+    """Contiguous (T_k, H, D) K and V of a paged cache ("HSTU Attention
+    (Blackwell SM100/SM103)", Mask support: paged_kv is (num_pages, 2, 128,
+    H, D), K/V selected by the second index; page_ids[page_indptrs[b] + p] is
+    the page holding keys 128 p .. 128 p + 127 of sequence b).  Key j of
+    sequence b lands at row cu_seqlens_k[b] + j.  Values are copied, exactly."""
+    kv = _f64(paged_kv)
+    ids, ptr, ck = _i32(page_ids), _i32(page_indptrs), _i32(cu_seqlens_k)
+    T = int(ck[-1])
+    H, D = kv.shape[3], kv.shape[4]
+    k = np.zeros((T, H, D))
+    v = np.zeros((T, H, D))
+    for b in range(ck.shape[0] - 1):
+        for j in range(int(ck[b + 1] - ck[b])):
+            page = int(ids[int(ptr[b]) + j // 128])
+            k[ck[b] + j] = kv[page, 0, j % 128]
+            v[ck[b] + j] = kv[page, 1, j % 128]
+    return k, v
+
+
+def fwd_paged(q, paged_kv, page_ids, page_indptrs, cu_seqlens_q, cu_seqlens_k, alpha,
+              L_scale, n_threads: int = 0) -> np.ndarray:
+    """Forward over a paged K/V cache, causal (the page's paged path is causal
+    only): the keys are gathered into contiguous storage and the ordinary
+    forward runs on them."""
+    k, v = gather_paged(paged_kv, page_ids, page_indptrs, cu_seqlens_k)
+    return fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, True, n_threads)
+
+
 def bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
         n_threads: int = 0):
     """Full (dQ, dK, dV), shapes of q, k, v, fp64."""

@@ -475,6 +475,45 @@ def test_band_additivity(left, right):
 
 
 # --------------------------------------------------------------------------
+# paged K/V
+# --------------------------------------------------------------------------
+def test_paged_gather_is_the_contiguous_forward():
+    """Keys scattered over shuffled 128-row pages (with unused pages and
+    garbage past each sequence's last key) give exactly the forward of the
+    contiguous keys; a page holding keys of the wrong offset would not."""
+    lens_q, lens_k = [130, 1, 300, 0, 256], [200, 1, 300, 5, 256]
+    H, D = 2, 8
+    x = _rand(lens_q, lens_k, H, D, seed=51)
+    rng = np.random.default_rng(5)
+    ck = x["cu_seqlens_k"].tolist()
+    n_pages = [-(-L // 128) for L in lens_k]
+    total_pages = sum(n_pages) + 3
+    perm = rng.permutation(total_pages)
+    kv = rng.standard_normal((total_pages, 2, 128, H, D)) * 100.0   # finite garbage
+    ids, ptr, used = [], [0], 0
+    for b, L in enumerate(lens_k):
+        for p in range(n_pages[b]):
+            page = int(perm[used]); used += 1
+            ids.append(page)
+            rows = slice(ck[b] + 128 * p, ck[b] + min(L, 128 * p + 128))
+            n = rows.stop - rows.start
+            kv[page, 0, :n] = x["k"][rows].numpy()
+            kv[page, 1, :n] = x["v"][rows].numpy()
+        ptr.append(len(ids))
+    alpha, L = 0.7, 9.0
+    got = oracle.fwd_paged(x["q"], kv, np.array(ids, np.int32), np.array(ptr, np.int32),
+                           x["cu_seqlens_q"], x["cu_seqlens_k"], alpha, L)
+    want = _fwd(x, alpha, L, True)
+    np.testing.assert_array_equal(got, want)
+    # swapping two pages of one sequence changes the result
+    ids2 = list(ids)
+    ids2[ptr[2]], ids2[ptr[2] + 1] = ids2[ptr[2] + 1], ids2[ptr[2]]
+    bad = oracle.fwd_paged(x["q"], kv, np.array(ids2, np.int32), np.array(ptr, np.int32),
+                           x["cu_seqlens_q"], x["cu_seqlens_k"], alpha, L)
+    assert np.abs(bad - want).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
 # limits, empty and ragged cases, row entry points
 # --------------------------------------------------------------------------
 def test_huge_scores_no_nan():
