@@ -23,7 +23,8 @@ from typing import Optional, Tuple
 from ._lib import (HstuError, HSTU_BF16, HSTU_FP16, library, library_path,
                    workspace_size, last_device_status, selftest_timeout, CTen, Ten)
 
-__all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "workspace_size", "last_device_status",
+__all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_paged", "workspace_size",
+           "last_device_status",
            "selftest_timeout", "HstuError", "library", "library_path"]
 
 
@@ -146,6 +147,50 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     else:
         arr, n = _event_array(events)
         st = lib.hstu_attn_fwd_profiled(*args, arr, n)
+    if st != 0:
+        raise HstuError(st)
+    return out
+
+
+def hstu_attn_fwd_paged(q, paged_kv, page_ids, page_indptrs, cu_seqlens_q, cu_seqlens_k,
+                        max_seqlen_q: int, max_seqlen_k: int,
+                        scaling_seqlen: Optional[int] = None, alpha: float = 1.0, out=None,
+                        workspace=None):
+    """Causal forward over a paged K/V cache; returns ``out`` (shape of q).
+
+    paged_kv: contiguous (num_pages, 2, 128, H, D), K at [:, 0] and V at [:, 1];
+    page_ids: int32 physical page of each 128-key block, per sequence the
+    slice page_indptrs[b] : page_indptrs[b + 1]; page_indptrs: int32 (B + 1,).
+    cu_seqlens_k gives the key counts.  Values are trusted, never copied to
+    the host.  Rows of a page past its sequence's keys must be finite.
+    """
+    import torch
+    lib = library()
+    T_q, H, D = q.shape
+    dev = q.device
+    _check_thd("q", q, T_q, H, D, q.dtype, dev)
+    if (paged_kv.dim() != 5 or paged_kv.shape[1] != 2 or paged_kv.shape[2] != 128
+            or paged_kv.shape[3] != H or paged_kv.shape[4] != D):
+        raise ValueError(f"paged_kv: shape {tuple(paged_kv.shape)}, expected (P, 2, 128, {H}, {D})")
+    if paged_kv.dtype != q.dtype or paged_kv.device != dev or not paged_kv.is_contiguous():
+        raise ValueError("paged_kv: q's dtype and device, contiguous")
+    for name, t in (("page_ids", page_ids), ("page_indptrs", page_indptrs)):
+        if t.dtype != torch.int32 or t.device != dev or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name}: contiguous 1-D int32 on {dev}")
+    B = _meta(cu_seqlens_q, cu_seqlens_k, dev)
+    if page_indptrs.shape[0] != B + 1:
+        raise ValueError("page_indptrs: shape (B + 1,)")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    _check_thd("out", out, T_q, H, D, q.dtype, dev)
+    ws = _workspace(workspace, workspace_size(B, T_q, 0, H, D, max_seqlen_q, max_seqlen_k,
+                                              False), dev)
+    st = lib.hstu_attn_fwd_paged(_cten(q), paged_kv.data_ptr(), paged_kv.shape[0],
+                                 page_ids.data_ptr(), page_indptrs.data_ptr(), _ten(out),
+                                 cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, H, D,
+                                 _dtype_code(q), int(max_seqlen_q), int(max_seqlen_k),
+                                 float(alpha), _scaling(scaling_seqlen), ws.data_ptr(),
+                                 ws.numel(), _stream(dev))
     if st != 0:
         raise HstuError(st)
     return out

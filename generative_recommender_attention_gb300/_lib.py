@@ -24,7 +24,8 @@ STATUS = {0: "HSTU_OK", 1: "HSTU_ERR_INVALID_ARG", 2: "HSTU_ERR_UNSUPPORTED",
 EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_attn_bwd_profiled",
            "hstu_attn_workspace_size",
            "hstu_attn_status_string", "hstu_attn_last_device_status",
-           "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc")
+           "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc",
+           "hstu_attn_fwd_paged")
 
 
 class CTen(ctypes.Structure):
@@ -77,6 +78,11 @@ def _declare(lib):
     lib.hstu_attn_selftest_timeout.restype = ctypes.c_int
     lib.hstu_attn_fwd_noalloc.argtypes = [CTen, CTen, CTen, Ten] + scal[:14] + [P]
     lib.hstu_attn_fwd_noalloc.restype = ctypes.c_int
+    # q, paged_kv, num_pages, page_ids, page_indptrs, out, cu_q, cu_k, B, T_q, H, D, dtype,
+    # max_q, max_k, alpha, scaling_seqlen, workspace, bytes, stream
+    lib.hstu_attn_fwd_paged.argtypes = [CTen, P, i64, P, P, Ten, P, P, i32, i64, i32, i32,
+                                        ctypes.c_int, i32, i32, f32, i32, P, S, P]
+    lib.hstu_attn_fwd_paged.restype = ctypes.c_int
     lib.hstu_attn_version.argtypes = []
     lib.hstu_attn_version.restype = i32
 

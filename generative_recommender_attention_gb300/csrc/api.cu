@@ -258,13 +258,23 @@ struct EventMarks {
   }
 };
 
+// A paged K/V cache: contiguous (num_pages, 2, 128, H, D) storage and the
+// device page tables.
+struct PagedKV {
+  const void* kv;
+  int64_t num_pages;
+  const int32_t* page_ids;
+  const int32_t* page_indptrs;
+};
+
 hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
                        int64_t total_q, int64_t total_k, int32_t num_heads, int32_t head_dim,
                        hstu_dtype_t dtype, int32_t max_seqlen_q, int32_t max_seqlen_k,
                        float alpha, int32_t scaling_seqlen, int32_t window_left,
                        int32_t window_right, void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
+                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em,
+                       const PagedKV* paged = nullptr) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
@@ -272,8 +282,16 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   if (s != HSTU_OK) return s;
   const int H = num_heads, D = head_dim;
   if ((s = check_tensor(q.ptr, q.stride_t, q.stride_h, total_q, H, D)) != HSTU_OK) return s;
-  if ((s = check_tensor(k.ptr, k.stride_t, k.stride_h, total_k, H, D)) != HSTU_OK) return s;
-  if ((s = check_tensor(v.ptr, v.stride_t, v.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  if (paged == nullptr) {
+    if ((s = check_tensor(k.ptr, k.stride_t, k.stride_h, total_k, H, D)) != HSTU_OK) return s;
+    if ((s = check_tensor(v.ptr, v.stride_t, v.stride_h, total_k, H, D)) != HSTU_OK) return s;
+  } else {
+    if (paged->num_pages <= 0 || paged->num_pages > (INT32_MAX / 256)) return HSTU_ERR_INVALID_ARG;
+    if (batch > 0 && (paged->page_ids == nullptr || paged->page_indptrs == nullptr))
+      return HSTU_ERR_INVALID_ARG;
+    if ((s = check_tensor(paged->kv, int64_t(H) * D, D, paged->num_pages * 256, H, D)) != HSTU_OK)
+      return s;
+  }
   if ((s = check_tensor(out.ptr, out.stride_t, out.stride_h, total_q, H, D)) != HSTU_OK) return s;
   if (batch == 0 || total_q == 0) return HSTU_OK;
   const size_t need =
@@ -294,10 +312,17 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   const void* vptr = total_k > 0 ? v.ptr : q.ptr;
   const int64_t kst = total_k > 0 ? k.stride_t : q.stride_t, ksh = total_k > 0 ? k.stride_h : q.stride_h;
   const int64_t vst = total_k > 0 ? v.stride_t : q.stride_t, vsh = total_k > 0 ? v.stride_h : q.stride_h;
-  if (!encode_thd(&tq, q.ptr, total_q, H, D, q.stride_t, q.stride_h, kBM, c.bf16) ||
-      !encode_thd(&tk, kptr, total_k, H, D, kst, ksh, BN, c.bf16) ||
-      !encode_thd(&tv, vptr, total_k, H, D, vst, vsh, BN, c.bf16))
+  if (!encode_thd(&tq, q.ptr, total_q, H, D, q.stride_t, q.stride_h, kBM, c.bf16))
     return HSTU_ERR_CUDA;
+  if (paged != nullptr) {
+    // one map over the whole cache, 256 rows per page (128 K rows, then 128 V rows)
+    if (!encode_thd(&tk, paged->kv, paged->num_pages * 256, H, D, int64_t(H) * D, D, BN, c.bf16))
+      return HSTU_ERR_CUDA;
+    tv = tk;
+  } else if (!encode_thd(&tk, kptr, total_k, H, D, kst, ksh, BN, c.bf16) ||
+             !encode_thd(&tv, vptr, total_k, H, D, vst, vsh, BN, c.bf16)) {
+    return HSTU_ERR_CUDA;
+  }
 
   int* header = static_cast<int*>(workspace);
   int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
@@ -315,6 +340,10 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
+  if (paged != nullptr) {
+    a.page_ids = paged->page_ids;
+    a.page_indptrs = paged->page_indptrs;
+  }
   const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
   if (launch_fwd(kernel_dim(D), c.bf16, grid, stream, em.pdl(), tq, tk, tv, a) != cudaSuccess)
     return HSTU_ERR_CUDA;
@@ -547,6 +576,22 @@ bool noalloc_scratch(void** out) {
 }
 
 }  // namespace
+
+extern "C" hstu_status_t hstu_attn_fwd_paged(
+    hstu_cten_t q, const void* paged_kv, int64_t num_pages, const int32_t* page_ids,
+    const int32_t* page_indptrs, hstu_ten_t out, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q, int32_t num_heads,
+    int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+    int32_t scaling_seqlen, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (paged_kv == nullptr) return HSTU_ERR_INVALID_ARG;
+  const PagedKV pg{paged_kv, num_pages, page_ids, page_indptrs};
+  const hstu_cten_t none{nullptr, 0, 0};
+  // causal only; total_k bounds the keys the pages can hold
+  return fwd_impl(q, none, none, out, cu_seqlens_q, cu_seqlens_k, batch, total_q,
+                  num_pages * 128, num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha,
+                  scaling_seqlen, -1, 0, workspace, workspace_bytes, stream,
+                  EventMarks{nullptr, 0}, &pg);
+}
 
 extern "C" hstu_status_t hstu_attn_fwd_noalloc(
     hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out, const int32_t* cu_seqlens_q,

@@ -153,6 +153,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
         query_tile_keys(U.tile, U.Lq, U.Lk, a.win, BN, kt0, nkt);
         const int kv_row0 = U.k0 + BN * kt0;
+        // Paged K/V: key tile kt lives in page page_ids[page_indptrs[b] +
+        // kt BN / 128], whose K rows start at row 256 p and V rows at
+        // 256 p + 128 of the cache's map.  The next tile's page is looked up
+        // one tile ahead, so the lookup is off the load path.
+        const bool paged = a.page_ids != nullptr;
+        int pi0 = 0, pg_next = 0;
+        if (paged) {
+          pi0 = __ldg(a.page_indptrs + U.b);
+          pg_next = __ldg(a.page_ids + pi0 + (kt0 * BN) / 128);
+        }
         const int qb = qi % NQ;
         if (!wait_bar(bar(QEMPTY + qb), ((qi / NQ) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(QFULL + qb), C::Q_BYTES);
@@ -164,16 +174,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // No L2 warm-up here: measured, the extra prefetch requests slowed
         // the forward's own tile loads more than they saved.
         for (int n = 0; n < U.n; ++n) {
-          const int row = kv_row0 + BN * n;
+          int row = kv_row0 + BN * n, vrow = row;
+          if (paged) {
+            const int kt = kt0 + n, pg = pg_next;
+            if (n + 1 < U.n) pg_next = __ldg(a.page_ids + pi0 + ((kt + 1) * BN) / 128);
+            row = 256 * pg + (kt * BN) % 128;
+            vrow = row + 128;
+          }
           if (!load_kv(&tm_k, sK, NK, ki, KFULL, SFULL, row, h, 0x002)) { ok = false; break; }
           if (nv == LA) {
             if (!load_kv(&tm_v, sV, NV, vi, VFULL, VEMPTY, v_row0, v_h0, 0x003)) { ok = false; break; }
             v_row0 = v_row1; v_h0 = v_h1;
-            v_row1 = row; v_h1 = h;
+            v_row1 = vrow; v_h1 = h;
           } else if (nv == 1) {
-            v_row1 = row; v_h1 = h; nv = 2;
+            v_row1 = vrow; v_h1 = h; nv = 2;
           } else {
-            v_row0 = row; v_h0 = h; nv = 1;
+            v_row0 = vrow; v_h0 = h; nv = 1;
           }
         }
       }

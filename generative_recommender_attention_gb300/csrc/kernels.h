@@ -151,6 +151,8 @@ struct AttnArgs {
   int64_t o1_st, o1_sh;
   int d_out;            // output columns per head: the kernel's D, or 32 when a
                         // head dimension of 32 runs zero-padded through the D = 64 kernels
+  const int* page_ids;      // forward over a paged K/V cache: page of each 128-key block
+  const int* page_indptrs;  //   and each sequence's first entry in page_ids; null: contiguous K/V
   void* ds;             // backward: dS blocks (written by dK/dV, read by dQ)
   const int* ds_base;   // backward: first dS block of each sequence (B + 1)
   int ds_cap;           // backward: dS blocks the workspace holds

@@ -147,6 +147,35 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
                             cudaStream_t stream);
 
 /*
+ * Forward over a paged K/V cache (page "HSTU Attention (Blackwell
+ * SM100/SM103)", section "Mask support", paged-KV paragraph; the page's
+ * paged path is causal only and has no backward, and so has this one).
+ *   paged_kv: device, contiguous (num_pages, 2, 128, num_heads, head_dim) in
+ *     dtype, 16-byte aligned; [p][0] holds K and [p][1] V of 128 consecutive
+ *     keys.  num_pages > 0.
+ *   page_ids: device int32; page_indptrs: device int32 (batch + 1,).  Key j
+ *     of sequence b lives in row j % 128 of page
+ *     page_ids[page_indptrs[b] + j / 128].  Values are trusted (never copied to
+ *     the host, never range-checked), as the page requires.
+ *   cu_seqlens_k: its differences give each sequence's key count Lk_b (its
+ *     offsets are not used: the storage is the pages).  max_seqlen_k >= every
+ *     Lk_b, max_seqlen_q <= max_seqlen_k.
+ *   Rows of a page past its sequence's last key are multiplied by exact
+ *     zeros, so they must hold finite values (NaN or Inf there would leak).
+ *   Other arguments as for hstu_attn_fwd with window (-1, 0); workspace:
+ *     hstu_attn_workspace_size(batch, total_q, 0, num_heads, head_dim,
+ *     max_seqlen_q, max_seqlen_k, 0) bytes.
+ */
+hstu_status_t hstu_attn_fwd_paged(hstu_cten_t q, const void* paged_kv, int64_t num_pages,
+                                  const int32_t* page_ids, const int32_t* page_indptrs,
+                                  hstu_ten_t out, const int32_t* cu_seqlens_q,
+                                  const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q,
+                                  int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                  int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                  int32_t scaling_seqlen, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Profiling variants: identical to hstu_attn_fwd / hstu_attn_bwd (same
  * arguments, results and errors), and they additionally record the first
  * `n_events` of these caller-created CUDA events on `stream`:

@@ -166,6 +166,26 @@ def test_bwd_argument_errors(lib):
     assert _call_bwd(lib, batch=0, wl=5, wr=3) == OK
 
 
+def _call_paged(lib, **over):
+    a = dict(kv=0x20000, pages=4, ids=0x30000, ptr=0x40000, batch=2, D=64, max_q=60, max_k=60)
+    a.update(over)
+    return lib.hstu_attn_fwd_paged(L.CTen(0x10000, 256, 64), a["kv"], a["pages"], a["ids"],
+                                   a["ptr"], L.Ten(0x50000, 256, 64), 0x60000, 0x61000,
+                                   a["batch"], 100, 4, a["D"], L.HSTU_BF16, a["max_q"],
+                                   a["max_k"], 0.125, 0, 0x70000, 1 << 20, None)
+
+
+def test_paged_argument_errors(lib):
+    assert _call_paged(lib, kv=None) == INVALID
+    assert _call_paged(lib, pages=0) == INVALID
+    assert _call_paged(lib, ids=None) == INVALID
+    assert _call_paged(lib, ptr=None) == INVALID
+    assert _call_paged(lib, kv=0x20008) == MISALIGNED
+    assert _call_paged(lib, D=96) == UNSUPPORTED
+    assert _call_paged(lib, max_q=70) == INVALID
+    assert _call_paged(lib, batch=0) == OK
+
+
 def test_selftest_argument_errors(lib):
     assert lib.hstu_attn_selftest_timeout(None, 1000, None) == INVALID
     assert lib.hstu_attn_selftest_timeout(0x70000, 0, None) == INVALID

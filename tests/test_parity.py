@@ -14,7 +14,7 @@ from generative_recommender_attention_gb300 import workloads
 import generative_recommender_attention_gb300 as hstu
 
 from hstu_testlib import (TOL_BWD, TOL_FWD, check, full_compare, gpu_fwd_bwd,
-                          sampled_compare, to_dev)
+                          sample_rows, sampled_compare, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +83,74 @@ def test_window_recsys_sampled():
     w = _ws("recsys")
     x = workloads.make_inputs(w, seed=0)
     sampled_compare(x, w.scaling_seqlen, (256, 0), w.alpha, n_random=96)
+
+
+# ------------------------------------------------------------------ paged K/V forward
+def _paged_cache(x, n_extra, seed, garbage=1e3):
+    """Scatter x's K/V into shuffled 128-row pages (plus unused pages); rows
+    past each sequence's keys hold finite garbage."""
+    rng = np.random.default_rng(seed)
+    ck = x["cu_seqlens_k"].tolist()
+    lens = [ck[b + 1] - ck[b] for b in range(len(ck) - 1)]
+    n_pages = [-(-L // 128) for L in lens]
+    total = sum(n_pages) + n_extra
+    perm = rng.permutation(total)
+    H, D = x["k"].shape[1], x["k"].shape[2]
+    kv = (torch.from_numpy(rng.uniform(-garbage, garbage, (total, 2, 128, H, D)))
+          .to(x["k"].dtype))
+    ids, ptr, used = [], [0], 0
+    for b, L in enumerate(lens):
+        for p in range(n_pages[b]):
+            page = int(perm[used])
+            used += 1
+            ids.append(page)
+            lo, hi = ck[b] + 128 * p, ck[b] + min(L, 128 * p + 128)
+            kv[page, 0, :hi - lo] = x["k"][lo:hi]
+            kv[page, 1, :hi - lo] = x["v"][lo:hi]
+        ptr.append(len(ids))
+    return kv, torch.tensor(ids, dtype=torch.int32), torch.tensor(ptr, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("D,dtype", [(32, torch.bfloat16), (64, torch.float16),
+                                     (128, torch.bfloat16), (256, torch.float16)])
+def test_paged_forward(D, dtype):
+    lq = [300, 1, 129, 517, 0, 64, 256]
+    lk = [340, 1, 129, 600, 3, 64, 256]
+    x = workloads.random_inputs(lq, lk, 2, D, dtype, seed=D + 17)
+    x["max_seqlen_k"] = max(lk)
+    kv, ids, ptr = _paged_cache(x, n_extra=5, seed=D)
+    xd = to_dev(x)
+    alpha = 1.0 / math.sqrt(D)
+    o = hstu.hstu_attn_fwd_paged(xd["q"], kv.cuda(), ids.cuda(), ptr.cuda(), xd["cu_seqlens_q"],
+                                 xd["cu_seqlens_k"], x["max_seqlen_q"], x["max_seqlen_k"],
+                                 alpha=alpha)
+    torch.cuda.synchronize()
+    L = oracle.resolve_scaling(None, x["max_seqlen_q"])
+    ref = oracle.fwd_paged(x["q"], kv, ids, ptr, x["cu_seqlens_q"], x["cu_seqlens_k"], alpha, L)
+    check("O paged", o, ref, TOL_FWD)
+    # the same kernel over the contiguous keys computes the same numbers
+    oc = hstu.hstu_attn_fwd(xd["q"], xd["k"], xd["v"], xd["cu_seqlens_q"], xd["cu_seqlens_k"],
+                            x["max_seqlen_q"], x["max_seqlen_k"], causal=True, alpha=alpha)
+    torch.cuda.synchronize()
+    assert torch.equal(o, oc)
+
+
+def test_paged_forward_recsys_sampled():
+    """The recsys workload's sequences served from a shuffled page pool."""
+    w = _ws("recsys")
+    x = workloads.make_inputs(w, seed=0)
+    kv, ids, ptr = _paged_cache(x, n_extra=17, seed=1)
+    xd = to_dev(x)
+    o = hstu.hstu_attn_fwd_paged(xd["q"], kv.cuda(), ids.cuda(), ptr.cuda(), xd["cu_seqlens_q"],
+                                 xd["cu_seqlens_k"], x["max_seqlen_q"], x["max_seqlen_k"],
+                                 alpha=w.alpha, scaling_seqlen=w.scaling_seqlen)
+    torch.cuda.synchronize()
+    L = oracle.resolve_scaling(w.scaling_seqlen, x["max_seqlen_q"])
+    toks, heads = sample_rows(x["cu_seqlens_q"], w.heads, 96, 0)
+    k, v = oracle.gather_paged(kv, ids, ptr, x["cu_seqlens_k"])
+    ref = oracle.fwd_rows(x["q"], k, v, x["cu_seqlens_q"], x["cu_seqlens_k"], w.alpha, L, True,
+                          toks, heads)
+    check("O paged", o.cpu()[torch.from_numpy(toks), torch.from_numpy(heads)], ref, TOL_FWD)
 
 
 # ------------------------------------------------------------------ edge cases
