@@ -151,6 +151,75 @@ def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0, mask=
     return flops, secs, n, threads
 
 
+def run_paged(args, w, hstu, dev):
+    """--paged: forward-only throughput over a paged K/V cache (the page's
+    paged path is a causal forward), the contiguous forward timed beside it."""
+    import torch
+    from generative_recommender_attention_gb300 import workloads
+    x = workloads.make_inputs(w, seed=0)
+    lengths = x["lengths"]
+    H, D = w.heads, w.head_dim
+    ck = x["cu_seqlens_k"].tolist()
+    n_pages = [-(-L // 128) for L in lengths]
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(sum(n_pages))
+    kv = torch.zeros(sum(n_pages), 2, 128, H, D, dtype=x["k"].dtype)
+    ids, ptr, used = [], [0], 0
+    for b, L in enumerate(lengths):
+        for p in range(n_pages[b]):
+            page = int(perm[used])
+            used += 1
+            ids.append(page)
+            lo, hi = ck[b] + 128 * p, ck[b] + min(L, 128 * p + 128)
+            kv[page, 0, :hi - lo] = x["k"][lo:hi]
+            kv[page, 1, :hi - lo] = x["v"][lo:hi]
+        ptr.append(len(ids))
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    kv, ids, ptr = kv.to(dev), torch.tensor(ids, dtype=torch.int32, device=dev), \
+        torch.tensor(ptr, dtype=torch.int32, device=dev)
+    mq, mk = x["max_seqlen_q"], x["max_seqlen_k"]
+    o = torch.empty_like(d["q"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flops = 4.0 * D * pairs(lengths, H, True)
+
+    def paged():
+        hstu.hstu_attn_fwd_paged(d["q"], kv, ids, ptr, d["cu_seqlens_q"], d["cu_seqlens_k"], mq,
+                                 mk, scaling_seqlen=w.scaling_seqlen, alpha=w.alpha, out=o)
+
+    def contiguous():
+        hstu.hstu_attn_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], mq, mk,
+                           scaling_seqlen=w.scaling_seqlen, alpha=w.alpha, causal=True, out=o)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    ms_p, ms_c = timed(paged), timed(contiguous)
+    print(json.dumps({
+        "metric": "HSTU paged-KV attn fwd TFLOP/s (causal, 128-row pages)",
+        "value": flops / (ms_p * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_p,
+        "higher_is_better": True, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f16",
+        "data": "synthetic",
+        "contiguous_fwd": {"value": flops / (ms_c * 1e-3) / 1e12, "ms_per_step": ms_c},
+        "config": dict(workload_config(w, lengths), pages=int(kv.shape[0]),
+                       page_order="shuffled", l2="flushed between steps (256 MiB write)",
+                       launch="direct calls, CUDA events around each forward"),
+    }))
+    return 0
+
+
 def run_reference(args, w):
     """--impl reference: the oracle, as it stands, on the host cores."""
     import torch
@@ -201,6 +270,9 @@ def main():
                     help="launch every step through the Python binding instead of replaying a "
                          "CUDA graph of it")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--paged", action="store_true",
+                    help="time the causal forward over a paged K/V cache (the workload's keys "
+                         "in shuffled 128-row pages) beside the contiguous forward; one JSON line")
     ap.add_argument("--kernels-only", action="store_true",
                     help="run warm-up and timed steps only (no second pass, end-to-end, clocks or "
                          "CPU baseline) and print no JSON line: for wrapping in a profiler")
@@ -230,6 +302,8 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.paged:
+        return run_paged(args, w, hstu, dev)
 
     x = workloads.make_inputs(w, seed=0)
     lengths = x["lengths"]

@@ -313,11 +313,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
+          } else if (jc >= lo_all) {
+            // only the upper bound (the diagonal or the sequence end) cuts
+            // this chunk: every causal and full mask chunk
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = jc + 2 * e;
+              const uint32_t s0 = j < hi ? x[2 * e] : 0u;  // SiLU(0) = 0
+              const uint32_t s1 = j + 1 < hi ? x[2 * e + 1] : 0u;
+              p[e] = silu_pair<BF16>(s0, s1, half_alpha);
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int j = jc + 2 * e;
-              const uint32_t s0 = (j >= lo && j < hi) ? x[2 * e] : 0u;  // SiLU(0) = 0
+              const uint32_t s0 = (j >= lo && j < hi) ? x[2 * e] : 0u;
               const uint32_t s1 = (j + 1 >= lo && j + 1 < hi) ? x[2 * e + 1] : 0u;
               p[e] = silu_pair<BF16>(s0, s1, half_alpha);
             }
