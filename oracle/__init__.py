@@ -15,7 +15,10 @@ sequence and head, O = (1/L_scale) (M (.) SiLU(alpha Q K^T)) V, no softmax.
 ``scaling_seqlen`` None or 0 means max_seqlen_q (same page, Overview and
 "High-level functions").  The mask argument ``causal`` of every entry point is
 either a bool (True: window (-1, 0), False: window (-1, -1)) or a window pair
-(left, right) as in the page's section "Mask support", -1 meaning unbounded.
+(left, right) as in the page's section "Mask support", -1 meaning unbounded,
+or ``{"func": F}`` for the arbitrary mask of the same section: F an int32
+array (N, L), N odd, whose column t holds query token t's endpoints
+F0, F1, ..., valid keys [0, F0) U [F1, F2) U ... (local key indices).
 """
 from __future__ import annotations
 
@@ -60,7 +63,7 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        common = [i64, i64, i32, f64, f64, i32, i32, P, P, i64]
+        common = [i64, i64, i32, f64, f64, i32, i32, P, i32, i64, P, P, i64]
         lib.hstu_oracle_fwd_rows.argtypes = [P, P, P, P, P] + common + [P, i32]
         lib.hstu_oracle_dq_rows.argtypes = [P, P, P, P, P, P] + common + [P, i32]
         lib.hstu_oracle_dkdv_rows.argtypes = [P, P, P, P, P, P] + common + [P, P, i32]
@@ -103,8 +106,32 @@ def resolve_scaling(scaling_seqlen, max_seqlen_q) -> float:
     return float(scaling_seqlen)
 
 
+def _func(mask):
+    """(pointer-keeping array, N, L) of an arbitrary mask, or (None, 0, 0)."""
+    if isinstance(mask, dict):
+        f = _i32(mask["func"])
+        if f.ndim == 3:
+            f = f[0]
+        if f.ndim != 2 or f.shape[0] % 2 != 1:
+            raise ValueError("func: (N, L) int32 endpoints with N odd")
+        f = np.ascontiguousarray(f)
+        return f, int(f.shape[0]), int(f.shape[1])
+    return None, 0, 0
+
+
+def _mask_args(mask):
+    """C arguments (left, right, func, func_n, func_len) of a mask; the
+    array is returned too so that it stays alive during the call."""
+    f, n, L = _func(mask)
+    left, right = window(mask)
+    return (left, right, _ptr(f) if f is not None else None, n, L), f
+
+
 def window(mask):
-    """(left, right) of a mask given as a bool (causal / full) or a pair."""
+    """(left, right) of a mask given as a bool (causal / full) or a pair;
+    an arbitrary (func) mask has no window: (-1, -1)."""
+    if isinstance(mask, dict):
+        return -1, -1
     if isinstance(mask, (tuple, list)):
         left, right = (int(x) for x in mask)
         if left < -1 or right < -1:
@@ -128,10 +155,12 @@ def fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
     hd = np.ascontiguousarray(heads, dtype=np.int64)
     H, D = q.shape[1], q.shape[2]
     out = np.zeros((tok.shape[0], D), dtype=np.float64)
+    margs, keep = _mask_args(causal)
     _load().hstu_oracle_fwd_rows(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck), cq.shape[0] - 1, H, D,
-        float(alpha), float(L_scale), *window(causal), _ptr(tok), _ptr(hd),
+        float(alpha), float(L_scale), *margs, _ptr(tok), _ptr(hd),
         tok.shape[0], _ptr(out), int(n_threads))
+    del keep
     return out
 
 
@@ -144,11 +173,13 @@ def dq_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale, causal,
     hd = np.ascontiguousarray(heads, dtype=np.int64)
     H, D = q.shape[1], q.shape[2]
     out = np.zeros((tok.shape[0], D), dtype=np.float64)
+    margs, keep = _mask_args(causal)
     _load().hstu_oracle_dq_rows(
         _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
         cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
-        *window(causal), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(out),
+        *margs, _ptr(tok), _ptr(hd), tok.shape[0], _ptr(out),
         int(n_threads))
+    del keep
     return out
 
 
@@ -162,11 +193,13 @@ def dkdv_rows(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, alpha, L_scale,
     H, D = k.shape[1], k.shape[2]
     dk = np.zeros((tok.shape[0], D), dtype=np.float64)
     dv = np.zeros((tok.shape[0], D), dtype=np.float64)
+    margs, keep = _mask_args(causal)
     _load().hstu_oracle_dkdv_rows(
         _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(cq), _ptr(ck),
         cq.shape[0] - 1, H, D, float(alpha), float(L_scale),
-        *window(causal), _ptr(tok), _ptr(hd), tok.shape[0], _ptr(dk),
+        *margs, _ptr(tok), _ptr(hd), tok.shape[0], _ptr(dk),
         _ptr(dv), int(n_threads))
+    del keep
     return dk, dv
 
 

@@ -26,6 +26,13 @@
  * In every mode a key must also lie inside the sequence: j < Lk.  A masked
  * score contributes exactly zero (M multiplies SiLU(S)).
  *
+ * Arbitrary mask (same section, func_tensor): with func given (N int32
+ * endpoint rows of length func_len, N odd; row n of query token t at
+ * func[n * func_len + t]), query token t's valid keys are the union
+ * [0, F0) U [F1, F2) U [F3, F4) ... of its endpoints F_n, key indices local
+ * to the sequence, each interval taken on its own (they may overlap or come
+ * in any order), still cut to j < Lk.  The window is then ignored.
+ *
  * Backward: the pages give the API (section "High-level functions") but not
  * the formulas.  They follow from the forward equations by the chain rule:
  *     dV_j  = sum_i A_ij dO_i
@@ -68,6 +75,29 @@ static int mask_valid(int64_t i, int64_t j, int64_t Lk, int left, int right) {
     return 1;
 }
 
+/* Arbitrary mask: key j against the endpoints of query token t. */
+typedef struct {
+    const int32_t *func; /* NULL: the window decides */
+    int n;
+    int64_t len;
+} Func;
+
+static int func_valid(const Func *f, int64_t t, int64_t j, int64_t Lk) {
+    if (j >= Lk) return 0;
+    if (j < f->func[t]) return 1; /* [0, F0) */
+    for (int m = 1; m + 1 < f->n; m += 2) {
+        int64_t lo = f->func[(int64_t)m * f->len + t];
+        int64_t hi = f->func[(int64_t)(m + 1) * f->len + t];
+        if (lo <= j && j < hi) return 1;
+    }
+    return 0;
+}
+
+static int valid(const Func *f, int64_t t, int64_t i, int64_t j, int64_t Lk, int left,
+                 int right) {
+    return f->func ? func_valid(f, t, j, Lk) : mask_valid(i, j, Lk, left, right);
+}
+
 static double dot(const double *a, const double *b, int D) {
     double s = 0.0;
     for (int d = 0; d < D; ++d) s += a[d] * b[d];
@@ -107,9 +137,12 @@ int hstu_oracle_threads(int threads) { return set_threads(threads); }
 int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
                          const int32_t *cu_q, const int32_t *cu_k, int64_t B,
                          int64_t H, int D, double alpha, double L_scale,
-                         int left, int right, const int64_t *tok, const int64_t *head,
+                         int left, int right,
+                         const int32_t *func, int func_n, int64_t func_len,
+                         const int64_t *tok, const int64_t *head,
                          int64_t n, double *out, int threads) {
     set_threads(threads);
+    const Func f = {func, func_n, func_len};
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t r = 0; r < n; ++r) {
         double *o = out + r * (int64_t)D;
@@ -121,7 +154,7 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
         int64_t ok = cu_k[b], Lk = (int64_t)cu_k[b + 1] - cu_k[b];
         const double *qi = row(q, tok[r], h, H, D);
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!mask_valid(i, j, Lk, left, right)) continue;
+            if (!valid(&f, tok[r], i, j, Lk, left, right)) continue;
             const double *kj = row(k, ok + j, h, H, D);
             const double *vj = row(v, ok + j, h, H, D);
             double s = alpha * dot(qi, kj, D);
@@ -137,9 +170,11 @@ int hstu_oracle_dq_rows(const double *dout, const double *q, const double *k,
                         const double *v, const int32_t *cu_q,
                         const int32_t *cu_k, int64_t B, int64_t H, int D,
                         double alpha, double L_scale, int left, int right,
+                        const int32_t *func, int func_n, int64_t func_len,
                         const int64_t *tok, const int64_t *head, int64_t n,
                         double *dq, int threads) {
     set_threads(threads);
+    const Func f = {func, func_n, func_len};
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t r = 0; r < n; ++r) {
         double *g = dq + r * (int64_t)D;
@@ -152,7 +187,7 @@ int hstu_oracle_dq_rows(const double *dout, const double *q, const double *k,
         const double *qi = row(q, tok[r], h, H, D);
         const double *doi = row(dout, tok[r], h, H, D);
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!mask_valid(i, j, Lk, left, right)) continue;
+            if (!valid(&f, tok[r], i, j, Lk, left, right)) continue;
             const double *kj = row(k, ok + j, h, H, D);
             const double *vj = row(v, ok + j, h, H, D);
             double s = alpha * dot(qi, kj, D);
@@ -169,9 +204,11 @@ int hstu_oracle_dkdv_rows(const double *dout, const double *q, const double *k,
                           const double *v, const int32_t *cu_q,
                           const int32_t *cu_k, int64_t B, int64_t H, int D,
                           double alpha, double L_scale, int left, int right,
+                          const int32_t *func, int func_n, int64_t func_len,
                           const int64_t *tok, const int64_t *head, int64_t n,
                           double *dk, double *dv, int threads) {
     set_threads(threads);
+    const Func f = {func, func_n, func_len};
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t r = 0; r < n; ++r) {
         double *gk = dk + r * (int64_t)D;
@@ -186,7 +223,7 @@ int hstu_oracle_dkdv_rows(const double *dout, const double *q, const double *k,
         const double *kj = row(k, tok[r], h, H, D);
         const double *vj = row(v, tok[r], h, H, D);
         for (int64_t i = 0; i < Lq; ++i) {
-            if (!mask_valid(i, j, Lk, left, right)) continue;
+            if (!valid(&f, oq + i, i, j, Lk, left, right)) continue;
             const double *qi = row(q, oq + i, h, H, D);
             const double *doi = row(dout, oq + i, h, H, D);
             double s = alpha * dot(qi, kj, D);

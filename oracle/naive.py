@@ -11,7 +11,10 @@ Inputs are nested Python lists indexed [t][h][d]; cu_seqlens are lists of
 ints.  ``causal`` is True for the top-left aligned causal mask (key j valid
 iff j <= i and j < Lk), False for the full mask (j < Lk), or a window pair
 (left, right): key j valid iff j < Lk, i - left <= j unless left == -1, and
-j <= i + right unless right == -1.
+j <= i + right unless right == -1; or {"func": F} with F a list of N rows
+(N odd) of per-query-token endpoints: key j valid for query token t iff
+j < Lk and j lies in [0, F[0][t]) or in one of [F[1][t], F[2][t]),
+[F[3][t], F[4][t]), ...
 """
 from __future__ import annotations
 
@@ -37,9 +40,14 @@ def _zeros(T, H, D):
     return [[[0.0] * D for _ in range(H)] for _ in range(T)]
 
 
-def _valid(i, j, Lk, causal):
+def _valid(i, j, Lk, causal, t=None):
     if j >= Lk:
         return False
+    if isinstance(causal, dict):
+        F = causal["func"]
+        if j < F[0][t]:
+            return True
+        return any(F[m][t] <= j < F[m + 1][t] for m in range(1, len(F) - 1, 2))
     if isinstance(causal, (tuple, list)):
         left, right = causal
         lo_ok = left == -1 or i - j <= left
@@ -57,7 +65,7 @@ def forward(q, k, v, cu_q, cu_k, alpha, L_scale, causal):
         for h in range(H):
             for i in range(Lq):
                 for j in range(Lk):
-                    if not _valid(i, j, Lk, causal):
+                    if not _valid(i, j, Lk, causal, oq + i):
                         continue
                     s = 0.0
                     for d in range(D):
@@ -78,7 +86,7 @@ def backward(dout, q, k, v, cu_q, cu_k, alpha, L_scale, causal):
         for h in range(H):
             for i in range(Lq):
                 for j in range(Lk):
-                    if not _valid(i, j, Lk, causal):
+                    if not _valid(i, j, Lk, causal, oq + i):
                         continue
                     s = 0.0
                     da = 0.0

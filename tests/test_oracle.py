@@ -15,6 +15,9 @@ to mathematics it does not share code with:
 * gradients: central finite differences of <dO, O>, and torch.autograd on a
   dense masked fp64 formulation built from torch primitives;
 * limits: no NaN at |score| = 1e4;
+* arbitrary masks ("Mask support", func_tensor): brute force with random
+  endpoints, the func masks that equal causal, full and window masks, and
+  inclusion-exclusion over a union of two intervals;
 * windows ("Mask support", window_size = (left, right)): brute force with
   random windows, the degenerate windows that equal the causal and full
   masks, the diagonal-only window (0, 0) in closed form, the band built with
@@ -472,6 +475,88 @@ def test_band_additivity(left, right):
         np.testing.assert_allclose(ta - tb, tc - td, rtol=1e-11, atol=1e-13)
     # and the band really excludes something on each side
     assert np.abs(a[0] - f((-1, -1))[0]).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# arbitrary (func) masks
+# --------------------------------------------------------------------------
+def _local_rows(x):
+    """Local query index and its sequence's key count for every query token."""
+    cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_k"].tolist()
+    T = cq[-1]
+    i = np.zeros(T, np.int64)
+    lk = np.zeros(T, np.int64)
+    for b in range(len(cq) - 1):
+        i[cq[b]:cq[b + 1]] = np.arange(cq[b + 1] - cq[b])
+        lk[cq[b]:cq[b + 1]] = ck[b + 1] - ck[b]
+    return i, lk
+
+
+def _func(*rows):
+    return {"func": np.stack([np.asarray(r, dtype=np.int32) for r in rows])}
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("n", [1, 3, 5])
+def test_func_brute_force_tiny(seed, n):
+    """Random endpoints (overlapping, unordered, negative, past the
+    sequence) against the pure-Python restatement."""
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 4))
+    lq = [int(v) for v in rng.integers(0, 9, size=B)]
+    lk = [L + int(rng.integers(0, 3)) for L in lq]
+    H, D = int(rng.integers(1, 3)), int(rng.integers(1, 6))
+    x = _rand(lq, lk, H, D, seed)
+    T = sum(lq)
+    F = rng.integers(-2, 12, size=(n, T + 3)).astype(np.int32)
+    mask = {"func": F}
+    alpha, L = float(rng.uniform(-1.5, 1.5)), float(rng.integers(1, 12))
+    o = _fwd(x, alpha, L, mask)
+    dq, dk, dv = _bwd(x, alpha, L, mask)
+    lst = {k: x[k].tolist() for k in ("q", "k", "v", "do")}
+    cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_k"].tolist()
+    nm = {"func": F.tolist()}
+    o_n = np.array(naive.forward(lst["q"], lst["k"], lst["v"], cq, ck, alpha, L, nm))
+    dq_n, dk_n, dv_n = (np.array(a) for a in
+                        naive.backward(lst["do"], lst["q"], lst["k"], lst["v"], cq, ck, alpha, L, nm))
+    for got, want in ((o, o_n), (dq, dq_n), (dk, dk_n), (dv, dv_n)):
+        np.testing.assert_allclose(got.reshape(want.shape), want, rtol=1e-12, atol=1e-12)
+
+
+def test_func_masks_that_are_windows():
+    """F0 = i + 1 is the causal mask, F0 >= Lk the full mask, and
+    [0, 0) U [i - l, i + r + 1) the window (l, r), exactly."""
+    lq, lk = [9, 1, 14, 0, 6], [9, 3, 16, 2, 6]
+    x = _rand(lq, lk, 2, 5, seed=61)
+    i, klen = _local_rows(x)
+    alpha, L = 0.8, 7.0
+    cases = [(_func(i + 1), True), (_func(klen + 5), False),
+             (_func(np.zeros_like(i), i - 2, i + 2), (2, 1)),
+             (_func(np.zeros_like(i), np.maximum(0, i - 3), i + 1), (3, 0))]
+    for fm, ref in cases:
+        np.testing.assert_array_equal(_fwd(x, alpha, L, fm), _fwd(x, alpha, L, ref))
+        for g, h in zip(_bwd(x, alpha, L, fm), _bwd(x, alpha, L, ref)):
+            np.testing.assert_array_equal(g, h)
+
+
+def test_func_union_inclusion_exclusion():
+    """Outputs are sums over valid pairs, so for A = [0, F0), B = [F1, F2):
+    F(A u B) + F(A n B) = F(A) + F(B); and [0, 5) u [3, 8) = [0, 8)."""
+    lens = [12, 7, 10]
+    x = _rand(lens, lens, 2, 4, seed=62)
+    i, klen = _local_rows(x)
+    alpha, L = 0.7, 6.0
+    f0, f1, f2 = i + 1, np.maximum(0, klen - 4), klen
+    zero = np.zeros_like(i)
+    masks = [_func(f0, f1, f2), _func(zero, np.maximum(zero, f1), np.minimum(f0, f2)),
+             _func(f0), _func(zero, f1, f2)]
+    out = [[_fwd(x, alpha, L, m)] + list(_bwd(x, alpha, L, m)) for m in masks]
+    for a, b, c, d in zip(*out):
+        np.testing.assert_allclose(a + b, c + d, rtol=1e-11, atol=1e-13)
+    assert np.abs(out[0][0] - out[2][0]).max() > 1e-3  # B adds keys past the diagonal
+    five = np.full_like(i, 5)
+    np.testing.assert_array_equal(_fwd(x, alpha, L, _func(five, five - 2, five + 3)),
+                                  _fwd(x, alpha, L, _func(five + 3)))
 
 
 # --------------------------------------------------------------------------
