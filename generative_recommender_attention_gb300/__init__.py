@@ -21,7 +21,8 @@ from __future__ import annotations
 from typing import Optional, Tuple
 
 from ._lib import (HstuError, HSTU_BF16, HSTU_FP16, library, library_path,
-                   workspace_size, last_device_status, selftest_timeout, CTen, Ten)
+                   workspace_size, workspace_size_func, last_device_status, selftest_timeout,
+                   CTen, Ten)
 
 __all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_paged", "workspace_size",
            "last_device_status",
@@ -65,6 +66,18 @@ def _window(causal, window_size):
     if len(w) != 2 or w[0] < -1 or w[1] < -1:
         raise ValueError(f"window_size {window_size}: two bounds, each -1 (none) or >= 0")
     return w
+
+
+def _func_args(func, T_q, device):
+    """(pointer, N, L) of an arbitrary-mask endpoint tensor: int32, (1, N, L)
+    or (N, L), contiguous, N odd, L >= T_q, on the device."""
+    import torch
+    f = func[0] if func.dim() == 3 else func
+    if func.dtype != torch.int32 or f.dim() != 2 or func.device != device:
+        raise ValueError(f"func: int32 (1, N, L) or (N, L) on {device}")
+    if not func.is_contiguous() or f.shape[0] % 2 != 1 or f.shape[1] < T_q:
+        raise ValueError("func: contiguous, N odd, L >= total_q")
+    return func.data_ptr(), int(f.shape[0]), int(f.shape[1])
 
 
 def _scaling(scaling_seqlen):
@@ -114,7 +127,7 @@ def _stream(device):
 def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                   scaling_seqlen: Optional[int] = None, causal: bool = True,
                   alpha: float = 1.0, out=None, workspace=None, window_size=None,
-                  events=None):
+                  events=None, func=None):
     """Forward HSTU attention; returns ``out`` of shape ``q.shape``.
 
     q: (T_q, H, D); k, v: (T_k, H, D); fp16 or bf16 on a CUDA device.
@@ -122,6 +135,8 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     never copied to the host).  ``out`` may be supplied (overwritten).
     ``events``: optional list of 3 torch.cuda.Event recorded before the
     scheduler, after it and after the forward kernel (profiling).
+    ``func``: optional arbitrary-mask endpoints (the page's func_tensor, int32
+    (1, N, L)); it replaces ``causal`` / ``window_size``.
     """
     import torch
     lib = library()
@@ -136,6 +151,18 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     _check_thd("out", out, T_q, H, D, q.dtype, dev)
     win = _window(causal, window_size)
+    if func is not None:
+        fp, fn, fl = _func_args(func, T_q, dev)
+        ws = _workspace(workspace, workspace_size_func(B, T_q, T_k, H, D, max_seqlen_q,
+                                                       max_seqlen_k, False), dev)
+        st = lib.hstu_attn_fwd_func(_cten(q), _cten(k), _cten(v), _ten(out),
+                                    cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, T_k,
+                                    H, D, _dtype_code(q), int(max_seqlen_q), int(max_seqlen_k),
+                                    float(alpha), _scaling(scaling_seqlen), fp, fn, fl,
+                                    ws.data_ptr(), ws.numel(), _stream(dev))
+        if st != 0:
+            raise HstuError(st)
+        return out
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
                                               False), dev)
     args = (_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
@@ -199,7 +226,7 @@ def hstu_attn_fwd_paged(q, paged_kv, page_ids, page_indptrs, cu_seqlens_q, cu_se
 def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, scaling_seqlen: Optional[int] = None,
                   causal: bool = True, alpha: float = 1.0, dq=None, dk=None, dv=None,
-                  workspace=None, window_size=None, events=None) -> Tuple:
+                  workspace=None, window_size=None, events=None, func=None) -> Tuple:
     """Backward HSTU attention; returns ``(dq, dk, dv)``.
 
     Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
@@ -228,6 +255,19 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     _check_thd("dk", dk, T_k, H, D, q.dtype, dev)
     _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
     win = _window(causal, window_size)
+    if func is not None:
+        fp, fn, fl = _func_args(func, T_q, dev)
+        ws = _workspace(workspace, workspace_size_func(B, T_q, T_k, H, D, max_seqlen_q,
+                                                       max_seqlen_k, True), dev)
+        st = lib.hstu_attn_bwd_func(_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq),
+                                    _ten(dk), _ten(dv), cu_seqlens_q.data_ptr(),
+                                    cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
+                                    int(max_seqlen_q), int(max_seqlen_k), float(alpha),
+                                    _scaling(scaling_seqlen), fp, fn, fl, ws.data_ptr(),
+                                    ws.numel(), _stream(dev))
+        if st != 0:
+            raise HstuError(st)
+        return dq, dk, dv
     ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
                                               True), dev)
     args = (_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk), _ten(dv),

@@ -25,7 +25,8 @@ EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_att
            "hstu_attn_workspace_size",
            "hstu_attn_status_string", "hstu_attn_last_device_status",
            "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc",
-           "hstu_attn_fwd_paged")
+           "hstu_attn_fwd_paged", "hstu_attn_fwd_func", "hstu_attn_bwd_func",
+           "hstu_attn_workspace_size_func")
 
 
 class CTen(ctypes.Structure):
@@ -83,6 +84,14 @@ def _declare(lib):
     lib.hstu_attn_fwd_paged.argtypes = [CTen, P, i64, P, P, Ten, P, P, i32, i64, i32, i32,
                                         ctypes.c_int, i32, i32, f32, i32, P, S, P]
     lib.hstu_attn_fwd_paged.restype = ctypes.c_int
+    # the window pair of the regular calls replaced by func, func_n, func_len
+    fscal = scal[:12] + [P, i32, i64] + scal[14:]
+    lib.hstu_attn_fwd_func.argtypes = [CTen, CTen, CTen, Ten] + fscal
+    lib.hstu_attn_fwd_func.restype = ctypes.c_int
+    lib.hstu_attn_bwd_func.argtypes = [CTen, CTen, CTen, CTen, Ten, Ten, Ten] + fscal
+    lib.hstu_attn_bwd_func.restype = ctypes.c_int
+    lib.hstu_attn_workspace_size_func.argtypes = lib.hstu_attn_workspace_size.argtypes
+    lib.hstu_attn_workspace_size_func.restype = S
     lib.hstu_attn_version.argtypes = []
     lib.hstu_attn_version.restype = i32
 
@@ -110,6 +119,18 @@ def workspace_size(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, m
                                            int(max_seqlen_k), int(bool(is_bwd)))
     if n == 0:
         raise ValueError("invalid sizes for hstu_attn_workspace_size")
+    return int(n)
+
+
+def workspace_size_func(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
+                        max_seqlen_k, is_bwd) -> int:
+    """Workspace bytes of a call with an arbitrary (func) mask."""
+    n = library().hstu_attn_workspace_size_func(int(batch), int(total_q), int(total_k),
+                                                int(num_heads), int(head_dim),
+                                                int(max_seqlen_q), int(max_seqlen_k),
+                                                int(bool(is_bwd)))
+    if n == 0:
+        raise ValueError("invalid sizes for hstu_attn_workspace_size_func")
     return int(n)
 
 

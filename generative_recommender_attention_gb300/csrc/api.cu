@@ -191,6 +191,21 @@ bool bwd_layout(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int3
   return true;
 }
 
+// Arbitrary mask: the key hull of every query-block slot, and (backward)
+// the query-block hull of every key-tile slot, appended to the workspace.
+size_t func_extra(int32_t batch, int64_t total_q, int64_t total_k, bool bwd) {
+  const size_t qb = 8 * static_cast<size_t>(total_q / 64 + batch + 1);
+  const size_t kt = bwd ? 8 * static_cast<size_t>(total_k / kBM + batch + 1) : 0;
+  return ((qb + 255) & ~size_t(255)) + kt;
+}
+
+// Arbitrary-mask arguments of a call (func null: none).
+struct FuncArgs {
+  const int32_t* func;
+  int32_t n;
+  int64_t len;
+};
+
 // Shared memory of the scheduler block: one int per cost bucket, then (for
 // up to kSchedCacheSeqs sequences) one 16-byte record per sequence.
 bool sched_smem(int cmax, int batch, const DevInfo& dev, int* bytes, int* cache) {
@@ -242,6 +257,15 @@ size_t hstu_attn_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
   return (L.total + 255) & ~size_t(255);
 }
 
+size_t hstu_attn_workspace_size_func(int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k, int32_t is_bwd) {
+  const size_t base = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim,
+                                               max_seqlen_q, max_seqlen_k, is_bwd);
+  if (base == 0) return 0;
+  return base + func_extra(batch, total_q, total_k, is_bwd != 0);
+}
+
 }  // extern "C"
 
 namespace {
@@ -257,6 +281,27 @@ struct EventMarks {
     return ev == nullptr || i >= n || cudaEventRecord(ev[i], st) == cudaSuccess;
   }
 };
+
+// Validates the arbitrary-mask arguments and builds the device view over
+// the workspace tail that starts at `tail` (bytes into the workspace).
+hstu_status_t func_setup(const FuncArgs* fn, int32_t batch, int64_t total_q, int64_t total_k,
+                         char* ws, size_t tail, bool bwd, Common* c, FuncMask* fm) {
+  *fm = FuncMask{};
+  if (fn == nullptr) return HSTU_OK;
+  if (fn->n < 1 || fn->n % 2 != 1 || fn->len < total_q) return HSTU_ERR_INVALID_ARG;
+  if (batch > 0 && total_q > 0 && fn->func == nullptr) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(fn->func) % 4 != 0) return HSTU_ERR_MISALIGNED;
+  c->win = Window{-1, -1};  // the endpoints decide; the dS blocks use the full layout
+  fm->func = fn->func;
+  fm->n = fn->n;
+  fm->len = fn->len;
+  fm->qb_range = reinterpret_cast<int2*>(ws + tail);
+  if (bwd)
+    fm->kt_range = reinterpret_cast<int2*>(
+        ws + tail + ((8 * static_cast<size_t>(total_q / 64 + batch + 1) + 255) & ~size_t(255)));
+  (void)total_k;
+  return HSTU_OK;
+}
 
 // A paged K/V cache: contiguous (num_pages, 2, 128, H, D) storage and the
 // device page tables.
@@ -274,7 +319,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
                        float alpha, int32_t scaling_seqlen, int32_t window_left,
                        int32_t window_right, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream, const EventMarks& em,
-                       const PagedKV* paged = nullptr) {
+                       const PagedKV* paged = nullptr, const FuncArgs* fn = nullptr) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
@@ -294,10 +339,15 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   }
   if ((s = check_tensor(out.ptr, out.stride_t, out.stride_h, total_q, H, D)) != HSTU_OK) return s;
   if (batch == 0 || total_q == 0) return HSTU_OK;
-  const size_t need =
+  const size_t base_need =
       hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 0);
+  const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, false) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  FuncMask fm;
+  if ((s = func_setup(fn, batch, total_q, total_k, static_cast<char*>(workspace), base_need, false,
+                      &c, &fm)) != HSTU_OK)
+    return s;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
@@ -329,8 +379,13 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
-  sa.header = header; sa.cache_seqs = sched_cache;
+  sa.header = header; sa.cache_seqs = sched_cache; sa.fm = fm;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
+  if (fm.func != nullptr &&
+      launch_func_ranges(cu_seqlens_q, cu_seqlens_k, batch,
+                         static_cast<int>(cdiv(std::max<int32_t>(max_seqlen_q, 1), 64)), fm, stream,
+                         em.pdl()) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   if (launch_sched(1, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
@@ -340,6 +395,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
+  a.fm = fm;
   if (paged != nullptr) {
     a.page_ids = paged->page_ids;
     a.page_indptrs = paged->page_indptrs;
@@ -358,7 +414,8 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
                        int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
                        int32_t scaling_seqlen, int32_t window_left, int32_t window_right,
                        void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em) {
+                       size_t workspace_bytes, cudaStream_t stream, const EventMarks& em,
+                       const FuncArgs* fn = nullptr) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
@@ -375,10 +432,15 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (batch == 0 || (total_q == 0 && total_k == 0)) return HSTU_OK;
   BwdLayout lay;
   if (!bwd_layout(batch, total_q, total_k, H, D, max_seqlen_q, &lay)) return HSTU_ERR_UNSUPPORTED;
-  const size_t need =
+  const size_t base_need =
       hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 1);
+  const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, true) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  FuncMask fm;
+  if ((s = func_setup(fn, batch, total_q, total_k, static_cast<char*>(workspace), base_need, true,
+                      &c, &fm)) != HSTU_OK)
+    return s;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
@@ -415,7 +477,13 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
   sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks); sa.cache_seqs = sched_cache;
+  sa.fm = fm;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
+  if (fm.func != nullptr &&
+      launch_func_ranges(cu_seqlens_q, cu_seqlens_k, batch,
+                         static_cast<int>(cdiv(std::max<int32_t>(max_seqlen_q, 1), 64)), fm, stream,
+                         em.pdl()) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   if (launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
@@ -424,6 +492,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   a.H = H; a.win = c.win; a.d_out = D; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
+  a.fm = fm;
   // dK/dV first: it also stores the dS blocks that the dQ kernel reads
   if (total_k > 0) {
     AttnArgs ak = a;
@@ -576,6 +645,31 @@ bool noalloc_scratch(void** out) {
 }
 
 }  // namespace
+
+extern "C" hstu_status_t hstu_attn_fwd_func(
+    hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int32_t batch, int64_t total_q, int64_t total_k,
+    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype, int32_t max_seqlen_q,
+    int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen, const int32_t* func, int32_t func_n,
+    int64_t func_len, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const FuncArgs fn{func, func_n, func_len};
+  return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, -1, -1,
+                  workspace, workspace_bytes, stream, EventMarks{nullptr, 0}, nullptr, &fn);
+}
+
+extern "C" hstu_status_t hstu_attn_bwd_func(
+    hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t dq, hstu_ten_t dk,
+    hstu_ten_t dv, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+    int64_t total_q, int64_t total_k, int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha, int32_t scaling_seqlen,
+    const int32_t* func, int32_t func_n, int64_t func_len, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream) {
+  const FuncArgs fn{func, func_n, func_len};
+  return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
+                  -1, -1, workspace, workspace_bytes, stream, EventMarks{nullptr, 0}, &fn);
+}
 
 extern "C" hstu_status_t hstu_attn_fwd_paged(
     hstu_cten_t q, const void* paged_kv, int64_t num_pages, const int32_t* page_ids,

@@ -50,6 +50,15 @@ namespace hstu {
 
 namespace {
 
+// First 64-query block a key tile visits (count: U.n): the window's rule, or
+// under an arbitrary mask the hull the scheduler recorded.
+__device__ __forceinline__ int unit_first_qblock(const AttnArgs& a, const UnitInfo& U, int bq) {
+  if (a.fm.func != nullptr) return a.fm.kt_range[kt_slot(U.k0, U.b, U.tile)].x;
+  int m0, cnt;
+  key_tile_queries(U.tile, U.Lq, U.Lk, a.win, bq, m0, cnt);
+  return m0;
+}
+
 // A key tile whose 128 rows all belong to its sequence (and to the tensor)
 // can leave through a TMA store of the whole tile; a ragged last tile is
 // stored row by row, since the box would also cover the next sequence.
@@ -58,7 +67,7 @@ __device__ __forceinline__ bool tile_full(const UnitInfo& U, int64_t total_k) {
   return end <= U.Lk && static_cast<int64_t>(U.k0) + end <= total_k;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FUNC>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -90,6 +99,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
   static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
   static_assert(C::SMEM <= 232448, "shared memory budget");
+  static_assert(CW == 32, "one query per lane in the arbitrary-mask transpose");
   static_assert(BQ == kDsQueries && kBM == kDsKeys && CW % 8 == 0 && CW <= 32,
                 "one stored dS block per half-step");
 
@@ -217,8 +227,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int h = U.hz / SPLIT;
         const int k_row0 = U.k0 + kBM * U.tile;
         const int q_seq0 = U.q0;
-        int m0, nqt;  // the unit's query tiles: m0 .. m0 + U.n - 1
-        key_tile_queries(U.tile, U.Lq, U.Lk, a.win, BQ, m0, nqt);
+        const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
         const int kb = kvi % NKV;
         if constexpr (STAGE) {
           // buffer kb last held the unit before the previous one
@@ -256,8 +265,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                 tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
               }
             }
-            int nm0, nqt;
-            key_tile_queries(nx.tile, nx.Lq, nx.Lk, a.win, BQ, nm0, nqt);
+            const int nm0 = unit_first_qblock(a, nx, BQ);
             prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
           }
           const int s = qi % NS;
@@ -442,8 +450,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (out_rows(U, dvrow, dkrow)) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
         continue;
       }
-      int m0, nqt;  // the unit's query tiles: m0 .. m0 + U.n - 1
-      key_tile_queries(U.tile, Lq, Lk, a.win, BQ, m0, nqt);
+      const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
+      constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
       // valid queries of this key row: lo <= i < hi; every key row of the
       // warp is seen by queries [lo_all, hi_all)
       const int lo = a.win.right < 0 ? 0 : j - a.win.right;
@@ -465,7 +473,22 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         // valid queries of this warp's columns (bit e: query ic + e), the run
         // of bits [lo - ic, hi - ic) clamped to [0, CW)
         uint32_t valid = CW == 32 ? 0xffffffffu : (1u << CW) - 1u;
-        if (need_mask) {
+        if constexpr (func) {
+          // arbitrary mask: lane l forms query ic + l's valid keys among the
+          // warp's 32 key rows from its endpoints; 32 ballots transpose them
+          // into each key row's valid queries
+          const int jw = j_warp_last - 31, iq = ic + lane;
+          const uint32_t mq = iq < Lq ? static_cast<uint32_t>(func_row_bits(
+                                            a.fm, static_cast<int64_t>(U.q0) + iq, jw, Lk))
+                                      : 0u;
+          uint32_t mine = 0;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const uint32_t col = __ballot_sync(0xffffffffu, (mq >> k) & 1u);
+            if (lane == k) mine = col;
+          }
+          valid = mine;
+        } else if (need_mask) {
           const int e0 = min(max(lo - ic, 0), CW), e1 = min(max(hi - ic, 0), CW);
           const uint32_t below_e1 = e1 >= 32 ? 0xffffffffu : (1u << e1) - 1u;
           const uint32_t below_e0 = e0 >= 32 ? 0xffffffffu : (1u << e0) - 1u;
@@ -541,11 +564,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   }
 }
 
-template <int D, bool BF16>
-cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
+template <int D, bool BF16, bool FUNC>
+cudaError_t launch_dkdv_f(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tdk,
                           const CUtensorMap& tdv, const AttnArgs& a) {
-  auto kern = hstu_bwd_dkdv_kernel<D, BF16>;
+  auto kern = hstu_bwd_dkdv_kernel<D, BF16, FUNC>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -555,6 +578,17 @@ cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap
   }
   return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, tdk,
                      tdv, a);
+}
+
+// The arbitrary-mask path (its endpoint loads and ballot transpose) is a
+// separate instantiation, so that the window kernels keep their registers.
+template <int D, bool BF16>
+cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                          const CUtensorMap& tdv, const AttnArgs& a) {
+  if (a.fm.func != nullptr)
+    return launch_dkdv_f<D, BF16, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
+  return launch_dkdv_f<D, BF16, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
 }
 
 }  // namespace

@@ -151,7 +151,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int h = U.hz;
         const int q_row0 = U.q0 + kBM * U.tile;
         int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
-        query_tile_keys(U.tile, U.Lq, U.Lk, a.win, BN, kt0, nkt);
+        if (a.fm.func != nullptr)
+          kt0 = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq).x / BN;
+        else
+          query_tile_keys(U.tile, U.Lq, U.Lk, a.win, BN, kt0, nkt);
         const int kv_row0 = U.k0 + BN * kt0;
         // Paged K/V: key tile kt lives in page page_ids[page_indptrs[b] +
         // kt BN / 128], whose K rows start at row 256 p and V rows at
@@ -291,7 +294,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int i = kBM * U.tile + r;
       const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
       int kt0, nkt;
-      query_tile_keys(U.tile, U.Lq, Lk, a.win, BN, kt0, nkt);
+      const bool func = a.fm.func != nullptr;
+      if (func)
+        kt0 = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq).x / BN;
+      else
+        query_tile_keys(U.tile, U.Lq, Lk, a.win, BN, kt0, nkt);
+      const int64_t t_row = static_cast<int64_t>(U.q0) + (i < U.Lq ? i : 0);  // func row (any, if past Lq)
       // valid keys of this row: lo <= j < hi; every row of the warp sees
       // [lo_all, hi_all)
       const int lo = a.win.left < 0 ? 0 : i - a.win.left;
@@ -310,7 +318,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint32_t x[64];
           tmem_ld64(tS + sb * BN + 64 * c, x);
           uint32_t p[32];
-          if (!need_mask) {
+          if (func) {
+            // arbitrary mask: this row's valid keys of the chunk, from its endpoints
+            const uint64_t fb = func_row_bits(a.fm, t_row, jc, Lk);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t s0 = ((fb >> (2 * e)) & 1ull) ? x[2 * e] : 0u;
+              const uint32_t s1 = ((fb >> (2 * e + 1)) & 1ull) ? x[2 * e + 1] : 0u;
+              p[e] = silu_pair<BF16>(s0, s1, half_alpha);
+            }
+          } else if (!need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
           } else if (jc >= lo_all) {

@@ -81,11 +81,61 @@ __host__ __device__ inline void key_tile_queries(int s, int Lq, int Lk, Window w
   count = (c1 > c0 && i1 > i0) ? (i1 + bq - 1) / bq - first : 0;
 }
 
+// ---------------------------------------------------------------- arbitrary mask
+// func_tensor ("Mask support"): query token t's valid keys are the union
+// [0, F0) U [F1, F2) U ... of its N endpoints F_n = func[n * len + t] (N odd,
+// local key indices), cut to j < Lk.  Units iterate the contiguous hull of
+// the tiles their rows can see, and the exact predicate is applied inside:
+//   qb_range[qb_slot(b, m)]: {kmin, kmax}, the key hull of 64-row query block
+//     m of sequence b (kmin >= kmax: no key), written by the range kernel;
+//   kt_range[kt_slot(b, s)]: {first query block, count}, the hull of the
+//     query blocks whose key hull meets 128-key tile s, written by the
+//     scheduler.
+// Slots are floor(offset / tile) + b + index, disjoint between sequences
+// without a scan (floor((o + L) / n) + 1 >= floor(o / n) + ceil(L / n)).
+struct FuncMask {
+  const int32_t* func;  // null: no arbitrary mask (the window decides)
+  int n;
+  int64_t len;
+  int2* qb_range;
+  int2* kt_range;
+};
+__host__ __device__ inline int qb_slot(int q0, int b, int m) { return q0 / 64 + b + m; }
+__host__ __device__ inline int kt_slot(int k0, int b, int s) { return k0 / kBM + b + s; }
+// Key hull of 128-row query tile t from its two blocks' hulls.
+__device__ inline int2 func_tile_keys(const FuncMask& f, int q0, int b, int t, int Lq) {
+  const int2 a = f.qb_range[qb_slot(q0, b, 2 * t)];
+  int2 h = a;
+  if (kBM * t + 64 < Lq) {
+    const int2 c = f.qb_range[qb_slot(q0, b, 2 * t + 1)];
+    if (c.x < c.y) h = a.x < a.y ? make_int2(imin(a.x, c.x), imax(a.y, c.y)) : c;
+  }
+  return h;
+}
+
+// Bits [lo - base, hi - base) of an n-bit word (n = 32 or 64), clamped.
+__device__ __forceinline__ uint64_t bit_range64(int lo, int hi, int base) {
+  const int e0 = imin(imax(lo - base, 0), 64), e1 = imin(imax(hi - base, 0), 64);
+  if (e1 <= e0) return 0;
+  const uint64_t below1 = e1 >= 64 ? ~0ull : (1ull << e1) - 1;
+  return below1 & ~((1ull << e0) - 1);
+}
+// Arbitrary mask: valid keys of query token t among keys [base, base + 64),
+// cut to j < Lk, as bits (bit e: key base + e).
+__device__ __forceinline__ uint64_t func_row_bits(const FuncMask& f, int64_t t, int base, int Lk) {
+  uint64_t m = bit_range64(0, imin(__ldg(f.func + t), Lk), base);
+  for (int n = 1; n + 1 < f.n; n += 2)
+    m |= bit_range64(__ldg(f.func + n * f.len + t), imin(__ldg(f.func + (n + 1) * f.len + t), Lk),
+                     base);
+  return m;
+}
+
 struct SchedArgs {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int B, H;
   Window win;
+  FuncMask fm;               // arbitrary mask (fm.func null: none)
   int bn_a, cmax_a, cap_a;   // list A: query tiles, inner tiles of bn_a keys
   int4* units_a;
   int bq_b, split_b, cmax_b, cap_b;  // list B: key tiles, inner tiles of bq_b queries
@@ -151,6 +201,7 @@ struct AttnArgs {
   int64_t o1_st, o1_sh;
   int d_out;            // output columns per head: the kernel's D, or 32 when a
                         // head dimension of 32 runs zero-padded through the D = 64 kernels
+  FuncMask fm;              // arbitrary mask (fm.func null: the window decides)
   const int* page_ids;      // forward over a paged K/V cache: page of each 128-key block
   const int* page_indptrs;  //   and each sequence's first entry in page_ids; null: contiguous K/V
   void* ds;             // backward: dS blocks (written by dK/dV, read by dQ)
@@ -214,6 +265,10 @@ static_assert(FwdCfg<64>::SMEM <= 232448 && DqCfg<64>::SMEM <= 232448 &&
               "smem");
 
 __global__ void hstu_sched_kernel(SchedArgs a);
+// Arbitrary mask: key hull of every 64-row query block (grid: blocks of 8
+// query blocks x sequences; one warp per query block).
+cudaError_t launch_func_ranges(const int32_t* cu_q, const int32_t* cu_k, int B, int max_qb,
+                               const FuncMask& fm, cudaStream_t st, bool pdl);
 // Scheduler launch: `lists` blocks (1: list A only, 2: lists A and B).
 cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a);
 

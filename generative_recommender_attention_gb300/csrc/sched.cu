@@ -16,6 +16,8 @@
 // whatever the atomics give; it only changes timing, never results.  For the
 // backward, the list-B block also writes ds_base: the first stored dS block
 // of every sequence (an exclusive scan of H * ds_blocks_head over them).
+#include <climits>
+
 #include "kernels.h"
 
 namespace hstu {
@@ -31,16 +33,38 @@ __device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
 }
 
 // Cost of query tile t (list A).
-__device__ __forceinline__ int cost_a(const SchedArgs& a, int t, int Lq, int Lk) {
+__device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t) {
   int first, n;
-  query_tile_keys(t, Lq, Lk, a.win, a.bn_a, first, n);
+  if (a.fm.func != nullptr) {  // arbitrary mask: the tile's key hull
+    const int2 h = func_tile_keys(a.fm, sq.x, b, t, sq.y);
+    first = h.x / a.bn_a;
+    return h.x < h.y ? (h.y + a.bn_a - 1) / a.bn_a - first : 0;
+  }
+  query_tile_keys(t, sq.y, sq.w, a.win, a.bn_a, first, n);
   return n;
 }
 
+// Arbitrary mask: the hull [first, first + count) of the 64-row query
+// blocks whose key hull meets 128-key tile s.
+__device__ __forceinline__ int2 func_key_tile_queries(const SchedArgs& a, int4 sq, int b, int s) {
+  const int c0 = kBM * s, c1 = min(kBM * s + kBM, sq.w);
+  const int n_qb = ceil_div(sq.y, 64);
+  int m0 = n_qb, m1 = 0;
+  for (int m = 0; m < n_qb; ++m) {
+    const int2 h = a.fm.qb_range[qb_slot(sq.x, b, m)];
+    if (h.x < h.y && h.x < c1 && h.y > c0) {
+      m0 = min(m0, m);
+      m1 = m + 1;
+    }
+  }
+  return m1 > m0 ? make_int2(m0, m1 - m0) : make_int2(0, 0);
+}
+
 // Cost of key tile s (list B).
-__device__ __forceinline__ int cost_b(const SchedArgs& a, int s, int Lq, int Lk) {
+__device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int b, int s) {
+  if (a.fm.func != nullptr) return func_key_tile_queries(a, sq, b, s).y;  // bq_b == 64
   int first, n;
-  key_tile_queries(s, Lq, Lk, a.win, a.bq_b, first, n);
+  key_tile_queries(s, sq.y, sq.w, a.win, a.bq_b, first, n);
   return n;
 }
 
@@ -126,7 +150,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int Lq = sq.y, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, t, Lq, Lk) : cost_a(a, t, Lq, Lk);
+      const int cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t);
       atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
@@ -156,7 +180,14 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, t, Lq, Lk) : cost_a(a, t, Lq, Lk);
+      int cost;
+      if (list_b && a.fm.func != nullptr) {  // also record the key tile's query hull
+        const int2 r = func_key_tile_queries(a, sq, b, t);
+        a.fm.kt_range[kt_slot(k0, b, t)] = r;
+        cost = r.y;
+      } else {
+        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t);
+      }
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       for (int e = 0; e < per_tile; ++e) {
         if (pos + e < cap) {
@@ -194,6 +225,51 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
       if (all > a.ds_cap || all < 0) atomicExch(a.header + kHdrOverflowB, 1);
     }
   }
+}
+
+// Arbitrary mask: one warp per 64-row query block; each lane takes two rows,
+// forms each row's key hull from its endpoints (every interval cut to
+// [0, Lk)), and the warp reduces the 64 hulls to the block's.
+__global__ void __launch_bounds__(256) hstu_func_ranges_kernel(const int32_t* cu_q,
+                                                               const int32_t* cu_k, FuncMask fm) {
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * 8 + warp;
+  // the previous grid of the stream may still read this workspace
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  const int q0 = __ldg(cu_q + b), Lq = __ldg(cu_q + b + 1) - q0;
+  const int Lk = __ldg(cu_k + b + 1) - __ldg(cu_k + b);
+  if (64 * m >= Lq) return;
+  int lo = INT_MAX, hi = INT_MIN;
+  for (int rr = 0; rr < 2; ++rr) {
+    const int i = 64 * m + 32 * rr + lane;
+    if (i >= Lq) continue;
+    const int64_t t = static_cast<int64_t>(q0) + i;
+    const int f0 = min(__ldg(fm.func + t), Lk);  // [0, F0)
+    if (f0 > 0) { lo = 0; hi = max(hi, f0); }
+    for (int n = 1; n + 1 < fm.n; n += 2) {
+      const int a = max(__ldg(fm.func + n * fm.len + t), 0);
+      const int c = min(__ldg(fm.func + (n + 1) * fm.len + t), Lk);
+      if (a < c) { lo = min(lo, a); hi = max(hi, c); }
+    }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) fm.qb_range[qb_slot(q0, b, m)] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
+}
+
+cudaError_t launch_func_ranges(const int32_t* cu_q, const int32_t* cu_k, int B, int max_qb,
+                               const FuncMask& fm, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>((max_qb + 7) / 8), static_cast<unsigned>(B));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, hstu_func_ranges_kernel, cu_q, cu_k, fm);
 }
 
 cudaError_t launch_sched(int lists, int smem, cudaStream_t st, bool pdl, const SchedArgs& a) {

@@ -147,6 +147,49 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
                             cudaStream_t stream);
 
 /*
+ * Arbitrary mask (page "HSTU Attention (Blackwell SM100/SM103)", section
+ * "Mask support", func_tensor): forward and backward with the same arguments
+ * as hstu_attn_fwd / hstu_attn_bwd, the window replaced by
+ *   func: device int32 endpoints, row n of query token t at
+ *     func[n * func_len + t] (the page's (1, N, L) tensor); func_n = N, odd,
+ *     >= 1; func_len = L >= total_q (the page's 256 padding columns are
+ *     accepted and unused).  Query token t's valid keys are
+ *     [0, F0) U [F1, F2) U [F3, F4) ... of its endpoints F_n (key indices
+ *     local to the sequence; intervals may overlap or come in any order),
+ *     cut to the sequence's keys.  Values are trusted and never copied to
+ *     the host.
+ *   workspace: hstu_attn_workspace_size_func(...) bytes (the regular size
+ *     plus the per-tile key and query ranges the library derives from the
+ *     endpoints on every call, so in-place changes of func are seen, also
+ *     under CUDA graph replay).
+ * Each unit visits the hull of the tiles its rows can see and applies the
+ * exact predicate inside it.  Errors as for hstu_attn_fwd/_bwd, plus
+ * HSTU_ERR_INVALID_ARG for an even or non-positive func_n or
+ * func_len < total_q, HSTU_ERR_MISALIGNED for a func pointer that is not
+ * 4-byte aligned.
+ */
+size_t hstu_attn_workspace_size_func(int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k, int32_t is_bwd);
+hstu_status_t hstu_attn_fwd_func(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                 int32_t batch, int64_t total_q, int64_t total_k,
+                                 int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                 int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                 int32_t scaling_seqlen, const int32_t* func, int32_t func_n,
+                                 int64_t func_len, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+hstu_status_t hstu_attn_bwd_func(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                                 hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                 int32_t batch, int64_t total_q, int64_t total_k,
+                                 int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                 int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                 int32_t scaling_seqlen, const int32_t* func, int32_t func_n,
+                                 int64_t func_len, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * Forward over a paged K/V cache (page "HSTU Attention (Blackwell
  * SM100/SM103)", section "Mask support", paged-KV paragraph; the page's
  * paged path is causal only and has no backward, and so has this one).

@@ -26,7 +26,11 @@ def to_dev(x, device="cuda"):
 
 
 def mask_kwargs(causal):
-    """Binding keywords of a mask given as a bool or a (left, right) window."""
+    """Binding keywords of a mask given as a bool, a (left, right) window or
+    {"func": (N, L) int32 endpoints} (an arbitrary mask)."""
+    if isinstance(causal, dict):
+        f = torch.as_tensor(np.ascontiguousarray(causal["func"]), dtype=torch.int32)
+        return {"func": f[None].contiguous().cuda()}
     if isinstance(causal, tuple):
         return {"window_size": causal}
     return {"causal": bool(causal)}

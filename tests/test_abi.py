@@ -186,6 +186,28 @@ def test_paged_argument_errors(lib):
     assert _call_paged(lib, batch=0) == OK
 
 
+def _call_fwd_func(lib, **over):
+    a = dict(func=0x80000, n=3, L=100, batch=2, D=64, ws_bytes=1 << 20)
+    a.update(over)
+    t = L.CTen(0x10000, 256, 64)
+    return lib.hstu_attn_fwd_func(t, t, t, L.Ten(0x40000, 256, 64), 0x50000, 0x60000,
+                                  a["batch"], 100, 100, 4, a["D"], L.HSTU_BF16, 60, 60, 0.125,
+                                  0, a["func"], a["n"], a["L"], 0x70000, a["ws_bytes"], None)
+
+
+def test_func_argument_errors(lib):
+    assert _call_fwd_func(lib, n=2) == INVALID          # N must be odd
+    assert _call_fwd_func(lib, n=0) == INVALID
+    assert _call_fwd_func(lib, L=99) == INVALID         # L >= total_q
+    assert _call_fwd_func(lib, func=None) == INVALID
+    assert _call_fwd_func(lib, func=0x80002) == MISALIGNED
+    assert _call_fwd_func(lib, D=48) == UNSUPPORTED
+    need = lib.hstu_attn_workspace_size_func(2, 100, 100, 4, 64, 60, 60, 0)
+    assert need > lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 60, 60, 0)
+    assert _call_fwd_func(lib, ws_bytes=need - 1) == INVALID
+    assert _call_fwd_func(lib, batch=0) == OK
+
+
 def test_selftest_argument_errors(lib):
     assert lib.hstu_attn_selftest_timeout(None, 1000, None) == INVALID
     assert lib.hstu_attn_selftest_timeout(0x70000, 0, None) == INVALID

@@ -5,6 +5,7 @@ stride leave gaps between logical elements, extra rows follow the last
 sequence, and guard rows sit before and after the tensor.  After the forward
 and backward calls, every byte outside the logical outputs must still hold the
 sentinel, and every logical element must have been written."""
+import numpy as np
 import pytest
 import torch
 
@@ -40,7 +41,7 @@ def _guarded(T, H, D, dtype, extra_rows=3, pad_h=8, pad_t=16, guard=64):
 @pytest.mark.parametrize("D,dtype,causal", [(64, torch.bfloat16, True), (128, torch.float16, False),
                                             (256, torch.bfloat16, True),
                                             (128, torch.bfloat16, (100, 20)),
-                                            (32, torch.float16, True)])
+                                            (32, torch.float16, True), (128, torch.bfloat16, "func")])
 def test_no_write_outside_logical_outputs(D, dtype, causal):
     lens = [129, 1, 300, 0, 64]
     H = 2
@@ -52,6 +53,10 @@ def test_no_write_outside_logical_outputs(D, dtype, causal):
     pad = lambda t: torch.cat([t, torch.zeros(3, H, D, dtype=dtype, device="cuda")])  # noqa
     q, k, v, do = pad(dev["q"]), pad(dev["k"]), pad(dev["v"]), pad(dev["do"])
     bufs = [_guarded(T, H, D, dtype) for _ in range(4)]
+    if causal == "func":  # causal plus the last 5 keys of each sequence
+        i = np.concatenate([np.arange(L) for L in lens] + [np.zeros(3, np.int64)])
+        lk = np.concatenate([np.full(L, L) for L in lens] + [np.zeros(3, np.int64)])
+        causal = {"func": np.stack([i + 1, lk - 5, lk]).astype(np.int32)}
     mk = mask_kwargs(causal)
     o = hstu.hstu_attn_fwd(q, k, v, dev["cu_seqlens_q"], dev["cu_seqlens_k"], 300, 300,
                            alpha=0.1, out=bufs[0][1], **mk)

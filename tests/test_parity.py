@@ -85,6 +85,62 @@ def test_window_recsys_sampled():
     sampled_compare(x, w.scaling_seqlen, (256, 0), w.alpha, n_random=96)
 
 
+# ------------------------------------------------------------------ arbitrary (func) masks
+def _local(x):
+    cq, ck = x["cu_seqlens_q"].tolist(), x["cu_seqlens_k"].tolist()
+    T = cq[-1]
+    i, lk = np.zeros(T, np.int64), np.zeros(T, np.int64)
+    for b in range(len(cq) - 1):
+        i[cq[b]:cq[b + 1]] = np.arange(cq[b + 1] - cq[b])
+        lk[cq[b]:cq[b + 1]] = ck[b + 1] - ck[b]
+    return i, lk
+
+
+def _func_mask(kind, x, seed=0, pad=256):
+    """Endpoint patterns: causal with the last 8 keys as targets; a band with
+    a hole; random endpoints (N = 5)."""
+    i, lk = _local(x)
+    rng = np.random.default_rng(seed)
+    if kind == "causal_targets":
+        rows = [i + 1, lk - 8, lk]
+    elif kind == "band_hole":
+        rows = [np.minimum(i + 1, 64), np.maximum(0, i - 200), np.maximum(0, i - 100),
+                np.maximum(0, i - 40), i + 30]
+    else:
+        rows = [rng.integers(-50, int(lk.max()) + 50, size=i.shape[0]) for _ in range(5)]
+    F = np.stack([np.asarray(r) for r in rows]).astype(np.int32)
+    return {"func": np.concatenate([F, np.zeros((F.shape[0], pad), np.int32)], axis=1)}
+
+
+@pytest.mark.parametrize("D,dtype", [(32, torch.float16), (64, torch.bfloat16),
+                                     (128, torch.float16), (256, torch.bfloat16)])
+@pytest.mark.parametrize("kind", ["causal_targets", "band_hole", "random"])
+def test_func_masks(D, dtype, kind):
+    x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, D, dtype, seed=D + len(kind))
+    full_compare(x, None, _func_mask(kind, x, seed=D), 1.0 / math.sqrt(D))
+
+
+def test_func_mask_equal_to_causal_is_bitwise_causal():
+    x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, 128, torch.bfloat16, seed=5)
+    i, _ = _local(x)
+    fm = {"func": np.concatenate([(i + 1)[None].astype(np.int32), np.zeros((1, 3), np.int32)], 1)}
+    xd = to_dev(x)
+    a = gpu_fwd_bwd(xd, None, fm, 0.09)
+    b = gpu_fwd_bwd(xd, None, True, 0.09)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_func_mask_recsys_sampled():
+    """The recsys workload with causal attention plus the last 16 keys of
+    every sequence as targets."""
+    w = _ws("recsys")
+    x = workloads.make_inputs(w, seed=0)
+    i, lk = _local(x)
+    fm = {"func": np.stack([i + 1, lk - 16, lk]).astype(np.int32)}
+    sampled_compare(x, w.scaling_seqlen, fm, w.alpha, n_random=96)
+
+
 # ------------------------------------------------------------------ paged K/V forward
 def _paged_cache(x, n_extra, seed, garbage=1e3):
     """Scatter x's K/V into shuffled 128-row pages (plus unused pages); rows
