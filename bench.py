@@ -47,8 +47,16 @@ def peaks():
 
 
 def pairs(lengths, H, causal):
-    """Attended (query, key) pairs times heads; ``causal`` is a bool or a
-    (left, right) token window (-1: unbounded side), Lq = Lk per sequence."""
+    """Attended (query, key) pairs times heads; ``causal`` is a bool, a
+    (left, right) token window (-1: unbounded side), or ("targets", n): causal
+    plus the last n keys of the sequence; Lq = Lk per sequence."""
+    if isinstance(causal, tuple) and causal[0] == "targets":
+        n = 0
+        for L in lengths:
+            i = np.arange(L, dtype=np.int64)
+            extra = np.maximum(0, L - np.maximum(i + 1, L - causal[1]))  # target keys past i
+            n += int((i + 1).sum() + extra.sum())
+        return H * n
     if isinstance(causal, tuple):
         left, right = causal
         n = 0
@@ -67,7 +75,9 @@ def workload_config(w, lengths, mask=None):
     d = w.describe()
     d["T"] = int(sum(lengths))
     d["max_seqlen"] = int(max(lengths))
-    if mask is not None and isinstance(mask, tuple):
+    if mask is not None and isinstance(mask, tuple) and mask[0] == "targets":
+        d["mask"] = f"func_tensor: causal plus the last {mask[1]} keys of each sequence"
+    elif mask is not None and isinstance(mask, tuple):
         d["mask"] = f"window {mask}"
     d["N_pairs"] = int(pairs(lengths, w.heads, w.causal if mask is None else mask))
     return d
@@ -141,8 +151,13 @@ def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0, mask=
         sub = {k: x[k][s0:s1].double().numpy() for k in ("q", "k", "v", "do")}
         c1 = np.array([0, s1 - s0], dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.fwd(sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, mask, threads)
-        oracle.bwd(sub["do"], sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, mask,
+        om = mask
+        if isinstance(mask, tuple) and mask[0] == "targets":  # the sequence's endpoint rows
+            i = np.arange(s1 - s0)
+            om = {"func": np.stack([i + 1, np.full_like(i, s1 - s0 - mask[1]),
+                                    np.full_like(i, s1 - s0)]).astype(np.int32)}
+        oracle.fwd(sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, om, threads)
+        oracle.bwd(sub["do"], sub["q"], sub["k"], sub["v"], c1, c1, w.alpha, L_scale, om,
                    threads)
         secs += time.perf_counter() - t0
         flops += 14.0 * D * pairs([s1 - s0], w.heads, mask)
@@ -270,6 +285,9 @@ def main():
                     help="launch every step through the Python binding instead of replaying a "
                          "CUDA graph of it")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--func-targets", type=int, default=None,
+                    help="arbitrary (func_tensor) mask: causal plus the last N keys of every "
+                         "sequence as targets")
     ap.add_argument("--paged", action="store_true",
                     help="time the causal forward over a paged K/V cache (the workload's keys "
                          "in shuffled 128-row pages) beside the contiguous forward; one JSON line")
@@ -282,6 +300,8 @@ def main():
     if args.window:
         left, right = (int(v) for v in args.window.split(","))
         args.mask = (left, right)
+    if args.func_targets is not None:
+        args.mask = ("targets", int(args.func_targets))
 
     import torch
     from generative_recommender_attention_gb300 import workloads
@@ -323,6 +343,11 @@ def main():
     kw = dict(scaling_seqlen=w.scaling_seqlen, alpha=w.alpha)
     if args.mask is None:
         kw["causal"] = w.causal
+    elif args.mask[0] == "targets":
+        i = np.concatenate([np.arange(L) for L in lengths])
+        lk = np.concatenate([np.full(L, L) for L in lengths])
+        kw["func"] = torch.from_numpy(
+            np.stack([i + 1, lk - args.mask[1], lk]).astype(np.int32))[None].contiguous().to(dev)
     else:
         kw["window_size"] = args.mask
     flush = None if args.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
