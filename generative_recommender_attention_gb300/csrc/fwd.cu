@@ -39,7 +39,7 @@ namespace hstu {
 
 namespace {
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FUNC>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int i = kBM * U.tile + r;
       const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
       int kt0, nkt;
-      const bool func = a.fm.func != nullptr;
+      constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
       if (func)
         kt0 = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq).x / BN;
       else
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint32_t x[64];
           tmem_ld64(tS + sb * BN + 64 * c, x);
           uint32_t p[32];
-          if (func) {
+          if constexpr (func) {
             // arbitrary mask: this row's valid keys of the chunk, from its endpoints
             const uint64_t fb = func_row_bits(a.fm, t_row, jc, Lk);
 #pragma unroll
@@ -411,10 +411,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-template <int D, bool BF16>
-cudaError_t launch_fwd_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq, const CUtensorMap& tk,
+template <int D, bool BF16, bool FUNC>
+cudaError_t launch_fwd_f(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const AttnArgs& a) {
-  auto kern = hstu_fwd_kernel<D, BF16>;
+  auto kern = hstu_fwd_kernel<D, BF16, FUNC>;
   static bool attr_set = false;  // benign race: setting the attribute twice is harmless
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -423,6 +423,15 @@ cudaError_t launch_fwd_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap&
     attr_set = true;
   }
   return launch_attn(kern, grid, kAttnThreads, FwdCfg<D>::SMEM, st, pdl, tq, tk, tv, a);
+}
+
+// The arbitrary-mask SiLU path is a separate instantiation, so that the
+// window kernels keep their code size and registers.
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const AttnArgs& a) {
+  if (a.fm.func != nullptr) return launch_fwd_f<D, BF16, true>(grid, st, pdl, tq, tk, tv, a);
+  return launch_fwd_f<D, BF16, false>(grid, st, pdl, tq, tk, tv, a);
 }
 
 }  // namespace
