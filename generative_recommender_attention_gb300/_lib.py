@@ -26,7 +26,8 @@ EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_att
            "hstu_attn_status_string", "hstu_attn_last_device_status",
            "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc",
            "hstu_attn_fwd_paged", "hstu_attn_fwd_func", "hstu_attn_bwd_func",
-           "hstu_attn_workspace_size_func")
+           "hstu_attn_workspace_size_func", "hstu_lmsd_fwd", "hstu_lmsd_bwd",
+           "hstu_lmsd_bwd_workspace_size")
 
 
 class CTen(ctypes.Structure):
@@ -92,6 +93,16 @@ def _declare(lib):
     lib.hstu_attn_bwd_func.restype = ctypes.c_int
     lib.hstu_attn_workspace_size_func.argtypes = lib.hstu_attn_workspace_size.argtypes
     lib.hstu_attn_workspace_size_func.restype = S
+    # LMSD (include/hstu_lmsd.h)
+    i8p = P
+    lib.hstu_lmsd_fwd.argtypes = [P, i64, P, i64, P, P, i64, i32, f32, f32, i32, i32, i32, i64,
+                                  P, P, P, i8p, P]
+    lib.hstu_lmsd_fwd.restype = ctypes.c_int
+    lib.hstu_lmsd_bwd_workspace_size.argtypes = [i64, i32]
+    lib.hstu_lmsd_bwd_workspace_size.restype = S
+    lib.hstu_lmsd_bwd.argtypes = [P, i64, P, i64, P, i64, P, P, P, P, i8p, i64, i32, f32, i32, i32,
+                                  i32, i32, P, i64, P, i64, P, P, P, S, P]
+    lib.hstu_lmsd_bwd.restype = ctypes.c_int
     lib.hstu_attn_version.argtypes = []
     lib.hstu_attn_version.restype = i32
 

@@ -11,7 +11,7 @@ from generative_recommender_attention_gb300 import _lib as L
 from generative_recommender_attention_gb300 import build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "hstu_attn.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("hstu_attn.h", "hstu_lmsd.h")]
 
 OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
 
@@ -23,9 +23,9 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(hstu_attn_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(hstu_(?:attn|lmsd)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_exports():
@@ -206,6 +206,29 @@ def test_func_argument_errors(lib):
     assert need > lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 60, 60, 0)
     assert _call_fwd_func(lib, ws_bytes=need - 1) == INVALID
     assert _call_fwd_func(lib, batch=0) == OK
+
+
+def _lmsd_fwd(lib, **over):
+    a = dict(x=0x10000, xs=128, u=0x20000, us=128, w=0x30000, b=0x30100, n=10, d=128, eps=1e-5,
+             p=0.1, mask=0x50000, y=0x40000)
+    a.update(over)
+    return lib.hstu_lmsd_fwd(a["x"], a["xs"], a["u"], a["us"], a["w"], a["b"], a["n"], a["d"],
+                             a["eps"], a["p"], 1, 1, 1, 7, a["y"], 0x60000, 0x61000, a["mask"],
+                             None)
+
+
+def test_lmsd_argument_errors(lib):
+    assert _lmsd_fwd(lib, d=12) == UNSUPPORTED      # D multiple of 8
+    assert _lmsd_fwd(lib, d=1024) == UNSUPPORTED    # D < 1024
+    assert _lmsd_fwd(lib, p=1.0) == INVALID
+    assert _lmsd_fwd(lib, p=-0.1) == INVALID
+    assert _lmsd_fwd(lib, eps=0.0) == INVALID
+    assert _lmsd_fwd(lib, xs=100) == INVALID        # stride < D
+    assert _lmsd_fwd(lib, x=0x10008) == MISALIGNED
+    assert _lmsd_fwd(lib, mask=None) == INVALID     # dropout needs the mask
+    assert _lmsd_fwd(lib, n=0) == OK
+    assert lib.hstu_lmsd_bwd_workspace_size(1000, 128) > 0
+    assert lib.hstu_lmsd_bwd_workspace_size(1000, 7) == 0
 
 
 def test_selftest_argument_errors(lib):
