@@ -166,6 +166,71 @@ def oracle_sample(x, w, budget_s: float, start: int = 0, threads: int = 0, mask=
     return flops, secs, n, threads
 
 
+def run_lmsd(args, dev):
+    """--lmsd N,D: HBM throughput of the LMSD forward and backward (the op is
+    bandwidth-bound), with the bytes each call must move counted from the
+    tensors: forward reads x, u (and weight, bias) and writes y (3 segments),
+    mask, mean, rstd; backward reads dy, x, u, mask, mean, rstd and writes dx,
+    du (the column partials add 2 D floats per block)."""
+    import torch
+    from generative_recommender_attention_gb300 import lmsd
+    n, d = (int(v) for v in args.lmsd.split(","))
+    g = torch.Generator(device="cpu").manual_seed(0)
+    x = torch.randn(n, d, generator=g).to(torch.bfloat16).to(dev)
+    u = torch.randn(n, d, generator=g).to(torch.bfloat16).to(dev)
+    wt = torch.randn(d, generator=g).to(torch.bfloat16).to(dev)
+    bs = torch.randn(d, generator=g).to(torch.bfloat16).to(dev)
+    p = 0.1
+    out = lmsd.hstu_lmsd_forward(x, u, wt, bs, dropout_ratio=p, seed=1)
+    dy = torch.randn(out["y_tensor"].shape, generator=g).to(torch.bfloat16).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        lmsd.hstu_lmsd_forward(x, u, wt, bs, dropout_ratio=p, seed=1)
+
+    def bwd():
+        lmsd.hstu_lmsd_backward(dy, x, u, wt, bs, out["mean_tensor"], out["rstd_tensor"],
+                                out["mask_tensor"], dropout_ratio=p)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    ms_f, ms_b = timed(fwd), timed(bwd)
+    bytes_f = n * d * 2 * 2 + n * 3 * d * 2 + n * d + n * 8
+    bytes_b = n * 3 * d * 2 + n * d * 2 * 2 + n * d + n * 8 + n * d * 2 * 2
+    pk = peaks()
+    gf, gb = bytes_f / (ms_f * 1e-3) / 1e9, bytes_b / (ms_b * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "HSTU LMSD fwd and bwd HBM throughput (GB/s)",
+        "value": (bytes_f + bytes_b) / ((ms_f + ms_b) * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_f + ms_b, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "fwd": {"ms": ms_f, "gbs": gf, "bytes": bytes_f},
+        "bwd": {"ms": ms_b, "gbs": gb, "bytes": bytes_b},
+        "roofline": {"bound": "hbm", "achieved": (bytes_f + bytes_b) / ((ms_f + ms_b) * 1e-3) / 1e9,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": (bytes_f + bytes_b) / ((ms_f + ms_b) * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "traffic": None},
+        "config": {"workload": f"LMSD N={n} D={d}", "dropout_ratio": p, "apply_u_silu": True,
+                   "concat_u": True, "concat_x": True,
+                   "l2": "flushed between calls (256 MiB write)"},
+    }))
+    return 0
+
+
 def run_paged(args, w, hstu, dev):
     """--paged: forward-only throughput over a paged K/V cache (the page's
     paged path is a causal forward), the contiguous forward timed beside it."""
@@ -288,6 +353,9 @@ def main():
     ap.add_argument("--func-targets", type=int, default=None,
                     help="arbitrary (func_tensor) mask: causal plus the last N keys of every "
                          "sequence as targets")
+    ap.add_argument("--lmsd", default=None,
+                    help="time the LMSD forward and backward on an 'N,D' bf16 problem (dropout "
+                         "0.1, SiLU, both extra segments); one JSON line in GB/s")
     ap.add_argument("--paged", action="store_true",
                     help="time the causal forward over a paged K/V cache (the workload's keys "
                          "in shuffled 128-row pages) beside the contiguous forward; one JSON line")
@@ -324,6 +392,8 @@ def main():
     dev = torch.device("cuda", local)
     if args.paged:
         return run_paged(args, w, hstu, dev)
+    if args.lmsd:
+        return run_lmsd(args, dev)
 
     x = workloads.make_inputs(w, seed=0)
     lengths = x["lengths"]
