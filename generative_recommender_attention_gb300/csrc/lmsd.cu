@@ -337,13 +337,17 @@ __global__ void __launch_bounds__(32 * kLmsdWarps) hstu_lmsd_bwd_kernel(BwdArgs 
   }
 }
 
-// Column sums of the per-block partials, in block order: dweight, dbias.
+// Column sums of the per-block partials, one warp per column: lane l adds
+// partials l, l + 32, ... in order, then a fixed shuffle tree adds the lanes
+// (the same order on every run): dweight, dbias.
 __global__ void hstu_lmsd_colsum_kernel(const float* part, int blocks, int d, int dweight,
                                         __nv_bfloat16* dw, __nv_bfloat16* db) {
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  const int col = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (col >= 2 * d) return;
   float t = 0.f;
-  for (int k = 0; k < blocks; ++k) t += part[static_cast<int64_t>(k) * 2 * d + col];
+  for (int k = lane; k < blocks; k += 32) t += part[static_cast<int64_t>(k) * 2 * d + col];
+  t = warp_sum(t);
+  if (lane != 0) return;
   if (col < d) {
     if (dweight) dw[col] = __float2bfloat16_rn(t);
   } else {
@@ -351,14 +355,17 @@ __global__ void hstu_lmsd_colsum_kernel(const float* part, int blocks, int d, in
   }
 }
 
-int lmsd_grid(int64_t n) {
+// Persistent grids: `per_sm` blocks of 8 rows per SM (the backward keeps it
+// small, each block adds a row of column partials).
+int lmsd_grid(int64_t n, int per_sm) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (n + kLmsdWarps - 1) / kLmsdWarps;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;   // persistent: 8 blocks of 8 rows per SM
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<int>(want < cap ? want : cap);
 }
+constexpr int kFwdBlocksPerSm = 8, kBwdBlocksPerSm = 2;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -414,13 +421,13 @@ hstu_lmsd_status_t hstu_lmsd_fwd(const void* x, int64_t x_stride, const void* u,
   const int nc = (d / 8 + 31) / 32;
   auto kern = nc == 1 ? hstu_lmsd_fwd_kernel<1> : nc == 2 ? hstu_lmsd_fwd_kernel<2>
             : nc == 3 ? hstu_lmsd_fwd_kernel<3> : hstu_lmsd_fwd_kernel<4>;
-  kern<<<lmsd_grid(n), 32 * kLmsdWarps, 0, stream>>>(a);
+  kern<<<lmsd_grid(n, kFwdBlocksPerSm), 32 * kLmsdWarps, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? HSTU_LMSD_OK : HSTU_LMSD_ERR_CUDA;
 }
 
 size_t hstu_lmsd_bwd_workspace_size(int64_t n, int32_t d) {
   if (n < 0 || d < 8 || d >= 1024 || d % 8 != 0) return 0;
-  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n)) * 2 * d * sizeof(float);
+  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n, kBwdBlocksPerSm)) * 2 * d * sizeof(float);
 }
 
 hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* x,
@@ -451,7 +458,7 @@ hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* 
   const size_t need = hstu_lmsd_bwd_workspace_size(n, d);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_LMSD_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return HSTU_LMSD_ERR_MISALIGNED;
-  const int grid = n > 0 ? lmsd_grid(n) : 1;
+  const int grid = n > 0 ? lmsd_grid(n, kBwdBlocksPerSm) : 1;
   const size_t smem = static_cast<size_t>(kLmsdWarps) * 2 * d * sizeof(float);
   const int nc = (d / 8 + 31) / 32;
   auto kern = nc == 1 ? hstu_lmsd_bwd_kernel<1> : nc == 2 ? hstu_lmsd_bwd_kernel<2>
@@ -478,7 +485,7 @@ hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* 
   a.part = static_cast<float*>(workspace);
   if (n > 0) kern<<<grid, 32 * kLmsdWarps, smem, stream>>>(a);
   else cudaMemsetAsync(workspace, 0, need, stream);
-  hstu_lmsd_colsum_kernel<<<(2 * d + 255) / 256, 256, 0, stream>>>(
+  hstu_lmsd_colsum_kernel<<<(2 * d * 32 + 255) / 256, 256, 0, stream>>>(
       a.part, grid, d, a.dweight, static_cast<__nv_bfloat16*>(dweight),
       static_cast<__nv_bfloat16*>(dbias));
   return cudaGetLastError() == cudaSuccess ? HSTU_LMSD_OK : HSTU_LMSD_ERR_CUDA;
