@@ -532,6 +532,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           }
         }
         tmem_st_w<CW / 2>(tDPT + b * BQ, pd);  // in place over this warp's dP^T columns
+        tmem_st_wait();
+        warp_arrive(bar(DSFULL + b));  // dK += dS^T Q may start; the global copy follows
         if (ds_row != nullptr) {
           // pd[e] = (dS[q0 + 2e][r], dS[q0 + 2e + 1][r]); the even lane keeps
           // query q0 + 2e for keys (r, r + 1), the odd lane query q0 + 2e + 1
@@ -544,8 +546,6 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             dst[e * kDsKeys] = __byte_perm(mine, other, odd ? 0x3276u : 0x5410u);
           }
         }
-        tmem_st_wait();
-        warp_arrive(bar(DSFULL + b));
       }
       if (!ok) break;
       if (!epilogue(U)) { ok = false; break; }
