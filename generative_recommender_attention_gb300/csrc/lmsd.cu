@@ -5,17 +5,20 @@
 // inverted dropout with one int8 mask per element (bit 0 main, bit 1 x
 // segment, bit 2 u segment; set = kept), row mean and rstd saved for the
 // backward.  The op is HBM-bound: one warp per row, 16-byte loads and stores
-// (8 bf16 per lane per chunk), fp32 arithmetic, no shared memory in the
-// forward.  The backward forms dx and du per row the same way; dweight and
-// dbias are column sums over rows, reduced deterministically: each warp sums
-// its rows in registers, each block sums its warps in a fixed order into a
-// partial row of the workspace, and a second kernel sums the partials in
-// block order.
+// (8 bf16 per lane per chunk) kept packed in registers, fp32 arithmetic.  The
+// forward loads the next row of its warp while it computes the current one.
+// The backward makes two passes over each row (the row means of dxhat and
+// dxhat xhat, then dx and du); dweight and dbias are column sums
+// over rows, reduced deterministically: each warp adds its rows' terms to
+// its own shared-memory accumulators, each block sums its warps in a fixed
+// order into a partial row of the workspace, and a second kernel sums the
+// partials in block order.
 //
 // Dropout decisions: Philox4x32-10 (Salmon et al., SC 2011), implemented
-// here from its definition; element e = row * D + col of segment k uses word
-// e % 4 of Philox(counter (e / 4 low, high, k, 0), key (seed low, high)) and
-// is kept iff the word >= floor(p 2^32).
+// here from its definition.  One call decides 8 elements: element
+// e = row * D + col of segment k uses the 16-bit half e % 2 (low first) of
+// word (e % 8) / 2 of Philox(counter (e / 8 low, high, k, 0), key (seed low,
+// high)) and is kept iff that half >= floor(p 2^16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,56 +35,74 @@ struct Philox4 {
   uint32_t v[4];
 };
 
+// Round keys of one seed: round r uses (seed low + r W0, seed high + r W1).
+// Computed on the host and passed in the kernel parameters, so the rounds
+// read them as constants.
+struct PhiloxKeys {
+  uint32_t k[20];
+};
+
+PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys p;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    p.k[2 * r] = k0;
+    p.k[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;  // key increments
+    k1 += 0xBB67AE85u;
+  }
+  return p;
+}
+
 __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
-                                                 uint32_t c3, uint32_t k0, uint32_t k1) {
+                                                 uint32_t c3, const PhiloxKeys& key) {
   constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;   // round multipliers
-  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;   // key increments
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint32_t hi0 = __umulhi(kM0, c0), lo0 = kM0 * c0;
     const uint32_t hi1 = __umulhi(kM1, c2), lo1 = kM1 * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    const uint32_t n0 = hi1 ^ c1 ^ key.k[2 * r], n2 = hi0 ^ c3 ^ key.k[2 * r + 1];
     c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
-    k0 += kW0;
-    k1 += kW1;
   }
   return Philox4{{c0, c1, c2, c3}};
 }
 
-// Keep bits of 8 consecutive elements starting at flat index e0 (a multiple
-// of 8) of segment k.
-__device__ __forceinline__ uint32_t keep8(uint64_t e0, uint32_t k, uint64_t seed, uint32_t thr) {
-  const uint64_t g = e0 >> 2;
-  const Philox4 a = philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), k, 0u,
-                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-  const Philox4 b = philox4x32_10(static_cast<uint32_t>(g + 1),
-                                  static_cast<uint32_t>((g + 1) >> 32), k, 0u,
-                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-  uint32_t bits = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    bits |= (a.v[i] >= thr ? 1u : 0u) << i;
-    bits |= (b.v[i] >= thr ? 1u : 0u) << (4 + i);
-  }
-  return bits;
+// The Philox words deciding the 8 elements e0 .. e0 + 7 (e0 a multiple of 8)
+// of segment k.
+__device__ __forceinline__ Philox4 draw8(uint64_t e0, uint32_t k, const PhiloxKeys& key) {
+  const uint64_t g = e0 >> 3;
+  return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), k, 0u, key);
+}
+
+// Element 2 j + h of a draw is kept iff its 16-bit half (h = 0: low) is at
+// least thr, i.e. iff that half, moved to the top, is at least thr_hi =
+// thr << 16.
+__device__ __forceinline__ bool kept(const Philox4& r, int j, int h, uint32_t thr_hi) {
+  return (h == 0 ? r.v[j] << 16 : r.v[j]) >= thr_hi;
+}
+
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+// 32-bit word j (two bf16, element 2 j in the low half) of a 16-byte chunk.
+__device__ __forceinline__ uint32_t word(const uint4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(h[i]);
+    const float2 t = bf2(v[i]);
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
   }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  uint4 w;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-  return w;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -90,10 +111,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu(float u) { return u / (1.f + __expf(-u)); }
-__device__ __forceinline__ float silu_grad(float u) {
-  const float s = 1.f / (1.f + __expf(-u));
-  return s * (1.f + u * (1.f - s));
+// sigmoid(u) = 1 / (1 + e^-u) with the fast exponential and reciprocal
+// (e^-u = inf for u < -88 gives 0, the limit).
+__device__ __forceinline__ float sigmoid(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
+
+__device__ __forceinline__ uint4 ld16(const __nv_bfloat16* p, int ch) {
+  return __ldg(reinterpret_cast<const uint4*>(p) + ch);
 }
 
 struct FwdArgs {
@@ -107,45 +130,66 @@ struct FwdArgs {
   int d;
   float eps;
   float p;          // dropout ratio (fp32)
-  uint32_t thr;     // keep iff word >= thr
+  uint32_t thr_hi;  // keep iff the 16-bit half << 16 >= thr_hi (0 without dropout)
   float scale;      // 1 / (1 - p)
   int silu, concat_u, concat_x;
-  uint64_t seed;
+  PhiloxKeys keys;
   __nv_bfloat16* y;
   float* mean;
   float* rstd;
   int8_t* mask;
 };
 
-// NC: 8-element chunks per lane (D <= 256 NC, so a row's x stays in registers).
+// Blocks of 8 warps resident per SM (the register budget of the kernels
+// below), by 8-element chunks per lane.
+__host__ __device__ constexpr int fwd_blocks_per_sm(int nc) { return nc <= 1 ? 4 : nc == 2 ? 3 : 2; }
+__host__ __device__ constexpr int bwd_blocks_per_sm(int nc) { return nc <= 2 ? 4 : 2; }
+
+// NC: 8-element chunks per lane (D <= 256 NC).  Lanes past the row's last
+// chunk hold zeros.
 template <int NC>
-__global__ void __launch_bounds__(32 * kLmsdWarps) hstu_lmsd_fwd_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
+    hstu_lmsd_fwd_kernel(FwdArgs a) {
   const int lane = threadIdx.x & 31;
   const int nch = a.d / 8;
   const int S = 1 + a.concat_u + a.concat_x;
   const bool drop = a.p > 0.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps;
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kLmsdWarps + (threadIdx.x >> 5);
-       row < a.n; row += stride) {
-    float x[NC][8];
-    float s = 0.f;
+  int64_t row = static_cast<int64_t>(blockIdx.x) * kLmsdWarps + (threadIdx.x >> 5);
+  auto load = [&](int64_t r, uint4 (&xo)[NC], uint4 (&uo)[NC]) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
-      if (ch < nch) {
-        unpack8(reinterpret_cast<const uint4*>(a.x + row * a.xs)[ch], x[c]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s += x[c][i];
+      xo[c] = uo[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < a.n && ch < nch) {
+        xo[c] = ld16(a.x + r * a.xs, ch);
+        uo[c] = ld16(a.u + r * a.us, ch);
       }
+    }
+  };
+  uint4 xv[NC], uv[NC];
+  load(row, xv, uv);
+  for (; row < a.n; row += stride) {
+    uint4 xn[NC], un[NC];
+    load(row + stride, xn, un);  // the warp's next row, in flight during this one
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float f[8];
+      unpack8(xv[c], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s += f[i];
     }
     const float mean = warp_sum(s) / a.d;
     float v = 0.f;
 #pragma unroll
-    for (int c = 0; c < NC; ++c)
-      if (lane + 32 * c < nch) {
+    for (int c = 0; c < NC; ++c) {
+      if (lane + 32 * c >= nch) continue;
+      float f[8];
+      unpack8(xv[c], f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v += (x[c][i] - mean) * (x[c][i] - mean);
-      }
+      for (int i = 0; i < 8; ++i) v += (f[i] - mean) * (f[i] - mean);
+    }
     const float rstd = rsqrtf(warp_sum(v) / a.d + a.eps);
     if (lane == 0) { a.mean[row] = mean; a.rstd[row] = rstd; }
     uint4* yrow = reinterpret_cast<uint4*>(a.y + row * static_cast<int64_t>(S) * a.d);
@@ -153,48 +197,50 @@ __global__ void __launch_bounds__(32 * kLmsdWarps) hstu_lmsd_fwd_kernel(FwdArgs 
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
       if (ch >= nch) continue;
-      const uint64_t e0 = static_cast<uint64_t>(row) * a.d + 8 * ch;
-      uint32_t k0 = 0xffu, k1 = 0xffu, k2 = 0xffu;
+      // without dropout every draw is 0 and thr_hi 0: everything is kept
+      Philox4 r0{}, r1{}, r2{};
       if (drop) {
-        k0 = keep8(e0, 0u, a.seed, a.thr);
-        if (a.concat_x) k1 = keep8(e0, 1u, a.seed, a.thr);
-        if (a.concat_u) k2 = keep8(e0, 2u, a.seed, a.thr);
-        uint64_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t byte = ((k0 >> i) & 1u) | (a.concat_x ? ((k1 >> i) & 1u) << 1 : 0u) |
-                                (a.concat_u ? ((k2 >> i) & 1u) << 2 : 0u);
-          m |= byte << (8 * i);
-        }
-        reinterpret_cast<uint64_t*>(a.mask + row * a.d)[ch] = m;
+        const uint64_t e0 = static_cast<uint64_t>(row) * a.d + 8 * ch;
+        r0 = draw8(e0, 0u, a.keys);
+        if (a.concat_x) r1 = draw8(e0, 1u, a.keys);
+        if (a.concat_u) r2 = draw8(e0, 2u, a.keys);
       }
       const float sc = drop ? a.scale : 1.f;
-      float u[8], w[8], bb[8], act[8], out[8];
-      unpack8(reinterpret_cast<const uint4*>(a.u + row * a.us)[ch], u);
-      unpack8(reinterpret_cast<const uint4*>(a.w)[ch], w);
-      unpack8(reinterpret_cast<const uint4*>(a.b)[ch], bb);
+      const uint4 wv = ld16(a.w, ch), bv = ld16(a.b, ch);
+      uint32_t ya[4], yx[4], ym[4], mw[2] = {0u, 0u};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) act[i] = a.silu ? silu(u[i]) : u[i];
+      for (int j = 0; j < 4; ++j) {
+        const float2 x2 = bf2(word(xv[c], j)), u2 = bf2(word(uv[c], j));
+        const float2 w2 = bf2(word(wv, j)), b2 = bf2(word(bv, j));
+        const float xs[2] = {x2.x, x2.y}, us[2] = {u2.x, u2.y};
+        const float ws[2] = {w2.x, w2.y}, bs[2] = {b2.x, b2.y};
+        float oa[2], ox[2], om[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const bool p0 = kept(r0, j, h, a.thr_hi);
+          const bool p1 = a.concat_x && kept(r1, j, h, a.thr_hi);
+          const bool p2 = a.concat_u && kept(r2, j, h, a.thr_hi);
+          const float act = a.silu ? us[h] * sigmoid(us[h]) : us[h];
+          const float l = (xs[h] - mean) * rstd * ws[h] + bs[h];
+          oa[h] = p2 ? act * sc : 0.f;
+          ox[h] = p1 ? xs[h] * sc : 0.f;
+          om[h] = p0 ? l * act * sc : 0.f;
+          const int i = 2 * j + h;
+          mw[i >> 2] |= (static_cast<uint32_t>(p0) | static_cast<uint32_t>(p1) << 1 |
+                         static_cast<uint32_t>(p2) << 2) << (8 * (i & 3));
+        }
+        ya[j] = pack2(oa[0], oa[1]);
+        yx[j] = pack2(ox[0], ox[1]);
+        ym[j] = pack2(om[0], om[1]);
+      }
+      if (drop) reinterpret_cast<uint2*>(a.mask + row * a.d)[ch] = make_uint2(mw[0], mw[1]);
       int seg = 0;
-      if (a.concat_u) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = ((k2 >> i) & 1u) ? act[i] * sc : 0.f;
-        yrow[seg * nch + ch] = pack8(out);
-        ++seg;
-      }
-      if (a.concat_x) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) out[i] = ((k1 >> i) & 1u) ? x[c][i] * sc : 0.f;
-        yrow[seg * nch + ch] = pack8(out);
-        ++seg;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float l = (x[c][i] - mean) * rstd * w[i] + bb[i];
-        out[i] = ((k0 >> i) & 1u) ? l * act[i] * sc : 0.f;
-      }
-      yrow[seg * nch + ch] = pack8(out);
+      if (a.concat_u) yrow[seg++ * nch + ch] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+      if (a.concat_x) yrow[seg++ * nch + ch] = make_uint4(yx[0], yx[1], yx[2], yx[3]);
+      yrow[seg * nch + ch] = make_uint4(ym[0], ym[1], ym[2], ym[3]);
     }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) { xv[c] = xn[c]; uv[c] = un[c]; }
   }
 }
 
@@ -221,80 +267,74 @@ struct BwdArgs {
   float* part;  // gridDim.x rows of [dweight partial (d) | dbias partial (d)]
 };
 
-// One row term of the backward at element i of a chunk: returns dl (the
-// gradient of l), and the pieces of dx and du.
-struct BwdTerms {
-  float xh, dl, da, dxh, dx_extra;
-};
-
-__device__ __forceinline__ BwdTerms bwd_terms(const BwdArgs& a, float x, float u, float w, float b,
-                                              float mean, float rstd, float dm, float dyu,
-                                              float dyx, uint32_t mb) {
-  BwdTerms t;
-  const float s0 = (mb & 1u) ? a.scale : 0.f;
-  const float sx = (mb & 2u) ? a.scale : 0.f;
-  const float su = (mb & 4u) ? a.scale : 0.f;
-  t.xh = (x - mean) * rstd;
-  const float l = t.xh * w + b;
-  const float act = a.silu ? silu(u) : u;
-  const float g = dm * s0;  // gradient of l * a
-  t.dl = g * act;
-  t.da = g * l + (a.concat_u ? dyu * su : 0.f);
-  t.dxh = t.dl * w;
-  t.dx_extra = a.concat_x ? dyx * sx : 0.f;
-  return t;
-}
-
-// Loads chunk ch of a row's inputs: x, u, the dy segments, the mask bytes.
-__device__ __forceinline__ void bwd_load(const BwdArgs& a, int64_t row, int ch, int nch,
-                                         float (&x)[8], float (&u)[8], float (&dm)[8],
-                                         float (&dyu)[8], float (&dyx)[8], uint64_t& m) {
-  const uint4* dyrow = reinterpret_cast<const uint4*>(a.dy + row * a.dys);
-  unpack8(reinterpret_cast<const uint4*>(a.x + row * a.xs)[ch], x);
-  unpack8(reinterpret_cast<const uint4*>(a.u + row * a.us)[ch], u);
-  int seg = 0;
-  if (a.concat_u) unpack8(dyrow[seg++ * nch + ch], dyu);
-  if (a.concat_x) unpack8(dyrow[seg++ * nch + ch], dyx);
-  unpack8(dyrow[seg * nch + ch], dm);
-  m = a.drop ? reinterpret_cast<const uint64_t*>(a.mask + row * a.d)[ch] : ~0ull;
-}
-
-// Two passes per row: the first forms the row means of dxh and dxh xhat and
-// the dweight / dbias contributions, the second reloads the row (from L1 /
-// L2) and writes dx and du, so that only the column accumulators stay in
-// registers across rows.
+// Shared-memory column accumulators of one warp: [dweight | dbias][NC][8][32
+// lanes], so that lane l's columns 8 (l + 32 c) + i sit in its own bank.
 template <int NC>
-__global__ void __launch_bounds__(32 * kLmsdWarps) hstu_lmsd_bwd_kernel(BwdArgs a) {
-  extern __shared__ float red[];  // [warp][2 d]
+__host__ __device__ constexpr int acc_floats() { return 2 * NC * 8 * 32; }
+template <int NC>
+__device__ __forceinline__ int acc_slot(int which, int c, int i, int lane) {
+  return ((which * NC + c) * 8 + i) * 32 + lane;
+}
+
+// Two passes over a row: the first forms the row means of dxh = dl * weight
+// and dxh * xhat and adds the row's dweight / dbias terms to the warp's
+// accumulators; the second reads the row again (from L1 / L2) and writes dx
+// and du, which keeps registers for more warps.
+template <int NC>
+__global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
+    hstu_lmsd_bwd_kernel(BwdArgs a) {
+  extern __shared__ float acc_all[];  // [warp][acc_floats<NC>()]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* acc = acc_all + warp * acc_floats<NC>();
+  for (int k = lane; k < acc_floats<NC>(); k += 32) acc[k] = 0.f;  // warp-private
   const int nch = a.d / 8;
-  float gw[NC][8], gb[NC][8];
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { gw[c][i] = 0.f; gb[c][i] = 0.f; }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * kLmsdWarps + warp; row < a.n;
        row += stride) {
-    const float mean = a.mean[row], rstd = a.rstd[row];
+    const float mean = __ldg(a.mean + row), rstd = __ldg(a.rstd + row);
+    const __nv_bfloat16* dyrow = a.dy + row * a.dys;
+    uint4 xv[NC], uv[NC], dmv[NC], duv[NC], dxv[NC];
+    uint64_t mv[NC];
+    auto load = [&](int c) {
+      const int ch = lane + 32 * c;
+      xv[c] = uv[c] = dmv[c] = duv[c] = dxv[c] = zero;
+      mv[c] = 0;
+      if (ch >= nch) return;
+      xv[c] = ld16(a.x + row * a.xs, ch);
+      uv[c] = ld16(a.u + row * a.us, ch);
+      int seg = 0;
+      if (a.concat_u) duv[c] = ld16(dyrow, seg++ * nch + ch);
+      if (a.concat_x) dxv[c] = ld16(dyrow, seg++ * nch + ch);
+      dmv[c] = ld16(dyrow, seg * nch + ch);
+      mv[c] = a.drop ? __ldg(reinterpret_cast<const unsigned long long*>(a.mask + row * a.d) + ch)
+                     : ~0ull;
+    };
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
       if (ch >= nch) continue;
-      float x[8], u[8], dm[8], dyu[8], dyx[8], w[8], b[8];
-      uint64_t m;
-      bwd_load(a, row, ch, nch, x, u, dm, dyu, dyx, m);
-      unpack8(reinterpret_cast<const uint4*>(a.w)[ch], w);
-      unpack8(reinterpret_cast<const uint4*>(a.b)[ch], b);
+      load(c);
+      const uint4 wv = ld16(a.w, ch);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const BwdTerms t = bwd_terms(a, x[i], u[i], w[i], b[i], mean, rstd, dm[i], dyu[i], dyx[i],
-                                     static_cast<uint32_t>(m >> (8 * i)) & 0xffu);
-        gw[c][i] += t.dl * t.xh;
-        gb[c][i] += t.dl;
-        s1 += t.dxh;
-        s2 += t.dxh * t.xh;
+      for (int j = 0; j < 4; ++j) {
+        const float2 x2 = bf2(word(xv[c], j)), u2 = bf2(word(uv[c], j));
+        const float2 d2 = bf2(word(dmv[c], j)), w2 = bf2(word(wv, j));
+        const float xs[2] = {x2.x, x2.y}, us[2] = {u2.x, u2.y};
+        const float ds[2] = {d2.x, d2.y}, ws[2] = {w2.x, w2.y};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * j + h;
+          const float xh = (xs[h] - mean) * rstd;
+          const float act = a.silu ? us[h] * sigmoid(us[h]) : us[h];
+          const float g = ((mv[c] >> (8 * i)) & 1u) ? ds[h] * a.scale : 0.f;
+          const float dl = g * act, dxh = dl * ws[h];
+          s1 += dxh;
+          s2 += dxh * xh;
+          acc[acc_slot<NC>(0, c, i, lane)] += dl * xh;
+          acc[acc_slot<NC>(1, c, i, lane)] += dl;
+        }
       }
     }
     const float m1 = warp_sum(s1) / a.d, m2 = warp_sum(s2) / a.d;
@@ -302,37 +342,45 @@ __global__ void __launch_bounds__(32 * kLmsdWarps) hstu_lmsd_bwd_kernel(BwdArgs 
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
       if (ch >= nch) continue;
-      float x[8], u[8], dm[8], dyu[8], dyx[8], w[8], b[8], ox[8], ou[8];
-      uint64_t m;
-      bwd_load(a, row, ch, nch, x, u, dm, dyu, dyx, m);
-      unpack8(reinterpret_cast<const uint4*>(a.w)[ch], w);
-      unpack8(reinterpret_cast<const uint4*>(a.b)[ch], b);
+      load(c);  // again: from L1 / L2
+      const uint4 wv = ld16(a.w, ch), bv = ld16(a.b, ch);
+      uint32_t ox[4], ou[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const BwdTerms t = bwd_terms(a, x[i], u[i], w[i], b[i], mean, rstd, dm[i], dyu[i], dyx[i],
-                                     static_cast<uint32_t>(m >> (8 * i)) & 0xffu);
-        ox[i] = rstd * (t.dxh - m1 - t.xh * m2) + t.dx_extra;
-        ou[i] = a.silu ? t.da * silu_grad(u[i]) : t.da;
+      for (int j = 0; j < 4; ++j) {
+        const float2 x2 = bf2(word(xv[c], j)), u2 = bf2(word(uv[c], j));
+        const float2 d2 = bf2(word(dmv[c], j)), w2 = bf2(word(wv, j)), b2 = bf2(word(bv, j));
+        const float2 yu2 = bf2(word(duv[c], j)), yx2 = bf2(word(dxv[c], j));
+        const float xs[2] = {x2.x, x2.y}, us[2] = {u2.x, u2.y}, ds[2] = {d2.x, d2.y};
+        const float ws[2] = {w2.x, w2.y}, bs[2] = {b2.x, b2.y};
+        const float yus[2] = {yu2.x, yu2.y}, yxs[2] = {yx2.x, yx2.y};
+        float rx[2], ru[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t mb = static_cast<uint32_t>(mv[c] >> (8 * (2 * j + h)));
+          const float xh = (xs[h] - mean) * rstd;
+          const float l = xh * ws[h] + bs[h];
+          const float sg = a.silu ? sigmoid(us[h]) : 0.f;
+          const float act = a.silu ? us[h] * sg : us[h];
+          const float g = (mb & 1u) ? ds[h] * a.scale : 0.f;
+          const float dxh = g * act * ws[h];
+          const float da = g * l + ((mb & 4u) ? yus[h] * a.scale : 0.f);
+          rx[h] = rstd * (dxh - m1 - xh * m2) + ((mb & 2u) ? yxs[h] * a.scale : 0.f);
+          ru[h] = a.silu ? da * sg * (1.f + us[h] * (1.f - sg)) : da;
+        }
+        ox[j] = pack2(rx[0], rx[1]);
+        ou[j] = pack2(ru[0], ru[1]);
       }
-      reinterpret_cast<uint4*>(a.dx + row * a.dxs)[ch] = pack8(ox);
-      reinterpret_cast<uint4*>(a.du + row * a.dus)[ch] = pack8(ou);
+      reinterpret_cast<uint4*>(a.dx + row * a.dxs)[ch] = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+      reinterpret_cast<uint4*>(a.du + row * a.dus)[ch] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
     }
   }
-  // column partials: warps in a fixed order, then one partial row per block
-#pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const int ch = lane + 32 * c;
-    if (ch >= nch) continue;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      red[warp * 2 * a.d + 8 * ch + i] = gw[c][i];
-      red[warp * 2 * a.d + a.d + 8 * ch + i] = gb[c][i];
-    }
-  }
+  // column partials: the block's warps in a fixed order, one partial row per block
   __syncthreads();
   for (int col = threadIdx.x; col < 2 * a.d; col += blockDim.x) {
+    const int which = col >= a.d ? 1 : 0, cc = col - which * a.d, ch = cc >> 3;
+    const int slot = acc_slot<NC>(which, ch >> 5, cc & 7, ch & 31);
     float t = 0.f;
-    for (int k = 0; k < kLmsdWarps; ++k) t += red[k * 2 * a.d + col];
+    for (int k = 0; k < kLmsdWarps; ++k) t += acc_all[k * acc_floats<NC>() + slot];
     a.part[static_cast<int64_t>(blockIdx.x) * 2 * a.d + col] = t;
   }
 }
@@ -355,8 +403,7 @@ __global__ void hstu_lmsd_colsum_kernel(const float* part, int blocks, int d, in
   }
 }
 
-// Persistent grids: `per_sm` blocks of 8 rows per SM (the backward keeps it
-// small, each block adds a row of column partials).
+// Persistent grids: `per_sm` blocks of 8 rows per SM, the blocks that fit.
 int lmsd_grid(int64_t n, int per_sm) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
@@ -365,7 +412,10 @@ int lmsd_grid(int64_t n, int per_sm) {
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<int>(want < cap ? want : cap);
 }
-constexpr int kFwdBlocksPerSm = 8, kBwdBlocksPerSm = 2;
+int chunks_per_lane(int32_t d) { return (d / 8 + 31) / 32; }
+
+// Bytes of the backward's shared-memory column accumulators.
+size_t bwd_smem(int nc) { return static_cast<size_t>(kLmsdWarps) * 2 * nc * 8 * 32 * sizeof(float); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -412,22 +462,24 @@ hstu_lmsd_status_t hstu_lmsd_fwd(const void* x, int64_t x_stride, const void* u,
   a.u = static_cast<const __nv_bfloat16*>(u); a.us = u_stride;
   a.w = static_cast<const __nv_bfloat16*>(weight); a.b = static_cast<const __nv_bfloat16*>(bias);
   a.n = n; a.d = d; a.eps = eps; a.p = dropout_ratio;
-  const double t = std::floor(static_cast<double>(dropout_ratio) * 4294967296.0);
-  a.thr = static_cast<uint32_t>(t > 4294967295.0 ? 4294967295.0 : t);
+  a.thr_hi = drop ? static_cast<uint32_t>(std::floor(static_cast<double>(dropout_ratio) * 65536.0))
+                       << 16
+                 : 0u;
   a.scale = drop ? 1.f / (1.f - dropout_ratio) : 1.f;
   a.silu = apply_u_silu != 0; a.concat_u = concat_u != 0; a.concat_x = concat_x != 0;
-  a.seed = static_cast<uint64_t>(seed);
+  a.keys = philox_keys(static_cast<uint64_t>(seed));
   a.y = static_cast<__nv_bfloat16*>(y); a.mean = mean; a.rstd = rstd; a.mask = mask;
-  const int nc = (d / 8 + 31) / 32;
+  const int nc = chunks_per_lane(d);
   auto kern = nc == 1 ? hstu_lmsd_fwd_kernel<1> : nc == 2 ? hstu_lmsd_fwd_kernel<2>
             : nc == 3 ? hstu_lmsd_fwd_kernel<3> : hstu_lmsd_fwd_kernel<4>;
-  kern<<<lmsd_grid(n, kFwdBlocksPerSm), 32 * kLmsdWarps, 0, stream>>>(a);
+  kern<<<lmsd_grid(n, fwd_blocks_per_sm(nc)), 32 * kLmsdWarps, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? HSTU_LMSD_OK : HSTU_LMSD_ERR_CUDA;
 }
 
 size_t hstu_lmsd_bwd_workspace_size(int64_t n, int32_t d) {
   if (n < 0 || d < 8 || d >= 1024 || d % 8 != 0) return 0;
-  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n, kBwdBlocksPerSm)) * 2 * d * sizeof(float);
+  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n, bwd_blocks_per_sm(chunks_per_lane(d)))) * 2 *
+         d * sizeof(float);
 }
 
 hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* x,
@@ -458,16 +510,15 @@ hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* 
   const size_t need = hstu_lmsd_bwd_workspace_size(n, d);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_LMSD_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return HSTU_LMSD_ERR_MISALIGNED;
-  const int grid = n > 0 ? lmsd_grid(n, kBwdBlocksPerSm) : 1;
-  const size_t smem = static_cast<size_t>(kLmsdWarps) * 2 * d * sizeof(float);
-  const int nc = (d / 8 + 31) / 32;
+  const int nc = chunks_per_lane(d);
+  const int grid = n > 0 ? lmsd_grid(n, bwd_blocks_per_sm(nc)) : 1;
+  const size_t smem = bwd_smem(nc);
   auto kern = nc == 1 ? hstu_lmsd_bwd_kernel<1> : nc == 2 ? hstu_lmsd_bwd_kernel<2>
             : nc == 3 ? hstu_lmsd_bwd_kernel<3> : hstu_lmsd_bwd_kernel<4>;
   static bool attr[5] = {false, false, false, false, false};
   if (!attr[nc]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kLmsdWarps * 2 * 1024 * sizeof(float))) !=
-        cudaSuccess)
+                             static_cast<int>(smem)) != cudaSuccess)
       return HSTU_LMSD_ERR_CUDA;
     attr[nc] = true;
   }

@@ -14,12 +14,13 @@
  * a set bit means kept; disabled segments leave their bits clear.  With
  * p = 0 no random numbers are drawn and no mask is written.
  *
- * Random numbers: Philox4x32-10 (Salmon et al., SC 2011).  The element at
- * flat index e = row * D + col of segment k (0 main, 1 x, 2 u) is decided by
- * word e % 4 of Philox(counter = (e / 4 mod 2^32, e / 4 >> 32, k, 0),
- * key = (seed mod 2^32, seed >> 32)) and kept iff that word is at least
- * floor(p * 2^32).  (The page fixes Philox but not the counter layout; this
- * one is a reading.)
+ * Random numbers: Philox4x32-10 (Salmon et al., SC 2011), one call per 8
+ * elements.  The element at flat index e = row * D + col of segment k
+ * (0 main, 1 x, 2 u) is decided by the 16-bit half e % 2 (0 = low) of word
+ * (e % 8) / 2 of Philox(counter = (e / 8 mod 2^32, e / 8 >> 32, k, 0),
+ * key = (seed mod 2^32, seed >> 32)) and kept iff that half is at least
+ * floor(p * 2^16), so the drop rate is p to within 2^-16.  (The page fixes
+ * Philox but not the counter layout; this one is a reading.)
  *
  * Backward (chain rule; the page gives the API): with s_k = mask bit k /
  * (1 - p), or 1 when p = 0,

@@ -19,11 +19,12 @@ and returns no mask.
 The random decisions come from Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
 "Parallel random numbers: as easy as 1, 2, 3", SC 2011), written here from
 that definition.  The pages do not say how counters map to elements; the
-reading taken here (and in the CUDA library, written separately): the
-element at flat index e = row * D + col of segment k (0 main, 1 x, 2 u)
-uses output word e % 4 of Philox(counter = (g mod 2^32, g >> 32, k, 0),
-key = (seed mod 2^32, (seed >> 32) mod 2^32)) with g = e // 4, and is kept
-iff that word >= floor(p * 2^32) (p taken as fp32, then exactly).
+reading taken here (and in the CUDA library, written separately): one
+Philox call decides 8 elements.  The element at flat index e = row * D + col
+of segment k (0 main, 1 x, 2 u) uses the 16-bit half e % 2 (0 = low) of
+output word (e % 8) // 2 of Philox(counter = (g mod 2^32, g >> 32, k, 0),
+key = (seed mod 2^32, (seed >> 32) mod 2^32)) with g = e // 8, and is kept
+iff that half >= floor(p * 2^16) (p taken as fp32, then exactly).
 
 Backward (chain rule of the forward; the page gives the API, not the
 formulas): with s_k = mask bit k / (1 - p) (1 when p = 0),
@@ -59,21 +60,21 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
     return c
 
 
-def keep_words(n, d, segment, seed):
-    """The Philox word deciding each element of an (n, d) segment."""
+def keep_halves(n, d, segment, seed):
+    """The 16-bit Philox half deciding each element of an (n, d) segment."""
     e = np.arange(n * d, dtype=np.uint64)
-    g = e // np.uint64(4)
+    g = e // np.uint64(8)
     s = int(seed) & 0xFFFFFFFFFFFFFFFF
     words = philox4x32_10(g & _MASK32, g >> np.uint64(32), np.full_like(g, segment),
                           np.zeros_like(g), s & 0xFFFFFFFF, s >> 32)
-    sel = (e % np.uint64(4)).astype(np.int64)
-    out = np.choose(sel, words)
-    return out.reshape(n, d)
+    word = np.choose(((e % np.uint64(8)) // np.uint64(2)).astype(np.int64), words)
+    half = (word >> (np.uint64(16) * (e % np.uint64(2)))) & np.uint64(0xFFFF)
+    return half.reshape(n, d)
 
 
 def threshold(p):
-    """Keep iff word >= floor(p * 2^32), with p rounded to fp32 first."""
-    return int(np.floor(float(np.float32(p)) * 4294967296.0))
+    """Keep iff half >= floor(p * 2^16), with p rounded to fp32 first."""
+    return int(np.floor(float(np.float32(p)) * 65536.0))
 
 
 def _silu(u):
@@ -109,7 +110,7 @@ def forward(x, u, weight, bias, eps, dropout_ratio, seed, apply_u_silu=True, con
     if p > 0.0:
         t = threshold(p)
         scale = 1.0 / (1.0 - p)
-        keep = {k: keep_words(n, d, k, seed) >= np.uint64(t) for k in (0, 1, 2)}
+        keep = {k: keep_halves(n, d, k, seed) >= np.uint64(t) for k in (0, 1, 2)}
         mask = keep[0].astype(np.int8)
         if concat_x:
             mask |= (keep[1].astype(np.int8) << 1)

@@ -11,10 +11,13 @@
 * Philox4x32-10: full avalanche (one flipped counter or key bit changes about
   half of the output bits, which a generator with too few or broken rounds
   does not), uniform words, independent segments.
-The Philox stream itself has no published value pinned here (see the design doc:
-that part of the parity is unpinned to an external value; the GPU and CPU
-implementations, written separately, must agree bit for bit).
+* Philox4x32-10 against the generator authors' published known-answer
+  values (tests/golden/philox4x32_10_kat.txt).
+The mapping of Philox words to elements is a reading (the page fixes only
+the generator); the GPU and CPU implementations, written separately, must
+agree on it bit for bit.
 """
+import pathlib
 import numpy as np
 import pytest
 import torch
@@ -101,6 +104,16 @@ def test_backward_matches_autograd(flags, p):
     np.testing.assert_allclose(db, bs.grad.numpy(), rtol=1e-9, atol=1e-11)
 
 
+def test_philox_known_answers():
+    path = pathlib.Path(__file__).parent / "golden" / "philox4x32_10_kat.txt"
+    rows = [ln.split() for ln in path.read_text().splitlines() if ln and not ln.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(t, 16) for t in r]
+        out = lmsd.philox4x32_10(*[[t] for t in v[:4]], v[4], v[5])
+        assert [int(o[0]) for o in out] == v[6:], r
+
+
 def _popcount(v):
     v = np.asarray(v, dtype=np.uint64)
     return np.array([bin(int(t)).count("1") for t in v.ravel()]).reshape(v.shape)
@@ -125,6 +138,19 @@ def test_philox_avalanche_and_uniformity():
     words = np.concatenate(base).astype(np.float64) / 2**32
     assert abs(words.mean() - 0.5) < 0.01 and abs(words.var() - 1 / 12) < 0.005
     # a stream counted from zero, as the dropout uses it, is uniform too
-    w0 = lmsd.keep_words(512, 512, 0, 42).astype(np.float64) / 2**32
+    w0 = lmsd.keep_halves(512, 512, 0, 42).astype(np.float64) / 2**16
     hist = np.histogram(w0, bins=16, range=(0, 1))[0] / w0.size
     assert np.all(np.abs(hist - 1 / 16) < 0.003)
+
+
+def test_keep_halves_layout():
+    """Eight elements per Philox call: element e takes the 16-bit half e % 2
+    (low first) of word (e % 8) // 2 of the call with counter e // 8."""
+    n, d, seed = 3, 24, (7 << 32) | 5
+    h = lmsd.keep_halves(n, d, 2, seed).ravel()
+    for e in (0, 1, 6, 7, 8, 15, 40, 71):
+        g = e // 8
+        words = lmsd.philox4x32_10([g], [0], [2], [0], 5, 7)
+        want = (int(words[(e % 8) // 2][0]) >> (16 * (e % 2))) & 0xFFFF
+        assert int(h[e]) == want, e
+    assert lmsd.threshold(0.5) == 32768 and lmsd.threshold(0.1) == 6553
