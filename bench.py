@@ -398,6 +398,9 @@ def main():
     ap.add_argument("--paged", action="store_true",
                     help="time the causal forward over a paged K/V cache (the workload's keys "
                          "in shuffled 128-row pages) beside the contiguous forward; one JSON line")
+    ap.add_argument("--plan", action="store_true",
+                    help="one hstu_attn_plan launch per step shared by the planned forward and "
+                         "backward, instead of hstu_attn_fwd + hstu_attn_bwd scheduling each call")
     ap.add_argument("--kernels-only", action="store_true",
                     help="run warm-up and timed steps only (no second pass, end-to-end, clocks or "
                          "CPU baseline) and print no JSON line: for wrapping in a profiler")
@@ -462,8 +465,27 @@ def main():
     flush = None if args.no_flush else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     func_mode = "func" in kw
+    # One plan per step (the scheduling launch shared by the forward and the
+    # backward); the arbitrary-mask calls are not planned.
+    use_plan = args.plan and not func_mode
+    ws_p = torch.empty(hstu.plan_workspace_size(B, T, T, H, D, mq, mk), dtype=torch.uint8,
+                       device=dev) if use_plan else None
+    win_kw = {k: kw[k] for k in ("causal", "window_size") if k in kw}
+
+    def planned_step(g, o_, dq_, dk_, dv_):
+        p = hstu.hstu_attn_plan(g["cu_seqlens_q"], g["cu_seqlens_k"], T, T, H, D, mq, mk,
+                                workspace=ws_p, **win_kw)
+        hstu.hstu_attn_fwd(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_k"], mq, mk,
+                           out=o_, plan=p, **kw)
+        hstu.hstu_attn_bwd(g["do"], g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_k"],
+                           mq, mk, dq=dq_, dk=dk_, dv=dv_, plan=p, **kw)
+
+    status_ws = [ws_p] if use_plan else [ws_f, ws_b]
 
     def step(evs=None):
+        if evs is None and use_plan:
+            planned_step(d, o, dq, dk, dv)
+            return
         if evs is not None and func_mode:
             # the arbitrary-mask calls have no profiled variant: events go
             # around whole calls (the second event of each call is its start)
@@ -527,7 +549,7 @@ def main():
                 flush.zero_()
             run()
         torch.cuda.synchronize()
-        assert hstu.last_device_status(ws_b) == 0 and hstu.last_device_status(ws_f) == 0
+        assert all(hstu.last_device_status(ws) == 0 for ws in status_ws)
         return 0
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
         if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/hstu_clocks.csv")
@@ -543,7 +565,7 @@ def main():
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    assert hstu.last_device_status(ws_b) == 0 and hstu.last_device_status(ws_f) == 0
+    assert all(hstu.last_device_status(ws) == 0 for ws in status_ws)
     t_step = [b.elapsed_time(e) for b, e in zip(e_beg, e_end)]
 
     # Per-kernel pass: events between the kernels (one launch each, in
@@ -571,6 +593,19 @@ def main():
     w1.record()
     torch.cuda.synchronize()
     ms_warm = w0.elapsed_time(w1) / n_warm
+    t_plan = []
+    if use_plan:  # the plan launch alone, as it runs at the head of each planned step
+        for _ in range(n_prof):
+            if flush is not None:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            hstu.hstu_attn_plan(d["cu_seqlens_q"], d["cu_seqlens_k"], T, T, H, D, mq, mk,
+                                workspace=ws_p, **win_kw)
+            e1.record()
+            t_plan.append((e0, e1))
+        torch.cuda.synchronize()
+        t_plan = [a.elapsed_time(b) for a, b in t_plan]
     t_sched_f = [r[0].elapsed_time(r[1]) for r in timed]
     t_fwd = [r[1].elapsed_time(r[2]) for r in timed]
     t_sched_b = [r[3].elapsed_time(r[4]) for r in timed]
@@ -640,11 +675,14 @@ def main():
                 s_comp.wait_event(ev_out[b])  # step i-2's results have left this set
             g = dev_in[b]
             o_, dq_, dk_, dv_ = dev_out[b]
-            hstu.hstu_attn_fwd(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_k"], mq, mk,
-                               out=o_, workspace=ws_f, **kw)
-            hstu.hstu_attn_bwd(g["do"], g["q"], g["k"], g["v"], g["cu_seqlens_q"],
-                               g["cu_seqlens_k"], mq, mk, dq=dq_, dk=dk_, dv=dv_, workspace=ws_b,
-                               **kw)
+            if use_plan:
+                planned_step(g, o_, dq_, dk_, dv_)
+            else:
+                hstu.hstu_attn_fwd(g["q"], g["k"], g["v"], g["cu_seqlens_q"], g["cu_seqlens_k"],
+                                   mq, mk, out=o_, workspace=ws_f, **kw)
+                hstu.hstu_attn_bwd(g["do"], g["q"], g["k"], g["v"], g["cu_seqlens_q"],
+                                   g["cu_seqlens_k"], mq, mk, dq=dq_, dk=dk_, dv=dv_,
+                                   workspace=ws_b, **kw)
             ev_comp[b].record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[b])
@@ -676,15 +714,20 @@ def main():
         "config": dict(workload_config(w, lengths, args.mask),
                        l2="flushed between steps (256 MiB write)" if flush is not None else "not flushed",
                        launch=graph_note,
+                       schedule=("one hstu_attn_plan launch per step, shared by the planned "
+                                 "forward and backward" if use_plan else
+                                 "each call schedules its own work"),
                        parallelism="replicas" if world > 1 else "single GPU",
                        flops_per_step=flops_step, peaks_source=pk["source"]),
-        "per_kernel_ms": {"sched_fwd": mean(t_sched_f), "fwd": mean(t_fwd),
+        "per_kernel_ms": {"plan": mean(t_plan) if t_plan else None,
+                          "sched_fwd": mean(t_sched_f), "fwd": mean(t_fwd),
                           "sched_bwd": mean(t_sched_b), "bwd_dq": mean(t_dq),
                           "bwd_dkdv": mean(t_dkdv),
                           "sum": mean([a + b + c + e + f for a, b, c, e, f in
                                        zip(t_sched_f, t_fwd, t_sched_b, t_dq, t_dkdv)]),
                           "steps": len(timed),
-                          "note": "second pass with events between kernels (no launch overlap)"},
+                          "note": "second pass with events between kernels (no launch overlap), "
+                                  "each call scheduling its own work"},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
                      "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops_sustained"], "traffic": traffic,
@@ -693,7 +736,7 @@ def main():
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e2e_ms_step,
                 "note": "copy-in, compute and copy-out of consecutive steps overlap on three "
                         "streams; L2 not flushed (each step's inputs arrive fresh from the host)"},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": (4 if use_plan else 7 if func_mode else 5) * args.steps,
         "clocks": clk,
         "wall_s_timed_loop": wall,
     }

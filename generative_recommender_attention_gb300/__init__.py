@@ -21,11 +21,11 @@ from __future__ import annotations
 from typing import Optional, Tuple
 
 from ._lib import (HstuError, HSTU_BF16, HSTU_FP16, library, library_path,
-                   workspace_size, workspace_size_func, last_device_status, selftest_timeout,
-                   CTen, Ten)
+                   workspace_size, workspace_size_func, plan_workspace_size, last_device_status,
+                   selftest_timeout, CTen, Ten)
 
-__all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_paged", "workspace_size",
-           "last_device_status",
+__all__ = ["hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_paged", "hstu_attn_plan",
+           "HstuPlan", "workspace_size", "plan_workspace_size", "last_device_status",
            "selftest_timeout", "HstuError", "library", "library_path"]
 
 
@@ -124,11 +124,48 @@ def _stream(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
+class HstuPlan:
+    """The schedule of one batch layout (``hstu_attn_plan``): the forward's
+    and the backward's work lists, built in one launch and shared by any
+    number of ``plan=`` calls in stream order.  ``workspace`` holds it and
+    also serves as the backward's workspace."""
+
+    def __init__(self, workspace, key):
+        self.workspace = workspace
+        self.key = key
+
+    def check(self, key):
+        if key != self.key:
+            raise ValueError(f"call sizes {key} differ from the plan's {self.key}")
+
+
+def hstu_attn_plan(cu_seqlens_q, cu_seqlens_k, total_q: int, total_k: int, num_heads: int,
+                   head_dim: int, max_seqlen_q: int, max_seqlen_k: int, causal: bool = True,
+                   window_size=None, workspace=None) -> HstuPlan:
+    """Builds the schedule of one batch layout for planned calls (no host
+    synchronization: cu_seqlens are read on the device)."""
+    lib = library()
+    dev = cu_seqlens_q.device
+    B = _meta(cu_seqlens_q, cu_seqlens_k, dev)
+    win = _window(causal, window_size)
+    key = (B, int(total_q), int(total_k), int(num_heads), int(head_dim), int(max_seqlen_q),
+           int(max_seqlen_k), win)
+    ws = _workspace(workspace, plan_workspace_size(*key[:7]), dev)
+    st = lib.hstu_attn_plan(cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), *key[:7],
+                            win[0], win[1], ws.data_ptr(), ws.numel(), _stream(dev))
+    if st != 0:
+        raise HstuError(st)
+    return HstuPlan(ws, key)
+
+
 def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                   scaling_seqlen: Optional[int] = None, causal: bool = True,
                   alpha: float = 1.0, out=None, workspace=None, window_size=None,
-                  events=None, func=None):
+                  events=None, func=None, plan: Optional[HstuPlan] = None):
     """Forward HSTU attention; returns ``out`` of shape ``q.shape``.
+
+    ``plan``: an ``HstuPlan`` of this batch layout; the call then uses its
+    schedule (and ignores ``workspace``).
 
     q: (T_q, H, D); k, v: (T_k, H, D); fp16 or bf16 on a CUDA device.
     cu_seqlens_q/k: int32 (B + 1,) on the same device (values are trusted and
@@ -152,6 +189,8 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
     _check_thd("out", out, T_q, H, D, q.dtype, dev)
     win = _window(causal, window_size)
     if func is not None:
+        if plan is not None:
+            raise ValueError("arbitrary (func) masks are not planned")
         fp, fn, fl = _func_args(func, T_q, dev)
         ws = _workspace(workspace, workspace_size_func(B, T_q, T_k, H, D, max_seqlen_q,
                                                        max_seqlen_k, False), dev)
@@ -163,13 +202,21 @@ def hstu_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
         if st != 0:
             raise HstuError(st)
         return out
-    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
-                                              False), dev)
+    if plan is not None:
+        if events is not None:
+            raise ValueError("events are not recorded by planned calls")
+        plan.check((B, T_q, T_k, H, D, int(max_seqlen_q), int(max_seqlen_k), win))
+        ws = plan.workspace
+    else:
+        ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q,
+                                                  max_seqlen_k, False), dev)
     args = (_cten(q), _cten(k), _cten(v), _ten(out), cu_seqlens_q.data_ptr(),
             cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q), int(max_seqlen_q),
             int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen), win[0], win[1],
             ws.data_ptr(), ws.numel(), _stream(dev))
-    if events is None:
+    if plan is not None:
+        st = lib.hstu_attn_fwd_planned(*args)
+    elif events is None:
         st = lib.hstu_attn_fwd(*args)
     else:
         arr, n = _event_array(events)
@@ -226,7 +273,8 @@ def hstu_attn_fwd_paged(q, paged_kv, page_ids, page_indptrs, cu_seqlens_q, cu_se
 def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, scaling_seqlen: Optional[int] = None,
                   causal: bool = True, alpha: float = 1.0, dq=None, dk=None, dv=None,
-                  workspace=None, window_size=None, events=None, func=None) -> Tuple:
+                  workspace=None, window_size=None, events=None, func=None,
+                  plan: Optional[HstuPlan] = None) -> Tuple:
     """Backward HSTU attention; returns ``(dq, dk, dv)``.
 
     Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
@@ -256,6 +304,8 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     _check_thd("dv", dv, T_k, H, D, q.dtype, dev)
     win = _window(causal, window_size)
     if func is not None:
+        if plan is not None:
+            raise ValueError("arbitrary (func) masks are not planned")
         fp, fn, fl = _func_args(func, T_q, dev)
         ws = _workspace(workspace, workspace_size_func(B, T_q, T_k, H, D, max_seqlen_q,
                                                        max_seqlen_k, True), dev)
@@ -268,13 +318,21 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
         if st != 0:
             raise HstuError(st)
         return dq, dk, dv
-    ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q, max_seqlen_k,
-                                              True), dev)
+    if plan is not None:
+        if events is not None:
+            raise ValueError("events are not recorded by planned calls")
+        plan.check((B, T_q, T_k, H, D, int(max_seqlen_q), int(max_seqlen_k), win))
+        ws = plan.workspace
+    else:
+        ws = _workspace(workspace, workspace_size(B, T_q, T_k, H, D, max_seqlen_q,
+                                                  max_seqlen_k, True), dev)
     args = (_cten(dout), _cten(q), _cten(k), _cten(v), _ten(dq), _ten(dk), _ten(dv),
             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, T_q, T_k, H, D, _dtype_code(q),
             int(max_seqlen_q), int(max_seqlen_k), float(alpha), _scaling(scaling_seqlen),
             win[0], win[1], ws.data_ptr(), ws.numel(), _stream(dev))
-    if events is None:
+    if plan is not None:
+        st = lib.hstu_attn_bwd_planned(*args)
+    elif events is None:
         st = lib.hstu_attn_bwd(*args)
     else:
         arr, n = _event_array(events)

@@ -26,7 +26,8 @@ EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_att
            "hstu_attn_status_string", "hstu_attn_last_device_status",
            "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc",
            "hstu_attn_fwd_paged", "hstu_attn_fwd_func", "hstu_attn_bwd_func",
-           "hstu_attn_workspace_size_func", "hstu_lmsd_fwd", "hstu_lmsd_bwd",
+           "hstu_attn_workspace_size_func", "hstu_attn_plan_workspace_size", "hstu_attn_plan",
+           "hstu_attn_fwd_planned", "hstu_attn_bwd_planned", "hstu_lmsd_fwd", "hstu_lmsd_bwd",
            "hstu_lmsd_bwd_workspace_size")
 
 
@@ -92,6 +93,14 @@ def _declare(lib):
     lib.hstu_attn_bwd_func.argtypes = [CTen, CTen, CTen, CTen, Ten, Ten, Ten] + fscal
     lib.hstu_attn_bwd_func.restype = ctypes.c_int
     lib.hstu_attn_workspace_size_func.argtypes = lib.hstu_attn_workspace_size.argtypes
+    lib.hstu_attn_plan_workspace_size.argtypes = [i32, i64, i64, i32, i32, i32, i32]
+    lib.hstu_attn_plan_workspace_size.restype = ctypes.c_size_t
+    lib.hstu_attn_plan.argtypes = [P, P, i32, i64, i64, i32, i32, i32, i32, i32, i32, P, S, P]
+    lib.hstu_attn_plan.restype = ctypes.c_int
+    lib.hstu_attn_fwd_planned.argtypes = lib.hstu_attn_fwd.argtypes
+    lib.hstu_attn_fwd_planned.restype = ctypes.c_int
+    lib.hstu_attn_bwd_planned.argtypes = lib.hstu_attn_bwd.argtypes
+    lib.hstu_attn_bwd_planned.restype = ctypes.c_int
     lib.hstu_attn_workspace_size_func.restype = S
     # LMSD (include/hstu_lmsd.h)
     i8p = P
@@ -142,6 +151,17 @@ def workspace_size_func(batch, total_q, total_k, num_heads, head_dim, max_seqlen
                                                 int(bool(is_bwd)))
     if n == 0:
         raise ValueError("invalid sizes for hstu_attn_workspace_size_func")
+    return int(n)
+
+
+def plan_workspace_size(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
+                        max_seqlen_k) -> int:
+    """Bytes of a plan (the schedule shared by planned forward and backward calls)."""
+    n = library().hstu_attn_plan_workspace_size(int(batch), int(total_q), int(total_k),
+                                                int(num_heads), int(head_dim),
+                                                int(max_seqlen_q), int(max_seqlen_k))
+    if n == 0:
+        raise ValueError("invalid sizes for hstu_attn_plan_workspace_size")
     return int(n)
 
 

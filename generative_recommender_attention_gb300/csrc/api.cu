@@ -191,6 +191,20 @@ bool bwd_layout(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int3
   return true;
 }
 
+// A plan is the backward workspace followed by list F, the forward's query
+// tiles.  Its header records the sizes it was made for (plan_key), which
+// every planned kernel compares with its own before it starts.
+size_t plan_list_f(const BwdLayout& L) { return (L.total + 255) & ~size_t(255); }
+
+constexpr int kPlanMagic = 0x504c414e;
+
+void plan_key(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_t D, int32_t max_q,
+              int32_t max_k, Window w, int* key) {
+  const int k[kPlanKeyInts] = {kPlanMagic, batch, static_cast<int>(total_q),
+                               static_cast<int>(total_k), H, D, max_q, max_k, w.left, w.right};
+  std::memcpy(key, k, sizeof(k));
+}
+
 // Arbitrary mask: the key hull of every query-block slot, and (backward)
 // the query-block hull of every key-tile slot, appended to the workspace.
 size_t func_extra(int32_t batch, int64_t total_q, int64_t total_k, bool bwd) {
@@ -266,6 +280,18 @@ size_t hstu_attn_workspace_size_func(int32_t batch, int64_t total_q, int64_t tot
   return base + func_extra(batch, total_q, total_k, is_bwd != 0);
 }
 
+size_t hstu_attn_plan_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k) {
+  if (hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q,
+                               max_seqlen_k, 1) == 0)
+    return 0;
+  BwdLayout L;
+  if (!bwd_layout(batch, total_q, total_k, num_heads, head_dim, max_seqlen_q, &L)) return 0;
+  const size_t bytes = plan_list_f(L) + 32 * static_cast<size_t>(cap_a(batch, total_q, num_heads));
+  return (bytes + 255) & ~size_t(255);
+}
+
 }  // extern "C"
 
 namespace {
@@ -319,7 +345,8 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
                        float alpha, int32_t scaling_seqlen, int32_t window_left,
                        int32_t window_right, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream, const EventMarks& em,
-                       const PagedKV* paged = nullptr, const FuncArgs* fn = nullptr) {
+                       const PagedKV* paged = nullptr, const FuncArgs* fn = nullptr,
+                       bool planned = false) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
@@ -340,7 +367,11 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   if ((s = check_tensor(out.ptr, out.stride_t, out.stride_h, total_q, H, D)) != HSTU_OK) return s;
   if (batch == 0 || total_q == 0) return HSTU_OK;
   const size_t base_need =
-      hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 0);
+      planned ? hstu_attn_plan_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q,
+                                              max_seqlen_k)
+              : hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k,
+                                         0);
+  if (base_need == 0) return HSTU_ERR_INVALID_ARG;
   const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, false) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
@@ -376,6 +407,11 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
 
   int* header = static_cast<int*>(workspace);
   int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + kHeaderBytes);
+  if (planned) {
+    BwdLayout L;
+    if (!bwd_layout(batch, total_q, total_k, H, D, max_seqlen_q, &L)) return HSTU_ERR_UNSUPPORTED;
+    units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + plan_list_f(L));
+  }
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
@@ -386,13 +422,18 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
                          static_cast<int>(cdiv(std::max<int32_t>(max_seqlen_q, 1), 64)), fm, stream,
                          em.pdl()) != cudaSuccess)
     return HSTU_ERR_CUDA;
-  if (launch_sched(1, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (!planned && launch_sched(1, sched_bytes, stream, em.pdl(), sa) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.win = c.win; a.d_out = D; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
-  a.units = units; a.units_slot = kHdrUnitsA; a.next_slot = kHdrNextA;
+  a.units = units;
+  a.units_slot = planned ? kHdrUnitsF : kHdrUnitsA;
+  a.next_slot = planned ? kHdrNextF : kHdrNextA;
+  a.planned = planned ? 1 : 0;
+  if (planned) plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, a.key);
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.o0 = out.ptr; a.o0_st = out.stride_t; a.o0_sh = out.stride_h;
   a.fm = fm;
@@ -415,7 +456,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
                        int32_t scaling_seqlen, int32_t window_left, int32_t window_right,
                        void* workspace,
                        size_t workspace_bytes, cudaStream_t stream, const EventMarks& em,
-                       const FuncArgs* fn = nullptr) {
+                       const FuncArgs* fn = nullptr, bool planned = false) {
   Common c;
   hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, dtype, max_seqlen_q,
                                  max_seqlen_k, alpha, scaling_seqlen, window_left, window_right,
@@ -433,7 +474,11 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   BwdLayout lay;
   if (!bwd_layout(batch, total_q, total_k, H, D, max_seqlen_q, &lay)) return HSTU_ERR_UNSUPPORTED;
   const size_t base_need =
-      hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, 1);
+      planned ? hstu_attn_plan_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q,
+                                              max_seqlen_k)
+              : hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k,
+                                         1);
+  if (base_need == 0) return HSTU_ERR_INVALID_ARG;
   const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, true) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
@@ -484,12 +529,15 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
                          static_cast<int>(cdiv(std::max<int32_t>(max_seqlen_q, 1), 64)), fm, stream,
                          em.pdl()) != cudaSuccess)
     return HSTU_ERR_CUDA;
-  if (launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (!planned && launch_sched(2, sched_bytes, stream, em.pdl(), sa) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   if (!em.mark(1, stream)) return HSTU_ERR_CUDA;
 
   AttnArgs a{};
   a.total_q = total_q; a.total_k = total_k;
   a.H = H; a.win = c.win; a.d_out = D; a.alpha = alpha; a.inv_L = c.inv_L; a.header = header;
+  a.planned = planned ? 1 : 0;
+  if (planned) plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, a.key);
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
   a.fm = fm;
@@ -591,14 +639,94 @@ hstu_status_t hstu_attn_bwd_profiled(hstu_cten_t dout, hstu_cten_t q, hstu_cten_
                   EventMarks{events, n_events});
 }
 
+hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                             int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                             int32_t window_left, int32_t window_right, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  Common c;
+  // the dtype, alpha and L_scale do not enter a schedule: any valid ones
+  hstu_status_t s = check_common(batch, total_q, total_k, num_heads, head_dim, HSTU_BF16,
+                                 max_seqlen_q, max_seqlen_k, 1.f, 0, window_left, window_right,
+                                 cu_seqlens_q, cu_seqlens_k, &c);
+  if (s != HSTU_OK) return s;
+  if (batch == 0 || (total_q == 0 && total_k == 0)) return HSTU_OK;  // planned calls do nothing
+  const int H = num_heads, D = head_dim;
+  BwdLayout lay;
+  if (!bwd_layout(batch, total_q, total_k, H, D, max_seqlen_q, &lay)) return HSTU_ERR_UNSUPPORTED;
+  const size_t need =
+      hstu_attn_plan_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k);
+  if (need == 0) return HSTU_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
+  if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
+  if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
+
+  const int BN = kDsKeys, BNF = bn_for(D);
+  const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;
+  const int64_t capA = cap_a(batch, total_q, H), capB = cap_b(batch, total_k, H, D);
+  const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
+  const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));
+  const int cmaxF = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BNF)));
+  int sched_bytes, sched_cache;
+  if (!sched_smem(std::max(cmaxF, std::max(cmaxA, cmaxB)), batch, c.dev, &sched_bytes,
+                  &sched_cache))
+    return HSTU_ERR_UNSUPPORTED;
+  char* ws = static_cast<char*>(workspace);
+  SchedArgs sa{};
+  sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
+  sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA);
+  sa.units_a = reinterpret_cast<int4*>(ws + kHeaderBytes);
+  sa.bq_b = BQ; sa.split_b = D == 256 ? 2 : 1; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
+  sa.units_b = reinterpret_cast<int4*>(ws + lay.units_b);
+  sa.bn_f = BNF; sa.cmax_f = cmaxF; sa.cap_f = static_cast<int>(capA);
+  sa.units_f = reinterpret_cast<int4*>(ws + plan_list_f(lay));
+  sa.header = reinterpret_cast<int*>(ws);
+  sa.ds_base = reinterpret_cast<int*>(ws + lay.ds_base);
+  sa.ds_cap = static_cast<int>(lay.ds_blocks);
+  sa.cache_seqs = sched_cache;
+  plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, sa.key);
+  return launch_sched(3, sched_bytes, stream, true, sa) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+hstu_status_t hstu_attn_fwd_planned(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t batch, int64_t total_q, int64_t total_k,
+                                    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                    int32_t scaling_seqlen, int32_t window_left,
+                                    int32_t window_right, void* plan, size_t plan_bytes,
+                                    cudaStream_t stream) {
+  return fwd_impl(q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, num_heads,
+                  head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen, window_left,
+                  window_right, plan, plan_bytes, stream, EventMarks{nullptr, 0}, nullptr, nullptr,
+                  true);
+}
+
+hstu_status_t hstu_attn_bwd_planned(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                                    hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t batch, int64_t total_q, int64_t total_k,
+                                    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                    int32_t scaling_seqlen, int32_t window_left,
+                                    int32_t window_right, void* plan, size_t plan_bytes,
+                                    cudaStream_t stream) {
+  return bwd_impl(dout, q, k, v, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                  num_heads, head_dim, dtype, max_seqlen_q, max_seqlen_k, alpha, scaling_seqlen,
+                  window_left, window_right, plan, plan_bytes, stream, EventMarks{nullptr, 0},
+                  nullptr, true);
+}
+
 hstu_status_t hstu_attn_last_device_status(const void* workspace, cudaStream_t stream) {
   if (workspace == nullptr) return HSTU_ERR_INVALID_ARG;
-  int h[8];
+  int h[16];
   if (cudaMemcpyAsync(h, workspace, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   if (h[kHdrStatus] != 0) return static_cast<hstu_status_t>(h[kHdrStatus]);
-  if (h[kHdrOverflow] != 0 || h[kHdrOverflowB] != 0) return HSTU_ERR_INVALID_ARG;
+  if (h[kHdrOverflow] != 0 || h[kHdrOverflowB] != 0 || h[kHdrOverflowF] != 0)
+    return HSTU_ERR_INVALID_ARG;
   return HSTU_OK;
 }
 

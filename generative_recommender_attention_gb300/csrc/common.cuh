@@ -13,7 +13,9 @@ namespace hstu {
 
 // ---------------------------------------------------------------- workspace
 // Bytes [0, 256): header of int32 words.  Then list A (query-tile work units)
-// and, for the backward, list B (key-tile work units), int4 each.
+// and, for the backward, list B (key-tile work units), int4 each.  A plan
+// (one schedule shared by forward and backward calls) adds list F, the
+// forward's query tiles, and records the sizes it was made for.
 enum HeaderWord : int {
   kHdrStatus = 0,     // 0 = ok, else an hstu_status_t recorded on the device
   kHdrUnitsA = 1,     // number of units in list A
@@ -23,7 +25,14 @@ enum HeaderWord : int {
   kHdrOverflowB = 5,  // same, list B
   kHdrNextA = 6,      // next unclaimed unit of list A (atomic counter)
   kHdrNextB = 7,      // next unclaimed unit of list B
+  kHdrUnitsF = 8,     // plan: number of units in list F
+  kHdrNextF = 9,      // plan: next unclaimed unit of list F
+  kHdrOverflowF = 10, // plan: units dropped from list F
+  kHdrDone = 11,      // plan: CTAs of the running kernel that have finished
+  kHdrKey = 16,       // plan: kPlanKeyInts words (16-byte aligned), the sizes the plan was made for
 };
+constexpr int kPlanKeyInts = 10;
+static_assert(kPlanKeyInts <= 12, "the plan key is read as three int4");
 constexpr int kHeaderBytes = 256;
 constexpr int kStatusTimeout = 5;     // == HSTU_ERR_DEVICE_TIMEOUT
 constexpr int kStatusBadMeta = 1;     // == HSTU_ERR_INVALID_ARG

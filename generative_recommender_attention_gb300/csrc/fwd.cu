@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // everything below reads what earlier grids wrote (work list, inputs)
   if (a.pdl_wait == 1) grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
-  const int n_units = *reinterpret_cast<volatile int*>(a.header + a.units_slot);
+  const int n_units = work_units(a);
   const UnitQueue uq{reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4)), bar(UFULL), bar(UEMPTY)};
 
   if (warp == 0) {
@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  release_work(a);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -140,10 +140,13 @@ struct SchedArgs {
   int4* units_a;
   int bq_b, split_b, cmax_b, cap_b;  // list B: key tiles, inner tiles of bq_b queries
   int4* units_b;
+  int bn_f, cmax_f, cap_f;   // list F (plans): the forward's query tiles, bn_f-key inner tiles
+  int4* units_f;
   int* header;
   int* ds_base;              // backward: (B + 1) first dS block of each sequence, or null
   int ds_cap;                // backward: dS blocks the workspace holds
   int cache_seqs;            // 1: sequence records cached in shared memory
+  int key[kPlanKeyInts];     // plans: the sizes recorded in the header
 };
 
 // ---------------------------------------------------------------- dS blocks
@@ -207,7 +210,44 @@ struct AttnArgs {
   void* ds;             // backward: dS blocks (written by dK/dV, read by dQ)
   const int* ds_base;   // backward: first dS block of each sequence (B + 1)
   int ds_cap;           // backward: dS blocks the workspace holds
+  int planned;          // 1: the work list comes from a plan (see below)
+  int key[kPlanKeyInts];  // planned: this call's sizes, which must be the plan's
 };
+
+// A planned call checks that the plan was made for its sizes (else it
+// records HSTU_ERR_INVALID_ARG and does no work) and returns the length of
+// its work list.  Call after the grid dependency wait.
+__device__ __forceinline__ int work_units(const AttnArgs& a) {
+  if (a.planned) {
+    // one round trip: the recorded sizes as three 16-byte loads (from L2;
+    // an earlier grid wrote them), compared without short-circuiting
+    const int4* k4 = reinterpret_cast<const int4*>(a.header + kHdrKey);
+    const int4 r0 = __ldcg(k4), r1 = __ldcg(k4 + 1), r2 = __ldcg(k4 + 2);
+    const int n = __ldcg(a.header + a.units_slot);
+    const int rec[12] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w, r2.x, r2.y, r2.z, r2.w};
+    bool same = true;
+#pragma unroll
+    for (int i = 0; i < kPlanKeyInts; ++i) same &= rec[i] == a.key[i];
+    if (!same) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) atomicCAS(a.header + kHdrStatus, 0, kStatusBadMeta);
+      return 0;
+    }
+    return n;
+  }
+  return *reinterpret_cast<volatile int*>(a.header + a.units_slot);
+}
+
+// A plan serves any number of calls in stream order, so a planned kernel
+// leaves its unit counter at zero: the last CTA to finish resets it (every
+// CTA has made its last claim by then).  Call once per CTA, at its end.
+__device__ __forceinline__ void release_work(const AttnArgs& a) {
+  if (!a.planned || threadIdx.x != 0) return;
+  __threadfence();
+  if (atomicAdd(a.header + kHdrDone, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(a.header + a.next_slot, 0);
+    atomicExch(a.header + kHdrDone, 0);
+  }
+}
 
 // ------------------------------------------------------------ forward config
 // Separate K and V rings: a K stage frees as soon as S = Q K^T completes, a V

@@ -8,7 +8,10 @@
 //           keys before the first row);
 //   list B: key tiles of 128 rows; cost = number of query tiles of `bq_b`
 //           rows that can see the tile; each key tile is emitted once per head
-//           and per D split.
+//           and per D split;
+//   list F: (plans only) list A again with inner tiles of `bn_f` keys, the
+//           forward's, so that one launch schedules a forward and a backward.
+// A plan's block 0 also records the sizes the plan was made for.
 // Each unit record is two int4: {sequence, tile, head (x split), cost} and
 // {q offset, q length, k offset, k length}, so a consumer needs one round
 // trip to global memory per unit.  Units with cost 0 are kept (their rows
@@ -32,15 +35,15 @@ __device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
   return make_int4(q0, max(0, __ldg(a.cu_q + b + 1) - q0), k0, max(0, __ldg(a.cu_k + b + 1) - k0));
 }
 
-// Cost of query tile t (list A).
-__device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t) {
+// Cost of query tile t (lists A and F): its inner tiles of bn keys.
+__device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t, int bn) {
   int first, n;
   if (a.fm.func != nullptr) {  // arbitrary mask: the tile's key hull
     const int2 h = func_tile_keys(a.fm, sq.x, b, t, sq.y);
-    first = h.x / a.bn_a;
-    return h.x < h.y ? (h.y + a.bn_a - 1) / a.bn_a - first : 0;
+    first = h.x / bn;
+    return h.x < h.y ? (h.y + bn - 1) / bn - first : 0;
   }
-  query_tile_keys(t, sq.y, sq.w, a.win, a.bn_a, first, n);
+  query_tile_keys(t, sq.y, sq.w, a.win, bn, first, n);
   return n;
 }
 
@@ -68,8 +71,9 @@ __device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int b, int s)
   return n;
 }
 
-__device__ __forceinline__ int list_cmax(const SchedArgs& a, bool list_b) {
-  return list_b ? a.cmax_b : a.cmax_a;
+// Block 0 builds list A, block 1 list B, block 2 (plans) list F.
+__device__ __forceinline__ int list_cmax(const SchedArgs& a, int list) {
+  return list == 0 ? a.cmax_a : list == 1 ? a.cmax_b : a.cmax_f;
 }
 
 // Exclusive prefix sum over 1024 threads; returns this thread's offset and
@@ -108,11 +112,16 @@ __device__ int block_exclusive_scan(int v, int* total) {
 
 __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) {
   extern __shared__ int hist[];  // cost buckets, then the cached sequence records
-  int4* seqs = reinterpret_cast<int4*>(hist + sched_hist_ints(list_cmax(a, blockIdx.x == 1)));
-  const bool list_b = blockIdx.x == 1;
-  const int cmax = list_b ? a.cmax_b : a.cmax_a;
-  const int cap = list_b ? a.cap_b : a.cap_a;
-  int4* units = list_b ? a.units_b : a.units_a;
+  const int list = blockIdx.x;
+  int4* seqs = reinterpret_cast<int4*>(hist + sched_hist_ints(list_cmax(a, list)));
+  const bool list_b = list == 1;
+  const int cmax = list_cmax(a, list);
+  const int cap = list == 0 ? a.cap_a : list == 1 ? a.cap_b : a.cap_f;
+  int4* units = list == 0 ? a.units_a : list == 1 ? a.units_b : a.units_f;
+  const int bn = list == 2 ? a.bn_f : a.bn_a;  // query-tile lists
+  const int units_slot = list == 0 ? kHdrUnitsA : list == 1 ? kHdrUnitsB : kHdrUnitsF;
+  const int next_slot = list == 0 ? kHdrNextA : list == 1 ? kHdrNextB : kHdrNextF;
+  const int overflow_slot = list == 0 ? kHdrOverflow : list == 1 ? kHdrOverflowB : kHdrOverflowF;
   const int per_tile = list_b ? a.H * a.split_b : a.H;
   const int nb = cmax + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -123,17 +132,23 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   grid_dependency_wait();
   // the attention grid queued behind this one may start its prologue now
   if (tid == 0) grid_launch_dependents();
-  if (!list_b && tid == 0) {
+  if (list == 0 && tid == 0) {
     a.header[kHdrStatus] = 0;
     a.header[kHdrWhere] = 0;
+    a.header[kHdrDone] = 0;
     if (gridDim.x == 1) {
       a.header[kHdrOverflowB] = 0;
       a.header[kHdrNextB] = 0;
     }
+    if (gridDim.x < 3) {
+      a.header[kHdrOverflowF] = 0;
+      a.header[kHdrUnitsF] = 0;
+    }
+    for (int i = 0; i < kPlanKeyInts; ++i) a.header[kHdrKey + i] = a.key[i];
   }
   if (tid == 0) {
-    a.header[list_b ? kHdrOverflowB : kHdrOverflow] = 0;
-    a.header[list_b ? kHdrNextB : kHdrNextA] = 0;
+    a.header[overflow_slot] = 0;
+    a.header[next_slot] = 0;
   }
 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
@@ -150,7 +165,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int Lq = sq.y, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
     for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t);
+      const int cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
       atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
@@ -186,7 +201,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
         a.fm.kt_range[kt_slot(k0, b, t)] = r;
         cost = r.y;
       } else {
-        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t);
+        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
       }
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       for (int e = 0; e < per_tile; ++e) {
@@ -199,8 +214,8 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
       }
     }
   }
-  if (overflow) atomicExch(a.header + (list_b ? kHdrOverflowB : kHdrOverflow), 1);
-  if (tid == 0) a.header[list_b ? kHdrUnitsB : kHdrUnitsA] = min(total, cap);
+  if (overflow) atomicExch(a.header + overflow_slot, 1);
+  if (tid == 0) a.header[units_slot] = min(total, cap);
 
   // pass 4 (backward, list-B block): first dS block of each sequence
   if (list_b && a.ds_base != nullptr) {

@@ -277,6 +277,62 @@ hstu_status_t hstu_attn_fwd_noalloc(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
                                     int32_t scaling_seqlen, int32_t window_left,
                                     int32_t window_right, cudaStream_t stream);
 
+/*
+ * Plans: one schedule for every call on one batch layout.
+ *
+ * A training step runs the forward and the backward of every layer on the
+ * same packed batch, and the work lists (the tiles of every sequence, sorted
+ * longest first) depend only on the layout: cu_seqlens, the sizes and the
+ * window.  hstu_attn_plan builds the forward's and the backward's lists in
+ * one launch; hstu_attn_fwd_planned / hstu_attn_bwd_planned then start their
+ * kernels directly, with no scheduling launch of their own.  Results are
+ * those of hstu_attn_fwd / hstu_attn_bwd, bit for bit.
+ *
+ *   workspace (the plan): hstu_attn_plan_workspace_size(...) bytes,
+ *     256-byte aligned, caller-owned; it also serves as the backward's
+ *     workspace (dS blocks).  Returns 0 for invalid or unsupported sizes.
+ *   hstu_attn_plan: reads cu_seqlens on the device; arguments and errors as
+ *     for hstu_attn_bwd (without the tensors, dtype, alpha or
+ *     scaling_seqlen, which do not enter a schedule).
+ *   hstu_attn_fwd_planned / hstu_attn_bwd_planned: the arguments of
+ *     hstu_attn_fwd / hstu_attn_bwd, with the plan as the workspace.  Their
+ *     cu_seqlens must hold the values the plan was built from; their sizes
+ *     (batch, totals, heads, head_dim, max_seqlen_q/k, window) must be the
+ *     plan's: each kernel compares them with those the plan recorded and, if
+ *     they differ, writes nothing and records HSTU_ERR_INVALID_ARG for
+ *     hstu_attn_last_device_status.  Arbitrary masks and paged K/V are not
+ *     planned.
+ * Any number of planned calls may share a plan, in stream order (each
+ * kernel leaves the plan ready for the next).  Calls sharing a plan on
+ * different streams race: serialize them.  After a device-side error
+ * (HSTU_ERR_DEVICE_TIMEOUT) build the plan again.
+ */
+size_t hstu_attn_plan_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
+                                     int32_t num_heads, int32_t head_dim, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k);
+hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int32_t batch, int64_t total_q, int64_t total_k, int32_t num_heads,
+                             int32_t head_dim, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                             int32_t window_left, int32_t window_right, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+hstu_status_t hstu_attn_fwd_planned(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t out,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t batch, int64_t total_q, int64_t total_k,
+                                    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                    int32_t scaling_seqlen, int32_t window_left,
+                                    int32_t window_right, void* plan, size_t plan_bytes,
+                                    cudaStream_t stream);
+hstu_status_t hstu_attn_bwd_planned(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
+                                    hstu_ten_t dq, hstu_ten_t dk, hstu_ten_t dv,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    int32_t batch, int64_t total_q, int64_t total_k,
+                                    int32_t num_heads, int32_t head_dim, hstu_dtype_t dtype,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k, float alpha,
+                                    int32_t scaling_seqlen, int32_t window_left,
+                                    int32_t window_right, void* plan, size_t plan_bytes,
+                                    cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* hstu_attn_status_string(hstu_status_t status);
 

@@ -166,6 +166,50 @@ def test_bwd_argument_errors(lib):
     assert _call_bwd(lib, batch=0, wl=5, wr=3) == OK
 
 
+def test_plan_workspace_size(lib):
+    cdiv = lambda a, b: -(-a // b)  # noqa: E731
+    ps = lib.hstu_attn_plan_workspace_size
+    for B, Tq, Tk, H, D, mq in ((32, 20480, 20480, 4, 128, 1024), (4, 309, 309, 2, 64, 128),
+                                (16, 65536, 65536, 2, 256, 4096)):
+        capA = H * (cdiv(Tq, 128) + B)
+        want = (_bwd_bytes(B, Tq, Tk, H, D, mq) + 32 * capA + 255) // 256 * 256
+        assert ps(B, Tq, Tk, H, D, mq, mq) == want
+    assert ps(1, 10, 10, 1, 96, 10, 10) == 0
+    assert ps(1 << 20, 1 << 30, 1 << 30, 64, 64, 1 << 30, 1 << 30) == 0
+
+
+def _call_plan(lib, **over):
+    a = dict(cu_q=0x50000, cu_k=0x60000, batch=2, total_q=100, total_k=100, H=4, D=64, max_q=60,
+             max_k=60, wl=-1, wr=0, ws=0x70000, ws_bytes=1 << 22)
+    a.update(over)
+    return lib.hstu_attn_plan(a["cu_q"], a["cu_k"], a["batch"], a["total_q"], a["total_k"],
+                              a["H"], a["D"], a["max_q"], a["max_k"], a["wl"], a["wr"], a["ws"],
+                              a["ws_bytes"], None)
+
+
+def test_plan_argument_errors(lib):
+    assert _call_plan(lib, D=96) == UNSUPPORTED
+    assert _call_plan(lib, max_q=61) == INVALID
+    assert _call_plan(lib, wl=-2) == INVALID
+    assert _call_plan(lib, cu_k=None) == INVALID
+    assert _call_plan(lib, ws=None) == INVALID
+    assert _call_plan(lib, ws_bytes=4096) == INVALID
+    assert _call_plan(lib, ws=0x70040) == MISALIGNED
+    assert _call_plan(lib, batch=0) == OK
+    # planned calls need a plan-sized workspace: a forward-sized one is refused
+    fwd_bytes = lib.hstu_attn_workspace_size(2, 100, 100, 4, 64, 60, 60, 0)
+    t = L.CTen(0x10000, 256, 64)
+    o = L.Ten(0x40000, 256, 64)
+    assert lib.hstu_attn_fwd_planned(t, t, t, o, 0x50000, 0x60000, 2, 100, 100, 4, 64,
+                                     L.HSTU_BF16, 60, 60, 0.125, 0, -1, 0, 0x70000, fwd_bytes,
+                                     None) == INVALID
+    assert lib.hstu_attn_bwd_planned(t, t, t, t, o, o, o, 0x50000, 0x60000, 2, 100, 100, 4, 64,
+                                     L.HSTU_BF16, 60, 60, 0.125, 0, -1, 0, 0x70000, 1 << 10,
+                                     None) == INVALID
+    assert lib.hstu_attn_fwd_planned(t, t, t, o, 0x50000, 0x60000, 0, 100, 100, 4, 64,
+                                     L.HSTU_BF16, 60, 60, 0.125, 0, -1, 0, None, 0, None) == OK
+
+
 def _call_paged(lib, **over):
     a = dict(kv=0x20000, pages=4, ids=0x30000, ptr=0x40000, batch=2, D=64, max_q=60, max_k=60)
     a.update(over)
@@ -373,3 +417,13 @@ def test_ds_block_layout_rule():
                                                for jj in range(128 * j, 128 * j + 128))
                         running += cnt
         assert base[-1] <= H * cdiv(max(Lq), 64) * (cdiv(sum(Lk), 128) + B)
+
+
+def test_plan_key_checked_by_the_binding():
+    import generative_recommender_attention_gb300 as hstu
+    p = hstu.HstuPlan(None, (2, 100, 100, 4, 64, 60, 60, (-1, 0)))
+    p.check((2, 100, 100, 4, 64, 60, 60, (-1, 0)))
+    with pytest.raises(ValueError):
+        p.check((2, 100, 100, 4, 64, 61, 61, (-1, 0)))
+    with pytest.raises(ValueError):
+        p.check((2, 100, 100, 4, 64, 60, 60, (-1, -1)))
