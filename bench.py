@@ -246,6 +246,15 @@ def run_lmsd(args, dev):
         return statistics.mean(a.elapsed_time(b) for a, b in ts)
 
     ms_f, ms_b = timed(fwd), timed(bwd)
+    # DRAM bytes of one forward and one backward launch, from the committed
+    # ncu summary of this size (lines "traffic <kernel> <bytes>"), if any
+    traffic = {}
+    tfile = os.path.join(ROOT, "profiles", f"kernels_lmsd_{n}x{d}.md")
+    if os.path.exists(tfile):
+        for tline in open(tfile):
+            parts = tline.split()
+            if len(parts) == 3 and parts[0] == "traffic":
+                traffic[parts[1]] = int(parts[2])
     bytes_f = n * d * 2 * 2 + n * 3 * d * 2 + n * d + n * 8
     bytes_b = n * 3 * d * 2 + n * d * 2 * 2 + n * d + n * 8 + n * d * 2 * 2
     pk = peaks()
@@ -261,7 +270,8 @@ def run_lmsd(args, dev):
         "roofline": {"bound": "hbm", "achieved": (bytes_f + bytes_b) / ((ms_f + ms_b) * 1e-3) / 1e9,
                      "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": (bytes_f + bytes_b) / ((ms_f + ms_b) * 1e-3) / 1e9 / pk["hbm_gbs"],
-                     "traffic": None},
+                     "traffic": (sum(traffic.values()) if len(traffic) == 2 else None),
+                     "traffic_note": "ncu DRAM bytes of one forward plus one backward launch"},
         "config": {"workload": f"LMSD N={n} D={d}", "dropout_ratio": p, "apply_u_silu": True,
                    "concat_u": True, "concat_x": True,
                    "l2": "flushed between calls (256 MiB write)", "launch": timed.note},
