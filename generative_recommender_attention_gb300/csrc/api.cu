@@ -207,10 +207,19 @@ void plan_key(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_
 
 // Arbitrary mask: the key hull of every query-block slot, and (backward)
 // the query-block hull of every key-tile slot, appended to the workspace.
-size_t func_extra(int32_t batch, int64_t total_q, int64_t total_k, bool bwd) {
+// Layout: qb_range | kt_range (backward) | qb_bits, each 256-byte aligned.
+int func_kt_words(int32_t max_k) {
+  return static_cast<int>(std::max<int64_t>(1, cdiv(cdiv(std::max<int32_t>(max_k, 1), kBM), 32)));
+}
+size_t func_bits_off(int32_t batch, int64_t total_q, int64_t total_k, bool bwd) {
   const size_t qb = 8 * static_cast<size_t>(total_q / 64 + batch + 1);
   const size_t kt = bwd ? 8 * static_cast<size_t>(total_k / kBM + batch + 1) : 0;
-  return ((qb + 255) & ~size_t(255)) + kt;
+  return ((qb + 255) & ~size_t(255)) + ((kt + 255) & ~size_t(255));
+}
+size_t func_extra(int32_t batch, int64_t total_q, int64_t total_k, int32_t max_k, bool bwd) {
+  return func_bits_off(batch, total_q, total_k, bwd) +
+         4 * static_cast<size_t>(func_kt_words(max_k)) *
+             static_cast<size_t>(total_q / 64 + batch + 1);
 }
 
 // Arbitrary-mask arguments of a call (func null: none).
@@ -277,7 +286,7 @@ size_t hstu_attn_workspace_size_func(int32_t batch, int64_t total_q, int64_t tot
   const size_t base = hstu_attn_workspace_size(batch, total_q, total_k, num_heads, head_dim,
                                                max_seqlen_q, max_seqlen_k, is_bwd);
   if (base == 0) return 0;
-  return base + func_extra(batch, total_q, total_k, is_bwd != 0);
+  return base + func_extra(batch, total_q, total_k, max_seqlen_k, is_bwd != 0);
 }
 
 size_t hstu_attn_plan_workspace_size(int32_t batch, int64_t total_q, int64_t total_k,
@@ -311,7 +320,8 @@ struct EventMarks {
 // Validates the arbitrary-mask arguments and builds the device view over
 // the workspace tail that starts at `tail` (bytes into the workspace).
 hstu_status_t func_setup(const FuncArgs* fn, int32_t batch, int64_t total_q, int64_t total_k,
-                         char* ws, size_t tail, bool bwd, Common* c, FuncMask* fm) {
+                         int32_t max_k, char* ws, size_t tail, bool bwd, Common* c,
+                         FuncMask* fm) {
   *fm = FuncMask{};
   if (fn == nullptr) return HSTU_OK;
   if (fn->n < 1 || fn->n % 2 != 1 || fn->len < total_q) return HSTU_ERR_INVALID_ARG;
@@ -325,7 +335,8 @@ hstu_status_t func_setup(const FuncArgs* fn, int32_t batch, int64_t total_q, int
   if (bwd)
     fm->kt_range = reinterpret_cast<int2*>(
         ws + tail + ((8 * static_cast<size_t>(total_q / 64 + batch + 1) + 255) & ~size_t(255)));
-  (void)total_k;
+  fm->qb_bits = reinterpret_cast<uint32_t*>(ws + tail + func_bits_off(batch, total_q, total_k, bwd));
+  fm->kt_words = func_kt_words(max_k);
   return HSTU_OK;
 }
 
@@ -372,11 +383,13 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
               : hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k,
                                          0);
   if (base_need == 0) return HSTU_ERR_INVALID_ARG;
-  const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, false) : 0);
+  const size_t need =
+      base_need + (fn ? func_extra(batch, total_q, total_k, max_seqlen_k, false) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
   FuncMask fm;
-  if ((s = func_setup(fn, batch, total_q, total_k, static_cast<char*>(workspace), base_need, false,
+  if ((s = func_setup(fn, batch, total_q, total_k, max_seqlen_k, static_cast<char*>(workspace),
+                      base_need, false,
                       &c, &fm)) != HSTU_OK)
     return s;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
@@ -479,11 +492,13 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
               : hstu_attn_workspace_size(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k,
                                          1);
   if (base_need == 0) return HSTU_ERR_INVALID_ARG;
-  const size_t need = base_need + (fn ? func_extra(batch, total_q, total_k, true) : 0);
+  const size_t need =
+      base_need + (fn ? func_extra(batch, total_q, total_k, max_seqlen_k, true) : 0);
   if (workspace == nullptr || workspace_bytes < need) return HSTU_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return HSTU_ERR_MISALIGNED;
   FuncMask fm;
-  if ((s = func_setup(fn, batch, total_q, total_k, static_cast<char*>(workspace), base_need, true,
+  if ((s = func_setup(fn, batch, total_q, total_k, max_seqlen_k, static_cast<char*>(workspace),
+                      base_need, true,
                       &c, &fm)) != HSTU_OK)
     return s;
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;

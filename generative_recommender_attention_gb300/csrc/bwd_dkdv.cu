@@ -51,12 +51,19 @@ namespace hstu {
 namespace {
 
 // First 64-query block a key tile visits (count: U.n): the window's rule, or
-// under an arbitrary mask the hull the scheduler recorded.
+// under an arbitrary mask the start of the hull the scheduler recorded (the
+// unit then visits the U.n live blocks of the hull).
 __device__ __forceinline__ int unit_first_qblock(const AttnArgs& a, const UnitInfo& U, int bq) {
   if (a.fm.func != nullptr) return a.fm.kt_range[kt_slot(U.k0, U.b, U.tile)].x;
   int m0, cnt;
   key_tile_queries(U.tile, U.Lq, U.Lk, a.win, bq, m0, cnt);
   return m0;
+}
+
+// Arbitrary mask: the end of that hull.
+__device__ __forceinline__ int unit_qblock_end(const AttnArgs& a, const UnitInfo& U) {
+  const int2 r = a.fm.kt_range[kt_slot(U.k0, U.b, U.tile)];
+  return r.x + r.y;
 }
 
 // A key tile whose 128 rows all belong to its sequence (and to the tensor)
@@ -218,7 +225,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
           const int blk = b0 + (U.hz / SPLIT) * ((b1 - b0) / a.H) +
                           ds_block_off(U.tile, U.Lq, U.Lk, a.win);
-          U.ds = (blk >= 0 && static_cast<int64_t>(blk) + U.n <= a.ds_cap) ? blk : -1;
+          // an arbitrary mask stores its live blocks at their places in the hull
+          const int span = FUNC ? unit_qblock_end(a, U) - unit_first_qblock(a, U, BQ) : U.n;
+          U.ds = (blk >= 0 && static_cast<int64_t>(blk) + span <= a.ds_cap) ? blk : -1;
         }
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
@@ -228,6 +237,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int k_row0 = U.k0 + kBM * U.tile;
         const int q_seq0 = U.q0;
         const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
+        const int m_end = FUNC ? unit_qblock_end(a, U) : 0;
+        int m_next = m0;  // live-block cursor (arbitrary mask)
         const int kb = kvi % NKV;
         if constexpr (STAGE) {
           // buffer kb last held the unit before the previous one
@@ -269,7 +280,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
           }
           const int s = qi % NS;
-          const int row = q_seq0 + BQ * (m0 + m);
+          int qm = m0 + m;
+          if constexpr (FUNC) {
+            qm = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+            m_next = qm + 1;
+          }
+          const int row = q_seq0 + BQ * qm;
           if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(QFULL + s), C::Q_BYTES);
 #pragma unroll
@@ -452,6 +468,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       }
       const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
       constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
+      const int m_end = func ? unit_qblock_end(a, U) : 0;
+      int m_next = m0;  // live-block cursor (arbitrary mask)
       // valid queries of this key row: lo <= i < hi; every key row of the
       // warp is seen by queries [lo_all, hi_all)
       const int lo = a.win.right < 0 ? 0 : j - a.win.right;
@@ -468,7 +486,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const bool key_ok = j < Lk;
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
-        const int ic = BQ * (m0 + m) + q_first;  // first query of this warp's columns
+        int qm = m0 + m;  // this step's query block
+        if constexpr (func) {
+          qm = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+          m_next = qm + 1;
+        }
+        const int ic = BQ * qm + q_first;  // first query of this warp's columns
         const bool need_mask = ic < lo_all || ic + CW > hi_all;
         // valid queries of this warp's columns (bit e: query ic + e), the run
         // of bits [lo - ic, hi - ic) clamped to [0, CW)
@@ -537,7 +560,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (ds_row != nullptr) {
           // pd[e] = (dS[q0 + 2e][r], dS[q0 + 2e + 1][r]); the even lane keeps
           // query q0 + 2e for keys (r, r + 1), the odd lane query q0 + 2e + 1
-          uint32_t* dst = reinterpret_cast<uint32_t*>(ds_row + static_cast<int64_t>(m) * kDsBlockBytes);
+          uint32_t* dst =
+              reinterpret_cast<uint32_t*>(ds_row + static_cast<int64_t>(qm - m0) * kDsBlockBytes);
           const bool odd = (lane & 1) != 0;
 #pragma unroll
           for (int e = 0; e < CW / 2; ++e) {

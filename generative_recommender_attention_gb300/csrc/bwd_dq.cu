@@ -104,33 +104,50 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int head_blk = b0 + h * ((b1 - b0) / a.H);  // this head's first block
         const bool second = 2 * i + 1 < n_qb;            // the tile's upper 64 queries exist
         const uint32_t bytes = (second ? 2 : 1) * kDsBlockBytes + C::K_BYTES;
-        int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
+        // the unit's key tiles: kt0 .. kt0 + U.n - 1, or under an arbitrary
+        // mask the U.n live tiles of the hull [kt0, kt_end)
+        int kt0, nkt, kt_end = 0;
         const bool func = a.fm.func != nullptr;
-        if (func)
-          kt0 = func_tile_keys(a.fm, U.q0, U.b, i, U.Lq).x / kDsKeys;
-        else
+        if (func) {
+          const int2 hk = func_tile_keys(a.fm, U.q0, U.b, i, U.Lq);
+          kt0 = hk.x / kDsKeys;
+          kt_end = (hk.y + kDsKeys - 1) / kDsKeys;
+        } else {
           query_tile_keys(i, U.Lq, U.Lk, a.win, kDsKeys, kt0, nkt);
+        }
         // blocks of the key tiles before (an arbitrary mask keeps n_qb slots per
         // key tile, the full mask's layout)
         int off = ds_block_off(kt0, U.Lq, U.Lk, a.win);
+        int kt_next = kt0;  // live-tile cursor (arbitrary mask)
         for (int jj = 0; jj < U.n; ++jj, ++g) {
-          const int s = g % NS, j = kt0 + jj;
+          const int s = g % NS;
+          int j = kt0 + jj;
+          if (func) {
+            j = func_next_tile(a.fm, U.q0, U.b, i, U.Lq, kDsKeys, kt_next, kt_end);
+            kt_next = j + 1;
+            off = j * n_qb;  // the full mask's layout
+          }
           if (!wait_bar(bar(EMPTY + s), ((g / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
-          // query blocks 2i and 2i + 1 of key tile j; a block the window leaves
+          // query blocks 2i and 2i + 1 of key tile j; a block the mask leaves
           // empty was never stored and is read as zeros from an out-of-range
           // block index (the TMA fill; the box still counts in full)
           int m0, cnt;
+          bool live0 = true, live1 = true;
           if (func) {
             const int2 r = a.fm.kt_range[kt_slot(U.k0, U.b, j)];
             m0 = r.x;
             cnt = r.y;
+            live0 = func_live(a.fm, U.q0, U.b, 2 * i, j);
+            live1 = second && func_live(a.fm, U.q0, U.b, 2 * i + 1, j);
           } else {
             ds_blocks_of(j, U.Lq, U.Lk, a.win, m0, cnt);
           }
-          const int blk0 = (2 * i >= m0 && 2 * i < m0 + cnt) ? head_blk + off + 2 * i - m0 : -1;
-          const int blk1 =
-              (2 * i + 1 >= m0 && 2 * i + 1 < m0 + cnt) ? head_blk + off + 2 * i + 1 - m0 : -1;
-          off += func ? n_qb : cnt;
+          const int blk0 =
+              (live0 && 2 * i >= m0 && 2 * i < m0 + cnt) ? head_blk + off + 2 * i - m0 : -1;
+          const int blk1 = (live1 && 2 * i + 1 >= m0 && 2 * i + 1 < m0 + cnt)
+                               ? head_blk + off + 2 * i + 1 - m0
+                               : -1;
+          if (!func) off += cnt;
           mbar_arrive_expect_tx(bar(FULL + s), bytes);
           // A tile: 64-key chunk c of query rows 0-63 (block 2i) and 64-127 (2i + 1)
 #pragma unroll

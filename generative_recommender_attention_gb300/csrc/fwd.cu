@@ -150,12 +150,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (U.n <= 0) continue;
         const int h = U.hz;
         const int q_row0 = U.q0 + kBM * U.tile;
-        int kt0, nkt;  // the unit's key tiles: kt0 .. kt0 + U.n - 1
-        if (a.fm.func != nullptr)
-          kt0 = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq).x / BN;
-        else
+        // the unit's key tiles: kt0 .. kt0 + U.n - 1, or under an arbitrary
+        // mask the U.n live tiles of the hull [kt0, kt_end)
+        int kt0, nkt, kt_end = 0;
+        if constexpr (FUNC) {
+          const int2 hk = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq);
+          kt0 = hk.x / BN;
+          kt_end = (hk.y + BN - 1) / BN;
+        } else {
           query_tile_keys(U.tile, U.Lq, U.Lk, a.win, BN, kt0, nkt);
+        }
         const int kv_row0 = U.k0 + BN * kt0;
+        int kt_next = kt0;  // live-tile cursor
         // Paged K/V: key tile kt lives in page page_ids[page_indptrs[b] +
         // kt BN / 128], whose K rows start at row 256 p and V rows at
         // 256 p + 128 of the cache's map.  The next tile's page is looked up
@@ -178,6 +184,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // the forward's own tile loads more than they saved.
         for (int n = 0; n < U.n; ++n) {
           int row = kv_row0 + BN * n, vrow = row;
+          if constexpr (FUNC) {
+            const int kt = func_next_tile(a.fm, U.q0, U.b, U.tile, U.Lq, BN, kt_next, kt_end);
+            kt_next = kt + 1;
+            row = vrow = U.k0 + BN * kt;
+          }
           if (paged) {
             const int kt = kt0 + n, pg = pg_next;
             if (n + 1 < U.n) pg_next = __ldg(a.page_ids + pi0 + ((kt + 1) * BN) / 128);
@@ -293,12 +304,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int Lk = U.Lk;
       const int i = kBM * U.tile + r;
       const int i_warp = kBM * U.tile + wq * 32;  // first row of this warp
-      int kt0, nkt;
+      int kt0, nkt, kt_end = 0;
       constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
-      if (func)
-        kt0 = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq).x / BN;
-      else
+      if constexpr (func) {
+        const int2 hk = func_tile_keys(a.fm, U.q0, U.b, U.tile, U.Lq);
+        kt0 = hk.x / BN;
+        kt_end = (hk.y + BN - 1) / BN;
+      } else {
         query_tile_keys(U.tile, U.Lq, Lk, a.win, BN, kt0, nkt);
+      }
+      int kt_next = kt0;  // live-tile cursor (arbitrary mask)
+      // arbitrary mask: this row's first endpoints, read once per unit
+      int fe0 = 0, fe1 = 0, fe2 = 0;
+      if constexpr (func) {
+        const int64_t tr = static_cast<int64_t>(U.q0) + (i < U.Lq ? i : 0);
+        fe0 = __ldg(a.fm.func + tr);
+        if (a.fm.n >= 3) {
+          fe1 = __ldg(a.fm.func + a.fm.len + tr);
+          fe2 = __ldg(a.fm.func + 2 * a.fm.len + tr);
+        }
+      }
       const int64_t t_row = static_cast<int64_t>(U.q0) + (i < U.Lq ? i : 0);  // func row (any, if past Lq)
       // valid keys of this row: lo <= j < hi; every row of the warp sees
       // [lo_all, hi_all)
@@ -307,27 +332,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int lo_all = a.win.left < 0 ? 0 : i_warp + 31 - a.win.left;
       const int hi_all = a.win.right < 0 ? Lk : min(Lk, i_warp + a.win.right + 1);
       for (int n = 0; n < U.n; ++n, ++g) {
+        int kt = kt0 + n;
+        if constexpr (func) {  // every warp walks every step to keep the cursor
+          kt = func_next_tile(a.fm, U.q0, U.b, U.tile, U.Lq, BN, kt_next, kt_end);
+          kt_next = kt + 1;
+        }
         if (static_cast<int>(g & 1) != par) continue;
         const int sb = g % NSB;
+        // arbitrary mask: the row's valid keys of each chunk, formed while S lands
+        uint64_t fbs[NCH];
+        if constexpr (func) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            fbs[c] = func_row_bits3(a.fm, t_row, fe0, fe1, fe2, BN * kt + 64 * c, Lk);
+        }
         if (!wait_bar_warp(bar(SFULL + sb), (g / NSB) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          const int jc = BN * (kt0 + n) + 64 * c;  // first key of this chunk
+          const int jc = BN * kt + 64 * c;  // first key of this chunk
           const bool need_mask = jc < lo_all || jc + 64 > hi_all;
           uint32_t x[64];
           tmem_ld64(tS + sb * BN + 64 * c, x);
           uint32_t p[32];
-          if constexpr (func) {
-            // arbitrary mask: this row's valid keys of the chunk, from its endpoints
-            const uint64_t fb = func_row_bits(a.fm, t_row, jc, Lk);
+          if (func && !__all_sync(0xffffffffu, fbs[c] == ~0ull)) {
+            // arbitrary mask, some key of the chunk invalid for some row
+            const uint64_t fb = fbs[c];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const uint32_t s0 = ((fb >> (2 * e)) & 1ull) ? x[2 * e] : 0u;
               const uint32_t s1 = ((fb >> (2 * e + 1)) & 1ull) ? x[2 * e + 1] : 0u;
               p[e] = silu_pair<BF16>(s0, s1, half_alpha);
             }
-          } else if (!need_mask) {
+          } else if (func || !need_mask) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) p[e] = silu_pair<BF16>(x[2 * e], x[2 * e + 1], half_alpha);
           } else if (jc >= lo_all) {

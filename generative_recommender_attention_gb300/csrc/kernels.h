@@ -93,12 +93,18 @@ __host__ __device__ inline void key_tile_queries(int s, int Lq, int Lk, Window w
 //     scheduler.
 // Slots are floor(offset / tile) + b + index, disjoint between sequences
 // without a scan (floor((o + L) / n) + 1 >= floor(o / n) + ceil(L / n)).
+//   qb_bits[qb_slot(b, m) * kt_words + s / 32], bit s % 32: 128-key tile s
+//     is live for query block m (some row of the block sees a key of the
+//     tile), written by the range kernel.  Units visit only live tiles (and
+//     key tiles only live query blocks) inside their hulls.
 struct FuncMask {
   const int32_t* func;  // null: no arbitrary mask (the window decides)
   int n;
   int64_t len;
   int2* qb_range;
   int2* kt_range;
+  uint32_t* qb_bits;
+  int kt_words;         // ceil(ceil(max_seqlen_k / 128) / 32)
 };
 __host__ __device__ inline int qb_slot(int q0, int b, int m) { return q0 / 64 + b + m; }
 __host__ __device__ inline int kt_slot(int k0, int b, int s) { return k0 / kBM + b + s; }
@@ -113,6 +119,33 @@ __device__ inline int2 func_tile_keys(const FuncMask& f, int q0, int b, int t, i
   return h;
 }
 
+// 128-key tile s is live for 64-row query block m of sequence b.
+__device__ __forceinline__ bool func_live(const FuncMask& f, int q0, int b, int m, int s) {
+  const uint32_t w =
+      __ldg(f.qb_bits + static_cast<int64_t>(qb_slot(q0, b, m)) * f.kt_words + (s >> 5));
+  return (w >> (s & 31)) & 1u;
+}
+
+// First tile t' >= t (tiles of bn = 64 or 128 keys) that is live for 128-row
+// query tile tq, i.e. for its block 2 tq or, inside the sequence, 2 tq + 1;
+// t_end if none before it.
+__device__ __forceinline__ int func_next_tile(const FuncMask& f, int q0, int b, int tq, int Lq,
+                                              int bn, int t, int t_end) {
+  const bool two = kBM * tq + 64 < Lq;
+  for (; t < t_end; ++t) {
+    const int s = t * bn / kBM;
+    if (func_live(f, q0, b, 2 * tq, s) || (two && func_live(f, q0, b, 2 * tq + 1, s))) break;
+  }
+  return t;
+}
+
+// First query block m' >= m for which 128-key tile s is live; m_end if none.
+__device__ __forceinline__ int func_next_qblock(const FuncMask& f, int q0, int b, int s, int m,
+                                                int m_end) {
+  while (m < m_end && !func_live(f, q0, b, m, s)) ++m;
+  return m;
+}
+
 // Bits [lo - base, hi - base) of an n-bit word (n = 32 or 64), clamped.
 __device__ __forceinline__ uint64_t bit_range64(int lo, int hi, int base) {
   const int e0 = imin(imax(lo - base, 0), 64), e1 = imin(imax(hi - base, 0), 64);
@@ -122,6 +155,18 @@ __device__ __forceinline__ uint64_t bit_range64(int lo, int hi, int base) {
 }
 // Arbitrary mask: valid keys of query token t among keys [base, base + 64),
 // cut to j < Lk, as bits (bit e: key base + e).
+// The same, with the row's first three endpoints already in registers
+// (e0 = F0, e1 = F1, e2 = F2; the rest, if any, are read).
+__device__ __forceinline__ uint64_t func_row_bits3(const FuncMask& f, int64_t t, int e0, int e1,
+                                                   int e2, int base, int Lk) {
+  uint64_t m = bit_range64(0, imin(e0, Lk), base);
+  if (f.n >= 3) m |= bit_range64(e1, imin(e2, Lk), base);
+  for (int n = 3; n + 1 < f.n; n += 2)
+    m |= bit_range64(__ldg(f.func + n * f.len + t), imin(__ldg(f.func + (n + 1) * f.len + t), Lk),
+                     base);
+  return m;
+}
+
 __device__ __forceinline__ uint64_t func_row_bits(const FuncMask& f, int64_t t, int base, int Lk) {
   uint64_t m = bit_range64(0, imin(__ldg(f.func + t), Lk), base);
   for (int n = 1; n + 1 < f.n; n += 2)

@@ -38,10 +38,15 @@ __device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
 // Cost of query tile t (lists A and F): its inner tiles of bn keys.
 __device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t, int bn) {
   int first, n;
-  if (a.fm.func != nullptr) {  // arbitrary mask: the tile's key hull
+  if (a.fm.func != nullptr) {  // arbitrary mask: the live tiles of the tile's key hull
     const int2 h = func_tile_keys(a.fm, sq.x, b, t, sq.y);
-    first = h.x / bn;
-    return h.x < h.y ? (h.y + bn - 1) / bn - first : 0;
+    if (h.x >= h.y) return 0;
+    const int t1 = (h.y + bn - 1) / bn;
+    n = 0;
+    for (int u = func_next_tile(a.fm, sq.x, b, t, sq.y, bn, h.x / bn, t1); u < t1;
+         u = func_next_tile(a.fm, sq.x, b, t, sq.y, bn, u + 1, t1))
+      ++n;
+    return n;
   }
   query_tile_keys(t, sq.y, sq.w, a.win, bn, first, n);
   return n;
@@ -63,9 +68,21 @@ __device__ __forceinline__ int2 func_key_tile_queries(const SchedArgs& a, int4 s
   return m1 > m0 ? make_int2(m0, m1 - m0) : make_int2(0, 0);
 }
 
+// Arbitrary mask: the query blocks of hull r (first, count) for which key
+// tile s is live.
+__device__ __forceinline__ int func_live_qblocks(const SchedArgs& a, int4 sq, int b, int s,
+                                                 int2 r) {
+  int n = 0;
+  for (int m = func_next_qblock(a.fm, sq.x, b, s, r.x, r.x + r.y); m < r.x + r.y;
+       m = func_next_qblock(a.fm, sq.x, b, s, m + 1, r.x + r.y))
+    ++n;
+  return n;
+}
+
 // Cost of key tile s (list B).
 __device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int b, int s) {
-  if (a.fm.func != nullptr) return func_key_tile_queries(a, sq, b, s).y;  // bq_b == 64
+  if (a.fm.func != nullptr)  // bq_b == 64: the live blocks of the hull
+    return func_live_qblocks(a, sq, b, s, func_key_tile_queries(a, sq, b, s));
   int first, n;
   key_tile_queries(s, sq.y, sq.w, a.win, a.bq_b, first, n);
   return n;
@@ -199,7 +216,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
       if (list_b && a.fm.func != nullptr) {  // also record the key tile's query hull
         const int2 r = func_key_tile_queries(a, sq, b, t);
         a.fm.kt_range[kt_slot(k0, b, t)] = r;
-        cost = r.y;
+        cost = func_live_qblocks(a, sq, b, t, r);
       } else {
         cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
       }
@@ -242,9 +259,19 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   }
 }
 
+// Bits of the 128-key tiles 32 w .. 32 w + 31 that keys [a, c) touch.
+__device__ __forceinline__ uint32_t tile_bits(int a, int c, int w) {
+  if (a >= c) return 0u;
+  const int t0 = max(a / kBM - 32 * w, 0), t1 = min((c - 1) / kBM - 32 * w, 31);
+  if (t0 > t1) return 0u;
+  const uint32_t upto = t1 == 31 ? 0xffffffffu : (2u << t1) - 1u;  // bits 0 .. t1
+  return upto & ~((1u << t0) - 1u);
+}
+
 // Arbitrary mask: one warp per 64-row query block; each lane takes two rows,
 // forms each row's key hull from its endpoints (every interval cut to
-// [0, Lk)), and the warp reduces the 64 hulls to the block's.
+// [0, Lk)), and the warp reduces the 64 hulls to the block's; the same for
+// the block's live-tile bitmap (OR of the tiles every interval touches).
 __global__ void __launch_bounds__(256) hstu_func_ranges_kernel(const int32_t* cu_q,
                                                                const int32_t* cu_k, FuncMask fm) {
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -271,6 +298,22 @@ __global__ void __launch_bounds__(256) hstu_func_ranges_kernel(const int32_t* cu
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
   if (lane == 0) fm.qb_range[qb_slot(q0, b, m)] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
+  // the block's live 128-key tiles, 32 per word: the tiles each interval touches
+  uint32_t* bits = fm.qb_bits + static_cast<int64_t>(qb_slot(q0, b, m)) * fm.kt_words;
+  for (int w = 0; w < fm.kt_words; ++w) {
+    uint32_t word = 0;
+    for (int rr = 0; rr < 2; ++rr) {
+      const int i = 64 * m + 32 * rr + lane;
+      if (i >= Lq) continue;
+      const int64_t t = static_cast<int64_t>(q0) + i;
+      word |= tile_bits(0, min(__ldg(fm.func + t), Lk), w);
+      for (int n = 1; n + 1 < fm.n; n += 2)
+        word |= tile_bits(max(__ldg(fm.func + n * fm.len + t), 0),
+                          min(__ldg(fm.func + (n + 1) * fm.len + t), Lk), w);
+    }
+    word = __reduce_or_sync(0xffffffffu, word);
+    if (lane == 0) bits[w] = word;
+  }
 }
 
 cudaError_t launch_func_ranges(const int32_t* cu_q, const int32_t* cu_k, int B, int max_qb,
