@@ -408,6 +408,9 @@ def main():
     ap.add_argument("--paged", action="store_true",
                     help="time the causal forward over a paged K/V cache (the workload's keys "
                          "in shuffled 128-row pages) beside the contiguous forward; one JSON line")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="run the workload with another head dimension (32, 64, 128 or 256), "
+                         "alpha = 1/sqrt(D); the name gets a _d<D> suffix")
     ap.add_argument("--plan", action="store_true",
                     help="one hstu_attn_plan launch per step shared by the planned forward and "
                          "backward, instead of hstu_attn_fwd + hstu_attn_bwd scheduling each call")
@@ -426,6 +429,10 @@ def main():
     import torch
     from generative_recommender_attention_gb300 import workloads
     w = workloads.WORKLOADS[args.workload]
+    if args.head_dim is not None and args.head_dim != w.head_dim:
+        import dataclasses as _dc
+        w = _dc.replace(w, name=f"{w.name}_d{args.head_dim}", head_dim=args.head_dim,
+                        alpha=1.0 / math.sqrt(args.head_dim))
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -470,6 +470,24 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
       const int m_end = func ? unit_qblock_end(a, U) : 0;
       int m_next = m0;  // live-block cursor (arbitrary mask)
+      // arbitrary mask: the first three endpoints of this lane's query row,
+      // loaded one step ahead so their latency hides behind a half-step
+      int qm_ahead = 0, e0 = 0, e1 = 0, e2 = 0;
+      auto ends = [&](int qm, int& f0, int& f1, int& f2) {
+        const int iq = BQ * qm + q_first + lane;
+        const int64_t t = static_cast<int64_t>(U.q0) + (iq < Lq ? iq : 0);
+        f0 = __ldg(a.fm.func + t);
+        f1 = f2 = 0;
+        if (a.fm.n >= 3) {
+          f1 = __ldg(a.fm.func + a.fm.len + t);
+          f2 = __ldg(a.fm.func + 2 * a.fm.len + t);
+        }
+      };
+      if constexpr (func) {
+        qm_ahead = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+        m_next = qm_ahead + 1;
+        ends(qm_ahead, e0, e1, e2);
+      }
       // valid queries of this key row: lo <= i < hi; every key row of the
       // warp is seen by queries [lo_all, hi_all)
       const int lo = a.win.right < 0 ? 0 : j - a.win.right;
@@ -487,9 +505,15 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       for (int m = 0; m < U.n; ++m, ++h) {
         const int b = h & 1;
         int qm = m0 + m;  // this step's query block
+        int f0 = 0, f1 = 0, f2 = 0;
         if constexpr (func) {
-          qm = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
-          m_next = qm + 1;
+          qm = qm_ahead;
+          f0 = e0; f1 = e1; f2 = e2;
+          if (m + 1 < U.n) {  // the next step's block and endpoints
+            qm_ahead = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+            m_next = qm_ahead + 1;
+            ends(qm_ahead, e0, e1, e2);
+          }
         }
         const int ic = BQ * qm + q_first;  // first query of this warp's columns
         const bool need_mask = ic < lo_all || ic + CW > hi_all;
@@ -501,8 +525,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           // warp's 32 key rows from its endpoints; 32 ballots transpose them
           // into each key row's valid queries
           const int jw = j_warp_last - 31, iq = ic + lane;
-          const uint32_t mq = iq < Lq ? static_cast<uint32_t>(func_row_bits(
-                                            a.fm, static_cast<int64_t>(U.q0) + iq, jw, Lk))
+          const uint32_t mq = iq < Lq ? static_cast<uint32_t>(func_row_bits3(
+                                            a.fm, static_cast<int64_t>(U.q0) + iq, f0, f1, f2,
+                                            jw, Lk))
                                       : 0u;
           uint32_t mine = 0;
 #pragma unroll
