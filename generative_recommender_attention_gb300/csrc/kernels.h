@@ -154,22 +154,14 @@ __device__ __forceinline__ uint64_t bit_range64(int lo, int hi, int base) {
   return below1 & ~((1ull << e0) - 1);
 }
 // Arbitrary mask: valid keys of query token t among keys [base, base + 64),
-// cut to j < Lk, as bits (bit e: key base + e).
-// The same, with the row's first three endpoints already in registers
-// (e0 = F0, e1 = F1, e2 = F2; the rest, if any, are read).
+// cut to j < Lk, as bits (bit e: key base + e).  The caller passes the row's
+// first three endpoints (e0 = F0, e1 = F1, e2 = F2, read ahead of use); the
+// rest, if any, are read here.
 __device__ __forceinline__ uint64_t func_row_bits3(const FuncMask& f, int64_t t, int e0, int e1,
                                                    int e2, int base, int Lk) {
   uint64_t m = bit_range64(0, imin(e0, Lk), base);
   if (f.n >= 3) m |= bit_range64(e1, imin(e2, Lk), base);
   for (int n = 3; n + 1 < f.n; n += 2)
-    m |= bit_range64(__ldg(f.func + n * f.len + t), imin(__ldg(f.func + (n + 1) * f.len + t), Lk),
-                     base);
-  return m;
-}
-
-__device__ __forceinline__ uint64_t func_row_bits(const FuncMask& f, int64_t t, int base, int Lk) {
-  uint64_t m = bit_range64(0, imin(__ldg(f.func + t), Lk), base);
-  for (int n = 1; n + 1 < f.n; n += 2)
     m |= bit_range64(__ldg(f.func + n * f.len + t), imin(__ldg(f.func + (n + 1) * f.len + t), Lk),
                      base);
   return m;

@@ -35,54 +35,90 @@ __device__ __forceinline__ int4 seq_global(const SchedArgs& a, int b) {
   return make_int4(q0, max(0, __ldg(a.cu_q + b + 1) - q0), k0, max(0, __ldg(a.cu_k + b + 1) - k0));
 }
 
+// Bits [lo, hi) of a 32-bit word, clamped to [0, 32).
+__device__ __forceinline__ uint32_t bits32(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t below_hi = hi == 32 ? 0xffffffffu : (1u << hi) - 1u;
+  return below_hi & ~((1u << lo) - 1u);
+}
+
+// Arbitrary mask: the live tiles of bn keys (64 or 128) among tiles
+// [u0, u1) of 128-row query tile tq, counted from its blocks' bit words (a
+// 64-key tile is live when its 128-key tile is).
+__device__ __forceinline__ int func_live_tiles(const FuncMask& f, int q0, int b, int tq, int Lq,
+                                               int bn, int u0, int u1) {
+  const bool two = kBM * tq + 64 < Lq;
+  const int64_t r0 = static_cast<int64_t>(qb_slot(q0, b, 2 * tq)) * f.kt_words;
+  auto word = [&](int w) {  // the tile's OR of its two blocks (slots are consecutive)
+    uint32_t x = __ldg(f.qb_bits + r0 + w);
+    if (two) x |= __ldg(f.qb_bits + r0 + f.kt_words + w);
+    return x;
+  };
+  int n = 0;
+  if (bn == kBM) {
+    for (int w = u0 >> 5; w <= (u1 - 1) >> 5; ++w)
+      n += __popc(word(w) & bits32(u0 - 32 * w, u1 - 32 * w));
+    return n;
+  }
+  for (int u = u0; u < u1; ++u) {  // 64-key tiles: tile u / 2 of 128 keys
+    const int s = u >> 1;
+    n += static_cast<int>((word(s >> 5) >> (s & 31)) & 1u);
+  }
+  return n;
+}
+
 // Cost of query tile t (lists A and F): its inner tiles of bn keys.
 __device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t, int bn) {
   int first, n;
   if (a.fm.func != nullptr) {  // arbitrary mask: the live tiles of the tile's key hull
     const int2 h = func_tile_keys(a.fm, sq.x, b, t, sq.y);
     if (h.x >= h.y) return 0;
-    const int t1 = (h.y + bn - 1) / bn;
-    n = 0;
-    for (int u = func_next_tile(a.fm, sq.x, b, t, sq.y, bn, h.x / bn, t1); u < t1;
-         u = func_next_tile(a.fm, sq.x, b, t, sq.y, bn, u + 1, t1))
-      ++n;
-    return n;
+    return func_live_tiles(a.fm, sq.x, b, t, sq.y, bn, h.x / bn, (h.y + bn - 1) / bn);
   }
   query_tile_keys(t, sq.y, sq.w, a.win, bn, first, n);
   return n;
 }
 
-// Arbitrary mask: the hull [first, first + count) of the 64-row query
-// blocks whose key hull meets 128-key tile s.
-__device__ __forceinline__ int2 func_key_tile_queries(const SchedArgs& a, int4 sq, int b, int s) {
-  const int c0 = kBM * s, c1 = min(kBM * s + kBM, sq.w);
+// Arbitrary mask, list B, warp-wide: for key tile t = tb + lane (tb a
+// multiple of 32, t < nt), the hull {first, count} of the 64-row query blocks
+// whose key hull meets the tile, and how many of them have the tile live.
+// The warp reads 32 blocks' hulls and bit words at a time and compares them
+// with each tile of the group by ballots.  Every lane of the warp calls it.
+__device__ void func_key_tiles_warp(const SchedArgs& a, int4 sq, int b, int tb, int nt,
+                                    int2& hull, int& live) {
+  const int lane = threadIdx.x & 31;
   const int n_qb = ceil_div(sq.y, 64);
-  int m0 = n_qb, m1 = 0;
-  for (int m = 0; m < n_qb; ++m) {
-    const int2 h = a.fm.qb_range[qb_slot(sq.x, b, m)];
-    if (h.x < h.y && h.x < c1 && h.y > c0) {
-      m0 = min(m0, m);
-      m1 = m + 1;
+  const int w = tb >> 5;  // the group's bit word
+  int first = INT_MAX, last = -1, n = 0;
+  for (int mb = 0; mb < n_qb; mb += 32) {
+    const int m = mb + lane;
+    int2 h = make_int2(0, 0);
+    uint32_t bits = 0;
+    if (m < n_qb) {
+      const int slot = qb_slot(sq.x, b, m);
+      h = a.fm.qb_range[slot];
+      bits = a.fm.qb_bits[static_cast<int64_t>(slot) * a.fm.kt_words + w];
+    }
+    for (int k = 0; k < 32 && tb + k < nt; ++k) {
+      const int c0 = kBM * (tb + k), c1 = min(c0 + kBM, sq.w);
+      const bool meets = h.x < h.y && h.x < c1 && h.y > c0;
+      const uint32_t bm = __ballot_sync(0xffffffffu, meets);
+      const uint32_t bl = __ballot_sync(0xffffffffu, (bits >> k) & 1u);
+      if (lane == k && bm != 0u) {
+        first = min(first, mb + __ffs(bm) - 1);
+        last = max(last, mb + 31 - __clz(bm));
+        n += __popc(bl);
+      }
     }
   }
-  return m1 > m0 ? make_int2(m0, m1 - m0) : make_int2(0, 0);
+  hull = last >= 0 ? make_int2(first, last - first + 1) : make_int2(0, 0);
+  live = n;
 }
 
-// Arbitrary mask: the query blocks of hull r (first, count) for which key
-// tile s is live.
-__device__ __forceinline__ int func_live_qblocks(const SchedArgs& a, int4 sq, int b, int s,
-                                                 int2 r) {
-  int n = 0;
-  for (int m = func_next_qblock(a.fm, sq.x, b, s, r.x, r.x + r.y); m < r.x + r.y;
-       m = func_next_qblock(a.fm, sq.x, b, s, m + 1, r.x + r.y))
-    ++n;
-  return n;
-}
-
-// Cost of key tile s (list B).
+// Cost of key tile s (list B; the arbitrary mask's walk is warp-wide).
 __device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int b, int s) {
-  if (a.fm.func != nullptr)  // bq_b == 64: the live blocks of the hull
-    return func_live_qblocks(a, sq, b, s, func_key_tile_queries(a, sq, b, s));
   int first, n;
   key_tile_queries(s, sq.y, sq.w, a.win, a.bq_b, first, n);
   return n;
@@ -177,13 +213,21 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   __syncthreads();
 
   // pass 1: histogram of costs; a warp per sequence, a lane per tile
+  const bool func_b = list_b && a.fm.func != nullptr;  // the warp-wide list-B walk
   for (int b = warp; b < a.B; b += nwarps) {
     const int4 sq = seq(b);
     const int Lq = sq.y, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
-    for (int t = lane; t < nt; t += 32) {
-      const int cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
-      atomicAdd(&hist[min(cost, cmax)], per_tile);
+    for (int tb = 0; tb < nt; tb += 32) {
+      const int t = tb + lane;
+      int cost = 0;
+      if (func_b) {
+        int2 r;
+        func_key_tiles_warp(a, sq, b, tb, nt, r, cost);
+      } else if (t < nt) {
+        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
+      }
+      if (t < nt) atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
   }
   __syncwarp();  // reconverge before the aligned CTA barrier
@@ -211,15 +255,17 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     const int4 sq = seq(b);
     const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
     const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
-    for (int t = lane; t < nt; t += 32) {
-      int cost;
-      if (list_b && a.fm.func != nullptr) {  // also record the key tile's query hull
-        const int2 r = func_key_tile_queries(a, sq, b, t);
-        a.fm.kt_range[kt_slot(k0, b, t)] = r;
-        cost = func_live_qblocks(a, sq, b, t, r);
-      } else {
+    for (int tb = 0; tb < nt; tb += 32) {
+      const int t = tb + lane;
+      int cost = 0;
+      if (func_b) {  // also record the key tile's query hull
+        int2 r;
+        func_key_tiles_warp(a, sq, b, tb, nt, r, cost);
+        if (t < nt) a.fm.kt_range[kt_slot(k0, b, t)] = r;
+      } else if (t < nt) {
         cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
       }
+      if (t >= nt) continue;
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       for (int e = 0; e < per_tile; ++e) {
         if (pos + e < cap) {
