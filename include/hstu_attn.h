@@ -159,11 +159,12 @@ hstu_status_t hstu_attn_bwd(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu
  *     cut to the sequence's keys.  Values are trusted and never copied to
  *     the host.
  *   workspace: hstu_attn_workspace_size_func(...) bytes (the regular size
- *     plus the per-tile key and query ranges the library derives from the
- *     endpoints on every call, so in-place changes of func are seen, also
- *     under CUDA graph replay).
- * Each unit visits the hull of the tiles its rows can see and applies the
- * exact predicate inside it.  Errors as for hstu_attn_fwd/_bwd, plus
+ *     plus the per-tile key and query ranges and live-tile bitmaps the
+ *     library derives from the endpoints on every call, so in-place changes
+ *     of func are seen, also under CUDA graph replay).
+ * Each unit visits the live tiles of the hull its rows can see (a tile is
+ * live when some row of a 64-row query block sees one of its 128 keys) and
+ * applies the exact predicate inside them.  Errors as for hstu_attn_fwd/_bwd, plus
  * HSTU_ERR_INVALID_ARG for an even or non-positive func_n or
  * func_len < total_q, HSTU_ERR_MISALIGNED for a func pointer that is not
  * 4-byte aligned.
