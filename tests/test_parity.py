@@ -120,6 +120,15 @@ def test_func_masks(D, dtype, kind):
     full_compare(x, None, _func_mask(kind, x, seed=D), 1.0 / math.sqrt(D))
 
 
+@pytest.mark.parametrize("kind", ["causal_targets", "band_hole"])
+def test_func_mask_long_sequence(kind):
+    """A sequence of more than 32 key tiles: the live-tile bitmaps take two
+    32-bit words per query block and the scheduler walks two tile groups."""
+    lens = [4500, 300, 1]
+    x = workloads.random_inputs(lens, lens, 2, 64, torch.bfloat16, seed=17)
+    full_compare(x, None, _func_mask(kind, x, seed=3), 0.125)
+
+
 def test_func_mask_equal_to_causal_is_bitwise_causal():
     x = workloads.random_inputs(MEDIUM_LENS, MEDIUM_LENS, 2, 128, torch.bfloat16, seed=5)
     i, _ = _local(x)
