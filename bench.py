@@ -22,6 +22,7 @@ import json
 import math
 import os
 import statistics
+import tempfile
 import subprocess
 import sys
 import time
@@ -568,8 +569,9 @@ def main():
         torch.cuda.synchronize()
         assert all(hstu.last_device_status(ws) == 0 for ws in status_ws)
         return 0
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/hstu_clocks.csv")
+    # raw nvidia-smi samples go to $HSTU_CLOCKS_DIR (default: the system temp dir)
+    clocks = ClockSampler(local, os.path.join(os.environ.get("HSTU_CLOCKS_DIR", tempfile.gettempdir()),
+                                              f"hstu_clocks_rank{rank}.csv"))
     wall0 = time.perf_counter()
     for i in range(args.steps):
         if flush is not None:
