@@ -111,6 +111,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Sum over the 32 / RPW lanes that share a row (RPW rows per warp).
+template <int RPW>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = 16 / RPW; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // sigmoid(u) = 1 / (1 + e^-u) with the fast exponential and reciprocal
 // (e^-u = inf for u < -88 gives 0, the limit).
 __device__ __forceinline__ float sigmoid(float u) { return __fdividef(1.f, 1.f + __expf(-u)); }
@@ -146,16 +154,19 @@ __host__ __device__ constexpr int fwd_blocks_per_sm(int nc) { return nc <= 1 ? 4
 __host__ __device__ constexpr int bwd_blocks_per_sm(int nc) { return nc <= 2 ? 4 : 2; }
 
 // NC: 8-element chunks per lane (D <= 256 NC).  Lanes past the row's last
-// chunk hold zeros.
-template <int NC>
+// chunk hold zeros.  RPW = 2 (rows of at most 16 chunks, D <= 128): each
+// half-warp takes a row, so no lane idles.
+template <int NC, int RPW>
 __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
     hstu_lmsd_fwd_kernel(FwdArgs a) {
-  const int lane = threadIdx.x & 31;
+  static_assert(RPW == 1 || (RPW == 2 && NC == 1), "two rows per warp only for one chunk");
+  const int lane = RPW == 2 ? (threadIdx.x & 15) : (threadIdx.x & 31);  // lane within the row
   const int nch = a.d / 8;
   const int S = 1 + a.concat_u + a.concat_x;
   const bool drop = a.p > 0.f;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps;
-  int64_t row = static_cast<int64_t>(blockIdx.x) * kLmsdWarps + (threadIdx.x >> 5);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps * RPW;
+  int64_t base = (static_cast<int64_t>(blockIdx.x) * kLmsdWarps + (threadIdx.x >> 5)) * RPW;
+  int64_t row = base + (RPW == 2 ? (threadIdx.x & 31) >> 4 : 0);
   auto load = [&](int64_t r, uint4 (&xo)[NC], uint4 (&uo)[NC]) {
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -169,7 +180,8 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
   };
   uint4 xv[NC], uv[NC];
   load(row, xv, uv);
-  for (; row < a.n; row += stride) {
+  for (; base < a.n; base += stride, row += stride) {
+    const bool live = row < a.n;  // (a half-warp's second row can be past the end)
     uint4 xn[NC], un[NC];
     load(row + stride, xn, un);  // the warp's next row, in flight during this one
     float s = 0.f;
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
 #pragma unroll
       for (int i = 0; i < 8; ++i) s += f[i];
     }
-    const float mean = warp_sum(s) / a.d;
+    const float mean = row_sum<RPW>(s) / a.d;
     float v = 0.f;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -190,7 +202,8 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
 #pragma unroll
       for (int i = 0; i < 8; ++i) v += (f[i] - mean) * (f[i] - mean);
     }
-    const float rstd = rsqrtf(warp_sum(v) / a.d + a.eps);
+    const float rstd = rsqrtf(row_sum<RPW>(v) / a.d + a.eps);
+    if (!live) continue;
     if (lane == 0) { a.mean[row] = mean; a.rstd[row] = rstd; }
     uint4* yrow = reinterpret_cast<uint4*>(a.y + row * static_cast<int64_t>(S) * a.d);
 #pragma unroll
@@ -280,19 +293,23 @@ __device__ __forceinline__ int acc_slot(int which, int c, int i, int lane) {
 // and dxh * xhat and adds the row's dweight / dbias terms to the warp's
 // accumulators; the second reads the row again (from L1 / L2) and writes dx
 // and du, which keeps registers for more warps.
-template <int NC>
+template <int NC, int RPW>
 __global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
     hstu_lmsd_bwd_kernel(BwdArgs a) {
+  static_assert(RPW == 1 || (RPW == 2 && NC == 1), "two rows per warp only for one chunk");
   extern __shared__ float acc_all[];  // [warp][acc_floats<NC>()]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wl = threadIdx.x & 31, warp = threadIdx.x >> 5;   // lane in the warp
+  const int lane = RPW == 2 ? (wl & 15) : wl;                  // lane within the row
   float* acc = acc_all + warp * acc_floats<NC>();
-  for (int k = lane; k < acc_floats<NC>(); k += 32) acc[k] = 0.f;  // warp-private
+  for (int k = wl; k < acc_floats<NC>(); k += 32) acc[k] = 0.f;  // warp-private
   const int nch = a.d / 8;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kLmsdWarps * RPW;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kLmsdWarps + warp; row < a.n;
-       row += stride) {
-    const float mean = __ldg(a.mean + row), rstd = __ldg(a.rstd + row);
+  int64_t row = (static_cast<int64_t>(blockIdx.x) * kLmsdWarps + warp) * RPW +
+                (RPW == 2 ? wl >> 4 : 0);
+  for (int64_t base = row - (RPW == 2 ? wl >> 4 : 0); base < a.n; base += stride, row += stride) {
+    const bool live = row < a.n;  // (a half-warp's second row can be past the end)
+    const float mean = live ? __ldg(a.mean + row) : 0.f, rstd = live ? __ldg(a.rstd + row) : 0.f;
     const __nv_bfloat16* dyrow = a.dy + row * a.dys;
     uint4 xv[NC], uv[NC], dmv[NC], duv[NC], dxv[NC];
     uint64_t mv[NC];
@@ -300,7 +317,7 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
       const int ch = lane + 32 * c;
       xv[c] = uv[c] = dmv[c] = duv[c] = dxv[c] = zero;
       mv[c] = 0;
-      if (ch >= nch) return;
+      if (ch >= nch || !live) return;
       xv[c] = ld16(a.x + row * a.xs, ch);
       uv[c] = ld16(a.u + row * a.us, ch);
       int seg = 0;
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
-      if (ch >= nch) continue;
+      if (ch >= nch || !live) continue;
       load(c);
       const uint4 wv = ld16(a.w, ch);
 #pragma unroll
@@ -332,16 +349,16 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
           const float dl = g * act, dxh = dl * ws[h];
           s1 += dxh;
           s2 += dxh * xh;
-          acc[acc_slot<NC>(0, c, i, lane)] += dl * xh;
-          acc[acc_slot<NC>(1, c, i, lane)] += dl;
+          acc[acc_slot<NC>(0, c, i, wl)] += dl * xh;
+          acc[acc_slot<NC>(1, c, i, wl)] += dl;
         }
       }
     }
-    const float m1 = warp_sum(s1) / a.d, m2 = warp_sum(s2) / a.d;
+    const float m1 = row_sum<RPW>(s1) / a.d, m2 = row_sum<RPW>(s2) / a.d;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int ch = lane + 32 * c;
-      if (ch >= nch) continue;
+      if (ch >= nch || !live) continue;
       load(c);  // again: from L1 / L2
       const uint4 wv = ld16(a.w, ch), bv = ld16(a.b, ch);
       uint32_t ox[4], ou[4];
@@ -380,7 +397,10 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, bwd_blocks_per_sm(NC))
     const int which = col >= a.d ? 1 : 0, cc = col - which * a.d, ch = cc >> 3;
     const int slot = acc_slot<NC>(which, ch >> 5, cc & 7, ch & 31);
     float t = 0.f;
-    for (int k = 0; k < kLmsdWarps; ++k) t += acc_all[k * acc_floats<NC>() + slot];
+    for (int k = 0; k < kLmsdWarps; ++k) {
+      t += acc_all[k * acc_floats<NC>() + slot];
+      if (RPW == 2) t += acc_all[k * acc_floats<NC>() + slot + 16];  // the other half-warp
+    }
     a.part[static_cast<int64_t>(blockIdx.x) * 2 * a.d + col] = t;
   }
 }
@@ -404,15 +424,19 @@ __global__ void hstu_lmsd_colsum_kernel(const float* part, int blocks, int d, in
 }
 
 // Persistent grids: `per_sm` blocks of 8 rows per SM, the blocks that fit.
-int lmsd_grid(int64_t n, int per_sm) {
+int lmsd_grid(int64_t n, int per_sm, int rpw) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (n + kLmsdWarps - 1) / kLmsdWarps;
+  const int64_t rows = static_cast<int64_t>(kLmsdWarps) * rpw;  // rows in flight per block
+  const int64_t want = (n + rows - 1) / rows;
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<int>(want < cap ? want : cap);
 }
 int chunks_per_lane(int32_t d) { return (d / 8 + 31) / 32; }
+
+// Rows of at most 16 chunks (D <= 128) go two to a warp, a half-warp each.
+int rows_per_warp(int32_t d) { return d / 8 <= 16 ? 2 : 1; }
 
 // Bytes of the backward's shared-memory column accumulators.
 size_t bwd_smem(int nc) { return static_cast<size_t>(kLmsdWarps) * 2 * nc * 8 * 32 * sizeof(float); }
@@ -470,15 +494,18 @@ hstu_lmsd_status_t hstu_lmsd_fwd(const void* x, int64_t x_stride, const void* u,
   a.keys = philox_keys(static_cast<uint64_t>(seed));
   a.y = static_cast<__nv_bfloat16*>(y); a.mean = mean; a.rstd = rstd; a.mask = mask;
   const int nc = chunks_per_lane(d);
-  auto kern = nc == 1 ? hstu_lmsd_fwd_kernel<1> : nc == 2 ? hstu_lmsd_fwd_kernel<2>
-            : nc == 3 ? hstu_lmsd_fwd_kernel<3> : hstu_lmsd_fwd_kernel<4>;
-  kern<<<lmsd_grid(n, fwd_blocks_per_sm(nc)), 32 * kLmsdWarps, 0, stream>>>(a);
+  const int rpw = rows_per_warp(d);
+  auto kern = rpw == 2 ? hstu_lmsd_fwd_kernel<1, 2>
+            : nc == 1 ? hstu_lmsd_fwd_kernel<1, 1> : nc == 2 ? hstu_lmsd_fwd_kernel<2, 1>
+            : nc == 3 ? hstu_lmsd_fwd_kernel<3, 1> : hstu_lmsd_fwd_kernel<4, 1>;
+  kern<<<lmsd_grid(n, fwd_blocks_per_sm(nc), rpw), 32 * kLmsdWarps, 0, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? HSTU_LMSD_OK : HSTU_LMSD_ERR_CUDA;
 }
 
 size_t hstu_lmsd_bwd_workspace_size(int64_t n, int32_t d) {
   if (n < 0 || d < 8 || d >= 1024 || d % 8 != 0) return 0;
-  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n, bwd_blocks_per_sm(chunks_per_lane(d)))) * 2 *
+  return static_cast<size_t>(lmsd_grid(n < 1 ? 1 : n, bwd_blocks_per_sm(chunks_per_lane(d)),
+                                      rows_per_warp(d))) * 2 *
          d * sizeof(float);
 }
 
@@ -511,16 +538,19 @@ hstu_lmsd_status_t hstu_lmsd_bwd(const void* dy, int64_t dy_stride, const void* 
   if (workspace == nullptr || workspace_bytes < need) return HSTU_LMSD_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return HSTU_LMSD_ERR_MISALIGNED;
   const int nc = chunks_per_lane(d);
-  const int grid = n > 0 ? lmsd_grid(n, bwd_blocks_per_sm(nc)) : 1;
+  const int rpw = rows_per_warp(d);
+  const int grid = n > 0 ? lmsd_grid(n, bwd_blocks_per_sm(nc), rpw) : 1;
   const size_t smem = bwd_smem(nc);
-  auto kern = nc == 1 ? hstu_lmsd_bwd_kernel<1> : nc == 2 ? hstu_lmsd_bwd_kernel<2>
-            : nc == 3 ? hstu_lmsd_bwd_kernel<3> : hstu_lmsd_bwd_kernel<4>;
-  static bool attr[5] = {false, false, false, false, false};
-  if (!attr[nc]) {
+  auto kern = rpw == 2 ? hstu_lmsd_bwd_kernel<1, 2>
+            : nc == 1 ? hstu_lmsd_bwd_kernel<1, 1> : nc == 2 ? hstu_lmsd_bwd_kernel<2, 1>
+            : nc == 3 ? hstu_lmsd_bwd_kernel<3, 1> : hstu_lmsd_bwd_kernel<4, 1>;
+  static bool attr[6] = {false, false, false, false, false, false};
+  const int ki = rpw == 2 ? 5 : nc;
+  if (!attr[ki]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return HSTU_LMSD_ERR_CUDA;
-    attr[nc] = true;
+    attr[ki] = true;
   }
   BwdArgs a{};
   a.dy = static_cast<const __nv_bfloat16*>(dy); a.dys = dy_stride;
