@@ -98,8 +98,67 @@ def workload_config(w, lengths, mask=None):
 
 
 # ---------------------------------------------------------------- clocks
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlClockSampler:
+    """SM clock and throttle reasons read through NVML (the driver's
+    management library, read-only queries) from a background thread every
+    `period_s`, so that even a timed region of a few milliseconds gets
+    samples.  The device is found by its UUID, so the index seen by CUDA need
+    not match NVML's."""
+
+    def __init__(self, device_index: int, period_s: float = 2e-4):
+        import ctypes
+        import threading
+        import torch
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise RuntimeError("NVML device not found")
+        mx = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0:  # 1: SM clock
+            self.max_mhz = float(mx.value)
+        reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.stop_flag = threading.Event()
+
+        def loop():
+            clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self.stop_flag.is_set():
+                if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(float(clk.value))
+                if reasons_fn(self.dev, ctypes.byref(rs)) == 0:
+                    for bit, name in _NVML_REASONS.items():
+                        if rs.value & bit:
+                            self.reasons.add(name)
+                self.stop_flag.wait(period_s)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:
+            pass
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples),
+                "sm_max_mhz": self.max_mhz if self.max_mhz else max(self.samples),
+                "samples": len(self.samples), "reasons": sorted(self.reasons), "source": "nvml"}
+
+
 class ClockSampler:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling during the timed region (used when NVML cannot be
+    loaded)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -141,7 +200,45 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons), "source": "nvidia-smi"}
+
+
+def start_clock_sampler(local: int, rank: int):
+    try:
+        return NvmlClockSampler(local)
+    except Exception:
+        return ClockSampler(local, os.path.join(os.environ.get("HSTU_CLOCKS_DIR",
+                                                               tempfile.gettempdir()),
+                                                f"hstu_clocks_rank{rank}.csv"))
+
+
+def kernel_sources_sha() -> str:
+    """sha256 (first 16 hex digits) over the CUDA sources of the library, in
+    name order: a committed ncu summary whose "sources" line differs was
+    taken on other kernels, and its DRAM figures are not reported."""
+    import hashlib
+    d = os.path.join(ROOT, "generative_recommender_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def summary_traffic(path: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary (lines
+    "traffic <kernel> <bytes>"), if the summary's "sources <sha>" line matches
+    the current kernel sources; else None."""
+    if not os.path.exists(path):
+        return None
+    lines = [ln.split() for ln in open(path)]
+    if not any(len(p) == 2 and p[0] == "sources" and p[1] == kernel_sources_sha() for p in lines):
+        return None
+    for p in lines:
+        if len(p) == 3 and p[0] == "traffic" and p[1] == kernel:
+            return int(p[2])
+    return None
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -248,14 +345,10 @@ def run_lmsd(args, dev):
 
     ms_f, ms_b = timed(fwd), timed(bwd)
     # DRAM bytes of one forward and one backward launch, from the committed
-    # ncu summary of this size (lines "traffic <kernel> <bytes>"), if any
-    traffic = {}
+    # ncu summary of this size, if it was taken on the current kernel sources
     tfile = os.path.join(ROOT, "profiles", f"kernels_lmsd_{n}x{d}.md")
-    if os.path.exists(tfile):
-        for tline in open(tfile):
-            parts = tline.split()
-            if len(parts) == 3 and parts[0] == "traffic":
-                traffic[parts[1]] = int(parts[2])
+    traffic = {k: summary_traffic(tfile, k) for k in ("hstu_lmsd_fwd_kernel", "hstu_lmsd_bwd_kernel")}
+    traffic = {k: v for k, v in traffic.items() if v is not None}
     bytes_f = n * d * 2 * 2 + n * 3 * d * 2 + n * d + n * 8
     bytes_b = n * 3 * d * 2 + n * d * 2 * 2 + n * d + n * 8 + n * d * 2 * 2
     pk = peaks()
@@ -647,14 +740,10 @@ def main():
     f_dom, ms_dom = kernels[dom]
     achieved = f_dom / (ms_dom * 1e-3) / 1e12
     # DRAM bytes of one launch of the dominant kernel, from the committed ncu
-    # summary of this workload (a line "traffic <kernel> <bytes>"), if any
+    # summary of this workload, if it was taken on the current kernel sources
     traffic = None
-    tfile = os.path.join(ROOT, "profiles", f"kernels_{w.name}_full.md")
-    if os.path.exists(tfile) and args.mask is None:  # the summary covers the default mask
-        for tline in open(tfile):
-            parts = tline.split()
-            if len(parts) == 3 and parts[0] == "traffic" and parts[1] == dom:
-                traffic = int(parts[2])
+    if args.mask is None:  # the summary covers the default mask
+        traffic = summary_traffic(os.path.join(ROOT, "profiles", f"kernels_{w.name}_full.md"), dom)
 
     # End to end through the public API: every step copies its inputs in from
     # pinned host memory and its results (O, dQ, dK, dV) back out.  Copy-in,
@@ -748,9 +837,11 @@ def main():
                           "note": "second pass with events between kernels (no launch overlap), "
                                   "each call scheduling its own work"},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
-                     "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16_tflops_sustained"], "traffic": traffic,
-                     "peak_kind": "bf16 sustained (kernel timed inside a long step loop)"},
+                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                     "peak_kind": "bf16 burst, of measured (the kernel's launches are timed "
+                                  "one by one between events, %d of them)" % len(timed),
+                     "frac_of_sustained": achieved / pk["bf16_tflops_sustained"]},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e2e_ms_step,
                 "note": "copy-in, compute and copy-out of consecutive steps overlap on three "

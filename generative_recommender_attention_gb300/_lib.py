@@ -25,6 +25,7 @@ EXPORTS = ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_profiled", "hstu_att
            "hstu_attn_workspace_size",
            "hstu_attn_status_string", "hstu_attn_last_device_status",
            "hstu_attn_selftest_timeout", "hstu_attn_version", "hstu_attn_fwd_noalloc",
+           "hstu_attn_noalloc_last_device_status",
            "hstu_attn_fwd_paged", "hstu_attn_fwd_func", "hstu_attn_bwd_func",
            "hstu_attn_workspace_size_func", "hstu_attn_plan_workspace_size", "hstu_attn_plan",
            "hstu_attn_fwd_planned", "hstu_attn_bwd_planned", "hstu_lmsd_fwd", "hstu_lmsd_bwd",
@@ -81,6 +82,8 @@ def _declare(lib):
     lib.hstu_attn_selftest_timeout.restype = ctypes.c_int
     lib.hstu_attn_fwd_noalloc.argtypes = [CTen, CTen, CTen, Ten] + scal[:14] + [P]
     lib.hstu_attn_fwd_noalloc.restype = ctypes.c_int
+    lib.hstu_attn_noalloc_last_device_status.argtypes = [P]
+    lib.hstu_attn_noalloc_last_device_status.restype = ctypes.c_int
     # q, paged_kv, num_pages, page_ids, page_indptrs, out, cu_q, cu_k, B, T_q, H, D, dtype,
     # max_q, max_k, alpha, scaling_seqlen, workspace, bytes, stream
     lib.hstu_attn_fwd_paged.argtypes = [CTen, P, i64, P, P, Ten, P, P, i32, i64, i32, i32,

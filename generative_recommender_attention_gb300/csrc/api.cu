@@ -850,3 +850,12 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(
                   window_right,
                   scratch, kNoAllocScratchBytes, stream, EventMarks{nullptr, 0});
 }
+
+// The status words of the no-allocation forward live in the same fixed
+// array, so the caller cannot name them; this reads them the way
+// hstu_attn_last_device_status reads a workspace's.
+extern "C" hstu_status_t hstu_attn_noalloc_last_device_status(cudaStream_t stream) {
+  void* scratch = nullptr;
+  if (!noalloc_scratch(&scratch)) return HSTU_ERR_CUDA;
+  return hstu_attn_last_device_status(scratch, stream);
+}

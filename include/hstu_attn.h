@@ -279,6 +279,18 @@ hstu_status_t hstu_attn_fwd_noalloc(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v,
                                     int32_t window_right, cudaStream_t stream);
 
 /*
+ * Device-side status of the most recent hstu_attn_fwd_noalloc call on the
+ * current device, in the order of `stream`: the same report as
+ * hstu_attn_last_device_status gives for a workspace (HSTU_OK, or
+ * HSTU_ERR_INVALID_ARG for metadata past the sizes, HSTU_ERR_DEVICE_TIMEOUT
+ * for a wait that gave up), read from the library's fixed array, which the
+ * caller cannot name.  Copies 64 bytes to the host and synchronizes
+ * `stream`: for debugging and tests, not for the hot path.  The pages have
+ * no counterpart.
+ */
+hstu_status_t hstu_attn_noalloc_last_device_status(cudaStream_t stream);
+
+/*
  * Plans: one schedule for every call on one batch layout.
  *
  * A training step runs the forward and the backward of every layer on the
