@@ -113,7 +113,7 @@ class NvmlClockSampler:
         import ctypes
         import threading
         import torch
-        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.samples, self.times, self.reasons, self.max_mhz = [], [], set(), None
         self.lib = ctypes.CDLL("libnvidia-ml.so.1")
         if self.lib.nvmlInit_v2() != 0:
             raise RuntimeError("nvmlInit failed")
@@ -133,18 +133,28 @@ class NvmlClockSampler:
             while not self.stop_flag.is_set():
                 if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk)) == 0:
                     self.samples.append(float(clk.value))
+                    self.times.append(time.perf_counter())
                 if reasons_fn(self.dev, ctypes.byref(rs)) == 0:
                     for bit, name in _NVML_REASONS.items():
                         if rs.value & bit:
                             self.reasons.add(name)
                 self.stop_flag.wait(period_s)
 
+        # the timed loop holds the interpreter lock between its (quick) calls:
+        # switch threads often while sampling, and start only once the
+        # sampler runs
+        self.switch = sys.getswitchinterval()
+        sys.setswitchinterval(1e-5)
         self.thread = threading.Thread(target=loop, daemon=True)
         self.thread.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 1.0:
+            time.sleep(1e-4)
 
     def stop(self):
         self.stop_flag.set()
         self.thread.join(timeout=5)
+        sys.setswitchinterval(self.switch)
         try:
             self.lib.nvmlShutdown()
         except Exception:
@@ -200,16 +210,19 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons), "source": "nvidia-smi"}
+                "reasons": sorted(reasons), "source": "nvidia-smi",
+                "nvml_error": getattr(self, "nvml_error", None)}
 
 
 def start_clock_sampler(local: int, rank: int):
     try:
         return NvmlClockSampler(local)
-    except Exception:
-        return ClockSampler(local, os.path.join(os.environ.get("HSTU_CLOCKS_DIR",
-                                                               tempfile.gettempdir()),
-                                                f"hstu_clocks_rank{rank}.csv"))
+    except Exception as exc:
+        c = ClockSampler(local, os.path.join(os.environ.get("HSTU_CLOCKS_DIR",
+                                                            tempfile.gettempdir()),
+                                             f"hstu_clocks_rank{rank}.csv"))
+        c.nvml_error = f"{type(exc).__name__}: {exc}"
+        return c
 
 
 def kernel_sources_sha() -> str:
@@ -662,9 +675,9 @@ def main():
         torch.cuda.synchronize()
         assert all(hstu.last_device_status(ws) == 0 for ws in status_ws)
         return 0
-    # raw nvidia-smi samples go to $HSTU_CLOCKS_DIR (default: the system temp dir)
-    clocks = ClockSampler(local, os.path.join(os.environ.get("HSTU_CLOCKS_DIR", tempfile.gettempdir()),
-                                              f"hstu_clocks_rank{rank}.csv"))
+    # SM clocks sampled through NVML while the timed steps run (nvidia-smi
+    # when NVML cannot be loaded; its raw samples go to $HSTU_CLOCKS_DIR)
+    clocks = start_clock_sampler(local, rank)
     wall0 = time.perf_counter()
     for i in range(args.steps):
         if flush is not None:
@@ -677,6 +690,8 @@ def main():
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
+    if clk is None and getattr(clocks, "nvml_error", None):
+        clk = {"error": "no samples; NVML: " + clocks.nvml_error}
     assert all(hstu.last_device_status(ws) == 0 for ws in status_ws)
     t_step = [b.elapsed_time(e) for b, e in zip(e_beg, e_end)]
 

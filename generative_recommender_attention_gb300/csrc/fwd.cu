@@ -12,12 +12,13 @@
 //               an issuing thread that stops to wait or to do bookkeeping
 //               leaves it idle; two issuers keep it fed while either waits,
 //               and S runs up to three steps ahead of P V.
-//   warps 2-9   SiLU row work, two warps per TMEM lane quarter taking
-//               alternate key steps (warps 2-5 even steps, 6-9 odd ones), so
-//               one warp's TMEM and barrier latencies overlap the other's
-//               MUFU work: tcgen05.ld S, alpha scale, SiLU, mask, round to 16
-//               bits, tcgen05.st P in place over the first half of the S
-//               columns.
+//   warps 2-9   SiLU row work, two warps per TMEM lane quarter: with 128-key
+//               steps each takes one 64-key half of every step (warps 2-5
+//               the first, 6-9 the second), so a step's SiLU takes half as
+//               long and S comes back to the issuer sooner; with 64-key steps
+//               (D = 256) they take alternate steps.  tcgen05.ld S, alpha
+//               scale, SiLU, mask, round to 16 bits, tcgen05.st P in place
+//               over the first half of the warp's S columns.
 //   warps 10-13 O epilogue, one per lane quarter: O * (1/L_scale) with
 //               predicated row stores; O is released as soon as it is read,
 //               so the SiLU warps never stop at a unit boundary.
@@ -30,9 +31,10 @@
 // K_g and S_g share ring slot g % 3: S_g completing frees K_g, so the producer
 // waits on the S barrier instead of a separate K-empty barrier.
 //
-// P_g (16-bit, two per column) overwrites the first half of its own S
-// buffer, which S_{g+3} overwrites again; S_{g+3} is issued only after the
-// commit of O += P_g V_g has arrived on that buffer's PV-done barrier.
+// P_g (16-bit, two per column) overwrites the first half of each 64-column
+// half of its own S buffer (the whole buffer's first half for 64-key steps),
+// which S_{g+3} overwrites again; S_{g+3} is issued only after the commit of
+// O += P_g V_g has arrived on that buffer's PV-done barrier.
 #include "kernels.h"
 
 namespace hstu {
@@ -48,6 +50,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
   constexpr int NSB = 3;        // S buffers in TMEM
   constexpr int NCH = BN / 64;  // 64-column chunks of one S tile
+  // 128-key steps: the two SiLU warps of a lane quarter split every step's
+  // columns (64 each), so a step's SiLU takes half as long; each writes its
+  // P over the first half of its own 64 S columns.  64-key steps (D = 256):
+  // the two warps take alternate steps and P fills the buffer's first half.
+  constexpr bool SPLIT = NCH == 2;
   static_assert(NK == NSB, "K slot g % NSB is freed by the S_g barrier");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BN, false, false);
   constexpr uint32_t IDESC_PV = idesc_f16(BF16, kBM, D, false, true);
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < NV; ++i) { mbar_init(bar(VFULL + i), 1); mbar_init(bar(VEMPTY + i), 1); }
     for (int i = 0; i < NSB; ++i) {
       mbar_init(bar(SFULL + i), 1);
-      mbar_init(bar(PFULL + i), 4);  // one arrival per warp of the step's parity
+      mbar_init(bar(PFULL + i), SPLIT ? kFwdRowWarps : 4);  // every SiLU warp of the step
       mbar_init(bar(PVDONE + i), 1);
     }
     mbar_init(bar(OFULL), 1);
@@ -273,9 +280,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const SDesc vd = mndesc<BN>(sV + vs * C::KV_BYTES);
           const uint32_t tP = tmem + COL_S + sb * BN;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)  // P of keys [16 kk, 16 kk + 16): columns 8 kk..
-            mma_ts(tO, tP + 8 * kk, desc_mnmajor<BN>(vd, kk, 0), IDESC_PV,
-                   (n > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BN / 16; ++kk)  // P of keys [16 kk, 16 kk + 16): 8 columns,
+            mma_ts(tO, tP + 8 * kk + (SPLIT ? 32 * (kk / 4) : 0),  // at 64 h + .. for key half h
+                   desc_mnmajor<BN>(vd, kk, 0), IDESC_PV, (n > 0 || kk > 0) ? 1u : 0u);
           mma_commit(bar(VEMPTY + vs));
           mma_commit(bar(PVDONE + sb));
           if (n == un - 1) mma_commit(bar(OFULL));
@@ -287,9 +294,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp < 2 + kFwdRowWarps) {
     // ------------------------------------------------------------ SiLU
-    // Warp w owns TMEM lane quarter w % 4 (its 32 rows) and the steps of
-    // parity par; it reads all BN columns of those S tiles in 64-column
-    // chunks and writes P over the first half of the buffer.
+    // Warp w owns TMEM lane quarter w % 4 (its 32 rows).  With 128-key steps
+    // it takes the 64-column half par of every step and writes P over that
+    // half's first 32 columns; with 64-key steps it takes the steps of parity
+    // par and writes P over the buffer's first half.
     const int wq = warp & 3, par = (warp - 2) >> 2;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -337,27 +345,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           kt = func_next_tile(a.fm, U.q0, U.b, U.tile, U.Lq, BN, kt_next, kt_end);
           kt_next = kt + 1;
         }
-        if (static_cast<int>(g & 1) != par) continue;
+        if (!SPLIT && static_cast<int>(g & 1) != par) continue;
         const int sb = g % NSB;
+        // this warp's 64-column chunks of the step: its half (split steps) or all
+        constexpr int C_N = SPLIT ? 1 : NCH;
         // arbitrary mask: the row's valid keys of each chunk, formed while S lands
-        uint64_t fbs[NCH];
+        uint64_t fbs[C_N];
         if constexpr (func) {
 #pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            fbs[c] = func_row_bits3(a.fm, t_row, fe0, fe1, fe2, BN * kt + 64 * c, Lk);
+          for (int ci = 0; ci < C_N; ++ci)
+            fbs[ci] = func_row_bits3(a.fm, t_row, fe0, fe1, fe2, BN * kt + 64 * (SPLIT ? par : ci),
+                                     Lk);
         }
         if (!wait_bar_warp(bar(SFULL + sb), (g / NSB) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
+        for (int ci = 0; ci < C_N; ++ci) {
+          const int c = SPLIT ? par : ci;
           const int jc = BN * kt + 64 * c;  // first key of this chunk
           const bool need_mask = jc < lo_all || jc + 64 > hi_all;
           uint32_t x[64];
           tmem_ld64(tS + sb * BN + 64 * c, x);
           uint32_t p[32];
-          if (func && !__all_sync(0xffffffffu, fbs[c] == ~0ull)) {
+          if (func && !__all_sync(0xffffffffu, fbs[ci] == ~0ull)) {
             // arbitrary mask, some key of the chunk invalid for some row
-            const uint64_t fb = fbs[c];
+            const uint64_t fb = fbs[ci];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const uint32_t s0 = ((fb >> (2 * e)) & 1ull) ? x[2 * e] : 0u;
@@ -386,8 +398,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               p[e] = silu_pair<BF16>(s0, s1, half_alpha);
             }
           }
-          // columns [32 c, 32 c + 32) were read by this chunk or the one before
-          tmem_st32(tS + sb * BN + 32 * c, p);
+          // split steps: P over this chunk's own first 32 columns; otherwise
+          // columns [32 c, 32 c + 32), read by this chunk or the one before
+          tmem_st32(tS + sb * BN + (SPLIT ? 64 : 32) * c, p);
         }
         tmem_st_wait();
         warp_arrive(bar(PFULL + sb));
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
 
-  // The role branches leave lanes of warps 0, 1 (and 18) on different paths;
+  // The role branches leave lanes of warps 0, 1 and 14 on different paths;
   // reconverge each warp so the aligned CTA barrier counts it exactly once
   // (otherwise it can release before the row warps finish reading TMEM).
   __syncwarp();
