@@ -736,8 +736,9 @@ def main():
     t_sched_f = [r[0].elapsed_time(r[1]) for r in timed]
     t_fwd = [r[1].elapsed_time(r[2]) for r in timed]
     t_sched_b = [r[3].elapsed_time(r[4]) for r in timed]
-    t_dkdv = [r[4].elapsed_time(r[5]) for r in timed]
-    t_dq = [r[5].elapsed_time(r[6]) for r in timed]
+    # one backward launch (dK/dV units, then dQ units) between marks 4 and 5;
+    # marks 5 and 6 are recorded back to back
+    t_bwd = [r[4].elapsed_time(r[6]) for r in timed]
     ms_step, value = replica_throughput(sum(t_step), args.steps, flops_step, world, dist, dev)
     pk = peaks()
 
@@ -745,12 +746,11 @@ def main():
     mean = lambda a: sum(a) / len(a)  # noqa: E731
     kernels = {
         "hstu_fwd_kernel": (4.0 * D * N, mean(t_fwd)),
-        "hstu_bwd_dq_kernel": (2.0 * D * N, mean(t_dq)),
-        "hstu_bwd_dkdv_kernel": (8.0 * D * N, mean(t_dkdv)),
+        "hstu_bwd_kernel": (10.0 * D * N, mean(t_bwd)),
     }
     if func_mode:  # whole calls (see step)
         kernels = {"hstu_attn_fwd (whole call)": (4.0 * D * N, mean(t_fwd)),
-                   "hstu_attn_bwd (whole call)": (10.0 * D * N, mean(t_dkdv))}
+                   "hstu_attn_bwd (whole call)": (10.0 * D * N, mean(t_bwd))}
     dom = max(kernels, key=lambda k: kernels[k][1])
     f_dom, ms_dom = kernels[dom]
     achieved = f_dom / (ms_dom * 1e-3) / 1e12
@@ -844,10 +844,9 @@ def main():
                        flops_per_step=flops_step, peaks_source=pk["source"]),
         "per_kernel_ms": {"plan": mean(t_plan) if t_plan else None,
                           "sched_fwd": mean(t_sched_f), "fwd": mean(t_fwd),
-                          "sched_bwd": mean(t_sched_b), "bwd_dq": mean(t_dq),
-                          "bwd_dkdv": mean(t_dkdv),
-                          "sum": mean([a + b + c + e + f for a, b, c, e, f in
-                                       zip(t_sched_f, t_fwd, t_sched_b, t_dq, t_dkdv)]),
+                          "sched_bwd": mean(t_sched_b), "bwd": mean(t_bwd),
+                          "sum": mean([a + b + c + e for a, b, c, e in
+                                       zip(t_sched_f, t_fwd, t_sched_b, t_bwd)]),
                           "steps": len(timed),
                           "note": "second pass with events between kernels (no launch overlap), "
                                   "each call scheduling its own work"},
@@ -861,7 +860,7 @@ def main():
                 "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": e2e_ms_step,
                 "note": "copy-in, compute and copy-out of consecutive steps overlap on three "
                         "streams; L2 not flushed (each step's inputs arrive fresh from the host)"},
-        "gpu_launches": (4 if use_plan else 7 if func_mode else 5) * args.steps,
+        "gpu_launches": (3 if use_plan else 6 if func_mode else 4) * args.steps,
         "clocks": clk,
         "wall_s_timed_loop": wall,
     }

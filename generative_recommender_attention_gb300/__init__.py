@@ -280,8 +280,8 @@ def hstu_attn_bwd(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     Same arguments as the forward plus ``dout`` (shape of q).  Caller-owned
     ``dq``/``dk``/``dv`` may be supplied (overwritten); dk and dv may be
     disjoint views of one packed KV buffer.  ``events``: optional list of 4
-    torch.cuda.Event (before the scheduler, after it, after the dK/dV kernel,
-    after the dQ kernel).
+    torch.cuda.Event (before the scheduler, after it, and twice after the
+    backward kernel, which runs the dK/dV units and then the dQ units).
     """
     import torch
     lib = library()

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhstu_attn.so")
-SOURCES = ["api.cu", "sched.cu", "fwd.cu", "bwd_dq.cu", "bwd_dkdv.cu", "lmsd.cu"]
+SOURCES = ["api.cu", "sched.cu", "fwd.cu", "bwd_dkdv.cu", "lmsd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -169,12 +169,12 @@ int64_t cap_b(int32_t batch, int64_t total_k, int32_t H, int32_t D) {
 
 int bn_for(int D) { return D == 256 ? 64 : 128; }
 
-// Backward workspace: header | list A | list B | ds_base (B + 1 ints) | dS
-// blocks.  The dS capacity bounds sum_b H ceil(Lk_b/128) ceil(Lq_b/64) from
+// Backward workspace: header | list A | list B | ds_base (B + 1 ints) |
+// readiness counts (B x H ints) | dS blocks.  The dS capacity bounds sum_b H ceil(Lk_b/128) ceil(Lq_b/64) from
 // the sizes alone (every Lq_b <= max_seqlen_q), so the host never needs the
 // sequence lengths.
 struct BwdLayout {
-  size_t units_b, ds_base, ds, total;
+  size_t units_b, ds_base, ready, ds, total;
   int64_t ds_blocks;
 };
 
@@ -183,7 +183,8 @@ bool bwd_layout(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int3
   const int64_t capA = cap_a(batch, total_q, H), capB = cap_b(batch, total_k, H, D);
   L->units_b = kHeaderBytes + 32 * static_cast<size_t>(capA);
   L->ds_base = L->units_b + 32 * static_cast<size_t>(capB);
-  L->ds = (L->ds_base + 4 * (static_cast<size_t>(batch) + 1) + 1023) & ~size_t(1023);
+  L->ready = L->ds_base + 4 * (static_cast<size_t>(batch) + 1);
+  L->ds = (L->ready + 4 * static_cast<size_t>(batch) * H + 1023) & ~size_t(1023);
   L->ds_blocks = static_cast<int64_t>(H) * cdiv(std::max<int32_t>(max_q, 0), kDsQueries) *
                  (cdiv(total_k, kDsKeys) + batch);
   if (L->ds_blocks > INT32_MAX) return false;  // block indices are int32 on the device
@@ -504,7 +505,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (!device_info(&c.dev)) return HSTU_ERR_CUDA;
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
-  const int BN = kDsKeys;                                         // dQ kernel key tile
+  const int BN = kDsKeys;                                         // dQ unit key tile
   const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;  // dK/dV query tile
   const int split = D == 256 ? 2 : 1;
   const int64_t capA = cap_a(batch, total_q, H);
@@ -531,12 +532,14 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   int4* unitsA = reinterpret_cast<int4*>(ws + kHeaderBytes);
   int4* unitsB = reinterpret_cast<int4*>(ws + lay.units_b);
   int* ds_base = reinterpret_cast<int*>(ws + lay.ds_base);
+  int* ready = reinterpret_cast<int*>(ws + lay.ready);
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmaxA; sa.cap_a = static_cast<int>(capA); sa.units_a = unitsA;
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
   sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks); sa.cache_seqs = sched_cache;
+  sa.ready = ready;
   sa.fm = fm;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   if (fm.func != nullptr &&
@@ -555,34 +558,31 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (planned) plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, a.key);
   a.timeout_ns = kWaitTimeoutNs; a.pdl_wait = 1;
   a.ds = ws + lay.ds; a.ds_base = ds_base; a.ds_cap = static_cast<int>(lay.ds_blocks);
+  a.ready = ready;
   a.fm = fm;
-  // dK/dV first: it also stores the dS blocks that the dQ kernel reads
-  if (total_k > 0) {
-    AttnArgs ak = a;
-    ak.units = unitsB; ak.units_slot = kHdrUnitsB; ak.next_slot = kHdrNextB;
-    ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
-    ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
-    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capB));
-    CUtensorMap m_dk128, m_dv128;  // whole key tiles leave through TMA stores
-    if (!encode_thd(&m_dk128, dk.ptr, total_k, H, D, dk.stride_t, dk.stride_h, kBM, c.bf16) ||
-        !encode_thd(&m_dv128, dv.ptr, total_k, H, D, dv.stride_t, dv.stride_h, kBM, c.bf16))
-      return HSTU_ERR_CUDA;
-    if (launch_dkdv(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m_k128, m_v128, m_q64, m_do64,
-                    m_dk128,
-                    m_dv128, ak) != cudaSuccess)
-      return HSTU_ERR_CUDA;
-  }
-  if (!em.mark(2, stream)) return HSTU_ERR_CUDA;
-  if (total_q > 0) {
-    AttnArgs aq = a;
-    aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA;
-    aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
-    const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, capA));
-    if (launch_dq(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m_ds, m_k128, aq) !=
-        cudaSuccess)
-      return HSTU_ERR_CUDA;
-  }
-  if (!em.mark(3, stream)) return HSTU_ERR_CUDA;
+  // One launch: each CTA takes dK/dV units (list B), which also store the
+  // dS blocks, then dQ units (list A), each of which waits until the dS
+  // blocks of its sequence and head are complete.
+  AttnArgs ak = a;
+  ak.units = unitsB; ak.units_slot = kHdrUnitsB; ak.next_slot = kHdrNextB;
+  ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
+  ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
+  AttnArgs aq = a;
+  aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA;
+  aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
+  const int grid = static_cast<int>(std::min<int64_t>(c.dev.sm_count, std::max(capA, capB)));
+  BwdMaps m;
+  m.k = m_k128; m.v = m_v128; m.q = m_q64; m.dout = m_do64; m.ds = m_ds;
+  // whole key tiles of dK / dV leave through TMA stores
+  const hstu_ten_t dkx = hk ? dk : dq, dvx = hk ? dv : dq;
+  if (!encode_thd(&m.dk, dkx.ptr, hk ? total_k : total_q, H, D, dkx.stride_t, dkx.stride_h, kBM,
+                  c.bf16) ||
+      !encode_thd(&m.dv, dvx.ptr, hk ? total_k : total_q, H, D, dvx.stride_t, dvx.stride_h, kBM,
+                  c.bf16))
+    return HSTU_ERR_CUDA;
+  if (launch_bwd(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m, ak, aq) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (!em.mark(2, stream) || !em.mark(3, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
 }
 
@@ -698,6 +698,7 @@ hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seql
   sa.units_f = reinterpret_cast<int4*>(ws + plan_list_f(lay));
   sa.header = reinterpret_cast<int*>(ws);
   sa.ds_base = reinterpret_cast<int*>(ws + lay.ds_base);
+  sa.ready = reinterpret_cast<int*>(ws + lay.ready);
   sa.ds_cap = static_cast<int>(lay.ds_blocks);
   sa.cache_seqs = sched_cache;
   plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, sa.key);

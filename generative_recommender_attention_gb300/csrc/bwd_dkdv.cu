@@ -11,7 +11,7 @@
 // element), writes both back in place as 16-bit, and accumulates
 // dV += A^T dO and dK += dS^T Q with the A operand read from TMEM.  No
 // atomics.  Each dS block (64 queries x 128 keys, query-major) is also
-// stored to the workspace, where the dQ kernel reads it for dQ = dS K; keys
+// stored to the workspace, where the dQ phase reads it for dQ = dS K; keys
 // past the sequence end store zeros there, so they add nothing to dQ.  A
 // thread holds one key row of dS^T; neighbouring lanes swap halves of their
 // packed pairs so that every 4-byte store writes two keys of one query and
@@ -37,6 +37,10 @@
 // 64-byte pieces (one cache line per lane) kept the row warps from the next
 // unit for several thousand cycles.  Ragged last tiles and D = 256 (one
 // K/V buffer) keep the per-row stores.
+// After its last dK/dV unit the CTA drains, re-initialises its barriers and
+// runs dQ units (bwd_dq.cuh) in the same shared memory and TMEM; each waits
+// for the readiness count of its sequence and head (ready_target), which
+// the row warps raise once per unit after fencing their dS stores.
 // TMEM: S^T0 | S^T1 | dP^T0 | dP^T1 | dV | dK.  The two dependency chains
 // (S^T -> A^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T) run side by side,
 // two half-steps deep, one per issuing thread, so while one thread waits
@@ -44,7 +48,7 @@
 // The N = 64 S^T / dP^T MMAs run at about two thirds of the tensor rate; that
 // costs less than serialising the row work with 128-query steps, for which
 // TMEM has no room to double-buffer.
-#include "kernels.h"
+#include "bwd_dq.cuh"
 
 namespace hstu {
 
@@ -74,14 +78,18 @@ __device__ __forceinline__ bool tile_full(const UnitInfo& U, int64_t total_k) {
   return end <= U.Lk && static_cast<int64_t>(U.k0) + end <= total_k;
 }
 
+// The backward kernel: this CTA's dK/dV units (list B, args `a`), then its
+// dQ units (list A, args `aq`; bwd_dq.cuh), in one launch.
 template <int D, bool BF16, bool FUNC>
 __global__ void __launch_bounds__(kDkdvThreads, 1)
-    hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dk,
-                         const __grid_constant__ CUtensorMap tm_dv, const AttnArgs a) {
+    hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv,
+                    const __grid_constant__ CUtensorMap tm_ds, const AttnArgs a,
+                    const AttnArgs aq) {
   using C = DkdvCfg<D>;
   constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV, NS = C::NS;
   constexpr int KCH = D / 64;
@@ -127,6 +135,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   };
   // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
   static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
+  // the dQ phase reuses the tile area and the barrier words
+  static_assert(DqCfg<D>::TILE_BYTES <= C::TILE_BYTES && dq::Bars<D>::NBARS <= NBARS,
+                "dQ phase fits the dK/dV layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -165,6 +176,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
     if (STAGE) { tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv); }
+    tma_prefetch_desc(&tm_ds);
   }
   if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
   __syncwarp();  // thread 0's set-up above diverged warp 0
@@ -178,7 +190,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   if (a.pdl_wait == 1) grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int n_units = work_units(a);
-  const UnitQueue uq{reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4)), bar(UFULL), bar(UEMPTY)};
+  UnitInfo* ring = reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4));
+  const UnitQueue uq{ring, bar(UFULL), bar(UEMPTY)};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -214,9 +227,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         return true;
       };
-      // units are claimed one ahead: the next claim overlaps this unit's loads
-      // the first unit of each CTA is its own index; later ones come from the counter
-      UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
+      // Units are claimed one ahead: the next claim overlaps this unit's
+      // loads.  Every dK/dV unit, the first included, comes from the counter,
+      // so only CTAs already running hold one: the dQ units that wait for
+      // them never wait on a CTA that has not started.
+      UnitInfo nx = load_unit_info(a.units, atomicAdd(a.header + a.next_slot, 1), n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U = nx;
         if (U.n > 0 && U.hz % SPLIT == 0) {
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        nx = load_unit_info(a.units, gridDim.x + atomicAdd(a.header + a.next_slot, 1), n_units);
+        nx = load_unit_info(a.units, atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz / SPLIT;
         const int k_row0 = U.k0 + kBM * U.tile;
@@ -396,6 +411,14 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const float dk_scale = 0.5f * a.alpha * a.inv_L;  // dS^T is stored doubled
     uint32_t h = 0, oi = 0;
     bool ok = true;
+    // This warp's dS stores of unit V are issued: fence them and count the
+    // unit toward the readiness of its sequence and head.
+    auto count_unit = [&](const UnitInfo& V) {
+      if (a.ready == nullptr) return;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(a.ready + V.b * a.H + V.hz / SPLIT, 1);
+    };
     // this lane's dV / dK row pieces of unit V, for the per-row stores
     // (formed only where they are used, so no pointer stays live across the
     // steps); returns whether the row exists
@@ -464,6 +487,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       if (U.n <= 0) {  // no key steps: zeros, no TMEM
         char *dvrow, *dkrow;
         if (out_rows(U, dvrow, dkrow)) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
+        count_unit(U);
         continue;
       }
       const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
@@ -597,17 +621,46 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
       }
       if (!ok) break;
+      count_unit(U);
       if (!epilogue(U)) { ok = false; break; }
     }
   }
 
-  // The role branches leave lanes of warps 0, 1 (and 18) on different paths;
+  // The role branches leave lanes of warps 0, 1 and 10 on different paths;
   // reconverge each warp so the aligned CTA barrier counts it exactly once
   // (otherwise it can release before the row warps finish reading TMEM).
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  release_work(a);
+
+  // ---------------------------------------------------------------- dQ phase
+  // Every dK/dV MMA, TMEM read and copy of this CTA has completed: the dQ
+  // phase takes over the tile area, the barrier words and TMEM.  A CTA whose
+  // dK/dV phase gave up skips it (the dQ units that wait for its counts then
+  // give up too, after the wait limit).
+  const bool dkdv_ok = flags[0] == 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBARS; ++i) mbar_inval(bar(i));
+    dq::init_bars<D>(bars);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (dkdv_ok) dq::run<D, BF16>(&tm_ds, &tm_k, aq, base, bars, flags, ring, tmem);
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  // planned calls: the last CTA leaves both unit counters at zero and
+  // advances the readiness epoch (every CTA has made its last claim and
+  // passed its last readiness wait by then)
+  if (a.planned && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.header + kHdrDone, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(a.header + a.next_slot, 0);
+      atomicExch(a.header + aq.next_slot, 0);
+      atomicAdd(a.header + kHdrEpoch, 1);
+      atomicExch(a.header + kHdrDone, 0);
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -615,10 +668,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 }
 
 template <int D, bool BF16, bool FUNC>
-cudaError_t launch_dkdv_f(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tdk,
-                          const CUtensorMap& tdv, const AttnArgs& a) {
-  auto kern = hstu_bwd_dkdv_kernel<D, BF16, FUNC>;
+cudaError_t launch_bwd_f(int grid, cudaStream_t st, bool pdl, const BwdMaps& m, const AttnArgs& a,
+                         const AttnArgs& aq) {
+  auto kern = hstu_bwd_kernel<D, BF16, FUNC>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -626,33 +678,30 @@ cudaError_t launch_dkdv_f(int grid, cudaStream_t st, bool pdl, const CUtensorMap
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, tk, tv, tq, tdo, tdk,
-                     tdv, a);
+  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, m.k, m.v, m.q, m.dout,
+                     m.dk, m.dv, m.ds, a, aq);
 }
 
 // The arbitrary-mask path (its endpoint loads and ballot transpose) is a
 // separate instantiation, so that the window kernels keep their registers.
 template <int D, bool BF16>
-cudaError_t launch_dkdv_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tdk,
-                          const CUtensorMap& tdv, const AttnArgs& a) {
-  if (a.fm.func != nullptr)
-    return launch_dkdv_f<D, BF16, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
-  return launch_dkdv_f<D, BF16, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
+cudaError_t launch_bwd_t(int grid, cudaStream_t st, bool pdl, const BwdMaps& m, const AttnArgs& a,
+                         const AttnArgs& aq) {
+  if (a.fm.func != nullptr) return launch_bwd_f<D, BF16, true>(grid, st, pdl, m, a, aq);
+  return launch_bwd_f<D, BF16, false>(grid, st, pdl, m, a, aq);
 }
 
 }  // namespace
 
-cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const CUtensorMap& tdk, const CUtensorMap& tdv, const AttnArgs& a) {
+cudaError_t launch_bwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const BwdMaps& m,
+                       const AttnArgs& a, const AttnArgs& aq) {
   switch (D) {
-    case 64: return bf16 ? launch_dkdv_t<64, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
-                         : launch_dkdv_t<64, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
-    case 128: return bf16 ? launch_dkdv_t<128, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
-                          : launch_dkdv_t<128, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
-    case 256: return bf16 ? launch_dkdv_t<256, true>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a)
-                          : launch_dkdv_t<256, false>(grid, st, pdl, tk, tv, tq, tdo, tdk, tdv, a);
+    case 64: return bf16 ? launch_bwd_t<64, true>(grid, st, pdl, m, a, aq)
+                         : launch_bwd_t<64, false>(grid, st, pdl, m, a, aq);
+    case 128: return bf16 ? launch_bwd_t<128, true>(grid, st, pdl, m, a, aq)
+                          : launch_bwd_t<128, false>(grid, st, pdl, m, a, aq);
+    case 256: return bf16 ? launch_bwd_t<256, true>(grid, st, pdl, m, a, aq)
+                          : launch_bwd_t<256, false>(grid, st, pdl, m, a, aq);
     default: return cudaErrorInvalidValue;
   }
 }

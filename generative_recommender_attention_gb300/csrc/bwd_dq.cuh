@@ -2,13 +2,17 @@
 // with dS'_ij = M_ij <dO_i, v_j> SiLU'(alpha q_i.k_j) (chain rule of "HSTU
 // Attention (Blackwell SM100/SM103)", Overview equations).
 //
-// The dK/dV kernel already forms dS' for every (key tile, 64-query block) the
+// The dK/dV units already form dS' for every (key tile, 64-query block) the
 // mask leaves non-empty and stores it (doubled, 16-bit) in the workspace;
-// this kernel is the remaining contraction dQ = dS' K, a plain tensor-core
-// GEMM with no recomputation of S or dP.  Query-stationary and atomic-free:
-// each 128-row query tile is owned by one CTA, which streams the tile's two
-// dS blocks and the matching key tile per 128-key step and accumulates dQ in
-// TMEM, so results do not depend on scheduling.
+// this phase is the remaining contraction dQ = dS' K, a plain tensor-core
+// GEMM with no recomputation of S or dP.  It runs in the backward kernel
+// after the CTA's dK/dV units (same launch, same shared memory and TMEM), so
+// a dQ unit starts as soon as the dK/dV units of its sequence and head have
+// stored their dS blocks (the readiness counts), not after the slowest CTA's
+// last dK/dV unit and a second launch.  Query-stationary and atomic-free on
+// data: each 128-row query tile is owned by one CTA, which streams the tile's
+// two dS blocks and the matching key tile per 128-key step and accumulates
+// dQ in TMEM, so results do not depend on scheduling.
 //   warp 0      TMA: per step the two 64-query dS blocks (16 KB each) and
 //               the 128-key K tile into one ring stage; the blocks land as
 //               rows 0-63 and 64-127 of one K-major 128 x 128 A tile.
@@ -20,77 +24,78 @@
 // Rows of a tile past the sequence end (or a second dS block the sequence
 // does not have) are computed from stale shared memory but never stored:
 // each output row depends only on its own A row.
+#pragma once
+
 #include "kernels.h"
 
 namespace hstu {
+namespace dq {
 
-namespace {
-
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kDqThreads, 1)
-    hstu_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_ds,
-                       const __grid_constant__ CUtensorMap tm_k, const AttnArgs a) {
-  using C = DqCfg<D>;
-  constexpr int NS = C::NS, KCH = D / 64;
-  constexpr int NACC = 2;  // TMEM accumulators
-  constexpr uint32_t IDESC = idesc_f16(BF16, kBM, D, false, true);
-  static_assert(NACC * D <= kTmemCols, "TMEM budget");
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw);
-  auto stage_a = [&](int s) { return base + s * C::STAGE_BYTES; };
-  auto stage_k = [&](int s) { return base + s * C::STAGE_BYTES + C::A_BYTES; };
-
+// Barrier slots of the dQ phase (NS ring stages, two TMEM accumulators).
+template <int D>
+struct Bars {
+  static constexpr int NS = DqCfg<D>::NS, NACC = 2;
   enum {
     FULL = 0, EMPTY = FULL + NS, ACCFULL = EMPTY + NS, ACCEMPTY = ACCFULL + NACC,
     UFULL = ACCEMPTY + NACC, UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing,
     NBARS = DRAIN + 1
   };
-  // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
-  static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  auto bar = [&](int i) { return smem_u32(bars + i); };
+};
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) { mbar_init(bar(FULL + i), 1); mbar_init(bar(EMPTY + i), 1); }
-    for (int i = 0; i < NACC; ++i) {
-      mbar_init(bar(ACCFULL + i), 1);
-      mbar_init(bar(ACCEMPTY + i), kDqEpiWarps);
-    }
-    for (int i = 0; i < kUnitRing; ++i) {
-      mbar_init(bar(UFULL + i), 1);
-      mbar_init(bar(UEMPTY + i), 1 + kDqEpiWarps);
-    }
-    mbar_init(bar(DRAIN), 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    fence_mbar_init();
+// Thread 0 initialises the phase's barriers at `bars`.
+template <int D>
+__device__ __forceinline__ void init_bars(uint64_t* bars) {
+  using B = Bars<D>;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  for (int i = 0; i < B::NS; ++i) { mbar_init(bar(B::FULL + i), 1); mbar_init(bar(B::EMPTY + i), 1); }
+  for (int i = 0; i < B::NACC; ++i) {
+    mbar_init(bar(B::ACCFULL + i), 1);
+    mbar_init(bar(B::ACCEMPTY + i), kDqEpiWarps);
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&tm_ds); tma_prefetch_desc(&tm_k); }
-  if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
-  __syncwarp();  // thread 0's set-up above diverged warp 0
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  for (int i = 0; i < kUnitRing; ++i) {
+    mbar_init(bar(B::UFULL + i), 1);
+    mbar_init(bar(B::UEMPTY + i), 1 + kDqEpiWarps);
+  }
+  mbar_init(bar(B::DRAIN), 1);
+  fence_mbar_init();
+}
+
+// The dQ phase: warp 0 TMA, warp 1 MMA issuer, warps 2-5 epilogue; other
+// warps return at once.  `base` is the 1024-aligned tile area, `bars` the
+// barriers set up by init_bars, `ring` the unit ring, `tmem` the CTA's TMEM
+// (2 D columns used).  The caller synchronises the block afterwards.
+template <int D, bool BF16>
+__device__ __forceinline__ void run(const CUtensorMap* tm_ds, const CUtensorMap* tm_k,
+                                    const AttnArgs& a, uint32_t base, uint64_t* bars,
+                                    volatile int* flags, UnitInfo* ring, uint32_t tmem) {
+  using C = DqCfg<D>;
+  using B = Bars<D>;
+  constexpr int NS = C::NS, KCH = D / 64, NACC = B::NACC;
+  constexpr uint32_t IDESC = idesc_f16(BF16, kBM, D, false, true);
+  static_assert(NACC * D <= kTmemCols, "TMEM budget");
+  enum { FULL = B::FULL, EMPTY = B::EMPTY, ACCFULL = B::ACCFULL, ACCEMPTY = B::ACCEMPTY,
+         UFULL = B::UFULL, UEMPTY = B::UEMPTY, DRAIN = B::DRAIN };
+  auto stage_a = [&](int s) { return base + s * C::STAGE_BYTES; };
+  auto stage_k = [&](int s) { return base + s * C::STAGE_BYTES + C::A_BYTES; };
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtl wc{a.header, flags, a.timeout_ns};
   const WaitCtl drain{a.header, flags + 1, a.timeout_ns};
-  // everything below reads what earlier grids wrote (work list, dS blocks)
-  if (a.pdl_wait == 1) grid_dependency_wait();
-  if (threadIdx.x == 0) grid_launch_dependents();
   const int n_units = work_units(a);
-  const UnitQueue uq{reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4)), bar(UFULL), bar(UEMPTY)};
+  const UnitQueue uq{ring, bar(UFULL), bar(UEMPTY)};
+  const int split = D == 256 ? 2 : 1;  // dK/dV units per key tile and head
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
+      // planned calls count on from the calls before (see ready_target)
+      const uint32_t epoch =
+          a.ready != nullptr && a.planned ? static_cast<uint32_t>(__ldcg(a.header + kHdrEpoch)) : 0u;
+      // metadata beyond the sizes dropped dK/dV units (the call reports an
+      // invalid argument): their counts would never complete, so skip the waits
+      const bool counted = a.ready != nullptr && __ldcg(a.header + kHdrOverflowB) == 0;
       UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         const UnitInfo U = nx;
@@ -118,6 +123,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         // blocks of the key tiles before (an arbitrary mask keeps n_qb slots per
         // key tile, the full mask's layout)
         int off = ds_block_off(kt0, U.Lq, U.Lk, a.win);
+        // the dS blocks of (b, h) are read only once all its dK/dV units stored them
+        if (counted) {
+          const uint32_t target = static_cast<uint32_t>(ready_target(U.Lk, split));
+          if (!wait_count(a.ready + U.b * a.H + h, epoch * target, target, a.header, flags,
+                          a.timeout_ns, 0x007)) {
+            ok = false;
+            break;
+          }
+        }
         int kt_next = kt0;  // live-tile cursor (arbitrary mask)
         for (int jj = 0; jj < U.n; ++jj, ++g) {
           const int s = g % NS;
@@ -152,14 +166,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           // A tile: 64-key chunk c of query rows 0-63 (block 2i) and 64-127 (2i + 1)
 #pragma unroll
           for (int c = 0; c < kDsKeys / 64; ++c) {
-            tma_load_3d(stage_a(s) + c * (kBM * 128), &tm_ds, bar(FULL + s), 64 * c, 0, blk0);
+            tma_load_3d(stage_a(s) + c * (kBM * 128), tm_ds, bar(FULL + s), 64 * c, 0, blk0);
             if (second)
-              tma_load_3d(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, &tm_ds, bar(FULL + s),
+              tma_load_3d(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, tm_ds, bar(FULL + s),
                           64 * c, 0, blk1);
           }
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
-            tma_load_3d(stage_k(s) + c * (kDsKeys * 128), &tm_k, bar(FULL + s), 64 * c, h,
+            tma_load_3d(stage_k(s) + c * (kDsKeys * 128), tm_k, bar(FULL + s), 64 * c, h,
                         U.k0 + kDsKeys * j);
         }
       }
@@ -200,7 +214,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mma_commit(bar(DRAIN));
       wait_bar(bar(DRAIN), 0, drain, 0x1ff);
     }
-  } else {
+  } else if (warp < 2 + kDqEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
@@ -238,47 +252,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ++oi;
     }
   }
-
-  // The role branches leave lanes of warps 0 and 1 on different paths;
-  // reconverge each warp so the aligned CTA barrier counts it exactly once
-  // (otherwise it can release before the epilogue warps finish reading TMEM).
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  release_work(a);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
 }
 
-template <int D, bool BF16>
-cudaError_t launch_dq_t(int grid, cudaStream_t st, bool pdl, const CUtensorMap& tds,
-                        const CUtensorMap& tk, const AttnArgs& a) {
-  auto kern = hstu_bwd_dq_kernel<D, BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqCfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  return launch_attn(kern, grid, kDqThreads, DqCfg<D>::SMEM, st, pdl, tds, tk, a);
-}
-
-}  // namespace
-
-cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tds,
-                      const CUtensorMap& tk, const AttnArgs& a) {
-  switch (D) {
-    case 64: return bf16 ? launch_dq_t<64, true>(grid, st, pdl, tds, tk, a)
-                         : launch_dq_t<64, false>(grid, st, pdl, tds, tk, a);
-    case 128: return bf16 ? launch_dq_t<128, true>(grid, st, pdl, tds, tk, a)
-                          : launch_dq_t<128, false>(grid, st, pdl, tds, tk, a);
-    case 256: return bf16 ? launch_dq_t<256, true>(grid, st, pdl, tds, tk, a)
-                          : launch_dq_t<256, false>(grid, st, pdl, tds, tk, a);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
+}  // namespace dq
 }  // namespace hstu

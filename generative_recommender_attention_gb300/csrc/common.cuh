@@ -29,6 +29,7 @@ enum HeaderWord : int {
   kHdrNextF = 9,      // plan: next unclaimed unit of list F
   kHdrOverflowF = 10, // plan: units dropped from list F
   kHdrDone = 11,      // plan: CTAs of the running kernel that have finished
+  kHdrEpoch = 12,     // backward: calls completed since the readiness counts were zeroed
   kHdrKey = 16,       // plan: kPlanKeyInts words (16-byte aligned), the sizes the plan was made for
 };
 constexpr int kPlanKeyInts = 10;
@@ -89,6 +90,32 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
                                          int where) {
   if (mbar_try_wait(bar, parity)) return true;
   return wait_slow(bar, parity, c.status, c.abort_flag, c.timeout_ns, where);
+}
+
+// Bounded wait until a global counter that other CTAs raise has grown by
+// `target` past `start` (acquire at GPU scope; modulo 2^32, so a count may
+// wrap), with the same give-up rules as a barrier wait.  On success the
+// counted data may be read by TMA.
+static __device__ __noinline__ bool wait_count(const int* cnt, uint32_t start, uint32_t target,
+                                               int* status, volatile int* abort_flag,
+                                               uint64_t timeout_ns, int where) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (static_cast<uint32_t>(ld_acquire_gpu(cnt)) - start >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicCAS(status + kHdrStatus, 0, kStatusTimeout);
+        atomicExch(status + kHdrWhere, where);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
 }
 
 // Work-unit record plus the packed-sequence offsets and lengths it needs,

@@ -22,17 +22,16 @@ constexpr int kFwdRowWarps = 8;
 constexpr int kFwdEpiWarps = 4;
 constexpr int kFwdPvWarp = 2 + kFwdRowWarps + kFwdEpiWarps;
 constexpr int kAttnThreads = 32 * (kFwdPvWarp + 1);
-// dK/dV kernel: warp 0 TMA, warp 1 MMA, warps 2-9 row work (two warps per
+// Backward kernel, dK/dV phase: warp 0 TMA, warp 1 MMA, warps 2-9 row work (two warps per
 // TMEM lane quarter, one per half of the columns), warp 10 issues the
 // accumulation MMAs, so the two MMA streams wait on their own barriers
 // without stalling each other.  Few row warps per SM sub-partition leave
 // the issuing threads more of its issue slots.
 constexpr int kDkdvRowWarps = 8;
 constexpr int kDkdvThreads = 64 + 32 * kDkdvRowWarps + 32;
-// dQ kernel (dQ = dS K from the stored dS blocks): warp 0 TMA, warp 1 MMA,
+// Backward kernel, dQ phase (dQ = dS K from the stored dS blocks): warp 0 TMA, warp 1 MMA,
 // warps 2-5 epilogue (one per TMEM lane quarter).
 constexpr int kDqEpiWarps = 4;
-constexpr int kDqThreads = 64 + 32 * kDqEpiWarps;
 constexpr int kTmemCols = 512;
 
 // Bytes of shared memory a kernel needs beyond its tiles: barriers, the TMEM
@@ -40,7 +39,7 @@ constexpr int kTmemCols = 512;
 constexpr int kCtlBytes = 1024;
 constexpr int kAlignSlack = 1024;
 // K/V steps warmed in L2 ahead of the TMA loads (and of the next unit);
-// the dK/dV kernel's 64-query steps run twice as many Q/dO tiles ahead.
+// the dK/dV units' 64-query steps run twice as many Q/dO tiles ahead.
 constexpr int kPrefetch = 4;
 constexpr int kPrefetchQ = 8;
 
@@ -181,6 +180,7 @@ struct SchedArgs {
   int4* units_f;
   int* header;
   int* ds_base;              // backward: (B + 1) first dS block of each sequence, or null
+  int* ready;                // backward: B x H readiness counts, zeroed here, or null
   int ds_cap;                // backward: dS blocks the workspace holds
   int cache_seqs;            // 1: sequence records cached in shared memory
   int key[kPlanKeyInts];     // plans: the sizes recorded in the header
@@ -196,6 +196,18 @@ struct SchedArgs {
 // ds_block_off(j, ...) and hold its query blocks in order.
 constexpr int kDsKeys = 128, kDsQueries = 64;
 constexpr int kDsBlockBytes = kDsKeys * kDsQueries * 2;
+
+// The backward is one launch: each CTA runs dK/dV units, then dQ units.  Every
+// row warp of a dK/dV unit of sequence b and head h (each D half of it at
+// D = 256) adds 1 to ready[b H + h] once its dS stores of the unit are
+// fenced, so a call raises the count by ready_target(Lk_b), and the dS
+// blocks of (b, h) are complete once it has; a dQ unit of (b, h) waits for
+// that before it reads them.  The scheduler zeroes the counts and the epoch
+// word; a planned call, which has no scheduling launch of its own, counts
+// from epoch x target, and its last CTA advances the epoch.
+__host__ __device__ inline int ready_target(int Lk, int split) {
+  return kDkdvRowWarps * split * ((Lk + kDsKeys - 1) / kDsKeys);
+}
 
 // Stored blocks of key tile j: first query block and count.
 __host__ __device__ inline void ds_blocks_of(int j, int Lq, int Lk, Window w, int& m0, int& n) {
@@ -235,7 +247,7 @@ struct AttnArgs {
   uint64_t timeout_ns;  // limit of every barrier wait
   int next_slot;        // header word counting units claimed so far
   int pdl_wait;         // 0: none, 1: wait for the previous grid first, 2: only before exit
-  void* o0;             // fwd: out, dq kernel: dq, dkdv kernel: dv
+  void* o0;             // fwd: out, dQ units: dq, dK/dV units: dv
   int64_t o0_st, o0_sh;
   void* o1;             // dkdv kernel: dk
   int64_t o1_st, o1_sh;
@@ -247,6 +259,7 @@ struct AttnArgs {
   void* ds;             // backward: dS blocks (written by dK/dV, read by dQ)
   const int* ds_base;   // backward: first dS block of each sequence (B + 1)
   int ds_cap;           // backward: dS blocks the workspace holds
+  int* ready;           // backward: B x H readiness counts (see ready_target)
   int planned;          // 1: the work list comes from a plan (see below)
   int key[kPlanKeyInts];  // planned: this call's sizes, which must be the plan's
 };
@@ -375,11 +388,14 @@ inline cudaError_t launch_attn(void (*kern)(KArgs...), int grid, int threads, in
 
 cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a);
-cudaError_t launch_dq(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tds,
-                      const CUtensorMap& tk, const AttnArgs& a);
-cudaError_t launch_dkdv(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const CUtensorMap& tk,
-                        const CUtensorMap& tv, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const CUtensorMap& tdk, const CUtensorMap& tdv, const AttnArgs& a);
+// Tensor maps of the backward kernel: K, V (128-row boxes), Q, dO (the
+// dK/dV query tile), dK, dV (TMA-stored whole key tiles) and the dS blocks.
+struct BwdMaps {
+  CUtensorMap k, v, q, dout, dk, dv, ds;
+};
+// The backward: dK/dV units (list B, `a`), then dQ units (list A, `aq`).
+cudaError_t launch_bwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const BwdMaps& m,
+                       const AttnArgs& a, const AttnArgs& aq);
 cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace hstu

@@ -203,6 +203,11 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     a.header[overflow_slot] = 0;
     a.header[next_slot] = 0;
   }
+  // backward: the readiness counts of the dK/dV -> dQ hand-over start at zero
+  if (list_b && a.ready != nullptr) {
+    for (int i = tid; i < a.B * a.H; i += blockDim.x) a.ready[i] = 0;
+    if (tid == 0) a.header[kHdrEpoch] = 0;
+  }
 
   for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
   // every pass reads the sequences: one coalesced read of cu_seqlens
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
     if (tid == 0) {
       a.ds_base[a.B] = all;
       // sequences longer than the caller's max_seqlen_q: the blocks would not
-      // fit; the dK/dV kernel then skips the stores past the end
+      // fit; the dK/dV units then skip the stores past the end
       if (all > a.ds_cap || all < 0) atomicExch(a.header + kHdrOverflowB, 1);
     }
   }

@@ -226,7 +226,8 @@ hstu_status_t hstu_attn_fwd_paged(hstu_cten_t q, const void* paged_kv, int64_t n
  *   forward:  events[0] before the scheduler launch, events[1] after it,
  *             events[2] after the forward kernel;
  *   backward: events[0] before the scheduler launch, events[1] after it,
- *             events[2] after the dK/dV kernel, events[3] after the dQ kernel.
+ *             events[2] and events[3] after the backward kernel (dK/dV then dQ units
+ *             in one launch; the two are recorded back to back).
  * Elapsed times between consecutive events are per-kernel device times.
  * events must be non-null (HSTU_ERR_INVALID_ARG otherwise).
  */
