@@ -232,14 +232,21 @@ struct FuncArgs {
 
 // Shared memory of the scheduler block: one int per cost bucket, then (for
 // up to kSchedCacheSeqs sequences) one 16-byte record per sequence.
-bool sched_smem(int cmax, int batch, const DevInfo& dev, int* bytes, int* cache) {
+bool sched_smem(int cmax, int batch, int64_t cap, const DevInfo& dev, int* bytes, int* cache,
+                int* stage_units) {
   *cache = batch <= kSchedCacheSeqs ? 1 : 0;
-  const int b = sched_hist_ints(cmax) * 4 + (*cache ? 16 * batch : 0);
-  if (b > dev.max_smem_optin) return false;
+  int b = sched_hist_ints(cmax) * 4 + (*cache ? 16 * batch : 0);
+  if (b > dev.max_smem_optin - 1024) return false;
+  // a list of up to kSchedStageUnits records is staged in shared memory
+  // and leaves in one coalesced copy
+  *stage_units = static_cast<int>(std::min<int64_t>(
+      cap, std::min<int64_t>(kSchedStageUnits, (dev.max_smem_optin - 1024 - b) / 32)));
+  b += 32 * std::max(*stage_units, 0);
+  // the opt-in limit less the kernel's static shared memory, set once
   static bool set = false;
   if (b > 48 * 1024 && !set) {
     if (cudaFuncSetAttribute(hstu_sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dev.max_smem_optin) != cudaSuccess)
+                             dev.max_smem_optin - 1024) != cudaSuccess)
       return false;
     set = true;
   }
@@ -399,8 +406,9 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   const int BN = bn_for(D);
   const int64_t capA = cap_a(batch, total_q, H);
   const int cmax = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
-  int sched_bytes, sched_cache;
-  if (!sched_smem(cmax, batch, c.dev, &sched_bytes, &sched_cache)) return HSTU_ERR_UNSUPPORTED;
+  int sched_bytes, sched_cache, sched_stage;
+  if (!sched_smem(cmax, batch, capA, c.dev, &sched_bytes, &sched_cache, &sched_stage))
+    return HSTU_ERR_UNSUPPORTED;
 
   CUtensorMap tq, tk, tv;
   const void* kptr = total_k > 0 ? k.ptr : q.ptr;  // stand-in, never read when total_k == 0
@@ -429,7 +437,7 @@ hstu_status_t fwd_impl(hstu_cten_t q, hstu_cten_t k, hstu_cten_t v, hstu_ten_t o
   SchedArgs sa{};
   sa.cu_q = cu_seqlens_q; sa.cu_k = cu_seqlens_k; sa.B = batch; sa.H = H; sa.win = c.win;
   sa.bn_a = BN; sa.cmax_a = cmax; sa.cap_a = static_cast<int>(capA); sa.units_a = units;
-  sa.header = header; sa.cache_seqs = sched_cache; sa.fm = fm;
+  sa.header = header; sa.cache_seqs = sched_cache; sa.stage_units = sched_stage; sa.fm = fm;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
   if (fm.func != nullptr &&
       launch_func_ranges(cu_seqlens_q, cu_seqlens_k, batch,
@@ -512,8 +520,9 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   const int64_t capB = cap_b(batch, total_k, H, D);
   const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
   const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));
-  int sched_bytes, sched_cache;
-  if (!sched_smem(std::max(cmaxA, cmaxB), batch, c.dev, &sched_bytes, &sched_cache))
+  int sched_bytes, sched_cache, sched_stage;
+  if (!sched_smem(std::max(cmaxA, cmaxB), batch, std::max(capA, capB), c.dev, &sched_bytes,
+                  &sched_cache, &sched_stage))
     return HSTU_ERR_UNSUPPORTED;
 
   // Stand-ins for empty sides: valid maps that no unit ever reads through.
@@ -539,6 +548,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   sa.bq_b = BQ; sa.split_b = split; sa.cmax_b = cmaxB; sa.cap_b = static_cast<int>(capB);
   sa.units_b = unitsB; sa.header = header;
   sa.ds_base = ds_base; sa.ds_cap = static_cast<int>(lay.ds_blocks); sa.cache_seqs = sched_cache;
+  sa.stage_units = sched_stage;
   sa.ready = ready;
   sa.fm = fm;
   if (!em.mark(0, stream)) return HSTU_ERR_CUDA;
@@ -683,9 +693,9 @@ hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seql
   const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
   const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));
   const int cmaxF = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BNF)));
-  int sched_bytes, sched_cache;
-  if (!sched_smem(std::max(cmaxF, std::max(cmaxA, cmaxB)), batch, c.dev, &sched_bytes,
-                  &sched_cache))
+  int sched_bytes, sched_cache, sched_stage;
+  if (!sched_smem(std::max(cmaxF, std::max(cmaxA, cmaxB)), batch, std::max(capA, capB), c.dev,
+                  &sched_bytes, &sched_cache, &sched_stage))
     return HSTU_ERR_UNSUPPORTED;
   char* ws = static_cast<char*>(workspace);
   SchedArgs sa{};
@@ -701,6 +711,7 @@ hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seql
   sa.ready = reinterpret_cast<int*>(ws + lay.ready);
   sa.ds_cap = static_cast<int>(lay.ds_blocks);
   sa.cache_seqs = sched_cache;
+  sa.stage_units = sched_stage;
   plan_key(batch, total_q, total_k, H, D, max_seqlen_q, max_seqlen_k, c.win, sa.key);
   return launch_sched(3, sched_bytes, stream, true, sa) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }

@@ -14,6 +14,9 @@ constexpr int kSchedThreads = 1024;
 // Up to this many sequences the scheduler keeps every sequence's offsets and
 // lengths in shared memory (16 bytes each), read from cu_seqlens once.
 constexpr int kSchedCacheSeqs = 4096;
+// Lists of up to this many units are assembled in shared memory (32 bytes
+// each) and written out in one coalesced copy.
+constexpr int kSchedStageUnits = 2048;
 __host__ __device__ constexpr int sched_hist_ints(int cmax) { return (cmax + 1 + 3) & ~3; }
 // Forward kernel: warp 0 TMA, warp 1 issues S = Q K^T, warps 2-9 SiLU row
 // work (two per TMEM lane quarter, taking alternate key steps), warps 10-13
@@ -183,6 +186,7 @@ struct SchedArgs {
   int* ready;                // backward: B x H readiness counts, zeroed here, or null
   int ds_cap;                // backward: dS blocks the workspace holds
   int cache_seqs;            // 1: sequence records cached in shared memory
+  int stage_units;           // lists of at most this many units are staged in shared memory
   int key[kPlanKeyInts];     // plans: the sizes recorded in the header
 };
 
@@ -354,7 +358,7 @@ static_assert(FwdCfg<64>::SMEM <= 232448 && DqCfg<64>::SMEM <= 232448 &&
                   DkdvCfg<64>::SMEM <= 232448,
               "smem");
 
-__global__ void hstu_sched_kernel(SchedArgs a);
+__global__ void hstu_sched_kernel(const __grid_constant__ SchedArgs a);
 // Arbitrary mask: key hull of every 64-row query block (grid: blocks of 8
 // query blocks x sequences; one warp per query block).
 cudaError_t launch_func_ranges(const int32_t* cu_q, const int32_t* cu_k, int B, int max_qb,

@@ -69,16 +69,20 @@ __device__ __forceinline__ int func_live_tiles(const FuncMask& f, int q0, int b,
   return n;
 }
 
-// Cost of query tile t (lists A and F): its inner tiles of bn keys.
-__device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t, int bn) {
-  int first, n;
-  if (a.fm.func != nullptr) {  // arbitrary mask: the live tiles of the tile's key hull
+// Cost of query tile t (lists A and F): its inner tiles of 2^lbn keys (the
+// window's rule of query_tile_keys, with shifts for the divisions).
+__device__ __forceinline__ int cost_a(const SchedArgs& a, int4 sq, int b, int t, int lbn,
+                                      bool func) {
+  if (func) {  // arbitrary mask: the live tiles of the tile's key hull
+    const int bn = 1 << lbn;
     const int2 h = func_tile_keys(a.fm, sq.x, b, t, sq.y);
     if (h.x >= h.y) return 0;
     return func_live_tiles(a.fm, sq.x, b, t, sq.y, bn, h.x / bn, (h.y + bn - 1) / bn);
   }
-  query_tile_keys(t, sq.y, sq.w, a.win, bn, first, n);
-  return n;
+  const int r0 = kBM * t, r1 = imin(kBM * t + kBM, sq.y);
+  const int j0 = a.win.left < 0 ? 0 : imax(0, r0 - a.win.left);
+  const int j1 = a.win.right < 0 ? sq.w : imin(sq.w, r1 + a.win.right);
+  return (r1 > r0 && j1 > j0) ? ((j1 + (1 << lbn) - 1) >> lbn) - (j0 >> lbn) : 0;
 }
 
 // Arbitrary mask, list B, warp-wide: for key tile t = tb + lane (tb a
@@ -117,11 +121,13 @@ __device__ void func_key_tiles_warp(const SchedArgs& a, int4 sq, int b, int tb, 
   live = n;
 }
 
-// Cost of key tile s (list B; the arbitrary mask's walk is warp-wide).
-__device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int b, int s) {
-  int first, n;
-  key_tile_queries(s, sq.y, sq.w, a.win, a.bq_b, first, n);
-  return n;
+// Cost of key tile s (list B; the arbitrary mask's walk is warp-wide): its
+// query blocks of 2^lbq rows (key_tile_queries, with shifts).
+__device__ __forceinline__ int cost_b(const SchedArgs& a, int4 sq, int s, int lbq) {
+  const int c0 = kBM * s, c1 = imin(kBM * s + kBM, sq.w);
+  const int i0 = a.win.right < 0 ? 0 : imax(0, c0 - a.win.right);
+  const int i1 = a.win.left < 0 ? sq.y : imin(sq.y, c1 + a.win.left);
+  return (c1 > c0 && i1 > i0) ? ((i1 + (1 << lbq) - 1) >> lbq) - (i0 >> lbq) : 0;
 }
 
 // Block 0 builds list A, block 1 list B, block 2 (plans) list F.
@@ -163,15 +169,22 @@ __device__ int block_exclusive_scan(int v, int* total) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) {
-  extern __shared__ int hist[];  // cost buckets, then the cached sequence records
+// One list's passes (block 0: list A, 1: B, 2: F).  Every block barrier
+// comes before the first global store: a barrier behind outstanding global
+// stores measured about a microsecond each, so the header words, the
+// readiness counts, the staged list and the dS bases all leave at the end.
+__global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_constant__ SchedArgs a) {
+  extern __shared__ int hist[];  // cost buckets | cached sequence records | staged records
+  __shared__ int ds_all;         // list B, backward: the dS blocks of the whole batch
   const int list = blockIdx.x;
-  int4* seqs = reinterpret_cast<int4*>(hist + sched_hist_ints(list_cmax(a, list)));
-  const bool list_b = list == 1;
   const int cmax = list_cmax(a, list);
+  int4* seqs = reinterpret_cast<int4*>(hist + sched_hist_ints(cmax));
+  int4* stage = seqs + (a.cache_seqs ? a.B : 0);
+  const bool list_b = list == 1;
   const int cap = list == 0 ? a.cap_a : list == 1 ? a.cap_b : a.cap_f;
   int4* units = list == 0 ? a.units_a : list == 1 ? a.units_b : a.units_f;
   const int bn = list == 2 ? a.bn_f : a.bn_a;  // query-tile lists
+  const int lbn = __ffs(bn) - 1, lbq = __ffs(a.bq_b) - 1;  // tile sizes are powers of two
   const int units_slot = list == 0 ? kHdrUnitsA : list == 1 ? kHdrUnitsB : kHdrUnitsF;
   const int next_slot = list == 0 ? kHdrNextA : list == 1 ? kHdrNextB : kHdrNextF;
   const int overflow_slot = list == 0 ? kHdrOverflow : list == 1 ? kHdrOverflowB : kHdrOverflowF;
@@ -179,37 +192,14 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   const int nb = cmax + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
+  const bool func = a.fm.func != nullptr;
 
+  for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
   // Launched early behind the previous grid of the stream, which may still
-  // read this workspace: wait for it before writing anything.
+  // read this workspace or write cu_seqlens: wait for it first.
   grid_dependency_wait();
   // the attention grid queued behind this one may start its prologue now
   if (tid == 0) grid_launch_dependents();
-  if (list == 0 && tid == 0) {
-    a.header[kHdrStatus] = 0;
-    a.header[kHdrWhere] = 0;
-    a.header[kHdrDone] = 0;
-    if (gridDim.x == 1) {
-      a.header[kHdrOverflowB] = 0;
-      a.header[kHdrNextB] = 0;
-    }
-    if (gridDim.x < 3) {
-      a.header[kHdrOverflowF] = 0;
-      a.header[kHdrUnitsF] = 0;
-    }
-    for (int i = 0; i < kPlanKeyInts; ++i) a.header[kHdrKey + i] = a.key[i];
-  }
-  if (tid == 0) {
-    a.header[overflow_slot] = 0;
-    a.header[next_slot] = 0;
-  }
-  // backward: the readiness counts of the dK/dV -> dQ hand-over start at zero
-  if (list_b && a.ready != nullptr) {
-    for (int i = tid; i < a.B * a.H; i += blockDim.x) a.ready[i] = 0;
-    if (tid == 0) a.header[kHdrEpoch] = 0;
-  }
-
-  for (int i = tid; i < nb; i += blockDim.x) hist[i] = 0;
   // every pass reads the sequences: one coalesced read of cu_seqlens
   if (a.cache_seqs)
     for (int b = tid; b < a.B; b += blockDim.x) seqs[b] = seq_global(a, b);
@@ -218,11 +208,11 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   __syncthreads();
 
   // pass 1: histogram of costs; a warp per sequence, a lane per tile
-  const bool func_b = list_b && a.fm.func != nullptr;  // the warp-wide list-B walk
+  const bool func_b = list_b && func;  // the warp-wide list-B walk
   for (int b = warp; b < a.B; b += nwarps) {
     const int4 sq = seq(b);
     const int Lq = sq.y, Lk = sq.w;
-    const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
+    const int nt = list_b ? (Lk + kBM - 1) / kBM : (Lq + kBM - 1) / kBM;
     for (int tb = 0; tb < nt; tb += 32) {
       const int t = tb + lane;
       int cost = 0;
@@ -230,7 +220,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
         int2 r;
         func_key_tiles_warp(a, sq, b, tb, nt, r, cost);
       } else if (t < nt) {
-        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
+        cost = list_b ? cost_b(a, sq, t, lbq) : cost_a(a, sq, b, t, lbn, func);
       }
       if (t < nt) atomicAdd(&hist[min(cost, cmax)], per_tile);
     }
@@ -254,12 +244,33 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
   __syncwarp();  // reconverge before the aligned CTA barrier
   __syncthreads();
 
-  // pass 3: emit complete unit records at their bucket cursors
+  // pass 3 (backward, list-B block): first dS block of each sequence, a scan
+  // over the sequences (written out at the end)
+  const bool ds_pass = list_b && a.ds_base != nullptr;
+  const int per = (a.B + blockDim.x - 1) / blockDim.x;
+  const int s0 = min(a.B, tid * per), s1 = min(a.B, s0 + per);
+  auto blocks = [&](int b) {
+    const int4 sq = seq(b);
+    return a.H * ds_blocks_head(sq.y, sq.w, a.win);
+  };
+  int ds_run = 0;
+  if (ds_pass) {  // block-uniform: every thread takes the scan's barriers
+    int sum = 0;
+    for (int b = s0; b < s1; ++b) sum += blocks(b);
+    int all;
+    ds_run = block_exclusive_scan(sum, &all);
+    if (tid == 0) ds_all = all;
+  }
+
+  // pass 4: complete unit records at their bucket cursors; into shared
+  // memory when the whole list fits there (one coalesced copy follows),
+  // else straight to global memory
+  const bool staged = total <= a.stage_units;
   int overflow = 0;
   for (int b = warp; b < a.B; b += nwarps) {
     const int4 sq = seq(b);
     const int q0 = sq.x, Lq = sq.y, k0 = sq.z, Lk = sq.w;
-    const int nt = list_b ? ceil_div(Lk, kBM) : ceil_div(Lq, kBM);
+    const int nt = list_b ? (Lk + kBM - 1) / kBM : (Lq + kBM - 1) / kBM;
     for (int tb = 0; tb < nt; tb += 32) {
       const int t = tb + lane;
       int cost = 0;
@@ -268,45 +279,60 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(SchedArgs a) 
         func_key_tiles_warp(a, sq, b, tb, nt, r, cost);
         if (t < nt) a.fm.kt_range[kt_slot(k0, b, t)] = r;
       } else if (t < nt) {
-        cost = list_b ? cost_b(a, sq, b, t) : cost_a(a, sq, b, t, bn);
+        cost = list_b ? cost_b(a, sq, t, lbq) : cost_a(a, sq, b, t, lbn, func);
       }
       if (t >= nt) continue;
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
+      int4* dst = staged ? stage : units;
       for (int e = 0; e < per_tile; ++e) {
         if (pos + e < cap) {
-          units[2 * (pos + e)] = make_int4(b, t, e, cost);
-          units[2 * (pos + e) + 1] = make_int4(q0, Lq, k0, Lk);
+          dst[2 * (pos + e)] = make_int4(b, t, e, cost);
+          dst[2 * (pos + e) + 1] = make_int4(q0, Lq, k0, Lk);
         } else {
           overflow = 1;
         }
       }
     }
   }
-  if (overflow) atomicExch(a.header + overflow_slot, 1);
-  if (tid == 0) a.header[units_slot] = min(total, cap);
+  __syncwarp();  // reconverge before the aligned CTA barrier
+  const bool dropped = __syncthreads_or(overflow) != 0;  // units beyond the list's capacity
+  if (staged)
+    for (int i = tid; i < 2 * min(total, cap); i += blockDim.x) units[i] = stage[i];
 
-  // pass 4 (backward, list-B block): first dS block of each sequence
-  if (list_b && a.ds_base != nullptr) {
-    auto blocks = [&](int b) {
-      const int4 sq = seq(b);
-      return a.H * ds_blocks_head(sq.y, sq.w, a.win);
-    };
-    const int per = (a.B + blockDim.x - 1) / blockDim.x;
-    const int s0 = min(a.B, tid * per), s1 = min(a.B, s0 + per);
-    int sum = 0;
-    for (int b = s0; b < s1; ++b) sum += blocks(b);
-    int all;
-    int run = block_exclusive_scan(sum, &all);
+  // the global words, after the last barrier
+  if (ds_pass) {
     for (int b = s0; b < s1; ++b) {
-      a.ds_base[b] = run;
-      run += blocks(b);
+      a.ds_base[b] = ds_run;
+      ds_run += blocks(b);
     }
-    if (tid == 0) {
-      a.ds_base[a.B] = all;
-      // sequences longer than the caller's max_seqlen_q: the blocks would not
-      // fit; the dK/dV units then skip the stores past the end
-      if (all > a.ds_cap || all < 0) atomicExch(a.header + kHdrOverflowB, 1);
+  }
+  if (list_b && a.ready != nullptr) {  // the dK/dV -> dQ readiness counts start at zero
+    for (int i = tid; i < a.B * a.H; i += blockDim.x) a.ready[i] = 0;
+  }
+  if (tid == 0) {
+    if (list == 0) {
+      a.header[kHdrStatus] = 0;
+      a.header[kHdrWhere] = 0;
+      a.header[kHdrDone] = 0;
+      if (gridDim.x == 1) {
+        a.header[kHdrOverflowB] = 0;
+        a.header[kHdrNextB] = 0;
+      }
+      if (gridDim.x < 3) {
+        a.header[kHdrOverflowF] = 0;
+        a.header[kHdrUnitsF] = 0;
+      }
+      for (int i = 0; i < kPlanKeyInts; ++i) a.header[kHdrKey + i] = a.key[i];
     }
+    a.header[next_slot] = 0;
+    a.header[units_slot] = min(total, cap);
+    if (list_b && a.ready != nullptr) a.header[kHdrEpoch] = 0;
+    // sequences longer than the caller's max_seqlen_q: the dS blocks would
+    // not fit; the dK/dV units then skip the stores past the end (list B's
+    // overflow word reports it)
+    const bool ds_over = ds_pass && (ds_all > a.ds_cap || ds_all < 0);
+    if (ds_pass) a.ds_base[a.B] = ds_all;
+    a.header[overflow_slot] = dropped || ds_over ? 1 : 0;
   }
 }
 
