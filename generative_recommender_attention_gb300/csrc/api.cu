@@ -208,7 +208,8 @@ void plan_key(int32_t batch, int64_t total_q, int64_t total_k, int32_t H, int32_
 
 // Arbitrary mask: the key hull of every query-block slot, and (backward)
 // the query-block hull of every key-tile slot, appended to the workspace.
-// Layout: qb_range | kt_range (backward) | qb_bits, each 256-byte aligned.
+// Layout: qb_range | kt_range (backward) | qb_bits | qb_full, each 256-byte
+// aligned (qb_bits and qb_full have the same size).
 int func_kt_words(int32_t max_k) {
   return static_cast<int>(std::max<int64_t>(1, cdiv(cdiv(std::max<int32_t>(max_k, 1), kBM), 32)));
 }
@@ -217,10 +218,13 @@ size_t func_bits_off(int32_t batch, int64_t total_q, int64_t total_k, bool bwd) 
   const size_t kt = bwd ? 8 * static_cast<size_t>(total_k / kBM + batch + 1) : 0;
   return ((qb + 255) & ~size_t(255)) + ((kt + 255) & ~size_t(255));
 }
+size_t func_bits_bytes(int32_t batch, int64_t total_q, int32_t max_k) {
+  const size_t n = 4 * static_cast<size_t>(func_kt_words(max_k)) *
+                   static_cast<size_t>(total_q / 64 + batch + 1);
+  return (n + 255) & ~size_t(255);
+}
 size_t func_extra(int32_t batch, int64_t total_q, int64_t total_k, int32_t max_k, bool bwd) {
-  return func_bits_off(batch, total_q, total_k, bwd) +
-         4 * static_cast<size_t>(func_kt_words(max_k)) *
-             static_cast<size_t>(total_q / 64 + batch + 1);
+  return func_bits_off(batch, total_q, total_k, bwd) + 2 * func_bits_bytes(batch, total_q, max_k);
 }
 
 // Arbitrary-mask arguments of a call (func null: none).
@@ -344,6 +348,8 @@ hstu_status_t func_setup(const FuncArgs* fn, int32_t batch, int64_t total_q, int
     fm->kt_range = reinterpret_cast<int2*>(
         ws + tail + ((8 * static_cast<size_t>(total_q / 64 + batch + 1) + 255) & ~size_t(255)));
   fm->qb_bits = reinterpret_cast<uint32_t*>(ws + tail + func_bits_off(batch, total_q, total_k, bwd));
+  fm->qb_full = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(fm->qb_bits) +
+                                            func_bits_bytes(batch, total_q, max_k));
   fm->kt_words = func_kt_words(max_k);
   return HSTU_OK;
 }

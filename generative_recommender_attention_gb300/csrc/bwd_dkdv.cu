@@ -254,6 +254,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int m0 = unit_first_qblock(a, U, BQ);  // query tiles m0 .. m0 + U.n - 1
         const int m_end = FUNC ? unit_qblock_end(a, U) : 0;
         int m_next = m0;  // live-block cursor (arbitrary mask)
+        BlockWalk bw;  // the live blocks, 32 at a time
+        bw.init();
         const int kb = kvi % NKV;
         if constexpr (STAGE) {
           // buffer kb last held the unit before the previous one
@@ -278,26 +280,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (prev_n < kPrefetchQ)
           for (int m = 0; m < min(U.n, kPrefetchQ - prev_n); ++m) prefetch_qdo(h, q_seq0 + BQ * (m0 + m));
         prev_n = U.n;
+        int nx_m0 = -1;  // the next unit's first query block, read when first needed
         for (int m = 0; m < U.n; ++m) {
-          const int t = m + kPrefetchQ;
-          if (t < U.n) {
-            prefetch_qdo(h, q_seq0 + BQ * (m0 + t));
-          } else if (t - U.n < nx.n) {
-            const int nh = nx.hz / SPLIT;
-            if (t == U.n) {
-#pragma unroll
-              for (int c = 0; c < KCH; ++c) {
-                tma_prefetch_3d(&tm_k, 64 * c, nh, nx.k0 + kBM * nx.tile);
-                tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
-              }
-            }
-            const int nm0 = unit_first_qblock(a, nx, BQ);
-            prefetch_qdo(nh, nx.q0 + BQ * (nm0 + t - U.n));
-          }
           const int s = qi % NS;
           int qm = m0 + m;
           if constexpr (FUNC) {
-            qm = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+            qm = bw.next<false>(a.fm, U.q0, U.b, U.tile, m_next, m_end);
             m_next = qm + 1;
           }
           const int row = q_seq0 + BQ * qm;
@@ -312,6 +300,23 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           for (int c = 0; c < KCH; ++c)
             tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(DOFULL + s), 64 * c, h, row);
           ++qi;
+          // the L2 warm-up of step m + kPrefetchQ, after this step's loads (under an
+          // arbitrary mask the next unit's first block is a global read)
+          const int t = m + kPrefetchQ;
+          if (t < U.n) {
+            prefetch_qdo(h, q_seq0 + BQ * (m0 + t));
+          } else if (t - U.n < nx.n) {
+            const int nh = nx.hz / SPLIT;
+            if (t == U.n) {
+#pragma unroll
+              for (int c = 0; c < KCH; ++c) {
+                tma_prefetch_3d(&tm_k, 64 * c, nh, nx.k0 + kBM * nx.tile);
+                tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
+              }
+            }
+            if (nx_m0 < 0) nx_m0 = unit_first_qblock(a, nx, BQ);
+            prefetch_qdo(nh, nx.q0 + BQ * (nx_m0 + t - U.n));
+          }
         }
       }
       if constexpr (STAGE) {
@@ -494,9 +499,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       constexpr bool func = FUNC;  // arbitrary mask: a separate instantiation
       const int m_end = func ? unit_qblock_end(a, U) : 0;
       int m_next = m0;  // live-block cursor (arbitrary mask)
+      BlockWalk bw;  // the live blocks and their full class, 32 at a time
+      bw.init();
       // arbitrary mask: the first three endpoints of this lane's query row,
       // loaded one step ahead so their latency hides behind a half-step
       int qm_ahead = 0, e0 = 0, e1 = 0, e2 = 0;
+      bool full_ahead = false;  // its block sees every key of the tile (no per-element mask)
       auto ends = [&](int qm, int& f0, int& f1, int& f2) {
         const int iq = BQ * qm + q_first + lane;
         const int64_t t = static_cast<int64_t>(U.q0) + (iq < Lq ? iq : 0);
@@ -508,8 +516,9 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
       };
       if constexpr (func) {
-        qm_ahead = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+        qm_ahead = bw.next<true>(a.fm, U.q0, U.b, U.tile, m_next, m_end);
         m_next = qm_ahead + 1;
+        full_ahead = bw.is_full(qm_ahead);
         ends(qm_ahead, e0, e1, e2);
       }
       // valid queries of this key row: lo <= i < hi; every key row of the
@@ -530,12 +539,15 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const int b = h & 1;
         int qm = m0 + m;  // this step's query block
         int f0 = 0, f1 = 0, f2 = 0;
+        bool full = false;
         if constexpr (func) {
           qm = qm_ahead;
+          full = full_ahead;
           f0 = e0; f1 = e1; f2 = e2;
-          if (m + 1 < U.n) {  // the next step's block and endpoints
-            qm_ahead = func_next_qblock(a.fm, U.q0, U.b, U.tile, m_next, m_end);
+          if (m + 1 < U.n) {  // the next step's block, class and endpoints
+            qm_ahead = bw.next<true>(a.fm, U.q0, U.b, U.tile, m_next, m_end);
             m_next = qm_ahead + 1;
+            full_ahead = bw.is_full(qm_ahead);
             ends(qm_ahead, e0, e1, e2);
           }
         }
@@ -544,7 +556,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         // valid queries of this warp's columns (bit e: query ic + e), the run
         // of bits [lo - ic, hi - ic) clamped to [0, CW)
         uint32_t valid = CW == 32 ? 0xffffffffu : (1u << CW) - 1u;
-        if constexpr (func) {
+        if (func && full) {
+          // arbitrary mask, a full block: every query of it sees every key
+          // row of the tile (keys past Lk are never stored); only the
+          // sequence end cuts the columns
+          const int nq = Lq - ic;
+          valid = nq >= CW ? valid : nq <= 0 ? 0u : (1u << nq) - 1u;
+        } else if constexpr (func) {
           // arbitrary mask: lane l forms query ic + l's valid keys among the
           // warp's 32 key rows from its endpoints; 32 ballots transpose them
           // into each key row's valid queries

@@ -133,11 +133,13 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_ds, const CUtensorMap*
           }
         }
         int kt_next = kt0;  // live-tile cursor (arbitrary mask)
+        TileWalk tw;  // the unit's live tiles, 32 per bit word
+        if (func) tw.init(a.fm, U.q0, U.b, i, U.Lq);
         for (int jj = 0; jj < U.n; ++jj, ++g) {
           const int s = g % NS;
           int j = kt0 + jj;
           if (func) {
-            j = func_next_tile(a.fm, U.q0, U.b, i, U.Lq, kDsKeys, kt_next, kt_end);
+            j = tw.next(kt_next, kt_end, 7);
             kt_next = j + 1;
             off = j * n_qb;  // the full mask's layout
           }
@@ -151,8 +153,8 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_ds, const CUtensorMap*
             const int2 r = a.fm.kt_range[kt_slot(U.k0, U.b, j)];
             m0 = r.x;
             cnt = r.y;
-            live0 = func_live(a.fm, U.q0, U.b, 2 * i, j);
-            live1 = second && func_live(a.fm, U.q0, U.b, 2 * i + 1, j);
+            live0 = tw.live(j, false);
+            live1 = second && tw.live(j, true);
           } else {
             ds_blocks_of(j, U.Lq, U.Lk, a.win, m0, cnt);
           }

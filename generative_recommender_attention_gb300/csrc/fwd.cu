@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using C = FwdCfg<D>;
   constexpr int BN = C::BN, NQ = C::NQ, NK = C::NK, NV = C::NV, KCH = D / 64;
+  constexpr int LBN = BN == 64 ? 6 : 7;  // log2 BN
   constexpr int NSB = 3;        // S buffers in TMEM
   constexpr int NCH = BN / 64;  // 64-column chunks of one S tile
   // 128-key steps: the two SiLU warps of a lane quarter split every step's
@@ -169,6 +170,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         const int kv_row0 = U.k0 + BN * kt0;
         int kt_next = kt0;  // live-tile cursor
+        TileWalk tw;  // arbitrary mask: the unit's live tiles, 32 per bit word
+        if constexpr (FUNC) tw.init(a.fm, U.q0, U.b, U.tile, U.Lq);
         // Paged K/V: key tile kt lives in page page_ids[page_indptrs[b] +
         // kt BN / 128], whose K rows start at row 256 p and V rows at
         // 256 p + 128 of the cache's map.  The next tile's page is looked up
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int n = 0; n < U.n; ++n) {
           int row = kv_row0 + BN * n, vrow = row;
           if constexpr (FUNC) {
-            const int kt = func_next_tile(a.fm, U.q0, U.b, U.tile, U.Lq, BN, kt_next, kt_end);
+            const int kt = tw.next(kt_next, kt_end, LBN);
             kt_next = kt + 1;
             row = vrow = U.k0 + BN * kt;
           }
@@ -322,6 +325,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         query_tile_keys(U.tile, U.Lq, Lk, a.win, BN, kt0, nkt);
       }
       int kt_next = kt0;  // live-tile cursor (arbitrary mask)
+      TileWalk tw;
+      if constexpr (func) tw.init(a.fm, U.q0, U.b, U.tile, U.Lq);
       // arbitrary mask: this row's first endpoints, read once per unit
       int fe0 = 0, fe1 = 0, fe2 = 0;
       if constexpr (func) {
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int n = 0; n < U.n; ++n, ++g) {
         int kt = kt0 + n;
         if constexpr (func) {  // every warp walks every step to keep the cursor
-          kt = func_next_tile(a.fm, U.q0, U.b, U.tile, U.Lq, BN, kt_next, kt_end);
+          kt = tw.next(kt_next, kt_end, LBN);
           kt_next = kt + 1;
         }
         if (!SPLIT && static_cast<int>(g & 1) != par) continue;

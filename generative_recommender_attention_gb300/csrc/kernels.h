@@ -106,6 +106,7 @@ struct FuncMask {
   int2* qb_range;
   int2* kt_range;
   uint32_t* qb_bits;
+  uint32_t* qb_full;    // same layout: every row of the block sees every key (< Lk) of the tile
   int kt_words;         // ceil(ceil(max_seqlen_k / 128) / 32)
 };
 __host__ __device__ inline int qb_slot(int q0, int b, int m) { return q0 / 64 + b + m; }
@@ -128,25 +129,120 @@ __device__ __forceinline__ bool func_live(const FuncMask& f, int q0, int b, int 
   return (w >> (s & 31)) & 1u;
 }
 
-// First tile t' >= t (tiles of bn = 64 or 128 keys) that is live for 128-row
-// query tile tq, i.e. for its block 2 tq or, inside the sequence, 2 tq + 1;
-// t_end if none before it.
-__device__ __forceinline__ int func_next_tile(const FuncMask& f, int q0, int b, int tq, int Lq,
-                                              int bn, int t, int t_end) {
-  const bool two = kBM * tq + 64 < Lq;
-  for (; t < t_end; ++t) {
-    const int s = t * bn / kBM;
-    if (func_live(f, q0, b, 2 * tq, s) || (two && func_live(f, q0, b, 2 * tq + 1, s))) break;
-  }
-  return t;
+// Every row of 64-row query block m sees every key of 128-key tile s (the
+// keys below Lk): the pair needs no per-element mask and no endpoints.
+__device__ __forceinline__ bool func_full(const FuncMask& f, int q0, int b, int m, int s) {
+  const uint32_t w =
+      __ldg(f.qb_full + static_cast<int64_t>(qb_slot(q0, b, m)) * f.kt_words + (s >> 5));
+  return (w >> (s & 31)) & 1u;
 }
 
-// First query block m' >= m for which 128-key tile s is live; m_end if none.
-__device__ __forceinline__ int func_next_qblock(const FuncMask& f, int q0, int b, int s, int m,
-                                                int m_end) {
-  while (m < m_end && !func_live(f, q0, b, m, s)) ++m;
-  return m;
-}
+// Walks, in order, the live tiles (bn = 64 or 128 keys) of 128-row query
+// tile tq: those whose 128-key tile is live for block 2 tq or, inside the
+// sequence, 2 tq + 1.  It keeps the two blocks' bit words of 32 tiles of 128
+// keys and loads the next pair only when the walk leaves them, so a step
+// costs no dependent load (one per 32 tiles of 128 keys).
+struct TileWalk {
+  const uint32_t* row0;  // qb_bits row of block 2 tq
+  const uint32_t* row1;  // of block 2 tq + 1 (null: past the sequence end)
+  int w;                 // index of the words held (-1: none)
+  uint32_t bits0, bits1;
+  __device__ __forceinline__ void init(const FuncMask& f, int q0, int b, int tq, int Lq) {
+    row0 = f.qb_bits + static_cast<int64_t>(qb_slot(q0, b, 2 * tq)) * f.kt_words;
+    row1 = kBM * tq + 64 < Lq ? row0 + f.kt_words : nullptr;  // slots are consecutive
+    w = -1;
+    bits0 = bits1 = 0u;
+  }
+  __device__ __forceinline__ void hold(int wi) {
+    if (wi == w) return;
+    w = wi;
+    bits0 = __ldg(row0 + wi);
+    bits1 = row1 != nullptr ? __ldg(row1 + wi) : 0u;
+  }
+  // First live tile t' >= t (in tiles of 2^lbn keys, lbn = 6 or 7); t_end if none.
+  __device__ __forceinline__ int next(int t, int t_end, int lbn) {
+    while (t < t_end) {
+      const int s = t >> (7 - lbn);  // its 128-key tile
+      hold(s >> 5);
+      const uint32_t rest = (bits0 | bits1) >> (s & 31);
+      if (rest == 0u) {  // none left in this word
+        t = (32 * (w + 1)) << (7 - lbn);
+        continue;
+      }
+      const int s2 = s + __ffs(rest) - 1;
+      return imax(t, s2 << (7 - lbn));
+    }
+    return t_end;
+  }
+  // Whether 128-key tile s (in the words held, after next) is live for block
+  // 2 tq (second = false) or 2 tq + 1.
+  __device__ __forceinline__ bool live(int s, bool second) const {
+    return (((second ? bits1 : bits0) >> (s & 31)) & 1u) != 0u;
+  }
+};
+
+// Walks, in order, the 64-row query blocks for which 128-key tile s is live
+// (and tells which of them see the whole tile).  The bits of 32 blocks sit in
+// 32 different rows; they are gathered 32 at a time: by the whole warp, one
+// load per lane, or by one thread, 32 independent loads.
+struct BlockWalk {
+  int base;            // first block of the masks held (-1: none)
+  uint32_t live, full;  // bit i: block base + i
+  __device__ __forceinline__ void init() { base = -1; live = full = 0u; }
+  template <bool WARP>
+  __device__ __forceinline__ void gather(const FuncMask& f, int q0, int b, int s, int m0, int m_end) {
+    base = m0;
+    const int64_t col = s >> 5;
+    const int sh = s & 31;
+    if constexpr (WARP) {
+      const int m = m0 + static_cast<int>(threadIdx.x & 31);
+      uint32_t lw = 0u, fw = 0u;
+      if (m < m_end) {
+        const int64_t r = static_cast<int64_t>(qb_slot(q0, b, m0)) * f.kt_words + col +
+                          static_cast<int64_t>(m - m0) * f.kt_words;
+        lw = __ldg(f.qb_bits + r);
+        fw = __ldg(f.qb_full + r);
+      }
+      live = __ballot_sync(0xffffffffu, (lw >> sh) & 1u);
+      full = __ballot_sync(0xffffffffu, (fw >> sh) & 1u);
+    } else {
+      // predicated, independent loads: one round trip for all 32
+      uint32_t lv = 0u, fl = 0u;
+      const int64_t r0 = static_cast<int64_t>(qb_slot(q0, b, m0)) * f.kt_words + col;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const bool in = m0 + i < m_end;
+        const int64_t r = r0 + static_cast<int64_t>(i) * f.kt_words;  // slots are consecutive
+        const uint32_t lw = in ? __ldg(f.qb_bits + r) : 0u;
+        const uint32_t fw = in ? __ldg(f.qb_full + r) : 0u;
+        lv |= ((lw >> sh) & 1u) << i;
+        fl |= ((fw >> sh) & 1u) << i;
+      }
+      live = lv;
+      full = fl;
+    }
+  }
+  // First block m' >= m live for tile s; m_end if none.  WARP: every lane
+  // of the warp calls it with the same arguments.
+  template <bool WARP>
+  __device__ __forceinline__ int next(const FuncMask& f, int q0, int b, int s, int m, int m_end) {
+    while (m < m_end) {
+      if (base < 0 || m < base || m >= base + 32) gather<WARP>(f, q0, b, s, m, m_end);
+      const uint32_t rest = live >> (m - base);
+      if (rest == 0u) {
+        m = base + 32;
+        continue;
+      }
+      return m + __ffs(rest) - 1;
+    }
+    return m_end;
+  }
+  // Block m (returned by next) sees every key of the tile.
+  __device__ __forceinline__ bool is_full(int m) const {
+    const int d = m - base;
+    return d >= 0 && d < 32 && ((full >> d) & 1u) != 0u;
+  }
+};
 
 // Bits [lo - base, hi - base) of an n-bit word (n = 32 or 64), clamped.
 __device__ __forceinline__ uint64_t bit_range64(int lo, int hi, int base) {

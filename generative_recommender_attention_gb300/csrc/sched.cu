@@ -336,6 +336,19 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
   }
 }
 
+// Bits of the 128-key tiles 32 w .. 32 w + 31 whose keys below Lk all lie in
+// [a, c) (c <= Lk): tiles from ceil(a / 128), up to the last one that ends
+// by c, or the sequence's last tile when c reaches Lk.
+__device__ __forceinline__ uint32_t full_tile_bits(int a, int c, int Lk, int w) {
+  if (a >= c) return 0u;
+  const int t0 = (a + kBM - 1) / kBM;
+  const int t1 = (c >= Lk ? (Lk + kBM - 1) / kBM : c / kBM) - 1;  // last tile, inclusive
+  const int u0 = max(t0 - 32 * w, 0), u1 = min(t1 - 32 * w, 31);
+  if (u0 > u1) return 0u;
+  const uint32_t upto = u1 == 31 ? 0xffffffffu : (2u << u1) - 1u;
+  return upto & ~((1u << u0) - 1u);
+}
+
 // Bits of the 128-key tiles 32 w .. 32 w + 31 that keys [a, c) touch.
 __device__ __forceinline__ uint32_t tile_bits(int a, int c, int w) {
   if (a >= c) return 0u;
@@ -375,21 +388,32 @@ __global__ void __launch_bounds__(256) hstu_func_ranges_kernel(const int32_t* cu
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
   if (lane == 0) fm.qb_range[qb_slot(q0, b, m)] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
-  // the block's live 128-key tiles, 32 per word: the tiles each interval touches
-  uint32_t* bits = fm.qb_bits + static_cast<int64_t>(qb_slot(q0, b, m)) * fm.kt_words;
+  // the block's live 128-key tiles, 32 per word: the tiles each interval
+  // touches; and its full tiles: those inside one interval of every row
+  const int64_t slot = static_cast<int64_t>(qb_slot(q0, b, m)) * fm.kt_words;
   for (int w = 0; w < fm.kt_words; ++w) {
-    uint32_t word = 0;
+    uint32_t word = 0, full = 0xffffffffu;
     for (int rr = 0; rr < 2; ++rr) {
       const int i = 64 * m + 32 * rr + lane;
       if (i >= Lq) continue;
       const int64_t t = static_cast<int64_t>(q0) + i;
-      word |= tile_bits(0, min(__ldg(fm.func + t), Lk), w);
-      for (int n = 1; n + 1 < fm.n; n += 2)
-        word |= tile_bits(max(__ldg(fm.func + n * fm.len + t), 0),
-                          min(__ldg(fm.func + (n + 1) * fm.len + t), Lk), w);
+      const int f0 = min(__ldg(fm.func + t), Lk);
+      word |= tile_bits(0, f0, w);
+      uint32_t row_full = full_tile_bits(0, f0, Lk, w);
+      for (int n = 1; n + 1 < fm.n; n += 2) {
+        const int a = max(__ldg(fm.func + n * fm.len + t), 0);
+        const int c = min(__ldg(fm.func + (n + 1) * fm.len + t), Lk);
+        word |= tile_bits(a, c, w);
+        row_full |= full_tile_bits(a, c, Lk, w);
+      }
+      full &= row_full;
     }
     word = __reduce_or_sync(0xffffffffu, word);
-    if (lane == 0) bits[w] = word;
+    full = __reduce_and_sync(0xffffffffu, full);
+    if (lane == 0) {
+      fm.qb_bits[slot + w] = word;
+      fm.qb_full[slot + w] = full & word;
+    }
   }
 }
 

@@ -97,3 +97,34 @@ def test_lmsd_backward_deterministic_and_dweight_optional():
     torch.cuda.synchronize()
     assert torch.equal(o2["mask_tensor"], out["mask_tensor"])
     assert not torch.equal(o3["mask_tensor"], out["mask_tensor"])
+
+
+@pytest.mark.parametrize("n,d,pad", [(257, 128, 8), (100, 1016, 16), (64, 256, 24)])
+def test_lmsd_backward_padded_dy_and_outputs(n, d, pad):
+    # dy may have a row stride larger than S * D, and dx / du row strides
+    # larger than D ("Tensor shapes and layouts"): the gradients are the same
+    # bit for bit as with contiguous tensors, and match the oracle.
+    p = 0.1
+    x, u, w, b = _inputs(n, d, seed=2 * n + d)
+    xd, ud, wd, bd = (t.cuda() for t in (x, u, w, b))
+    out = lmsd.hstu_lmsd_forward(xd, ud, wd, bd, eps=1e-5, dropout_ratio=p, seed=3 + n)
+    y = out["y_tensor"]
+    dy = torch.randn(y.shape, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16)
+    dy_pad = torch.empty(y.shape[0], y.shape[1] + pad, dtype=torch.bfloat16,
+                         device="cuda")[:, :y.shape[1]]
+    dy_pad.copy_(dy)
+    assert dy_pad.stride(0) == y.shape[1] + pad
+    dx_pad = torch.empty(n, d + pad, dtype=torch.bfloat16, device="cuda")[:, :d]
+    du_pad = torch.empty(n, d + 2 * pad, dtype=torch.bfloat16, device="cuda")[:, :d]
+    rest = (xd, ud, wd, bd, out["mean_tensor"], out["rstd_tensor"], out["mask_tensor"])
+    g0 = lmsd.hstu_lmsd_backward(dy.cuda(), *rest, dropout_ratio=p)
+    g1 = lmsd.hstu_lmsd_backward(dy_pad, *rest, dropout_ratio=p, dx=dx_pad, du=du_pad)
+    torch.cuda.synchronize()
+    for k in ("dx_tensor", "du_tensor", "dweight_tensor", "dbias_tensor"):
+        assert torch.equal(g0[k], g1[k]), k
+    _, mean, rstd, mask = ref.forward(x, u, w, b, 1e-5, p, 3 + n, True, True, True)
+    dx, du, dw, db = ref.backward(dy.double(), x, u, w, b, mean, rstd, mask, p, True, True, True)
+    _close("dx", g1["dx_tensor"], dx, 2e-2)
+    _close("du", g1["du_tensor"], du, 2e-2)
+    _close("dweight", g1["dweight_tensor"], dw, 2e-2)
+    _close("dbias", g1["dbias_tensor"], db, 2e-2)
