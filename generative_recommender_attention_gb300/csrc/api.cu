@@ -520,7 +520,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
   const int BN = kDsKeys;                                         // dQ unit key tile
-  const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;  // dK/dV query tile
+  const int BQ = DkdvCfg<128, kPassBoth>::BQ;  // dK/dV query tile (every D)
   const int split = D == 256 ? 2 : 1;
   const int64_t capA = cap_a(batch, total_q, H);
   const int64_t capB = cap_b(batch, total_k, H, D);
@@ -583,6 +583,13 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
   ak.units = unitsB; ak.units_slot = kHdrUnitsB; ak.next_slot = kHdrNextB;
   ak.o0 = dv.ptr; ak.o0_st = dv.stride_t; ak.o0_sh = dv.stride_h;
   ak.o1 = dk.ptr; ak.o1_st = dk.stride_t; ak.o1_sh = dk.stride_h;
+  // D = 256: list B's first half is the dV pass, its second half the dK pass
+  AttnArgs ak2 = ak;
+  if (D == 256) {
+    ak.part = 1;
+    ak2.part = 2;
+    ak2.next_slot = kHdrNextB2;
+  }
   AttnArgs aq = a;
   aq.units = unitsA; aq.units_slot = kHdrUnitsA; aq.next_slot = kHdrNextA;
   aq.o0 = dq.ptr; aq.o0_st = dq.stride_t; aq.o0_sh = dq.stride_h;
@@ -596,7 +603,7 @@ hstu_status_t bwd_impl(hstu_cten_t dout, hstu_cten_t q, hstu_cten_t k, hstu_cten
       !encode_thd(&m.dv, dvx.ptr, hk ? total_k : total_q, H, D, dvx.stride_t, dvx.stride_h, kBM,
                   c.bf16))
     return HSTU_ERR_CUDA;
-  if (launch_bwd(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m, ak, aq) != cudaSuccess)
+  if (launch_bwd(kernel_dim(D), c.bf16, grid, stream, em.pdl(), m, ak, ak2, aq) != cudaSuccess)
     return HSTU_ERR_CUDA;
   if (!em.mark(2, stream) || !em.mark(3, stream)) return HSTU_ERR_CUDA;
   return HSTU_OK;
@@ -694,7 +701,7 @@ hstu_status_t hstu_attn_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seql
   if (c.dev.major != 10 || c.dev.minor != 3) return HSTU_ERR_UNSUPPORTED;
 
   const int BN = kDsKeys, BNF = bn_for(D);
-  const int BQ = D == 256 ? DkdvCfg<256>::BQ : DkdvCfg<128>::BQ;
+  const int BQ = DkdvCfg<128, kPassBoth>::BQ;
   const int64_t capA = cap_a(batch, total_q, H), capB = cap_b(batch, total_k, H, D);
   const int cmaxA = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_k, BN)));
   const int cmaxB = static_cast<int>(std::max<int64_t>(1, cdiv(max_seqlen_q, BQ)));

@@ -3,9 +3,8 @@
 //   dV_j = (1/L_scale)     sum_i M_ij SiLU(alpha q_i.k_j) dO_i
 //   dK_j = (alpha/L_scale) sum_i M_ij <dO_i, v_j> SiLU'(alpha q_i.k_j) q_i
 //
-// Key-stationary: each CTA owns a 128-row key tile (and, for D = 256, one
-// 128-column half of dK/dV, so the accumulators fit in TMEM) and walks the
-// 64-row query tiles that can see it.  Per half-step h it recomputes
+// Key-stationary: each CTA owns a 128-row key tile and walks the 64-row
+// query tiles that can see it.  Per half-step h it recomputes
 // S^T = K Q^T and dP^T = V dO^T into TMEM, forms A^T = M (.) SiLU(alpha S^T)
 // and dS^T = M (.) dP^T (.) SiLU'(alpha S^T) in registers (one tanh per
 // element), writes both back in place as 16-bit, and accumulates
@@ -37,6 +36,15 @@
 // 64-byte pieces (one cache line per lane) kept the row warps from the next
 // unit for several thousand cycles.  Ragged last tiles and D = 256 (one
 // K/V buffer) keep the per-row stores.
+// D = 256: the dV and dK accumulators (256 fp32 columns each) do not fit in
+// TMEM together, so the key tiles are walked twice, in two phases of the
+// launch: a dV pass (S^T, A^T, dV += A^T dO: no V tile and no dP^T, so its
+// shared memory holds three Q and two dO stages) and a dK pass (S^T, dP^T,
+// dS^T, dK += dS^T Q, with dO released right after dP^T, so one dO stage
+// overlaps the next load).  The passes are list B's two halves; together
+// they do five of the six products that splitting the head into two
+// 128-column halves (each recomputing S^T and dP^T) took, and neither
+// waits for a Q / dO load with a single stage of both.
 // After its last dK/dV unit the CTA drains, re-initialises its barriers and
 // runs dQ units (bwd_dq.cuh) in the same shared memory and TMEM; each waits
 // for the readiness count of its sequence and head (ready_target), which
@@ -78,21 +86,24 @@ __device__ __forceinline__ bool tile_full(const UnitInfo& U, int64_t total_k) {
   return end <= U.Lk && static_cast<int64_t>(U.k0) + end <= total_k;
 }
 
-// The backward kernel: this CTA's dK/dV units (list B, args `a`), then its
-// dQ units (list A, args `aq`; bwd_dq.cuh), in one launch.
-template <int D, bool BF16, bool FUNC>
-__global__ void __launch_bounds__(kDkdvThreads, 1)
-    hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dk,
-                    const __grid_constant__ CUtensorMap tm_dv,
-                    const __grid_constant__ CUtensorMap tm_ds, const AttnArgs a,
-                    const AttnArgs aq) {
-  using C = DkdvCfg<D>;
-  constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV, NS = C::NS;
+// One dK/dV phase of the backward kernel over list `a` (or the half of it
+// that a.part names): the role code of every warp.  PASS: both
+// accumulators (D <= 128), or the dV or dK pass (D = 256).  The caller has
+// allocated TMEM and waited for the previous grid; the phase initialises
+// its barriers at `bars`, and on return the block has synchronised and the
+// barriers are invalidated (every MMA, TMEM read and copy has completed).
+template <int D, bool BF16, bool FUNC, int PASS>
+__device__ __forceinline__ void dkdv_phase(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                           const CUtensorMap* tm_q, const CUtensorMap* tm_do,
+                                           const CUtensorMap* tm_dk, const CUtensorMap* tm_dv,
+                                           const AttnArgs& a, uint32_t base, uint64_t* bars,
+                                           volatile int* flags, UnitInfo* ring, uint32_t tmem) {
+  using C = DkdvCfg<D, PASS>;
+  constexpr int BQ = C::BQ, DH = C::DH, SPLIT = C::SPLIT, NKV = C::NKV;
+  constexpr int NSQ = C::NSQ, NSD = C::NSD;
   constexpr int KCH = D / 64;
+  constexpr bool DO_V = PASS != kPassDK;  // accumulates dV
+  constexpr bool DO_K = PASS != kPassDV;  // forms dP^T and dS^T, accumulates dK
   constexpr int RW = kDkdvRowWarps;
   constexpr int WPQ = RW / 4;    // row warps per TMEM lane quarter
   constexpr int CW = BQ / WPQ;   // query columns per row warp
@@ -103,54 +114,55 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   // and the producer writes them out with TMA stores before it loads the
   // unit after next into that buffer.
   constexpr bool STAGE = NKV == 2;
-  static_assert(!STAGE || SPLIT == 1, "staging holds the whole dK / dV tile");
+  static_assert(!STAGE || PASS == kPassBoth, "staging holds both tiles");
   // Score tiles issued ahead of the accumulation that frees their buffer.
-  // Step h + LOOK needs a Q / dO stage that only step h + LOOK - NS releases,
-  // so LOOK < NS, or the two issuers could wait on each other.
-  constexpr int LOOK = NS >= 3 ? 2 : 1;
-  static_assert(LOOK < NS || NS == 1, "look-ahead must leave a free stage");
+  // Both accumulators: step h + LOOK needs a Q / dO stage that only step
+  // h + LOOK - NS releases, so LOOK < NS, or the two issuers could wait on
+  // each other.  The dV pass releases Q with S^T, the dK pass dO with dP^T,
+  // so those rings never hold up the look-ahead; the dK pass's Q ring (two
+  // stages) still limits it to one.
+  constexpr int LOOK = PASS == kPassDV ? 2 : PASS == kPassDK ? 1 : (NSQ >= 3 ? 2 : 1);
+  static_assert(PASS != kPassBoth || NSQ != NSD || LOOK < NSQ || NSQ == 1,
+                "look-ahead must leave a free stage");
+  static_assert(PASS != kPassDK || LOOK < NSQ, "look-ahead must leave a free Q stage");
   constexpr uint32_t IDESC_S = idesc_f16(BF16, kBM, BQ, false, false);
   constexpr uint32_t IDESC_ACC = idesc_f16(BF16, kBM, DH, false, true);
-  constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ, COL_DK = 4 * BQ + DH;
-  static_assert(COL_DK + DH <= kTmemCols, "TMEM budget");
-  static_assert(C::SMEM <= 232448, "shared memory budget");
+  constexpr uint32_t COL_ST = 0, COL_DPT = 2 * BQ, COL_DV = 4 * BQ,
+                     COL_DK = 4 * BQ + (DO_V ? DH : 0);
+  static_assert((DO_K ? COL_DK : COL_DV) + DH <= kTmemCols, "TMEM budget");
+  static_assert(C::TILE_BYTES <= BwdCfg<D>::TILE_BYTES, "tile area");
   static_assert(CW == 32, "one query per lane in the arbitrary-mask transpose");
   static_assert(BQ == kDsQueries && kBM == kDsKeys && CW % 8 == 0 && CW <= 32,
                 "one stored dS block per half-step");
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sKV = base;                          // NKV x (K, V)
-  const uint32_t sQ = sKV + 2 * NKV * C::KV_BYTES;    // NS x Q
-  const uint32_t sDO = sQ + NS * C::Q_BYTES;          // NS x dO
+  const uint32_t sKV = base;                          // NKV x (K[, V])
+  const uint32_t sQ = sKV + NKV * C::KV_STRIDE;       // NSQ x Q
+  const uint32_t sDO = sQ + NSQ * C::Q_BYTES;         // NSD x dO
 
   enum {
-    KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NS,
-    DOFULL = QEMPTY + NS, DOEMPTY = DOFULL + NS, SFULL = DOEMPTY + NS, PFULL = SFULL + 2,
+    KVFULL = 0, KVEMPTY = KVFULL + NKV, QFULL = KVEMPTY + NKV, QEMPTY = QFULL + NSQ,
+    DOFULL = QEMPTY + NSQ, DOEMPTY = DOFULL + NSD, SFULL = DOEMPTY + NSD, PFULL = SFULL + 2,
     AFULL = PFULL + 2, DSFULL = AFULL + 2,
     ACCFULL = DSFULL + 2, ACCEMPTY = ACCFULL + 1, STAGED = ACCEMPTY + 1, UFULL = STAGED + 2,
     UEMPTY = UFULL + kUnitRing, DRAIN = UEMPTY + kUnitRing, NBARS = DRAIN + 2
   };
-  // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
-  static_assert(NBARS * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
-  // the dQ phase reuses the tile area and the barrier words
-  static_assert(DqCfg<D>::TILE_BYTES <= C::TILE_BYTES && dq::Bars<D>::NBARS <= NBARS,
-                "dQ phase fits the dK/dV layout");
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + C::TILE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  static_assert(NBARS <= BwdCfg<D>::kBars, "barrier area");
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    // K / V and dO are released by both issuers, Q by the dK chain (dK_h is
-    // its last reader: the row warps read S^T_h before dS^T_h exists)
-    for (int i = 0; i < NKV; ++i) { mbar_init(bar(KVFULL + i), 1); mbar_init(bar(KVEMPTY + i), 2); }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1);
-      mbar_init(bar(DOFULL + i), 1); mbar_init(bar(DOEMPTY + i), 2);
+    // K / V: released by each issuer that reads them (the dV pass: the dV
+    // chain only); Q by its last reader (dK, or S^T in the dV pass); dO by
+    // dV and dP^T (both accumulators), else by its one reader
+    constexpr int kv_readers = PASS == kPassDV ? 1 : 2;
+    for (int i = 0; i < NKV; ++i) {
+      mbar_init(bar(KVFULL + i), 1);
+      mbar_init(bar(KVEMPTY + i), kv_readers);
+    }
+    for (int i = 0; i < NSQ; ++i) { mbar_init(bar(QFULL + i), 1); mbar_init(bar(QEMPTY + i), 1); }
+    for (int i = 0; i < NSD; ++i) {
+      mbar_init(bar(DOFULL + i), 1);
+      mbar_init(bar(DOEMPTY + i), PASS == kPassBoth ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SFULL + i), 1);
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       mbar_init(bar(AFULL + i), RW);
       mbar_init(bar(DSFULL + i), RW);
     }
-    mbar_init(bar(ACCFULL), 2);
+    mbar_init(bar(ACCFULL), PASS == kPassBoth ? 2 : 1);  // the accumulating chains
     mbar_init(bar(ACCEMPTY), RW);
     mbar_init(bar(STAGED), RW);
     mbar_init(bar(STAGED + 1), RW);
@@ -168,29 +180,16 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     }
     mbar_init(bar(DRAIN), 1);
     mbar_init(bar(DRAIN + 1), 1);
-    flags[0] = 0;
-    flags[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
-    if (STAGE) { tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv); }
-    tma_prefetch_desc(&tm_ds);
-  }
-  if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
   __syncwarp();  // thread 0's set-up above diverged warp 0
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{a.header, flags, a.timeout_ns};
   const WaitCtl drain{a.header, flags + 1, a.timeout_ns};
-  // everything below reads what earlier grids wrote (work list, inputs)
-  if (a.pdl_wait == 1) grid_dependency_wait();
-  if (threadIdx.x == 0) grid_launch_dependents();
-  const int n_units = work_units(a);
-  UnitInfo* ring = reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4));
+  // list B whole, or one of its halves (D = 256: the dV pass takes the first)
+  const int n_all = work_units(a);
+  const int n_units = a.part != 0 ? n_all / 2 : n_all;
+  const int4* ulist = a.units + (a.part == 2 ? 2 * static_cast<int64_t>(n_units) : 0);
   const UnitQueue uq{ring, bar(UFULL), bar(UEMPTY)};
 
   if (warp == 0) {
@@ -202,8 +201,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       auto prefetch_qdo = [&](int h, int row) {
 #pragma unroll
         for (int c = 0; c < KCH; ++c) {
-          tma_prefetch_3d(&tm_q, 64 * c, h, row);
-          tma_prefetch_3d(&tm_do, 64 * c, h, row);
+          tma_prefetch_3d(tm_q, 64 * c, h, row);
+          tma_prefetch_3d(tm_do, 64 * c, h, row);
         }
       };
       // Staged output tiles of K/V buffers 0 and 1: first key row (-1: the
@@ -216,11 +215,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (!wait_bar(bar(STAGED + kb), (u >> 1) & 1u, w, 0x005)) return false;
         const int row = kb ? st_row1 : st_row0, hd = kb ? st_hd1 : st_hd0;
         if (row >= 0) {
-          const uint32_t kt = sKV + kb * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
+          const uint32_t kt = sKV + kb * C::KV_STRIDE, vt = kt + C::KV_BYTES;
 #pragma unroll
           for (int c = 0; c < KCH; ++c) {
-            tma_store_3d(&tm_dk, kt + c * (kBM * 128), 64 * c, hd, row);
-            tma_store_3d(&tm_dv, vt + c * (kBM * 128), 64 * c, hd, row);
+            tma_store_3d(tm_dk, kt + c * (kBM * 128), 64 * c, hd, row);
+            tma_store_3d(tm_dv, vt + c * (kBM * 128), 64 * c, hd, row);
           }
           bulk_commit_group();
           bulk_wait_read_all();
@@ -231,12 +230,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       // loads.  Every dK/dV unit, the first included, comes from the counter,
       // so only CTAs already running hold one: the dQ units that wait for
       // them never wait on a CTA that has not started.
-      UnitInfo nx = load_unit_info(a.units, atomicAdd(a.header + a.next_slot, 1), n_units);
+      UnitInfo nx = load_unit_info(ulist, atomicAdd(a.header + a.next_slot, 1), n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U = nx;
-        if (U.n > 0 && U.hz % SPLIT == 0) {
-          // first stored dS block of this key tile (D half 0 stores them);
-          // -1 when the metadata outgrew the workspace
+        if (U.n > 0 && DO_K) {
+          // first stored dS block of this key tile (the units that form dS^T
+          // store it); -1 when the metadata outgrew the workspace
           const int b0 = __ldg(a.ds_base + U.b), b1 = __ldg(a.ds_base + U.b + 1);
           const int blk = b0 + (U.hz / SPLIT) * ((b1 - b0) / a.H) +
                           ds_block_off(U.tile, U.Lq, U.Lk, a.win);
@@ -246,7 +245,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         }
         if (!unit_push(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        nx = load_unit_info(a.units, atomicAdd(a.header + a.next_slot, 1), n_units);
+        nx = load_unit_info(ulist, atomicAdd(a.header + a.next_slot, 1), n_units);
         if (U.n <= 0) continue;
         const int h = U.hz / SPLIT;
         const int k_row0 = U.k0 + kBM * U.tile;
@@ -265,12 +264,13 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         } else {
           if (!wait_bar(bar(KVEMPTY + kb), ((kvi / NKV) & 1) ^ 1, wc, 0x001)) { ok = false; break; }
         }
-        mbar_arrive_expect_tx(bar(KVFULL + kb), 2 * C::KV_BYTES);
-        const uint32_t kt = sKV + kb * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
+        mbar_arrive_expect_tx(bar(KVFULL + kb), C::KV_STRIDE);
+        const uint32_t kt = sKV + kb * C::KV_STRIDE, vt = kt + C::KV_BYTES;
 #pragma unroll
         for (int c = 0; c < KCH; ++c) {
-          tma_load_3d(kt + c * (kBM * 128), &tm_k, bar(KVFULL + kb), 64 * c, h, k_row0);
-          tma_load_3d(vt + c * (kBM * 128), &tm_v, bar(KVFULL + kb), 64 * c, h, k_row0);
+          tma_load_3d(kt + c * (kBM * 128), tm_k, bar(KVFULL + kb), 64 * c, h, k_row0);
+          if constexpr (C::LOAD_V)
+            tma_load_3d(vt + c * (kBM * 128), tm_v, bar(KVFULL + kb), 64 * c, h, k_row0);
         }
         ++kvi;
         // L2 warm-up runs kPrefetchQ steps ahead of the loads along the flat
@@ -282,23 +282,24 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         prev_n = U.n;
         int nx_m0 = -1;  // the next unit's first query block, read when first needed
         for (int m = 0; m < U.n; ++m) {
-          const int s = qi % NS;
+          const int sq = qi % NSQ, sd = qi % NSD;
           int qm = m0 + m;
           if constexpr (FUNC) {
             qm = bw.next<false>(a.fm, U.q0, U.b, U.tile, m_next, m_end);
             m_next = qm + 1;
           }
           const int row = q_seq0 + BQ * qm;
-          if (!wait_bar(bar(QEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(QFULL + s), C::Q_BYTES);
+          if (!wait_bar(bar(QEMPTY + sq), ((qi / NSQ) & 1) ^ 1, wc, 0x002)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(QFULL + sq), C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sQ + s * C::Q_BYTES + c * (BQ * 128), &tm_q, bar(QFULL + s), 64 * c, h, row);
-          if (!wait_bar(bar(DOEMPTY + s), ((qi / NS) & 1) ^ 1, wc, 0x004)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(DOFULL + s), C::Q_BYTES);
+            tma_load_3d(sQ + sq * C::Q_BYTES + c * (BQ * 128), tm_q, bar(QFULL + sq), 64 * c, h, row);
+          if (!wait_bar(bar(DOEMPTY + sd), ((qi / NSD) & 1) ^ 1, wc, 0x004)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(DOFULL + sd), C::Q_BYTES);
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
-            tma_load_3d(sDO + s * C::Q_BYTES + c * (BQ * 128), &tm_do, bar(DOFULL + s), 64 * c, h, row);
+            tma_load_3d(sDO + sd * C::Q_BYTES + c * (BQ * 128), tm_do, bar(DOFULL + sd), 64 * c, h,
+                        row);
           ++qi;
           // the L2 warm-up of step m + kPrefetchQ, after this step's loads (under an
           // arbitrary mask the next unit's first block is a global read)
@@ -310,8 +311,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             if (t == U.n) {
 #pragma unroll
               for (int c = 0; c < KCH; ++c) {
-                tma_prefetch_3d(&tm_k, 64 * c, nh, nx.k0 + kBM * nx.tile);
-                tma_prefetch_3d(&tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
+                tma_prefetch_3d(tm_k, 64 * c, nh, nx.k0 + kBM * nx.tile);
+                if constexpr (C::LOAD_V) tma_prefetch_3d(tm_v, 64 * c, nh, nx.k0 + kBM * nx.tile);
               }
             }
             if (nx_m0 < 0) nx_m0 = unit_first_qblock(a, nx, BQ);
@@ -327,35 +328,41 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       }
       for (uint32_t i = kvi > NKV ? kvi - NKV : 0; i < kvi; ++i)
         wait_bar(bar(KVFULL + i % NKV), (i / NKV) & 1, drain, 0x0f1);
-      for (uint32_t i = qi > NS ? qi - NS : 0; i < qi; ++i) {
-        wait_bar(bar(QFULL + i % NS), (i / NS) & 1, drain, 0x0f2);
-        wait_bar(bar(DOFULL + i % NS), (i / NS) & 1, drain, 0x0f3);
-      }
+      for (uint32_t i = qi > NSQ ? qi - NSQ : 0; i < qi; ++i)
+        wait_bar(bar(QFULL + i % NSQ), (i / NSQ) & 1, drain, 0x0f2);
+      for (uint32_t i = qi > NSD ? qi - NSD : 0; i < qi; ++i)
+        wait_bar(bar(DOFULL + i % NSD), (i / NSD) & 1, drain, 0x0f3);
     }
   } else if (warp == 1 || warp == MMA_B) {
     // ------------------------------------------------------------ chain issuers
     // Warp 1: S^T = K Q^T and dV += A^T dO.  Warp MMA_B: dP^T = V dO^T and
-    // dK += dS^T Q.  Waits on TMA-filled stages need no tcgen05 fence; waits
-    // on the row warps' TMEM writes do.
+    // dK += dS^T Q.  In the dV pass the dK chain only keeps pace with the
+    // unit ring; in the dK pass the dV chain issues S^T only.  Waits on
+    // TMA-filled stages need no tcgen05 fence; waits on the row warps' TMEM
+    // accesses do.
     if (lane == 0) {
       const bool vchain = warp == 1;
+      const bool accumulates = vchain ? DO_V : DO_K;
+      const bool idle = !vchain && !DO_K;  // the dK chain in the dV pass
       // score MMA: A = K or V tile (K-major), B = Q or dO stage (K-major)
       const int kv_off = vchain ? 0 : C::KV_BYTES;
       const uint32_t sB = vchain ? sQ : sDO;
       const int bfull = vchain ? QFULL : DOFULL;
+      const int nsb = vchain ? NSQ : NSD;  // the score's B-operand ring
       const uint32_t tScore = tmem + (vchain ? COL_ST : COL_DPT);
       const int score_full = vchain ? SFULL : PFULL;
       // accumulation: A = the 16-bit operand written over the score buffer,
       // B = dO or Q stage (MN-major), into dV or dK
       const uint32_t sAccB = vchain ? sDO : sQ;
       const int accbfull = vchain ? DOFULL : QFULL;
+      const int nsa = vchain ? NSD : NSQ;  // the accumulation's B-operand ring
       const int ready = vchain ? AFULL : DSFULL;
       const uint32_t tAcc = tmem + (vchain ? COL_DV : COL_DK);
       uint32_t kvi = 0, h = 0, oi = 0;
       bool ok = true;
       auto score = [&](uint32_t hh, const SDesc& ad) -> bool {
-        const int s = hh % NS, b = hh & 1;
-        if (!wait_bar(bar(bfull + s), (hh / NS) & 1, wc, vchain ? 0x106 : 0x107)) return false;
+        const int s = hh % nsb, b = hh & 1;
+        if (!wait_bar(bar(bfull + s), (hh / nsb) & 1, wc, vchain ? 0x106 : 0x107)) return false;
         const SDesc bd = kdesc(sB + s * C::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -363,40 +370,45 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                  kk > 0 ? 1u : 0u);
         mma_commit(bar(score_full + b));
         if (!vchain) mma_commit(bar(DOEMPTY + s));  // dP^T is the dK chain's only dO reader
+        if (vchain && PASS == kPassDV) mma_commit(bar(QEMPTY + s));  // the dV pass's only Q reader
         return true;
       };
       for (uint32_t uk = 0; ok; ++uk) {
         UnitInfo U;
         if (!unit_pop(uq, uk, U, wc)) { ok = false; break; }
         if (U.n < 0) break;
-        if (U.n <= 0) continue;
+        if (U.n <= 0 || idle) continue;
         const int kb = kvi % NKV;
-        const int n0 = (U.hz % SPLIT) * DH;
         if (!wait_bar(bar(KVFULL + kb), (kvi / NKV) & 1, wc, 0x104)) { ok = false; break; }
-        const SDesc ad = kdesc(sKV + kb * 2 * C::KV_BYTES + kv_off);
+        const SDesc ad = kdesc(sKV + kb * C::KV_STRIDE + kv_off);
         // the first LOOK score tiles of the unit; later ones follow the
-        // accumulation that frees their buffer
+        // accumulation (or, without one, the row warps' read) that frees
+        // their buffer
         for (int m = 0; m < U.n && m < LOOK && ok; ++m) ok = score(h + m, ad);
         for (int m = 0; m < U.n && ok; ++m, ++h) {
-          const int s = h % NS, b = h & 1;
+          const int b = h & 1;
           if (!wait_bar(bar(ready + b), (h >> 1) & 1, wc, vchain ? 0x105 : 0x10a)) { ok = false; break; }
-          if (!wait_bar(bar(accbfull + s), (h / NS) & 1, wc, 0x10b)) { ok = false; break; }
-          if (m == 0 && !wait_bar(bar(ACCEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
           tc_fence_after();
-          const SDesc bd = mndesc<BQ>(sAccB + s * C::Q_BYTES);
-          // A^T / dS^T of queries [16 kk, 16 kk + 16) sit packed in the first
-          // half of their row warp's own CW columns
+          if (accumulates) {
+            const int s = h % nsa;
+            if (!wait_bar(bar(accbfull + s), (h / nsa) & 1, wc, 0x10b)) { ok = false; break; }
+            if (m == 0 && !wait_bar(bar(ACCEMPTY), (oi & 1) ^ 1, wc, 0x103)) { ok = false; break; }
+            tc_fence_after();
+            const SDesc bd = mndesc<BQ>(sAccB + s * C::Q_BYTES);
+            // A^T / dS^T of queries [16 kk, 16 kk + 16) sit packed in the first
+            // half of their row warp's own CW columns
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tAcc, tScore + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
-                   desc_mnmajor<BQ>(bd, kk, n0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar((vchain ? DOEMPTY : QEMPTY) + s));
-          if (m == U.n - 1) mma_commit(bar(ACCFULL));
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_ts(tAcc, tScore + b * BQ + (16 * kk / CW) * CW + (16 * kk % CW) / 2,
+                     desc_mnmajor<BQ>(bd, kk, 0), IDESC_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar((vchain ? DOEMPTY : QEMPTY) + s));
+            if (m == U.n - 1) mma_commit(bar(ACCFULL));
+          }
           if (m + LOOK < U.n && !score(h + LOOK, ad)) { ok = false; break; }
         }
         if (!STAGE) mma_commit(bar(KVEMPTY + kb));  // staged: the epilogue frees it
         ++kvi;
-        ++oi;
+        if (accumulates) ++oi;
       }
       mma_commit(bar(DRAIN + (vchain ? 0 : 1)));
       wait_bar(bar(DRAIN + (vchain ? 0 : 1)), 0, drain, vchain ? 0x1ff : 0x1fe);
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int jj = kBM * V.tile + r;
       const int64_t grow = static_cast<int64_t>(V.k0) + jj;
       const int64_t hd = V.hz / SPLIT;
-      const int64_t col0 = static_cast<int64_t>(V.hz % SPLIT) * DH + cg * DW;
+      const int64_t col0 = cg * DW;
       dvrow = static_cast<char*>(a.o0) + (grow * a.o0_st + hd * a.o0_sh + col0) * 2;
       dkrow = static_cast<char*>(a.o1) + (grow * a.o1_st + hd * a.o1_sh + col0) * 2;
       // columns past d_out (a zero-padded head dim 32) are not stored
@@ -446,7 +458,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       if (staged) {
         // dV into the V half and dK into the K half of the unit's (K, V)
         // buffer, which no MMA reads any more (ACCFULL covers them all)
-        const uint32_t kt = sKV + (oi & 1u) * 2 * C::KV_BYTES, vt = kt + C::KV_BYTES;
+        const uint32_t kt = sKV + (oi & 1u) * C::KV_STRIDE, vt = kt + C::KV_BYTES;
 #pragma unroll
         for (int c = 0; c < DW / 32; ++c) {
           uint32_t xv[32], xk[32];
@@ -458,20 +470,28 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         char *dvrow, *dkrow;
         const bool row_ok = out_rows(V, dvrow, dkrow);
         uint32_t x[DW];
-        tmem_ld_w<DW>(tDV, x);
-        if (row_ok) store_row_n<DW, BF16>(dvrow, x, a.inv_L);
-        tmem_ld_w<DW>(tDK, x);
-        if (row_ok) store_row_n<DW, BF16>(dkrow, x, dk_scale);
+        if constexpr (DO_V) {
+          tmem_ld_w<DW>(tDV, x);
+          if (row_ok) store_row_n<DW, BF16>(dvrow, x, a.inv_L);
+        }
+        if constexpr (DO_K) {
+          tmem_ld_w<DW>(tDK, x);
+          if (row_ok) store_row_n<DW, BF16>(dkrow, x, dk_scale);
+        }
       } else {
         char *dvrow, *dkrow;
         const bool row_ok = out_rows(V, dvrow, dkrow);
 #pragma unroll 1
         for (int c = 0; c < DW / 32; ++c) {
           uint32_t x[32];
-          tmem_ld32(tDV + 32 * c, x);
-          if (row_ok) store_row_n<32, BF16>(dvrow + c * 64, x, a.inv_L);
-          tmem_ld32(tDK + 32 * c, x);
-          if (row_ok) store_row_n<32, BF16>(dkrow + c * 64, x, dk_scale);
+          if constexpr (DO_V) {
+            tmem_ld32(tDV + 32 * c, x);
+            if (row_ok) store_row_n<32, BF16>(dvrow + c * 64, x, a.inv_L);
+          }
+          if constexpr (DO_K) {
+            tmem_ld32(tDK + 32 * c, x);
+            if (row_ok) store_row_n<32, BF16>(dkrow + c * 64, x, dk_scale);
+          }
         }
       }
       warp_arrive(bar(ACCEMPTY));
@@ -491,7 +511,10 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int j_warp_last = kBM * U.tile + wq * 32 + 31;
       if (U.n <= 0) {  // no key steps: zeros, no TMEM
         char *dvrow, *dkrow;
-        if (out_rows(U, dvrow, dkrow)) { store_zero_n<DW>(dvrow); store_zero_n<DW>(dkrow); }
+        if (out_rows(U, dvrow, dkrow)) {
+          if (DO_V) store_zero_n<DW>(dvrow);
+          if (DO_K) store_zero_n<DW>(dkrow);
+        }
         count_unit(U);
         continue;
       }
@@ -527,11 +550,11 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const int hi = a.win.left < 0 ? Lq : min(Lq, j + a.win.left + 1);
       const int lo_all = a.win.right < 0 ? 0 : j_warp_last - a.win.right;
       const int hi_all = a.win.left < 0 ? Lq : min(Lq, j_warp_last - 31 + a.win.left + 1);
-      // dS blocks of this key tile: one per half-step, stored by the D half 0
-      // unit; this lane writes keys (r & ~1, r | 1) of query rows q, q + 2,
-      // ..., q = cg * CW + (r & 1), at q * 256 + (r & ~1) * 2
+      // dS blocks of this key tile: one per half-step, stored by the units
+      // that form dS^T; this lane writes keys (r & ~1, r | 1) of query rows
+      // q, q + 2, ..., q = cg * CW + (r & 1), at q * 256 + (r & ~1) * 2
       char* ds_row = nullptr;
-      if (U.ds >= 0)  // set by the producer for D half 0 when the blocks fit
+      if (DO_K && U.ds >= 0)  // set by the producer when the blocks fit
         ds_row = static_cast<char*>(a.ds) + static_cast<int64_t>(U.ds) * kDsBlockBytes +
                  (cg * CW + (r & 1)) * (kDsKeys * 2) + (r & ~1) * 2;
       const bool key_ok = j < Lk;
@@ -589,7 +612,6 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         if (!wait_bar_warp(bar(SFULL + b), (h >> 1) & 1, wc, 0x201)) { ok = false; break; }
         tc_fence_after();
         float hv[CW], tv[CW];
-        uint32_t pk[CW / 2];
         {
           uint32_t xs[CW];
           tmem_ld_w<CW>(tST + b * BQ, xs);
@@ -598,14 +620,19 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             hv[e] = ((valid >> e) & 1u) ? __uint_as_float(xs[e]) * half_alpha : 0.f;  // SiLU(0) = 0
             tv[e] = tanh_approx(hv[e]);
           }
+        }
+        if constexpr (DO_V) {
+          uint32_t pk[CW / 2];
 #pragma unroll
           for (int e = 0; e < CW / 2; ++e)
             pk[e] = pack2<BF16>(fmaf(hv[2 * e], tv[2 * e], hv[2 * e]),
                                 fmaf(hv[2 * e + 1], tv[2 * e + 1], hv[2 * e + 1]));
+          tmem_st_w<CW / 2>(tST + b * BQ, pk);   // in place over this warp's S^T columns
+          tmem_st_wait();
         }
-        tmem_st_w<CW / 2>(tST + b * BQ, pk);   // in place over this warp's S^T columns
-        tmem_st_wait();
+        // A^T written (or, in the dK pass, S^T read): the buffer is free
         warp_arrive(bar(AFULL + b));
+        if constexpr (!DO_K) continue;
         // dS^T = dP^T SiLU'(alpha S^T) (doubled), masked entries exactly 0
         if (!wait_bar_warp(bar(PFULL + b), (h >> 1) & 1, wc, 0x203)) { ok = false; break; }
         tc_fence_after();
@@ -650,30 +677,92 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-
-  // ---------------------------------------------------------------- dQ phase
-  // Every dK/dV MMA, TMEM read and copy of this CTA has completed: the dQ
-  // phase takes over the tile area, the barrier words and TMEM.  A CTA whose
-  // dK/dV phase gave up skips it (the dQ units that wait for its counts then
-  // give up too, after the wait limit).
-  const bool dkdv_ok = flags[0] == 0;
-  if (threadIdx.x == 0) {
+  tc_fence_after();
+  // every phase of these barriers has completed: retire them for the next phase
+  if (threadIdx.x == 0)
     for (int i = 0; i < NBARS; ++i) mbar_inval(bar(i));
-    dq::init_bars<D>(bars);
+  __syncwarp();
+}
+
+// The backward kernel: this CTA's dK/dV units (list B: args `a`, and at
+// D = 256 its dV pass `a` then its dK pass `a2`), then its dQ units (list A,
+// args `aq`; bwd_dq.cuh), in one launch.  Each phase takes over the tile
+// area, the barrier words and TMEM once the one before has drained.
+template <int D, bool BF16, bool FUNC>
+__global__ void __launch_bounds__(kDkdvThreads, 1)
+    hstu_bwd_kernel(const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv,
+                    const __grid_constant__ CUtensorMap tm_ds, const AttnArgs a,
+                    const AttnArgs a2, const AttnArgs aq) {
+  using B = BwdCfg<D>;
+  static_assert(dq::Bars<D>::NBARS <= B::kBars, "dQ phase barriers");
+  // control block: barriers | TMEM slot (8 B) | flags (16 B) | unit ring
+  static_assert(B::kBars * 8 + 24 + kUnitRing * sizeof(UnitInfo) <= kCtlBytes, "control block");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + B::TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B::kBars);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  UnitInfo* ring = reinterpret_cast<UnitInfo*>(const_cast<int*>(flags + 4));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    flags[0] = 0;
+    flags[1] = 0;
   }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_do);
+    if (D <= 128) { tma_prefetch_desc(&tm_dk); tma_prefetch_desc(&tm_dv); }
+    tma_prefetch_desc(&tm_ds);
+  }
+  if (warp == 1) { tmem_alloc(smem_u32(tmem_slot), kTmemCols); tmem_relinquish(); }
+  __syncwarp();  // thread 0's set-up above diverged warp 0
+  tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // everything below reads what earlier grids wrote (work lists, inputs)
+  if (a.pdl_wait == 1) grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+
+  // ---------------------------------------------------------------- dK/dV phases
+  if constexpr (D == 256) {
+    dkdv_phase<D, BF16, FUNC, kPassDV>(&tm_k, &tm_v, &tm_q, &tm_do, &tm_dk, &tm_dv, a, base, bars,
+                                       flags, ring, tmem);
+    if (flags[0] == 0)
+      dkdv_phase<D, BF16, FUNC, kPassDK>(&tm_k, &tm_v, &tm_q, &tm_do, &tm_dk, &tm_dv, a2, base,
+                                         bars, flags, ring, tmem);
+  } else {
+    dkdv_phase<D, BF16, FUNC, kPassBoth>(&tm_k, &tm_v, &tm_q, &tm_do, &tm_dk, &tm_dv, a, base,
+                                         bars, flags, ring, tmem);
+  }
+
+  // ---------------------------------------------------------------- dQ phase
+  // A CTA whose dK/dV phases gave up skips it (the dQ units that wait for its
+  // counts then give up too, after the wait limit).
+  const bool dkdv_ok = flags[0] == 0;
+  if (threadIdx.x == 0) dq::init_bars<D>(bars);
+  __syncwarp();
+  __syncthreads();
   if (dkdv_ok) dq::run<D, BF16>(&tm_ds, &tm_k, aq, base, bars, flags, ring, tmem);
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  // planned calls: the last CTA leaves both unit counters at zero and
+  // planned calls: the last CTA leaves the unit counters at zero and
   // advances the readiness epoch (every CTA has made its last claim and
   // passed its last readiness wait by then)
   if (a.planned && threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(a.header + kHdrDone, 1) == static_cast<int>(gridDim.x) - 1) {
       atomicExch(a.header + a.next_slot, 0);
+      if (D == 256) atomicExch(a.header + a2.next_slot, 0);
       atomicExch(a.header + aq.next_slot, 0);
       atomicAdd(a.header + kHdrEpoch, 1);
       atomicExch(a.header + kHdrDone, 0);
@@ -687,39 +776,39 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
 template <int D, bool BF16, bool FUNC>
 cudaError_t launch_bwd_f(int grid, cudaStream_t st, bool pdl, const BwdMaps& m, const AttnArgs& a,
-                         const AttnArgs& aq) {
+                         const AttnArgs& a2, const AttnArgs& aq) {
   auto kern = hstu_bwd_kernel<D, BF16, FUNC>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DkdvCfg<D>::SMEM);
+                                         BwdCfg<D>::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_attn(kern, grid, kDkdvThreads, DkdvCfg<D>::SMEM, st, pdl, m.k, m.v, m.q, m.dout,
-                     m.dk, m.dv, m.ds, a, aq);
+  return launch_attn(kern, grid, kDkdvThreads, BwdCfg<D>::SMEM, st, pdl, m.k, m.v, m.q, m.dout,
+                     m.dk, m.dv, m.ds, a, a2, aq);
 }
 
 // The arbitrary-mask path (its endpoint loads and ballot transpose) is a
 // separate instantiation, so that the window kernels keep their registers.
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(int grid, cudaStream_t st, bool pdl, const BwdMaps& m, const AttnArgs& a,
-                         const AttnArgs& aq) {
-  if (a.fm.func != nullptr) return launch_bwd_f<D, BF16, true>(grid, st, pdl, m, a, aq);
-  return launch_bwd_f<D, BF16, false>(grid, st, pdl, m, a, aq);
+                         const AttnArgs& a2, const AttnArgs& aq) {
+  if (a.fm.func != nullptr) return launch_bwd_f<D, BF16, true>(grid, st, pdl, m, a, a2, aq);
+  return launch_bwd_f<D, BF16, false>(grid, st, pdl, m, a, a2, aq);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const BwdMaps& m,
-                       const AttnArgs& a, const AttnArgs& aq) {
+                       const AttnArgs& a, const AttnArgs& a2, const AttnArgs& aq) {
   switch (D) {
-    case 64: return bf16 ? launch_bwd_t<64, true>(grid, st, pdl, m, a, aq)
-                         : launch_bwd_t<64, false>(grid, st, pdl, m, a, aq);
-    case 128: return bf16 ? launch_bwd_t<128, true>(grid, st, pdl, m, a, aq)
-                          : launch_bwd_t<128, false>(grid, st, pdl, m, a, aq);
-    case 256: return bf16 ? launch_bwd_t<256, true>(grid, st, pdl, m, a, aq)
-                          : launch_bwd_t<256, false>(grid, st, pdl, m, a, aq);
+    case 64: return bf16 ? launch_bwd_t<64, true>(grid, st, pdl, m, a, a2, aq)
+                         : launch_bwd_t<64, false>(grid, st, pdl, m, a, a2, aq);
+    case 128: return bf16 ? launch_bwd_t<128, true>(grid, st, pdl, m, a, a2, aq)
+                          : launch_bwd_t<128, false>(grid, st, pdl, m, a, a2, aq);
+    case 256: return bf16 ? launch_bwd_t<256, true>(grid, st, pdl, m, a, a2, aq)
+                          : launch_bwd_t<256, false>(grid, st, pdl, m, a, a2, aq);
     default: return cudaErrorInvalidValue;
   }
 }

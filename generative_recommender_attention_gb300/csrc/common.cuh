@@ -30,6 +30,7 @@ enum HeaderWord : int {
   kHdrOverflowF = 10, // plan: units dropped from list F
   kHdrDone = 11,      // plan: CTAs of the running kernel that have finished
   kHdrEpoch = 12,     // backward: calls completed since the readiness counts were zeroed
+  kHdrNextB2 = 13,    // next unclaimed unit of list B's second half (D = 256: the dK pass)
   kHdrKey = 16,       // plan: kPlanKeyInts words (16-byte aligned), the sizes the plan was made for
 };
 constexpr int kPlanKeyInts = 10;

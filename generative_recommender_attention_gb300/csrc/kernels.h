@@ -361,6 +361,7 @@ struct AttnArgs {
   int ds_cap;           // backward: dS blocks the workspace holds
   int* ready;           // backward: B x H readiness counts (see ready_target)
   int planned;          // 1: the work list comes from a plan (see below)
+  int part;             // list B at D = 256: 0 whole list, 1 its first half (dV pass), 2 its second
   int key[kPlanKeyInts];  // planned: this call's sizes, which must be the plan's
 };
 
@@ -429,30 +430,43 @@ struct DqCfg {
 
 // ------------------------------------------------------------ dK/dV config
 // 64-query half-steps: S^T and dP^T are double-buffered in TMEM next to the
-// dV and dK accumulators, A^T and dS^T are written in place over them.
-// Separate Q and dO rings (Q is released after dK, dO after dV).
-template <int D>
+// accumulators, A^T and dS^T are written in place over them.  Separate Q and
+// dO rings.  At D <= 128 one pass accumulates dV and dK together (PASS
+// both).  At D = 256 the two fp32 accumulators would fill TMEM, so a key
+// tile is visited twice: a dV pass (S^T and dV += A^T dO, no V tile, so its
+// shared memory holds more Q / dO stages) and a dK pass (S^T, dP^T and
+// dK += dS^T Q, dO released right after dP^T); each keeps a 256-column
+// accumulator, and neither recomputes a product of the other's half.
+enum : int { kPassBoth = 0, kPassDV = 1, kPassDK = 2 };
+template <int D, int PASS>
 struct DkdvCfg {
   static constexpr int BQ = 64;                      // queries per inner tile
-  static constexpr int DH = D == 256 ? 128 : D;      // dK/dV columns per unit
-  static constexpr int SPLIT = D / DH;
-  static constexpr int NKV = D == 256 ? 1 : 2;       // stationary (K, V) buffers
-  static constexpr int NS = D == 64 ? 8 : (D == 128 ? 3 : 1);  // Q and dO stages each
+  static constexpr int DH = D;                       // accumulator columns
+  static constexpr int SPLIT = D == 256 ? 2 : 1;     // list-B units per key tile and head
+  static constexpr bool LOAD_V = PASS != kPassDV;    // the dV pass needs no V tile
+  static constexpr int NKV = PASS == kPassBoth ? 2 : 1;  // stationary (K, V) buffers
+  static constexpr int NSQ = D == 64 ? 8 : D == 128 ? 3 : PASS == kPassDV ? 3 : 2;  // Q stages
+  static constexpr int NSD = D == 64 ? 8 : D == 128 ? 3 : PASS == kPassDV ? 2 : 1;  // dO stages
   static constexpr int KV_BYTES = kBM * D * 2;
+  static constexpr int KV_STRIDE = (LOAD_V ? 2 : 1) * KV_BYTES;  // one (K, V) buffer
   static constexpr int Q_BYTES = BQ * D * 2;
-  static constexpr int TILE_BYTES = 2 * NKV * KV_BYTES + 2 * NS * Q_BYTES;
+  static constexpr int TILE_BYTES = NKV * KV_STRIDE + (NSQ + NSD) * Q_BYTES;
+};
+// The backward kernel's tile area: the largest of its phases.
+template <int D>
+struct BwdCfg {
+  static constexpr int T_DKDV = D == 256 ? imax(DkdvCfg<D, kPassDV>::TILE_BYTES,
+                                                DkdvCfg<D, kPassDK>::TILE_BYTES)
+                                         : DkdvCfg<D, kPassBoth>::TILE_BYTES;
+  static constexpr int TILE_BYTES = imax(T_DKDV, DqCfg<D>::TILE_BYTES);
   static constexpr int SMEM = TILE_BYTES + kCtlBytes + kAlignSlack;
+  // control block: barriers (at most kBars) | TMEM slot (8 B) | flags (16 B) | unit ring
+  static constexpr int kBars = 80;
 };
 
-static_assert(FwdCfg<128>::SMEM <= 232448, "smem");
-static_assert(DqCfg<128>::SMEM <= 232448, "smem");
-static_assert(DkdvCfg<128>::SMEM <= 232448, "smem");
-static_assert(FwdCfg<256>::SMEM <= 232448 && DqCfg<256>::SMEM <= 232448 &&
-                  DkdvCfg<256>::SMEM <= 232448,
-              "smem");
-static_assert(FwdCfg<64>::SMEM <= 232448 && DqCfg<64>::SMEM <= 232448 &&
-                  DkdvCfg<64>::SMEM <= 232448,
-              "smem");
+static_assert(FwdCfg<128>::SMEM <= 232448 && BwdCfg<128>::SMEM <= 232448, "smem");
+static_assert(FwdCfg<256>::SMEM <= 232448 && BwdCfg<256>::SMEM <= 232448, "smem");
+static_assert(FwdCfg<64>::SMEM <= 232448 && BwdCfg<64>::SMEM <= 232448, "smem");
 
 __global__ void hstu_sched_kernel(const __grid_constant__ SchedArgs a);
 // Arbitrary mask: key hull of every 64-row query block (grid: blocks of 8
@@ -493,9 +507,10 @@ cudaError_t launch_fwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, co
 struct BwdMaps {
   CUtensorMap k, v, q, dout, dk, dv, ds;
 };
-// The backward: dK/dV units (list B, `a`), then dQ units (list A, `aq`).
+// The backward: dK/dV units (list B, `a`; at D = 256 its first half, the dV
+// pass, and `a2` its second half, the dK pass), then dQ units (list A, `aq`).
 cudaError_t launch_bwd(int D, bool bf16, int grid, cudaStream_t st, bool pdl, const BwdMaps& m,
-                       const AttnArgs& a, const AttnArgs& aq);
+                       const AttnArgs& a, const AttnArgs& a2, const AttnArgs& aq);
 cudaError_t launch_selftest_timeout(int* header, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace hstu

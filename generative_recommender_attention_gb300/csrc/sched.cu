@@ -7,12 +7,13 @@
 //           tiles only need keys up to their last row, a left bound cuts
 //           keys before the first row);
 //   list B: key tiles of 128 rows; cost = number of query tiles of `bq_b`
-//           rows that can see the tile; each key tile is emitted once per head
-//           and per D split;
+//           rows that can see the tile; each key tile is emitted once per
+//           head, and with split_b = 2 (D = 256) the list has two halves, one
+//           pass over every tile each (head field: h * split_b + pass);
 //   list F: (plans only) list A again with inner tiles of `bn_f` keys, the
 //           forward's, so that one launch schedules a forward and a backward.
 // A plan's block 0 also records the sizes the plan was made for.
-// Each unit record is two int4: {sequence, tile, head (x split), cost} and
+// Each unit record is two int4: {sequence, tile, head (x split_b), cost} and
 // {q offset, q length, k offset, k length}, so a consumer needs one round
 // trip to global memory per unit.  Units with cost 0 are kept (their rows
 // must be written as zeros) and sort last.  Order inside one cost bucket is
@@ -188,7 +189,10 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
   const int units_slot = list == 0 ? kHdrUnitsA : list == 1 ? kHdrUnitsB : kHdrUnitsF;
   const int next_slot = list == 0 ? kHdrNextA : list == 1 ? kHdrNextB : kHdrNextF;
   const int overflow_slot = list == 0 ? kHdrOverflow : list == 1 ? kHdrOverflowB : kHdrOverflowF;
-  const int per_tile = list_b ? a.H * a.split_b : a.H;
+  // List B at D = 256 holds two passes over every key tile: the dV passes
+  // first, then the dK passes in the same order, each half sorted by cost.
+  const int split = list_b ? a.split_b : 1;
+  const int per_tile = a.H;  // units of one tile in one half
   const int nb = cmax + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nwarps = blockDim.x >> 5;
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
   // pass 4: complete unit records at their bucket cursors; into shared
   // memory when the whole list fits there (one coalesced copy follows),
   // else straight to global memory
-  const bool staged = total <= a.stage_units;
+  const bool staged = split * total <= a.stage_units;
   int overflow = 0;
   for (int b = warp; b < a.B; b += nwarps) {
     const int4 sq = seq(b);
@@ -284,12 +288,15 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
       if (t >= nt) continue;
       const int pos = atomicAdd(&hist[min(cost, cmax)], per_tile);
       int4* dst = staged ? stage : units;
-      for (int e = 0; e < per_tile; ++e) {
-        if (pos + e < cap) {
-          dst[2 * (pos + e)] = make_int4(b, t, e, cost);
-          dst[2 * (pos + e) + 1] = make_int4(q0, Lq, k0, Lk);
-        } else {
-          overflow = 1;
+      for (int p = 0; p < split; ++p) {
+        for (int e = 0; e < per_tile; ++e) {
+          const int u = p * total + pos + e;
+          if (u < cap) {
+            dst[2 * u] = make_int4(b, t, e * split + p, cost);
+            dst[2 * u + 1] = make_int4(q0, Lq, k0, Lk);
+          } else {
+            overflow = 1;
+          }
         }
       }
     }
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
   __syncwarp();  // reconverge before the aligned CTA barrier
   const bool dropped = __syncthreads_or(overflow) != 0;  // units beyond the list's capacity
   if (staged)
-    for (int i = tid; i < 2 * min(total, cap); i += blockDim.x) units[i] = stage[i];
+    for (int i = tid; i < 2 * min(split * total, cap); i += blockDim.x) units[i] = stage[i];
 
   // the global words, after the last barrier
   if (ds_pass) {
@@ -325,7 +332,8 @@ __global__ void __launch_bounds__(kSchedThreads) hstu_sched_kernel(const __grid_
       for (int i = 0; i < kPlanKeyInts; ++i) a.header[kHdrKey + i] = a.key[i];
     }
     a.header[next_slot] = 0;
-    a.header[units_slot] = min(total, cap);
+    if (list_b) a.header[kHdrNextB2] = 0;
+    a.header[units_slot] = min(split * total, cap);
     if (list_b && a.ready != nullptr) a.header[kHdrEpoch] = 0;
     // sequences longer than the caller's max_seqlen_q: the dS blocks would
     // not fit; the dK/dV units then skip the stores past the end (list B's
