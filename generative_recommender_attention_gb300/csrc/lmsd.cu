@@ -74,12 +74,8 @@ __device__ __forceinline__ Philox4 draw8(uint64_t e0, uint32_t k, const PhiloxKe
   return philox4x32_10(static_cast<uint32_t>(g), static_cast<uint32_t>(g >> 32), k, 0u, key);
 }
 
-// Element 2 j + h of a draw is kept iff its 16-bit half (h = 0: low) is at
-// least thr, i.e. iff that half, moved to the top, is at least thr_hi =
-// thr << 16.
-__device__ __forceinline__ bool kept(const Philox4& r, int j, int h, uint32_t thr_hi) {
-  return (h == 0 ? r.v[j] << 16 : r.v[j]) >= thr_hi;
-}
+// Element 2 j + h of a draw is kept iff its 16-bit half of word j (h = 0:
+// low) is at least thr = floor(p 2^16); the kernels pass thr_hi = thr << 16.
 
 __device__ __forceinline__ float2 bf2(uint32_t w) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
@@ -220,9 +216,16 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
       }
       const float sc = drop ? a.scale : 1.f;
       const uint4 wv = ld16(a.w, ch), bv = ld16(a.b, ch);
-      uint32_t ya[4], yx[4], ym[4], mw[2] = {0u, 0u};
+      // keep masks, two elements per word: 0xffff in each 16-bit half whose
+      // draw is at least the threshold (a segment that is not written keeps
+      // nothing); one SIMD compare decides two elements
+      const uint32_t thr2 = (a.thr_hi >> 16) * 0x00010001u;
+      uint32_t ya[4], yx[4], ym[4], k0[4], k1[4], k2[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
+        k0[j] = __vcmpgeu2(r0.v[j], thr2);
+        k1[j] = a.concat_x ? __vcmpgeu2(r1.v[j], thr2) : 0u;
+        k2[j] = a.concat_u ? __vcmpgeu2(r2.v[j], thr2) : 0u;
         const float2 x2 = bf2(word(xv[c], j)), u2 = bf2(word(uv[c], j));
         const float2 w2 = bf2(word(wv, j)), b2 = bf2(word(bv, j));
         const float xs[2] = {x2.x, x2.y}, us[2] = {u2.x, u2.y};
@@ -230,22 +233,25 @@ __global__ void __launch_bounds__(32 * kLmsdWarps, fwd_blocks_per_sm(NC))
         float oa[2], ox[2], om[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const bool p0 = kept(r0, j, h, a.thr_hi);
-          const bool p1 = a.concat_x && kept(r1, j, h, a.thr_hi);
-          const bool p2 = a.concat_u && kept(r2, j, h, a.thr_hi);
           const float act = a.silu ? us[h] * sigmoid(us[h]) : us[h];
           const float l = (xs[h] - mean) * rstd * ws[h] + bs[h];
-          oa[h] = p2 ? act * sc : 0.f;
-          ox[h] = p1 ? xs[h] * sc : 0.f;
-          om[h] = p0 ? l * act * sc : 0.f;
-          const int i = 2 * j + h;
-          mw[i >> 2] |= (static_cast<uint32_t>(p0) | static_cast<uint32_t>(p1) << 1 |
-                         static_cast<uint32_t>(p2) << 2) << (8 * (i & 3));
+          oa[h] = act * sc;
+          ox[h] = xs[h] * sc;
+          om[h] = l * act * sc;
         }
-        ya[j] = pack2(oa[0], oa[1]);
-        yx[j] = pack2(ox[0], ox[1]);
-        ym[j] = pack2(om[0], om[1]);
+        // a dropped element is +0 (its 16 bits cleared)
+        ya[j] = pack2(oa[0], oa[1]) & k2[j];
+        yx[j] = pack2(ox[0], ox[1]) & k1[j];
+        ym[j] = pack2(om[0], om[1]) & k0[j];
       }
+      // mask bytes of elements 4 i .. 4 i + 3: bit k set where segment k keeps
+      // it; each byte of a permuted keep word is 0xff or 0
+      uint32_t mw[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        mw[i] = (__byte_perm(k0[2 * i], k0[2 * i + 1], 0x6420u) & 0x01010101u) |
+                (__byte_perm(k1[2 * i], k1[2 * i + 1], 0x6420u) & 0x02020202u) |
+                (__byte_perm(k2[2 * i], k2[2 * i + 1], 0x6420u) & 0x04040404u);
       if (drop) reinterpret_cast<uint2*>(a.mask + row * a.d)[ch] = make_uint2(mw[0], mw[1]);
       int seg = 0;
       if (a.concat_u) yrow[seg++ * nch + ch] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
