@@ -518,6 +518,9 @@ def main():
     ap.add_argument("--head-dim", type=int, default=None,
                     help="run the workload with another head dimension (32, 64, 128 or 256), "
                          "alpha = 1/sqrt(D); the name gets a _d<D> suffix")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="draw only this many sequences of the workload (same length "
+                         "distribution; the name gets a _b<B> suffix): smaller captures for ncu")
     ap.add_argument("--plan", action="store_true",
                     help="one hstu_attn_plan launch per step shared by the planned forward and "
                          "backward, instead of hstu_attn_fwd + hstu_attn_bwd scheduling each call")
@@ -540,6 +543,9 @@ def main():
         import dataclasses as _dc
         w = _dc.replace(w, name=f"{w.name}_d{args.head_dim}", head_dim=args.head_dim,
                         alpha=1.0 / math.sqrt(args.head_dim))
+    if args.batch is not None and args.batch != w.batch:
+        import dataclasses as _dc
+        w = _dc.replace(w, name=f"{w.name}_b{args.batch}", batch=args.batch)
     if args.impl == "reference":
         return run_reference(args, w)
 
