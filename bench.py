@@ -9,8 +9,8 @@ causal.  Inputs are synthetic (seed 0) and resident in HBM before timing.
 
 The metric counts algorithmic tensor FLOPs only, causal-aware:
 N = H * sum_b L_b (L_b + 1) / 2 attended pairs; forward 4 D N, backward
-10 D N (S recompute, dO V^T, dV, dK in the dK/dV kernel, dQ = dS K in the dQ
-kernel).
+10 D N (S recompute, dO V^T, dV, dK in the dK/dV units, dQ = dS K in the dQ
+units, one backward launch).
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle
 instead, on a bounded sample of the same workload.

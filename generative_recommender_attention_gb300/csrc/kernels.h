@@ -298,8 +298,8 @@ constexpr int kDsKeys = 128, kDsQueries = 64;
 constexpr int kDsBlockBytes = kDsKeys * kDsQueries * 2;
 
 // The backward is one launch: each CTA runs dK/dV units, then dQ units.  Every
-// row warp of a dK/dV unit of sequence b and head h (each D half of it at
-// D = 256) adds 1 to ready[b H + h] once its dS stores of the unit are
+// row warp of a dK/dV unit of sequence b and head h (each of its two passes
+// at D = 256) adds 1 to ready[b H + h] once its dS stores of the unit are
 // fenced, so a call raises the count by ready_target(Lk_b), and the dS
 // blocks of (b, h) are complete once it has; a dQ unit of (b, h) waits for
 // that before it reads them.  The scheduler zeroes the counts and the epoch
