@@ -208,6 +208,12 @@ __device__ __forceinline__ void dkdv_phase(const CUtensorMap* tm_k, const CUtens
       // Staged output tiles of K/V buffers 0 and 1: first key row (-1: the
       // row warps stored that unit row by row) and head.
       int st_row0 = -1, st_hd0 = 0, st_row1 = -1, st_hd1 = 0;
+      // A unit reads its K / V tiles and writes its dK / dV tiles once: those
+      // lines leave L2 first, so that more of the dS blocks stay there until
+      // the dQ units read them (Q / dO tiles, which the other key tiles of the
+      // group read again, keep the normal priority).  Measured: recsys 127.5
+      // against 129.9 us per step, no workload slower.
+      const uint64_t stream_policy = l2_policy_evict_first();
       // Writes out the dV / dK tiles that the u-th unit (with key steps)
       // staged in its K/V buffer, and waits until TMA has read them.
       auto store_staged = [&](uint32_t u, const WaitCtl& w) -> bool {
@@ -218,8 +224,8 @@ __device__ __forceinline__ void dkdv_phase(const CUtensorMap* tm_k, const CUtens
           const uint32_t kt = sKV + kb * C::KV_STRIDE, vt = kt + C::KV_BYTES;
 #pragma unroll
           for (int c = 0; c < KCH; ++c) {
-            tma_store_3d(tm_dk, kt + c * (kBM * 128), 64 * c, hd, row);
-            tma_store_3d(tm_dv, vt + c * (kBM * 128), 64 * c, hd, row);
+            tma_store_3d_hint(tm_dk, kt + c * (kBM * 128), 64 * c, hd, row, stream_policy);
+            tma_store_3d_hint(tm_dv, vt + c * (kBM * 128), 64 * c, hd, row, stream_policy);
           }
           bulk_commit_group();
           bulk_wait_read_all();
@@ -268,9 +274,11 @@ __device__ __forceinline__ void dkdv_phase(const CUtensorMap* tm_k, const CUtens
         const uint32_t kt = sKV + kb * C::KV_STRIDE, vt = kt + C::KV_BYTES;
 #pragma unroll
         for (int c = 0; c < KCH; ++c) {
-          tma_load_3d(kt + c * (kBM * 128), tm_k, bar(KVFULL + kb), 64 * c, h, k_row0);
+          tma_load_3d_hint(kt + c * (kBM * 128), tm_k, bar(KVFULL + kb), 64 * c, h, k_row0,
+                           stream_policy);
           if constexpr (C::LOAD_V)
-            tma_load_3d(vt + c * (kBM * 128), tm_v, bar(KVFULL + kb), 64 * c, h, k_row0);
+            tma_load_3d_hint(vt + c * (kBM * 128), tm_v, bar(KVFULL + kb), 64 * c, h, k_row0,
+                             stream_policy);
         }
         ++kvi;
         // L2 warm-up runs kPrefetchQ steps ahead of the loads along the flat

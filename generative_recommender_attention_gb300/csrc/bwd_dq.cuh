@@ -96,6 +96,8 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_ds, const CUtensorMap*
       // metadata beyond the sizes dropped dK/dV units (the call reports an
       // invalid argument): their counts would never complete, so skip the waits
       const bool counted = a.ready != nullptr && __ldcg(a.header + kHdrOverflowB) == 0;
+      // the last read of each dS block: its lines may leave L2 first
+      const uint64_t ds_policy = l2_policy_evict_first();
       UnitInfo nx = load_unit_info(a.units, blockIdx.x, n_units);
       for (uint32_t uk = 0; ok; ++uk) {
         const UnitInfo U = nx;
@@ -168,10 +170,11 @@ __device__ __forceinline__ void run(const CUtensorMap* tm_ds, const CUtensorMap*
           // A tile: 64-key chunk c of query rows 0-63 (block 2i) and 64-127 (2i + 1)
 #pragma unroll
           for (int c = 0; c < kDsKeys / 64; ++c) {
-            tma_load_3d(stage_a(s) + c * (kBM * 128), tm_ds, bar(FULL + s), 64 * c, 0, blk0);
+            tma_load_3d_hint(stage_a(s) + c * (kBM * 128), tm_ds, bar(FULL + s), 64 * c, 0, blk0,
+                             ds_policy);
             if (second)
-              tma_load_3d(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, tm_ds, bar(FULL + s),
-                          64 * c, 0, blk1);
+              tma_load_3d_hint(stage_a(s) + c * (kBM * 128) + kDsQueries * 128, tm_ds,
+                               bar(FULL + s), 64 * c, 0, blk1, ds_policy);
           }
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
